@@ -1,0 +1,365 @@
+/*
+ * oracle.c -- plain fp64 CPU reference for paged decode attention and the
+ * KV-cache append.
+ *
+ * TEST INFRASTRUCTURE. Only the test-suite, the package smoke check and the
+ * CPU-baseline leg of the benchmark load this file's library. No product code
+ * path links or calls it, and it shares no code with the CUDA library: it has
+ * its own bf16 decoding, its own block-table gather and its own softmax.
+ *
+ * What it computes (definitions, written out with no blocking or fusion):
+ *
+ *  - Paged KV cache: K and V are each [num_blocks][block_size][num_kv_heads]
+ *    [head_dim] bf16 ("LLM Inference Serving", KV-cache shape section); a
+ *    sequence's block table maps logical block i (tokens 16i..16i+15) to a
+ *    physical block ("ML Interview Prep, Lesson 13", section 3.5 "Paged
+ *    attention"; "07 -- Inference", section 2.2 diagram A -> [0, 3, 5]).
+ *
+ *  - Append ("LLM Inference Serving", block-table pseudo-code: append in place
+ *    into the last block's free slot): new token i goes to physical block
+ *    slot/16, offset slot%16; a negative slot is padding and is skipped.
+ *
+ *  - Attention: PagedAttention gives exactly the attention of the sequence's
+ *    logical tokens ("07 -- Inference", section 5.1: the online softmax is exact,
+ *    not an approximation), so the oracle gathers the blocks into a contiguous
+ *    fp64 K_s, V_s and evaluates softmax(scale * q K_s^T) V_s in fp64. With
+ *    n_query_per_seq = nq, query j (0-based) of a sequence of T tokens sits at
+ *    position T - nq + j and sees positions 0 .. T - nq + j (the causal mask of
+ *    speculative verification: "LLM Serving: Continuous Batching &
+ *    PagedAttention", section on speculative decoding mechanics). Query head qh
+ *    reads kv head qh / (num_q_heads / num_kv_heads) (grouped-query attention,
+ *    "ML Interview Prep, Lesson 13", section 3.3). A row that sees no token
+ *    (T < nq) is defined as all zeros.
+ *
+ *  - Split and merge ("07 -- Inference", section 5.3 FlashDecoding): a token
+ *    range gives a partial (m, l, acc) with m = max score, l = sum exp(x - m),
+ *    acc = sum exp(x - m) V; partials merge with the same rescaling rule as the
+ *    online softmax. These two routines are separate from the definition above
+ *    so the tests can check the merge rule against it.
+ *
+ * Parity: pinned (dense library attention, permutation invariance, weight sums,
+ * shared == copied, closed forms, the page's block-table diagram, merge algebra).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* bf16 is the upper half of an IEEE binary32; widening it is exact. */
+static double bf16_to_double(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+int oracle_kv_append(const uint16_t *k_new, const uint16_t *v_new,
+                     const int64_t *slot_mapping, int64_t n_new,
+                     uint16_t *k_cache, uint16_t *v_cache, int64_t num_blocks,
+                     int32_t block_size, int32_t num_kv_heads, int32_t head_dim)
+{
+    const int64_t row = (int64_t)num_kv_heads * head_dim; /* elements per token */
+    int bad = 0;
+    for (int64_t i = 0; i < n_new; ++i) {
+        const int64_t slot = slot_mapping[i];
+        if (slot < 0)
+            continue; /* padding */
+        const int64_t blk = slot / block_size;
+        const int64_t off = slot % block_size;
+        if (blk >= num_blocks) {
+            bad = 1; /* out of the pool: nothing written */
+            continue;
+        }
+        const int64_t dst = (blk * block_size + off) * row;
+        for (int64_t e = 0; e < row; ++e) {
+            k_cache[dst + e] = k_new[i * row + e];
+            v_cache[dst + e] = v_new[i * row + e];
+        }
+    }
+    return bad ? -1 : 0;
+}
+
+/* Copy the first T tokens of (sequence s, kv head h) into contiguous fp64
+ * K[T][D] and V[T][D], following the block table. Returns -1 if a block id
+ * the context needs is outside the pool. */
+static int gather_kv(const uint16_t *k_cache, const uint16_t *v_cache, int64_t num_blocks,
+                     int32_t block_size, const int32_t *table, int32_t T,
+                     int32_t num_kv_heads, int32_t head_dim, int32_t h,
+                     double *K, double *V)
+{
+    for (int32_t t = 0; t < T; ++t) {
+        const int32_t logical = t / block_size;
+        const int32_t off = t % block_size;
+        const int64_t phys = table[logical];
+        if (phys < 0 || phys >= num_blocks)
+            return -1;
+        const int64_t base = ((phys * block_size + off) * num_kv_heads + h) * (int64_t)head_dim;
+        for (int32_t d = 0; d < head_dim; ++d) {
+            K[(int64_t)t * head_dim + d] = bf16_to_double(k_cache[base + d]);
+            V[(int64_t)t * head_dim + d] = bf16_to_double(v_cache[base + d]);
+        }
+    }
+    return 0;
+}
+
+/* Softmax weights of one query row over the visible tokens 0..lim (others 0).
+ * x_t = scale * <q, K_t>; w_t = exp(x_t - max x) / sum exp(x - max x). */
+static void row_weights(const double *qrow, const double *K, int32_t T, int32_t lim,
+                        int32_t head_dim, double scale, double *w)
+{
+    double mx = -INFINITY;
+    for (int32_t t = 0; t < T; ++t) {
+        if (t > lim) {
+            w[t] = 0.0;
+            continue;
+        }
+        double dot = 0.0;
+        for (int32_t d = 0; d < head_dim; ++d)
+            dot += qrow[d] * K[(int64_t)t * head_dim + d];
+        w[t] = scale * dot;
+        if (w[t] > mx)
+            mx = w[t];
+    }
+    double z = 0.0;
+    for (int32_t t = 0; t <= lim && t < T; ++t) {
+        w[t] = exp(w[t] - mx);
+        z += w[t];
+    }
+    for (int32_t t = 0; t <= lim && t < T; ++t)
+        w[t] /= z;
+}
+
+static int check_shapes(int32_t num_seqs, int32_t nq, int32_t num_q_heads,
+                        int32_t num_kv_heads, int32_t head_dim, int32_t block_size)
+{
+    if (num_seqs < 0 || nq < 1 || num_kv_heads < 1 || num_q_heads < 1 || head_dim < 1 ||
+        block_size < 1 || num_q_heads % num_kv_heads != 0)
+        return -1;
+    return 0;
+}
+
+/* T_s clamped to what the block table can hold (a longer context is invalid
+ * input; both sides of the parity tests treat it as the table's capacity). */
+static int32_t eff_len(const int32_t *context_lens, int32_t s, int32_t mb, int32_t block_size)
+{
+    int32_t T = context_lens[s];
+    if (T < 0)
+        T = 0;
+    if ((int64_t)T > (int64_t)mb * block_size)
+        T = mb * block_size;
+    return T;
+}
+
+/*
+ * out[(s*nq + j)][qh][d] (fp64), for every sequence s, query j, query head qh.
+ * pair_mask (optional, [num_seqs][num_kv_heads]) restricts the work to the
+ * selected (sequence, kv head) pairs; rows of other pairs are left untouched.
+ */
+int oracle_paged_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                           int64_t num_blocks, int32_t block_size,
+                           const int32_t *block_tables, int32_t max_blocks_per_seq,
+                           const int32_t *context_lens, int32_t num_seqs,
+                           int32_t n_query_per_seq, int32_t num_q_heads, int32_t num_kv_heads,
+                           int32_t head_dim, float scale, const uint8_t *pair_mask,
+                           double *out, int32_t num_threads)
+{
+    if (check_shapes(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim, block_size))
+        return -2;
+    const int32_t group = num_q_heads / num_kv_heads;
+    const int64_t npairs = (int64_t)num_seqs * num_kv_heads;
+    int status = 0;
+#ifdef _OPENMP
+    if (num_threads > 0)
+        omp_set_num_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t pair = 0; pair < npairs; ++pair) {
+        const int32_t s = (int32_t)(pair / num_kv_heads);
+        const int32_t h = (int32_t)(pair % num_kv_heads);
+        if (pair_mask && !pair_mask[pair])
+            continue;
+        const int32_t T = eff_len(context_lens, s, max_blocks_per_seq, block_size);
+        double *K = (double *)malloc(sizeof(double) * ((size_t)T * head_dim + 1));
+        double *V = (double *)malloc(sizeof(double) * ((size_t)T * head_dim + 1));
+        double *w = (double *)malloc(sizeof(double) * ((size_t)T + 1));
+        double *qrow = (double *)malloc(sizeof(double) * (size_t)head_dim);
+        int bad = gather_kv(k_cache, v_cache, num_blocks, block_size,
+                            block_tables + (int64_t)s * max_blocks_per_seq, T,
+                            num_kv_heads, head_dim, h, K, V);
+        if (bad) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            status = -1;
+        }
+        for (int32_t j = 0; j < n_query_per_seq && !bad; ++j) {
+            const int32_t lim = T - n_query_per_seq + j; /* last visible position */
+            for (int32_t g = 0; g < group; ++g) {
+                const int32_t qh = h * group + g;
+                const int64_t row = ((int64_t)s * n_query_per_seq + j) * num_q_heads + qh;
+                double *o = out + row * head_dim;
+                for (int32_t d = 0; d < head_dim; ++d)
+                    o[d] = 0.0;
+                if (lim < 0 || T == 0)
+                    continue; /* sees no token */
+                for (int32_t d = 0; d < head_dim; ++d)
+                    qrow[d] = bf16_to_double(q[row * head_dim + d]);
+                row_weights(qrow, K, T, lim, head_dim, (double)scale, w);
+                for (int32_t t = 0; t <= lim && t < T; ++t)
+                    for (int32_t d = 0; d < head_dim; ++d)
+                        o[d] += w[t] * V[(int64_t)t * head_dim + d];
+            }
+        }
+        free(K);
+        free(V);
+        free(w);
+        free(qrow);
+    }
+    return status;
+}
+
+/* The softmax weights of one query row (sequence s, query j, query head qh):
+ * w[0..T-1], zero past the row's causal limit. Returns T, or -1 on error. */
+int oracle_attention_weights(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                             int64_t num_blocks, int32_t block_size,
+                             const int32_t *block_tables, int32_t max_blocks_per_seq,
+                             const int32_t *context_lens, int32_t num_seqs,
+                             int32_t n_query_per_seq, int32_t num_q_heads, int32_t num_kv_heads,
+                             int32_t head_dim, float scale, int32_t s, int32_t j, int32_t qh,
+                             double *w)
+{
+    if (check_shapes(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim, block_size) ||
+        s < 0 || s >= num_seqs || j < 0 || j >= n_query_per_seq || qh < 0 || qh >= num_q_heads)
+        return -1;
+    const int32_t group = num_q_heads / num_kv_heads;
+    const int32_t h = qh / group;
+    const int32_t T = eff_len(context_lens, s, max_blocks_per_seq, block_size);
+    const int32_t lim = T - n_query_per_seq + j;
+    double *K = (double *)malloc(sizeof(double) * ((size_t)T * head_dim + 1));
+    double *V = (double *)malloc(sizeof(double) * ((size_t)T * head_dim + 1));
+    double *qrow = (double *)malloc(sizeof(double) * (size_t)head_dim);
+    int bad = gather_kv(k_cache, v_cache, num_blocks, block_size,
+                        block_tables + (int64_t)s * max_blocks_per_seq, T, num_kv_heads,
+                        head_dim, h, K, V);
+    if (!bad) {
+        const int64_t row = ((int64_t)s * n_query_per_seq + j) * num_q_heads + qh;
+        for (int32_t d = 0; d < head_dim; ++d)
+            qrow[d] = bf16_to_double(q[row * head_dim + d]);
+        if (lim < 0) {
+            for (int32_t t = 0; t < T; ++t)
+                w[t] = 0.0;
+        } else {
+            row_weights(qrow, K, T, lim, head_dim, (double)scale, w);
+        }
+    }
+    free(K);
+    free(V);
+    free(qrow);
+    return bad ? -1 : T;
+}
+
+/*
+ * The partial state of one query row over the token range [t_begin, t_end)
+ * intersected with its visible tokens ("07 -- Inference", section 5.3): m is the
+ * largest score in the range (-inf if none), l = sum exp(x_t - m) and
+ * acc[d] = sum exp(x_t - m) V_t[d] (both 0 if the range sees nothing).
+ */
+int oracle_partial_state(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                         int64_t num_blocks, int32_t block_size,
+                         const int32_t *block_tables, int32_t max_blocks_per_seq,
+                         const int32_t *context_lens, int32_t num_seqs,
+                         int32_t n_query_per_seq, int32_t num_q_heads, int32_t num_kv_heads,
+                         int32_t head_dim, float scale, int32_t s, int32_t j, int32_t qh,
+                         int32_t t_begin, int32_t t_end, double *m_out, double *l_out,
+                         double *acc)
+{
+    if (check_shapes(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim, block_size) ||
+        s < 0 || s >= num_seqs || j < 0 || j >= n_query_per_seq || qh < 0 || qh >= num_q_heads)
+        return -1;
+    const int32_t group = num_q_heads / num_kv_heads;
+    const int32_t h = qh / group;
+    const int32_t T = eff_len(context_lens, s, max_blocks_per_seq, block_size);
+    const int32_t lim = T - n_query_per_seq + j;
+    double *K = (double *)malloc(sizeof(double) * ((size_t)T * head_dim + 1));
+    double *V = (double *)malloc(sizeof(double) * ((size_t)T * head_dim + 1));
+    double *x = (double *)malloc(sizeof(double) * ((size_t)T + 1));
+    double *qrow = (double *)malloc(sizeof(double) * (size_t)head_dim);
+    int bad = gather_kv(k_cache, v_cache, num_blocks, block_size,
+                        block_tables + (int64_t)s * max_blocks_per_seq, T, num_kv_heads,
+                        head_dim, h, K, V);
+    double m = -INFINITY, l = 0.0;
+    for (int32_t d = 0; d < head_dim; ++d)
+        acc[d] = 0.0;
+    if (!bad) {
+        const int64_t row = ((int64_t)s * n_query_per_seq + j) * num_q_heads + qh;
+        for (int32_t d = 0; d < head_dim; ++d)
+            qrow[d] = bf16_to_double(q[row * head_dim + d]);
+        int32_t lo = t_begin < 0 ? 0 : t_begin;
+        int32_t hi = t_end;
+        if (hi > lim + 1)
+            hi = lim + 1;
+        if (hi > T)
+            hi = T;
+        for (int32_t t = lo; t < hi; ++t) {
+            double dot = 0.0;
+            for (int32_t d = 0; d < head_dim; ++d)
+                dot += qrow[d] * K[(int64_t)t * head_dim + d];
+            x[t] = (double)scale * dot;
+            if (x[t] > m)
+                m = x[t];
+        }
+        for (int32_t t = lo; t < hi; ++t) {
+            const double e = exp(x[t] - m);
+            l += e;
+            for (int32_t d = 0; d < head_dim; ++d)
+                acc[d] += e * V[(int64_t)t * head_dim + d];
+        }
+    }
+    *m_out = m;
+    *l_out = l;
+    free(K);
+    free(V);
+    free(x);
+    free(qrow);
+    return bad ? -1 : 0;
+}
+
+/* Merge n partial states (m[i], l[i], acc[i][D]) into the normalised output:
+ * M = max m_i, L = sum l_i exp(m_i - M), out = sum acc_i exp(m_i - M) / L
+ * (zeros if no partial saw a token). */
+void oracle_merge_states(int32_t n, int32_t head_dim, const double *m, const double *l,
+                         const double *acc, double *out)
+{
+    double M = -INFINITY;
+    for (int32_t i = 0; i < n; ++i)
+        if (m[i] > M)
+            M = m[i];
+    for (int32_t d = 0; d < head_dim; ++d)
+        out[d] = 0.0;
+    if (M == -INFINITY)
+        return;
+    double L = 0.0;
+    for (int32_t i = 0; i < n; ++i) {
+        if (m[i] == -INFINITY)
+            continue;
+        const double f = exp(m[i] - M);
+        L += l[i] * f;
+        for (int32_t d = 0; d < head_dim; ++d)
+            out[d] += acc[(int64_t)i * head_dim + d] * f;
+    }
+    for (int32_t d = 0; d < head_dim; ++d)
+        out[d] /= L;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
