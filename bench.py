@@ -1,0 +1,414 @@
+"""Benchmark of one paged decode step (KV append + paged decode attention) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl pkv|reference]
+
+Prints ONE JSON line (rank 0). A step is the whole hot path over one batch:
+``kv_append`` of the step's new tokens, then ``paged_decode_attention`` (main
+kernel + merge kernel). Inputs are seeded synthetic data resident in HBM; an L2
+flush (a 512 MiB memset) separates timed steps and is not timed. ``value`` is
+the step's algorithmic bytes (Q + K + V + block tables + context lengths read,
+output written, plus the append's rows) per second of step time, in GB/s;
+shared-prefix blocks count once.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead (the
+only reference this method has), on a bounded sample of the same workload.
+Under torchrun every rank runs its own copy of the workload (independent
+sequences: weak scaling, no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+from paged_kv_cache_101_gb300 import roofline as R  # noqa: E402
+
+METRIC = "paged decode-attention KV-read GB/s vs ~8 TB/s HBM peak; µs per decode step"
+DEFAULT_WORKLOAD = "llama3_8b_decode"
+FLUSH_BYTES = 512 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM traffic (read + write bytes per launch) of the main attention kernel from
+# one ncu capture, keyed by workload; valid only while the kernel source hashes
+# to `source_sha256` (otherwise the bench reports traffic = null).
+NCU_TRAFFIC = {}
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("paged_decode.cu", "pkv_common.cuh", "pkv_internal.h"):
+        with open(os.path.join(ROOT, "paged_kv_cache_101_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def start(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ pkv arm
+def run_pkv(args, rank, world, dist):
+    import torch
+
+    import paged_kv_cache_101_gb300 as pkv
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = W.make_workload(args.workload)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    q = up(w.q)
+    k_cache, v_cache = up(w.k_cache), up(w.v_cache)
+    k_new, v_new = up(w.k_new), up(w.v_new)
+    slots = torch.from_numpy(w.slot_mapping).to(dev)
+    tables = torch.from_numpy(w.block_tables).to(dev)
+    lens = torch.from_numpy(w.context_lens).to(dev)
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    ws = pkv.workspace(dev, pkv.workspace_size(w.num_seqs, w.n_query_per_seq, w.num_q_heads,
+                                                w.num_kv_heads, w.head_dim))
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    attn_bytes = R.workload_bytes(w, unique=True)
+    attn_bytes_logical = R.workload_bytes(w, unique=False)
+    app_bytes = R.append_bytes(int(w.slot_mapping.size), w.num_kv_heads, w.head_dim)
+    step_bytes = attn_bytes + app_bytes
+
+    def step():
+        pkv.kv_append(k_new, v_new, slots, k_cache, v_cache)
+        pkv.paged_decode_attention(q, k_cache, v_cache, tables, lens, w.n_query_per_seq,
+                                   w.scale, out, ws=ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_k0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_k1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for ev in ev_k0 + ev_k1:
+        ev.record()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        pkv.set_profiling_events(ev_k0[i], ev_k1[i])
+        ev_s[i].record()
+        step()
+        ev_e[i].record()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    pkv.set_profiling_events(None, None)
+    clk = clocks.stop()
+
+    step_ms = [a.elapsed_time(b) for a, b in zip(ev_s, ev_e)]
+    kern_ms = [a.elapsed_time(b) for a, b in zip(ev_k0, ev_k1)]
+    ms_per_step = sum(step_ms) / K
+    kern_mean = sum(kern_ms) / K
+    err = pkv.workspace_error(ws)
+
+    # ---- end to end: per-step inputs from pinned host memory, output back to host
+    h_q = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    h_q.copy_(q)
+    h_kn = torch.empty(k_new.shape, dtype=torch.bfloat16).pin_memory()
+    h_kn.copy_(k_new)
+    h_vn = torch.empty(v_new.shape, dtype=torch.bfloat16).pin_memory()
+    h_vn.copy_(v_new)
+    h_slots = slots.cpu().pin_memory()
+    h_tables = tables.cpu().pin_memory()
+    h_lens = lens.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_slots, h_tables, h_lens))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        q.copy_(h_q, non_blocking=True)
+        k_new.copy_(h_kn, non_blocking=True)
+        v_new.copy_(h_vn, non_blocking=True)
+        slots.copy_(h_slots, non_blocking=True)
+        tables.copy_(h_tables, non_blocking=True)
+        lens.copy_(h_lens, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        flush.zero_()
+        e2e_step()
+    torch.cuda.synchronize()
+    Ke = max(1, min(K, 200))
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    for i in range(Ke):
+        flush.zero_()
+        e_s[i].record()
+        e2e_step()
+        e_e[i].record()
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e_s, e_e)) / Ke
+
+    # max over ranks
+    if dist is not None:
+        t = torch.tensor([ms_per_step, kern_mean, e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step, kern_mean, e2e_ms = (float(x) for x in t.tolist())
+
+    peak, peak_kind = measured_peaks()
+    achieved = attn_bytes / (kern_mean * 1e-3) / 1e9
+    traffic = None
+    nt = NCU_TRAFFIC.get(args.workload)
+    if nt and nt.get("source_sha256") == kernel_source_sha():
+        traffic = nt["bytes"]
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    res = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 6),
+        "us_per_step": round(ms_per_step * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 K/V/Q; pools in HBM; inputs > L2 and a 512 MiB "
+                "L2 flush between timed steps)",
+        "config": {
+            "workload": args.workload,
+            "num_seqs": w.num_seqs, "n_query_per_seq": w.n_query_per_seq,
+            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "block_size": 16,
+            "context_tokens": int(w.context_lens.sum()),
+            "num_blocks": w.num_blocks, "parallelism": f"replicas x{world}",
+            "l2": "flushed between timed steps (512 MiB memset, untimed)",
+            "step": "kv_append + paged_decode_attention (main + merge kernels)",
+            "bytes_per_step": step_bytes, "attention_bytes_unique": attn_bytes,
+            "attention_bytes_logical": attn_bytes_logical,
+        },
+        "roofline": {
+            "bound": "hbm", "kernel": "paged_decode_kernel",
+            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs (burst)",
+            "traffic": traffic, "kernel_us": round(kern_mean * 1e3, 3),
+            "algorithmic_bytes_per_launch": attn_bytes,
+        },
+        "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 6), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "path": "pinned host inputs -> H2D -> kv_append + attention -> D2H output"},
+        "gpu_launches": K * 3,
+        "device_error_word": err,
+    }
+    if clk is not None:
+        res["clocks"] = clk
+    return res
+
+
+# ------------------------------------------------------------------ oracle (CPU)
+def oracle_sample(w, budget_s: float, threads: int):
+    """Time the fp64 oracle on whole decode steps of ``w`` for about budget_s seconds
+    (at least one pass). Returns (GB/s of algorithmic bytes, passes, seconds)."""
+    import oracle as O
+
+    o = O.Oracle()
+    step_bytes = R.workload_bytes(w, unique=True) + R.append_bytes(
+        int(w.slot_mapping.size), w.num_kv_heads, w.head_dim)
+    t0 = time.perf_counter()
+    passes = 0
+    while True:
+        o.step(w, threads=threads)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or el * (passes + 1) / passes > 3 * budget_s:
+            break
+    return passes * step_bytes / el / 1e9, passes, el
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def sample_workload(name: str, max_seqs: int):
+    """The first ``max_seqs`` sequences of a workload (same lengths, pool and values)."""
+    w = W.make_workload(name)
+    if w.num_seqs <= max_seqs:
+        return w, f"all {w.num_seqs} sequences"
+    keep = max_seqs
+    w.context_lens = w.context_lens[:keep].copy()
+    w.block_tables = w.block_tables[:keep].copy()
+    w.q = w.q[: keep * w.n_query_per_seq].copy()
+    w.k_new = w.k_new[: keep * w.n_query_per_seq].copy()
+    w.v_new = w.v_new[: keep * w.n_query_per_seq].copy()
+    w.slot_mapping = w.slot_mapping[: keep * w.n_query_per_seq].copy()
+    w.shared = w.shared[:keep].copy()
+    w.num_seqs = keep
+    return w, f"first {keep} of {len(W.workload_lengths(name)[0])} sequences"
+
+
+CPU_SAMPLE_SEQS = {"tiny": 4, "llama3_8b_decode": 64, "llama3_70b_mix": 64, "long_splitk": 2,
+                   "spec_verify": 16}
+
+
+def cpu_baseline(args):
+    threads = host_cores()
+    w, desc = sample_workload(args.workload, CPU_SAMPLE_SEQS.get(args.workload, 8))
+    gbs, passes, el = oracle_sample(w, args.cpu_seconds, threads)
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{desc} of {args.workload}, {passes} full decode step(s) (append + "
+                      f"fp64 attention), {el:.1f} s on {threads} threads"}
+
+
+def run_reference(args):
+    threads = host_cores()
+    w, desc = sample_workload(args.workload, CPU_SAMPLE_SEQS.get(args.workload, 8))
+    import oracle as O
+    o = O.Oracle()
+    step_bytes = R.workload_bytes(w, unique=True) + R.append_bytes(
+        int(w.slot_mapping.size), w.num_kv_heads, w.head_dim)
+    for _ in range(args.warmup):
+        o.step(w, threads=threads)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        o.step(w, threads=threads)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = step_bytes / (ms * 1e-3) / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16 inputs)",
+        "config": {"workload": args.workload, "sample": desc},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"{desc} of {args.workload}; each step = append + fp64 attention"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=W.WORKLOAD_ORDER)
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as td
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        td.init_process_group("nccl")
+        dist = td
+    res = run_pkv(args, rank, world, dist)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(args)
+        print(json.dumps(res), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,191 @@
+/*
+ * pkv.h -- C ABI of the paged KV-cache decode library for one NVIDIA GB300
+ * (sm_103a).
+ *
+ * Two operations make up one decode step of PagedAttention-style serving:
+ *
+ *   pkv_kv_append                writes the step's new K/V rows into their
+ *                                slots of the paged pool;
+ *   pkv_paged_decode_attention   attends one or a few query tokens per
+ *                                sequence over the pool, through per-sequence
+ *                                block tables.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers named as device buffers must point to memory of the current
+ *    CUDA device; the library never allocates, frees or copies them to the
+ *    host. The caller owns every buffer.
+ *  - `stream` is a cudaStream_t (passed as void* so this header needs no CUDA
+ *    include); NULL means the legacy default stream. Work is enqueued
+ *    asynchronously on it; a return of PKV_OK means the launch was accepted.
+ *  - Arguments are validated on the host before anything is enqueued; an
+ *    invalid argument returns its status code and enqueues nothing.
+ *    Values that live in device memory (block ids, slots, context lengths)
+ *    cannot be checked without a device-to-host copy: the kernels clamp or
+ *    skip out-of-range values instead of faulting (documented per call), and
+ *    the results for such inputs are unspecified.
+ *  - bf16 is IEEE bfloat16 (the upper half of a binary32), little endian.
+ *  - Physical block size is fixed at 16 tokens (vLLM's default, "ML Interview
+ *    Prep, Lesson 13" section 3.5; "Chapter 18" section 18.2.2 on why 16).
+ *  - KV pool layout ("LLM Inference Serving", KV-cache shape section): K and V
+ *    are separate buffers, each [num_blocks][16][num_kv_heads][head_dim] bf16,
+ *    row-major. Token slot `slot = physical_block * 16 + offset`.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_NULL = 1,        /* a required pointer is NULL                     */
+    PKV_ERR_SHAPE = 2,       /* inconsistent or non-positive sizes             */
+    PKV_ERR_DTYPE = 3,       /* unknown output dtype                           */
+    PKV_ERR_ALIGN = 4,       /* a buffer is not aligned as required            */
+    PKV_ERR_RANGE = 5,       /* a size is beyond what the library supports     */
+    PKV_ERR_WORKSPACE = 6,   /* workspace missing or smaller than required     */
+    PKV_ERR_CUDA = 7,        /* a CUDA runtime/driver call or launch failed    */
+    PKV_ERR_UNSUPPORTED = 8  /* a valid shape this build has no kernel for     */
+} pkv_status;
+
+typedef enum pkv_dtype {
+    PKV_BF16 = 0,
+    PKV_FP32 = 1
+} pkv_dtype;
+
+/*
+ * pkv_kv_append -- write this step's new K/V rows into the paged pool.
+ *
+ * Passage: "LLM Inference Serving", block-table pseudo-code (when a token is
+ * generated it is appended in place into the last block's free slot, a new
+ * physical block being allocated first when that block is full) and "LLM
+ * Serving: Continuous Batching & PagedAttention", section 4.1 (a new 16-token
+ * block is taken from the free list when the sequence crosses a block
+ * boundary). Block allocation is the caller's host-side job; this call only
+ * writes rows: for every i in [0, n_new) with slot_mapping[i] >= 0,
+ *     k_cache[slot/16][slot%16][h][:] = k_new[i][h][:]   for every kv head h,
+ *     v_cache[slot/16][slot%16][h][:] = v_new[i][h][:].
+ * The copy is bit-exact.
+ *
+ *   k_new, v_new   device, bf16 [n_new][num_kv_heads][head_dim], 16-byte aligned
+ *   slot_mapping   device, int64 [n_new]; < 0 means "skip" (padding).
+ *                  A slot >= num_blocks*16 is skipped as well (no write, no fault).
+ *                  Two entries naming the same slot give an unspecified row.
+ *   k_cache,v_cache device, bf16 [num_blocks][16][num_kv_heads][head_dim],
+ *                  16-byte aligned; rows not named by slot_mapping are untouched.
+ *   head_dim       a multiple of 8 (rows move in 16-byte vectors), <= 1024.
+ *   n_new == 0     is a no-op returning PKV_OK.
+ * Writing into a block shared by several sequences (reference count > 1) is
+ * the caller's error: copy-on-write must happen first ("ML Interview Prep,
+ * Lesson 13" section 3.5).
+ */
+pkv_status pkv_kv_append(const void *k_new, const void *v_new,
+                         const int64_t *slot_mapping, int64_t n_new,
+                         void *k_cache, void *v_cache, int64_t num_blocks,
+                         int32_t num_kv_heads, int32_t head_dim, void *stream);
+
+/*
+ * pkv_workspace_size -- bytes of device workspace pkv_paged_decode_attention
+ * needs for this geometry on the CURRENT CUDA device (the size depends on its
+ * SM count). Returns 0 if the geometry is unsupported or no device is usable.
+ * The workspace holds the split-K partial states (m, l, acc) that the merge
+ * step combines, a per-sequence block prefix sum and a 4-byte device error
+ * word at offset 0 (see pkv_paged_decode_attention).
+ */
+size_t pkv_workspace_size(int32_t num_seqs, int32_t n_query_per_seq, int32_t num_q_heads,
+                          int32_t num_kv_heads, int32_t head_dim);
+
+/*
+ * pkv_paged_decode_attention -- decode attention over the paged pool.
+ *
+ * Passages: "ML Interview Prep, Lesson 13" section 3.5 (the kernel follows the
+ * block table and reads keys and values one block at a time) and section 3.3
+ * (grouped-query heads); "07 -- Inference" section 5.1 (online softmax, exact)
+ * and section 5.3 (FlashDecoding: split the KV sequence into chunks handled by
+ * separate thread blocks, each giving a partial (m, l, acc), merged with the
+ * online-softmax rescaling rule); "LLM Serving: Continuous Batching &
+ * PagedAttention", speculative decoding mechanics (the target scores all draft
+ * positions in one pass under a causal mask).
+ *
+ * For every sequence s, query j in [0, n_query_per_seq), query head qh:
+ *     T   = context_lens[s]          (tokens INCLUDING this step's nq new ones)
+ *     lim = T - n_query_per_seq + j  (last position query j may see)
+ *     x_t = scale * <q[s*nq+j][qh], K_s[t][qh/G]>   for t in [0, lim]
+ *     out[s*nq+j][qh] = sum_t softmax(x)_t * V_s[t][qh/G]
+ * with G = num_q_heads / num_kv_heads and K_s[t] the row at
+ * block_tables[s][t/16], offset t%16. A row with lim < 0 is all zeros.
+ * Accumulation is fp32 from bf16 inputs; the result matches the fp64
+ * definition within |err| <= 2e-3 + 1e-2*|ref| (bf16 output) and is
+ * deterministic for a given device and input (no atomics in any reduction).
+ *
+ *   q              device, bf16 [num_seqs*n_query_per_seq][num_q_heads][head_dim],
+ *                  16-byte aligned; row s*nq+j is query j of sequence s.
+ *   k_cache,v_cache device pool as described above, 16-byte aligned.
+ *   num_blocks     pool size in blocks, 1 .. 2^31-1. A table entry outside
+ *                  [0, num_blocks) reads zeros (no fault) and ORs 8 into the
+ *                  workspace error word.
+ *   block_tables   device, int32 [num_seqs][max_blocks_per_seq]; entries at and
+ *                  past ceil(T/16) are never read (any value, e.g. -1).
+ *   context_lens   device, int32 [num_seqs]; a value above 16*max_blocks_per_seq
+ *                  is clamped to it, a negative value counts as 0.
+ *   n_query_per_seq 1..4; num_q_heads % num_kv_heads == 0;
+ *                  (num_q_heads/num_kv_heads) * n_query_per_seq <= 32.
+ *   head_dim       64 or 128.
+ *   scale          usually 1/sqrt(head_dim).
+ *   out            device, [num_seqs*n_query_per_seq][num_q_heads][head_dim] of
+ *                  out_dtype (PKV_BF16 rounds to nearest even), 16-byte aligned.
+ *   workspace      device, >= pkv_workspace_size(...) bytes, 256-byte aligned,
+ *                  ZERO-FILLED before its first use. Its first 4 bytes are a
+ *                  sticky device error word: a kernel that gives up on a wait
+ *                  (never expected; a bounded wait guards against a hang)
+ *                  stores a nonzero code there and returns early. The library
+ *                  never clears it. Calls sharing a workspace must be ordered
+ *                  on one stream (or otherwise serialised).
+ *   num_seqs == 0  is a no-op returning PKV_OK.
+ */
+pkv_status pkv_paged_decode_attention(const void *q, const void *k_cache, const void *v_cache,
+                                      int64_t num_blocks, const int32_t *block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                      int32_t num_seqs, int32_t n_query_per_seq,
+                                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                      float scale, void *out, int32_t out_dtype, void *workspace,
+                                      size_t workspace_bytes, void *stream);
+
+/* Text for a status code (static storage; never NULL). */
+const char *pkv_status_string(int32_t status);
+
+/*
+ * Tuning options (process-wide, not thread-safe against concurrent calls):
+ *   PKV_OPT_NUM_CTAS     persistent grid size of the attention kernel; 0 = one
+ *                        CTA per SM (default). Any value >= 1 gives the same
+ *                        result up to fp32 rounding order.
+ *   PKV_OPT_STAGES       pipeline depth (K/V stages in shared memory); 0 = as
+ *                        many as fit (default), else clamped to [2, 8].
+ * Returns the previous value, or -1 for an unknown option or a negative value.
+ */
+enum { PKV_OPT_NUM_CTAS = 1, PKV_OPT_STAGES = 2 };
+int32_t pkv_set_option(int32_t option, int32_t value);
+
+/*
+ * pkv_set_profiling_events -- measurement hook (process-wide). When both are
+ * non-NULL, every later pkv_paged_decode_attention call records `before` (a
+ * cudaEvent_t) on its stream just before its main attention kernel and `after`
+ * just after it, before the merge kernel; cudaEventElapsedTime of the pair is
+ * that kernel's device time. NULL, NULL turns the hook off. The events stay
+ * owned by the caller and must belong to the stream's device.
+ */
+void pkv_set_profiling_events(void *before, void *after);
+
+/* Library version as an integer (major*10000 + minor*100 + patch). */
+int32_t pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,1 +1,197 @@
-"""paged_kv_cache_101_gb300: placeholder until the binding lands."""
+"""Python binding of libpkv: paged decode attention and KV append on one GB300.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libpkv.so`` (built from ``csrc/`` for sm_103a). There is no CPU or
+PyTorch fallback: if the library is missing, every call raises.
+
+    kv_append(k_new, v_new, slot_mapping, k_cache, v_cache)
+    paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens,
+                           n_query_per_seq, scale, out)
+
+Tensors are torch CUDA tensors on the current device: bf16 K/V/Q laid out as
+``include/pkv.h`` describes (pools ``[num_blocks, 16, num_kv_heads, head_dim]``),
+int64 slot mapping, int32 block tables and context lengths. Calls are enqueued
+on ``torch.cuda.current_stream()``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY_PATH = os.path.join(_HERE, "libpkv.so")
+
+PKV_OK = 0
+PKV_BF16, PKV_FP32 = 0, 1
+PKV_OPT_NUM_CTAS, PKV_OPT_STAGES = 1, 2
+BLOCK_SIZE = 16
+
+# function name -> (argtypes, restype); mirrors include/pkv.h
+_P, _I32, _I64, _SZ, _F = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t,
+                          ctypes.c_float)
+SIGNATURES = {
+    "pkv_kv_append": ([_P, _P, _P, _I64, _P, _P, _I64, _I32, _I32, _P], ctypes.c_int),
+    "pkv_workspace_size": ([_I32, _I32, _I32, _I32, _I32], _SZ),
+    "pkv_paged_decode_attention": ([_P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32,
+                                    _F, _P, _I32, _P, _SZ, _P], ctypes.c_int),
+    "pkv_status_string": ([_I32], ctypes.c_char_p),
+    "pkv_set_option": ([_I32, _I32], _I32),
+    "pkv_version": ([], _I32),
+    "pkv_set_profiling_events": ([_P, _P], None),
+}
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+class PkvError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: status {status} ({status_string(status)})")
+
+
+def lib():
+    """The loaded libpkv (raises if it was not built: there is no fallback)."""
+    global _lib
+    if _lib is None:
+        with _lib_lock:
+            if _lib is None:
+                if not os.path.exists(LIBRARY_PATH):
+                    raise RuntimeError(
+                        f"{LIBRARY_PATH} is missing: build it with "
+                        "`python -c 'import __graft_entry__ as g; g.build()'` "
+                        "(the CUDA library is the only implementation)")
+                handle = ctypes.CDLL(LIBRARY_PATH)
+                for name, (argtypes, restype) in SIGNATURES.items():
+                    fn = getattr(handle, name)
+                    fn.argtypes = argtypes
+                    fn.restype = restype
+                _lib = handle
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().pkv_status_string(int(status)).decode()
+
+
+def set_option(option: int, value: int) -> int:
+    return int(lib().pkv_set_option(int(option), int(value)))
+
+
+def set_profiling_events(before, after):
+    """Record two torch.cuda.Events around the main attention kernel of later calls
+    (None, None turns this off)."""
+    if before is None or after is None:
+        lib().pkv_set_profiling_events(None, None)
+        return
+    for ev in (before, after):
+        if not ev.cuda_event:
+            ev.record()  # torch creates the underlying event lazily
+    lib().pkv_set_profiling_events(ctypes.c_void_p(before.cuda_event),
+                                   ctypes.c_void_p(after.cuda_event))
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(device):
+    torch = _torch()
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(t, name, dtype, ndim=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+
+
+def kv_append(k_new, v_new, slot_mapping, k_cache, v_cache):
+    """Write new K/V rows ``[n_new, Hkv, D]`` into the pools at ``slot_mapping`` (int64)."""
+    torch = _torch()
+    _check(k_new, "k_new", torch.bfloat16, 3)
+    _check(v_new, "v_new", torch.bfloat16, 3)
+    _check(slot_mapping, "slot_mapping", torch.int64, 1)
+    _check(k_cache, "k_cache", torch.bfloat16, 4)
+    _check(v_cache, "v_cache", torch.bfloat16, 4)
+    NB, bs, Hkv, D = k_cache.shape
+    if bs != BLOCK_SIZE or v_cache.shape != k_cache.shape:
+        raise ValueError("pools must be [num_blocks, 16, Hkv, D] and equal in shape")
+    n = slot_mapping.shape[0]
+    if k_new.shape != (n, Hkv, D) or v_new.shape != (n, Hkv, D):
+        raise ValueError("k_new/v_new must be [n_new, Hkv, D] matching the pool")
+    st = lib().pkv_kv_append(k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(), n,
+                             k_cache.data_ptr(), v_cache.data_ptr(), NB, Hkv, D,
+                             _stream_handle(k_cache.device))
+    if st != PKV_OK:
+        raise PkvError("pkv_kv_append", st)
+
+
+def workspace_size(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim) -> int:
+    return int(lib().pkv_workspace_size(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads,
+                                        head_dim))
+
+
+_workspaces = {}
+
+
+def workspace(device, nbytes: int):
+    """A cached, zero-initialised workspace of at least ``nbytes`` on ``device``."""
+    torch = _torch()
+    key = torch.device(device).index if torch.device(device).index is not None else \
+        torch.cuda.current_device()
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def workspace_error(ws) -> int:
+    """The device error word at the start of a workspace (0 = no bounded wait gave up)."""
+    return int(ws[:4].view(_torch().int32).item())
+
+
+def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, n_query_per_seq,
+                           scale, out, ws=None):
+    """Decode attention over the paged pools; writes ``out`` (bf16 or fp32)."""
+    torch = _torch()
+    _check(q, "q", torch.bfloat16, 3)
+    _check(k_cache, "k_cache", torch.bfloat16, 4)
+    _check(v_cache, "v_cache", torch.bfloat16, 4)
+    _check(block_tables, "block_tables", torch.int32, 2)
+    _check(context_lens, "context_lens", torch.int32, 1)
+    if out.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("out must be bfloat16 or float32")
+    _check(out, "out", out.dtype, 3)
+    NB, bs, Hkv, D = k_cache.shape
+    if bs != BLOCK_SIZE or v_cache.shape != k_cache.shape:
+        raise ValueError("pools must be [num_blocks, 16, Hkv, D] and equal in shape")
+    S = context_lens.shape[0]
+    nq = int(n_query_per_seq)
+    Hq = q.shape[1]
+    if q.shape != (S * nq, Hq, D) or out.shape != q.shape:
+        raise ValueError("q and out must be [num_seqs * n_query_per_seq, Hq, D]")
+    if block_tables.shape[0] != S:
+        raise ValueError("block_tables must have num_seqs rows")
+    need = workspace_size(S, nq, Hq, Hkv, D)
+    if ws is None:
+        ws = workspace(q.device, need)
+    st = lib().pkv_paged_decode_attention(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), NB, block_tables.data_ptr(),
+        block_tables.shape[1], context_lens.data_ptr(), S, nq, Hq, Hkv, D, float(scale),
+        out.data_ptr(), PKV_FP32 if out.dtype == torch.float32 else PKV_BF16, ws.data_ptr(),
+        ws.numel(), _stream_handle(q.device))
+    if st != PKV_OK:
+        raise PkvError("pkv_paged_decode_attention", st)
+    return out

@@ -1,0 +1,315 @@
+// api.cu -- the extern "C" entry points of libpkv (see include/pkv.h).
+//
+// Every argument that lives on the host is validated before any CUDA call, so
+// an invalid call returns its status without touching the device. Tensor maps
+// (TMA descriptors) for the K/V pools are encoded on the host through the
+// driver entry point the CUDA runtime exposes (no link-time libcuda
+// dependency) and cached per (pointer, shape, device).
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "pkv.h"
+#include "pkv_internal.h"
+
+namespace {
+
+int32_t g_opt_num_ctas = 0;
+int32_t g_opt_stages = 0;
+cudaEvent_t g_ev_before = nullptr;
+cudaEvent_t g_ev_after = nullptr;
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct DeviceInfo {
+    bool valid = false;
+    int num_sms = 0;
+    int smem_optin = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+
+cudaError_t device_info(DeviceInfo *out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_dev[dev].valid) {
+        DeviceInfo d;
+        e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return e;
+        e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess)
+            return e;
+        d.valid = true;
+        g_dev[dev] = d;
+    }
+    *out = g_dev[dev];
+    return cudaSuccess;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+cudaError_t get_encoder()
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_encode)
+        return cudaSuccess;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess)
+        return e;
+    if (q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return cudaErrorNotSupported;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return cudaSuccess;
+}
+
+// A pool [num_blocks][16][Hkv][D] bf16 seen as 5-D (64, D/64, Hkv, 16, num_blocks);
+// a box is one (head, 64-column half) tile of one block: 16 rows x 128 B,
+// stored with the 128-byte swizzle.
+CUresult encode_pool(CUtensorMap *map, const void *base, int64_t num_blocks, int Hkv, int D)
+{
+    const cuuint64_t dims[5] = {64, cuuint64_t(D / 64), cuuint64_t(Hkv), 16,
+                                cuuint64_t(num_blocks)};
+    const cuuint64_t strides[4] = {128, cuuint64_t(D) * 2, cuuint64_t(Hkv) * D * 2,
+                                   cuuint64_t(16) * Hkv * D * 2};
+    const cuuint32_t box[5] = {64, 1, 1, 16, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+struct MapEntry {
+    const void *base = nullptr;
+    int64_t nb = 0;
+    int hkv = 0, d = 0, dev = -1;
+    CUtensorMap map;
+};
+MapEntry g_maps[16];
+int g_map_next = 0;
+
+cudaError_t pool_map(const void *base, int64_t nb, int Hkv, int D, CUtensorMap *out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    e = get_encoder();
+    if (e != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (auto &m : g_maps)
+        if (m.base == base && m.nb == nb && m.hkv == Hkv && m.d == D && m.dev == dev) {
+            *out = m.map;
+            return cudaSuccess;
+        }
+    MapEntry &m = g_maps[g_map_next];
+    g_map_next = (g_map_next + 1) % 16;
+    if (encode_pool(&m.map, base, nb, Hkv, D) != CUDA_SUCCESS) {
+        m.base = nullptr;
+        return cudaErrorInvalidValue;
+    }
+    m.base = base;
+    m.nb = nb;
+    m.hkv = Hkv;
+    m.d = D;
+    m.dev = dev;
+    *out = m.map;
+    return cudaSuccess;
+}
+
+// Host-side checks shared by the workspace query and the attention call.
+pkv_status check_geometry(int32_t num_seqs, int32_t nq, int32_t Hq, int32_t Hkv, int32_t D)
+{
+    if (num_seqs < 0 || nq < 1 || Hq < 1 || Hkv < 1)
+        return PKV_ERR_SHAPE;
+    if (Hq % Hkv != 0)
+        return PKV_ERR_SHAPE;
+    if (D != 64 && D != 128)
+        return PKV_ERR_UNSUPPORTED;
+    if (nq > 4)
+        return PKV_ERR_UNSUPPORTED;
+    if ((Hq / Hkv) * nq > pkv::kMaxRows)
+        return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pkv_status_string(int32_t status)
+{
+    switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_NULL: return "a required pointer is NULL";
+    case PKV_ERR_SHAPE: return "inconsistent or non-positive sizes";
+    case PKV_ERR_DTYPE: return "unknown output dtype";
+    case PKV_ERR_ALIGN: return "a buffer is not aligned as required";
+    case PKV_ERR_RANGE: return "a size is beyond what the library supports";
+    case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case PKV_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case PKV_ERR_UNSUPPORTED: return "no kernel for this (valid) shape";
+    default: return "unknown status";
+    }
+}
+
+int32_t pkv_version(void) { return 100; }
+
+void pkv_set_profiling_events(void *before, void *after)
+{
+    if (before && after) {
+        g_ev_before = static_cast<cudaEvent_t>(before);
+        g_ev_after = static_cast<cudaEvent_t>(after);
+    } else {
+        g_ev_before = g_ev_after = nullptr;
+    }
+}
+
+int32_t pkv_set_option(int32_t option, int32_t value)
+{
+    if (value < 0)
+        return -1;
+    int32_t prev;
+    switch (option) {
+    case PKV_OPT_NUM_CTAS:
+        prev = g_opt_num_ctas;
+        g_opt_num_ctas = value;
+        return prev;
+    case PKV_OPT_STAGES:
+        prev = g_opt_stages;
+        g_opt_stages = value;
+        return prev;
+    default:
+        return -1;
+    }
+}
+
+pkv_status pkv_kv_append(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                         int64_t n_new, void *k_cache, void *v_cache, int64_t num_blocks,
+                         int32_t num_kv_heads, int32_t head_dim, void *stream)
+{
+    if (n_new < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 1)
+        return PKV_ERR_SHAPE;
+    if (n_new == 0)
+        return PKV_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache)
+        return PKV_ERR_NULL;
+    if (head_dim % 8 != 0)
+        return PKV_ERR_UNSUPPORTED;
+    if (head_dim > 1024 || num_kv_heads > 1024 || n_new > 0x7fffffffLL ||
+        num_blocks > (int64_t(1) << 40))
+        return PKV_ERR_RANGE;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+        !aligned(v_cache, 16) || !aligned(slot_mapping, 8))
+        return PKV_ERR_ALIGN;
+    cudaError_t e = pkv::launch_kv_append(k_new, v_new, slot_mapping, n_new, k_cache, v_cache,
+                                          num_blocks, num_kv_heads, head_dim,
+                                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+size_t pkv_workspace_size(int32_t num_seqs, int32_t n_query_per_seq, int32_t num_q_heads,
+                          int32_t num_kv_heads, int32_t head_dim)
+{
+    if (check_geometry(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim) != PKV_OK)
+        return 0;
+    if (num_seqs == 0)
+        return 256;
+    DeviceInfo d;
+    if (device_info(&d) != cudaSuccess)
+        return 0;
+    pkv::DecodePlan pl;
+    if (pkv::plan_decode(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim, 1,
+                         d.num_sms, g_opt_num_ctas, g_opt_stages, d.smem_optin, &pl) != 0)
+        return 0;
+    return pl.ws_bytes;
+}
+
+pkv_status pkv_paged_decode_attention(const void *q, const void *k_cache, const void *v_cache,
+                                      int64_t num_blocks, const int32_t *block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                      int32_t num_seqs, int32_t n_query_per_seq,
+                                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                      float scale, void *out, int32_t out_dtype, void *workspace,
+                                      size_t workspace_bytes, void *stream)
+{
+    pkv_status st = check_geometry(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim);
+    if (st != PKV_OK)
+        return st;
+    if (num_blocks < 1 || max_blocks_per_seq < 1)
+        return PKV_ERR_SHAPE;
+    if (out_dtype != PKV_BF16 && out_dtype != PKV_FP32)
+        return PKV_ERR_DTYPE;
+    if (num_seqs == 0)
+        return PKV_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+        return PKV_ERR_NULL;
+    if (!workspace)
+        return PKV_ERR_WORKSPACE;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(workspace, 256))
+        return PKV_ERR_ALIGN;
+    if (max_blocks_per_seq > (1 << 26) || num_blocks > 0x7fffffffLL || num_seqs > (1 << 24) ||
+        num_kv_heads > 65535)
+        return PKV_ERR_RANGE;
+
+    DeviceInfo d;
+    if (device_info(&d) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    pkv::DecodePlan pl;
+    if (pkv::plan_decode(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim,
+                         max_blocks_per_seq, d.num_sms, g_opt_num_ctas, g_opt_stages,
+                         d.smem_optin, &pl) != 0)
+        return PKV_ERR_UNSUPPORTED;
+    if (workspace_bytes < pl.ws_bytes)
+        return PKV_ERR_WORKSPACE;
+
+    CUtensorMap kmap, vmap;
+    if (pool_map(k_cache, num_blocks, num_kv_heads, head_dim, &kmap) != cudaSuccess ||
+        pool_map(v_cache, num_blocks, num_kv_heads, head_dim, &vmap) != cudaSuccess)
+        return PKV_ERR_CUDA;
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    pkv::DecodeParams p;
+    memset(&p, 0, sizeof p);
+    p.q = static_cast<const uint16_t *>(q);
+    p.out = out;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.err = reinterpret_cast<uint32_t *>(ws);
+    p.seq_start = reinterpret_cast<int32_t *>(ws + pl.off_seq);
+    p.ml = reinterpret_cast<float *>(ws + pl.off_ml);
+    p.part = reinterpret_cast<float *>(ws + pl.off_part);
+    p.num_blocks = num_blocks;
+    p.S = num_seqs;
+    p.MB = max_blocks_per_seq;
+    p.nq = n_query_per_seq;
+    p.Hq = num_q_heads;
+    p.Hkv = num_kv_heads;
+    p.G = pl.G;
+    p.rows = pl.rows;
+    p.rows_pad = pl.rows_pad;
+    p.HG = pl.HG;
+    p.n_hg = pl.n_hg;
+    p.out_f32 = out_dtype == PKV_FP32;
+    p.stage_bytes = pl.stage_bytes;
+    p.nst = pl.nst;
+    p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+    cudaError_t e = pkv::launch_decode(pl, p, kmap, vmap, static_cast<cudaStream_t>(stream),
+                                       g_ev_before, g_ev_after);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,743 @@
+// paged_decode.cu -- paged decode attention for sm_103a.
+//
+// What is computed: for every sequence s, query j < nq and query head qh,
+//   out = softmax_t(scale * <q, K_s[t]>) . V_s   over t <= T_s - nq + j,
+// with K_s/V_s the sequence's tokens reached through its block table
+// ("ML Interview Prep, Lesson 13" section 3.5: the kernel follows the block table
+// and reads keys and values one block at a time; "07 -- Inference" section 5.1:
+// online softmax with running max m, running sum l and a rescaled accumulator;
+// section 5.3: FlashDecoding split + merge with the same rescaling rule).
+//
+// How (GB300 design, not the pages' kernel):
+//  * Work space. Per head group (HG kv heads), the blocks of all sequences are
+//    laid end to end: unit u = hg * NB_total + block_prefix[s] + b. The
+//    persistent grid cuts this flat space into equal contiguous chunks, one per
+//    CTA, so every CTA streams the same number of 16-token blocks whatever the
+//    length mix (short and long sequences both fill all SMs). A sequence cut by
+//    a chunk boundary leaves a partial (m, l, acc) per CTA in the workspace; the
+//    merge kernel combines them. Sequences inside one chunk are finished in
+//    place (normalised output written directly).
+//  * Staging. Warp 0 is the producer: it walks its chunk, reads block-table
+//    entries 32 at a time (one coalesced load), and for each block issues TMA
+//    tensor loads of K and V for its HG heads into a ring of shared-memory
+//    stages (128-byte swizzle, mbarrier completion with byte counts). Stages are
+//    recycled through "empty" mbarriers the consumers arrive on.
+//  * Math. One or two consumer warps per kv head. Scores S^T = K.Q^T use bf16
+//    mma.sync m16n8k16 with M = the block's 16 tokens, N = 8 query rows, K =
+//    16 head dims (fp32 accumulate). The online softmax runs on the fragments
+//    (warp shuffles across the 8 token lanes). P is split into bf16 hi + lo
+//    parts (P = hi + lo to 2^-16) and transposed in registers with movmatrix,
+//    then O^T += V^T.P^T with V^T fragments from ldmatrix.trans. Rows of a
+//    sequence's last block past T_s are masked in the scores and zeroed in the
+//    V fragments, so stale or NaN pool contents never reach the output.
+//  * Safety. Every mbarrier wait is bounded (2 s of %globaltimer); on timeout
+//    the warp records a code in the workspace error word and unwinds; the
+//    producer waits (bounded) for its own TMA copies before leaving. TMA reads
+//    of an out-of-range block id return zeros instead of faulting.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "pkv_common.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+struct StageHdr {
+    int32_t s;      // sequence
+    int32_t b;      // logical block within the sequence
+    int32_t T;      // context length (clamped)
+    int32_t hg;     // head group
+    int32_t flags;  // F_*
+    int32_t slot;   // partial slot for a split sequence's segment (0: chunk's first)
+    int32_t pad0, pad1;
+};
+enum : int32_t { F_FIRST = 1, F_LAST = 2, F_DIRECT = 4, F_END = 8 };
+
+__device__ __forceinline__ int seq_tokens(const DecodeParams &p, int s)
+{
+    int T = __ldg(p.context_lens + s);
+    T = T < 0 ? 0 : T;
+    const int cap = p.MB * kBlockSize;
+    return T > cap ? cap : T;
+}
+
+__device__ __forceinline__ int seq_blocks(const DecodeParams &p, int s)
+{
+    return (seq_tokens(p, s) + kBlockSize - 1) / kBlockSize;
+}
+
+struct Smem {
+    uint8_t *stages;
+    StageHdr *hdr;
+    uint64_t *full;
+    uint64_t *empty;
+};
+
+__device__ __forceinline__ Smem carve(uint8_t *raw, const DecodeParams &p)
+{
+    uint8_t *base =
+        reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    Smem s;
+    s.stages = base;
+    s.hdr = reinterpret_cast<StageHdr *>(base + size_t(p.nst) * p.stage_bytes);
+    s.full = reinterpret_cast<uint64_t *>(s.hdr + p.nst);
+    s.empty = s.full + p.nst;
+    return s;
+}
+
+// ------------------------------------------------------------------ producer
+template <int D>
+__device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
+                              const DecodeParams &p, const Smem &sm, int lane)
+{
+    constexpr int NH = D / 64;
+    const unsigned FULLMASK = 0xffffffffu;
+    const int S = p.S;
+
+    // ---- block prefix sums over sequences (lane l owns a contiguous range)
+    const int per = (S + 31) / 32;
+    const int s_lo = min(S, lane * per), s_hi = min(S, s_lo + per);
+    int local = 0;
+    for (int s = s_lo; s < s_hi; ++s)
+        local += seq_blocks(p, s);
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(FULLMASK, incl, o);
+        if (lane >= o)
+            incl += v;
+    }
+    const int base = incl - local;
+    const int nb_total = __shfl_sync(FULLMASK, incl, 31);
+    if (blockIdx.x == 0) {
+        int run = base;
+        for (int s = s_lo; s < s_hi; ++s) {
+            p.seq_start[s] = run;
+            run += seq_blocks(p, s);
+        }
+        if (lane == 0)
+            p.seq_start[S] = nb_total;
+    }
+
+    const int64_t F = int64_t(p.n_hg) * nb_total;
+    const int64_t f0 = int64_t(blockIdx.x) * F / gridDim.x;
+    const int64_t f1 = int64_t(blockIdx.x + 1) * F / gridDim.x;
+
+    uint32_t st = 0, phase = 0;  // ring position of the next stage to fill
+    uint32_t issued = 0;         // stages filled so far
+    bool ok = true;
+
+    if (f0 < f1) {
+        // ---- locate the first unit of this chunk
+        int hg = int(f0 / nb_total);
+        const int r0 = int(f0 - int64_t(hg) * nb_total);
+        const unsigned own = __ballot_sync(FULLMASK, local > 0 && r0 >= base && r0 < base + local);
+        const int src = __ffs(own) - 1;
+        int s_f = 0, b_f = 0;
+        if (lane == src) {
+            int run = base;
+            for (int s = s_lo; s < s_hi; ++s) {
+                const int nb = seq_blocks(p, s);
+                if (r0 < run + nb) {
+                    s_f = s;
+                    b_f = r0 - run;
+                    break;
+                }
+                run += nb;
+            }
+        }
+        int s = __shfl_sync(FULLMASK, s_f, src);
+        int b = __shfl_sync(FULLMASK, b_f, src);
+        int T = seq_tokens(p, s);
+        int nb = (T + kBlockSize - 1) / kBlockSize;
+        int seg_b0 = b;
+        bool chunk_first = true;
+        int bt_base = -(1 << 30);
+        int bt_val = 0;
+        const uint64_t pol = policy_evict_first();
+
+        for (int64_t u = f0; u < f1; ++u) {
+            if (b < bt_base || b >= bt_base + 32) {
+                bt_base = b;
+                const int idx = b + lane;
+                bt_val = idx < nb ? __ldg(p.block_tables + int64_t(s) * p.MB + idx) : 0;
+            }
+            int phys = __shfl_sync(FULLMASK, bt_val, b - bt_base);
+            if (phys < 0 || int64_t(phys) >= p.num_blocks) {
+                // outside the pool: flag it; the TMA box past the tensor's end reads zeros
+                if (lane == 0)
+                    atomicOr(p.err, kErrBadBlock);
+                phys = int(p.num_blocks < 0x7fffffff ? p.num_blocks : 0x7fffffff);
+            }
+            if (issued >= uint32_t(p.nst)) {
+                int w_ok = 1;
+                if (lane == 0)
+                    w_ok = mbar_wait(smem_u32(&sm.empty[st]), phase ^ 1u, kWaitLimitNs);
+                w_ok = __shfl_sync(FULLMASK, w_ok, 0);
+                if (!w_ok) {
+                    ok = false;
+                    break;
+                }
+            }
+            const bool first = (u == f0) || (b == 0);
+            if (first)
+                seg_b0 = b;
+            const bool last = (u == f1 - 1) || (b == nb - 1);
+            int flags = (first ? F_FIRST : 0) | (last ? F_LAST : 0);
+            if (last && seg_b0 == 0 && b == nb - 1)
+                flags |= F_DIRECT;
+            if (lane == 0) {
+                StageHdr *h = &sm.hdr[st];
+                h->s = s;
+                h->b = b;
+                h->T = T;
+                h->hg = hg;
+                h->flags = flags;
+                h->slot = chunk_first ? 0 : 1;
+                const uint32_t bar = smem_u32(&sm.full[st]);
+                mbar_arrive_expect_tx(bar, uint32_t(p.stage_bytes));
+                const uint32_t kdst = smem_u32(sm.stages + size_t(st) * p.stage_bytes);
+                const uint32_t vdst = kdst + uint32_t(p.HG * NH * kTileBytes);
+                const int h0 = hg * p.HG;
+                for (int hl = 0; hl < p.HG; ++hl) {
+#pragma unroll
+                    for (int hf = 0; hf < NH; ++hf) {
+                        const uint32_t off = uint32_t((hl * NH + hf) * kTileBytes);
+                        tma_load_5d_hint(kdst + off, kmap, bar, 0, hf, h0 + hl, 0, phys, pol);
+                        tma_load_5d_hint(vdst + off, vmap, bar, 0, hf, h0 + hl, 0, phys, pol);
+                    }
+                }
+            }
+            __syncwarp();
+            ++issued;
+            if (++st == uint32_t(p.nst)) {
+                st = 0;
+                phase ^= 1u;
+            }
+            if (last)
+                chunk_first = false;
+            // advance to the next unit
+            ++b;
+            if (b == nb && u + 1 < f1) {
+                do {
+                    if (++s == S) {
+                        s = 0;
+                        ++hg;
+                    }
+                    T = seq_tokens(p, s);
+                    nb = (T + kBlockSize - 1) / kBlockSize;
+                } while (nb == 0);
+                b = 0;
+                bt_base = -(1 << 30);
+            }
+        }
+    }
+
+    if (ok) {
+        // end-of-work marker for the consumers (no bytes: a plain arrival)
+        if (issued >= uint32_t(p.nst)) {
+            int w_ok = 1;
+            if (lane == 0)
+                w_ok = mbar_wait(smem_u32(&sm.empty[st]), phase ^ 1u, kWaitLimitNs);
+            ok = __shfl_sync(FULLMASK, w_ok, 0) != 0;
+        }
+        if (ok && lane == 0) {
+            sm.hdr[st].flags = F_END;
+            mbar_arrive(smem_u32(&sm.full[st]));
+        }
+    }
+    if (!ok && lane == 0) {
+        atomicOr(p.err, kErrProducerWait);
+        // wait (bounded) for every copy this warp may still have in flight
+        const uint32_t n = issued < uint32_t(p.nst) ? issued : uint32_t(p.nst);
+        for (uint32_t k = 0; k < n; ++k) {
+            // the k-th most recent fill: ring position and its phase parity
+            uint32_t ps = st, pp = phase;
+            for (uint32_t back = 0; back <= k; ++back) {
+                if (ps == 0) {
+                    ps = uint32_t(p.nst) - 1;
+                    pp ^= 1u;
+                } else {
+                    --ps;
+                }
+            }
+            if (!mbar_wait(smem_u32(&sm.full[ps]), pp, kWaitLimitNs))
+                atomicOr(p.err, kErrDrainWait);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ consumer
+template <int D, int NTW, int WPH>
+__device__ void consumer_warp(const DecodeParams &p, const Smem &sm, int cw, int lane)
+{
+    constexpr int NH = D / 64;  // 64-column halves per head row
+    constexpr int KS = D / 16;  // k-steps of the score mma
+    constexpr int MT = D / 16;  // 16-dim m-tiles of the PV mma
+    const int hl = cw / WPH;    // kv head within the group
+    const int rh = cw % WPH;    // which n-tiles of the head's rows
+    const int g = lane >> 2, tq = lane & 3;
+
+    // ldmatrix row addresses inside a (head, half) tile: [16 tokens][8 x 16 B], 128B swizzle
+    const int k_tok = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int k_cadd = lane >> 4;
+    const int v_tok = (lane & 7) + ((lane >> 4) & 1) * 8;
+    const int v_cadd = (lane >> 3) & 1;
+    const int sw = lane & 7;  // == k_tok & 7 == v_tok & 7
+
+    float acc[MT][NTW][4];
+    uint32_t qf[KS][NTW][2];
+    float m_r[NTW][2], l_r[NTW][2];
+    int jrow[NTW][2];  // query index j of this lane's two score rows per n-tile
+#pragma unroll
+    for (int n = 0; n < NTW; ++n)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int row = (rh * NTW + n) * 8 + 2 * tq + r;
+            const int j = row / p.G;
+            jrow[n][r] = j < p.nq ? j : p.nq - 1;
+        }
+
+    const uint32_t stage_base = smem_u32(sm.stages);
+    uint32_t st = 0, phase = 0;
+    for (;;) {
+        if (!mbar_wait(smem_u32(&sm.full[st]), phase, kWaitLimitNs)) {
+            if (lane == 0)
+                atomicOr(p.err, kErrConsumerWait);
+            return;
+        }
+        const StageHdr h = sm.hdr[st];
+        if (h.flags & F_END)
+            return;
+        const int kvh = h.hg * p.HG + hl;
+
+        if (h.flags & F_FIRST) {
+#pragma unroll
+            for (int n = 0; n < NTW; ++n) {
+                const int row = (rh * NTW + n) * 8 + g;
+                if (row < p.rows) {
+                    const int j = row / p.G;
+                    const int gq = row - j * p.G;
+                    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+                        p.q + ((int64_t(h.s) * p.nq + j) * p.Hq + int64_t(kvh) * p.G + gq) * D);
+#pragma unroll
+                    for (int ks = 0; ks < KS; ++ks) {
+                        qf[ks][n][0] = __ldg(qrow + ks * 8 + tq);
+                        qf[ks][n][1] = __ldg(qrow + ks * 8 + 4 + tq);
+                    }
+                } else {
+#pragma unroll
+                    for (int ks = 0; ks < KS; ++ks)
+                        qf[ks][n][0] = qf[ks][n][1] = 0u;
+                }
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    m_r[n][r] = -INFINITY;
+                    l_r[n][r] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < MT; ++i)
+#pragma unroll
+                for (int n = 0; n < NTW; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        acc[i][n][e] = 0.f;
+        }
+
+        const uint32_t kb = stage_base + st * uint32_t(p.stage_bytes) + uint32_t(hl * NH * kTileBytes);
+        const uint32_t vb = kb + uint32_t(p.HG * NH * kTileBytes);  // same head in the V half
+
+        // ---- scores S^T[token][row] for the block's 16 tokens
+        float sc[NTW][4];
+#pragma unroll
+        for (int n = 0; n < NTW; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                sc[n][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const int chunk = 2 * ks + k_cadd;
+            const uint32_t addr = kb + uint32_t((chunk >> 3) * kTileBytes + k_tok * 128 +
+                                                (((chunk & 7) ^ sw) << 4));
+            uint32_t a[4];
+            ldsm_x4(addr, a);
+#pragma unroll
+            for (int n = 0; n < NTW; ++n)
+                mma_bf16_16816(sc[n], a, qf[ks][n][0], qf[ks][n][1]);
+        }
+
+        // ---- scale (log2 domain) and causal / tail mask
+        const int t0 = h.b * kBlockSize;
+        const bool need_mask = (t0 + kBlockSize - 1) > (h.T - p.nq);
+#pragma unroll
+        for (int n = 0; n < NTW; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float x = sc[n][e] * p.scale_log2;
+                if (need_mask) {
+                    const int tok = t0 + g + ((e >> 1) << 3);
+                    const int lim = h.T - p.nq + jrow[n][e & 1];
+                    x = tok > lim ? -INFINITY : x;
+                }
+                sc[n][e] = x;
+            }
+
+        // ---- online softmax (rows 2tq, 2tq+1 of each n-tile live in this lane)
+        float corr[NTW][2];
+#pragma unroll
+        for (int n = 0; n < NTW; ++n)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                float bm = fmaxf(sc[n][r], sc[n][r + 2]);
+                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+                const float mn = fmaxf(m_r[n][r], bm);
+                const float mu = (mn == -INFINITY) ? 0.f : mn;
+                corr[n][r] = ex2(m_r[n][r] - mu);
+                m_r[n][r] = mn;
+                const float p0 = ex2(sc[n][r] - mu);
+                const float p1 = ex2(sc[n][r + 2] - mu);
+                l_r[n][r] = l_r[n][r] * corr[n][r] + (p0 + p1);
+                sc[n][r] = p0;
+                sc[n][r + 2] = p1;
+            }
+#pragma unroll
+        for (int i = 0; i < MT; ++i)
+#pragma unroll
+            for (int n = 0; n < NTW; ++n) {
+                acc[i][n][0] *= corr[n][0];
+                acc[i][n][1] *= corr[n][1];
+                acc[i][n][2] *= corr[n][0];
+                acc[i][n][3] *= corr[n][1];
+            }
+
+        // ---- P = hi + lo (bf16 each), transposed into mma B fragments
+        uint32_t bh[NTW][2], bl[NTW][2];
+#pragma unroll
+        for (int n = 0; n < NTW; ++n) {
+            const uint32_t h01 = pack_bf16x2(sc[n][0], sc[n][1]);
+            const uint32_t h23 = pack_bf16x2(sc[n][2], sc[n][3]);
+            const uint32_t l01 =
+                pack_bf16x2(sc[n][0] - bf16lo_f32(h01), sc[n][1] - bf16hi_f32(h01));
+            const uint32_t l23 =
+                pack_bf16x2(sc[n][2] - bf16lo_f32(h23), sc[n][3] - bf16hi_f32(h23));
+            bh[n][0] = movmatrix_trans(h01);
+            bh[n][1] = movmatrix_trans(h23);
+            bl[n][0] = movmatrix_trans(l01);
+            bl[n][1] = movmatrix_trans(l23);
+        }
+
+        // ---- V rows past the context (stale or NaN slots) are zeroed
+        uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+        const int vc = h.T - t0;
+        if (vc < kBlockSize) {
+            const int k0 = 2 * tq;
+            mlo = (k0 < vc ? 0x0000ffffu : 0u) | (k0 + 1 < vc ? 0xffff0000u : 0u);
+            mhi = (k0 + 8 < vc ? 0x0000ffffu : 0u) | (k0 + 9 < vc ? 0xffff0000u : 0u);
+        }
+
+        // ---- O^T[d][row] += V^T[d][tok] . P^T[tok][row]
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+            const int chunk = 2 * i + v_cadd;
+            const uint32_t addr = vb + uint32_t((chunk >> 3) * kTileBytes + v_tok * 128 +
+                                                (((chunk & 7) ^ sw) << 4));
+            uint32_t a[4];
+            ldsm_x4_trans(addr, a);
+            a[0] &= mlo;
+            a[1] &= mlo;
+            a[2] &= mhi;
+            a[3] &= mhi;
+#pragma unroll
+            for (int n = 0; n < NTW; ++n) {
+                mma_bf16_16816(acc[i][n], a, bh[n][0], bh[n][1]);
+                mma_bf16_16816(acc[i][n], a, bl[n][0], bl[n][1]);
+            }
+        }
+
+        // the stage's shared memory is no longer needed: hand it back
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_u32(&sm.empty[st]));
+        if (++st == uint32_t(p.nst)) {
+            st = 0;
+            phase ^= 1u;
+        }
+
+        if (h.flags & F_LAST) {
+            // ---- finish the segment: full row sums, then output or partial
+            float lf[NTW][2];
+#pragma unroll
+            for (int n = 0; n < NTW; ++n)
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    float v = l_r[n][r];
+                    v += __shfl_xor_sync(0xffffffffu, v, 4);
+                    v += __shfl_xor_sync(0xffffffffu, v, 8);
+                    v += __shfl_xor_sync(0xffffffffu, v, 16);
+                    lf[n][r] = v;
+                }
+            if (h.flags & F_DIRECT) {
+#pragma unroll
+                for (int n = 0; n < NTW; ++n)
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const int row = (rh * NTW + n) * 8 + 2 * tq + r;
+                        if (row >= p.rows)
+                            continue;
+                        const int j = row / p.G;
+                        const int gq = row - j * p.G;
+                        const int64_t o = ((int64_t(h.s) * p.nq + j) * p.Hq + int64_t(kvh) * p.G + gq) * D;
+                        const float inv = lf[n][r] > 0.f ? 1.f / lf[n][r] : 0.f;
+                        if (p.out_f32) {
+                            float *out = static_cast<float *>(p.out) + o;
+#pragma unroll
+                            for (int i = 0; i < MT; ++i) {
+                                out[16 * i + g] = acc[i][n][r] * inv;
+                                out[16 * i + 8 + g] = acc[i][n][r + 2] * inv;
+                            }
+                        } else {
+                            __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out) + o;
+#pragma unroll
+                            for (int i = 0; i < MT; ++i) {
+                                out[16 * i + g] = __float2bfloat16_rn(acc[i][n][r] * inv);
+                                out[16 * i + 8 + g] = __float2bfloat16_rn(acc[i][n][r + 2] * inv);
+                            }
+                        }
+                    }
+            } else {
+                const int64_t cell = (int64_t(blockIdx.x) * 2 + h.slot) * p.HG + hl;
+#pragma unroll
+                for (int n = 0; n < NTW; ++n)
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const int row = (rh * NTW + n) * 8 + 2 * tq + r;
+                        if (row >= p.rows)
+                            continue;
+                        float *pa = p.part + (cell * p.rows_pad + row) * D;
+#pragma unroll
+                        for (int i = 0; i < MT; ++i) {
+                            pa[16 * i + g] = acc[i][n][r];
+                            pa[16 * i + 8 + g] = acc[i][n][r + 2];
+                        }
+                        if (g == 0) {
+                            float *ml = p.ml + (cell * p.rows_pad + row) * 2;
+                            ml[0] = m_r[n][r];
+                            ml[1] = lf[n][r];
+                        }
+                    }
+            }
+        }
+    }
+}
+
+template <int D, int NTW, int WPH>
+__global__ void __launch_bounds__(kThreadsMax, 1)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap, const DecodeParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const Smem sm = carve(smem_raw, p);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+        for (int i = 0; i < p.nst; ++i) {
+            mbar_init(smem_u32(&sm.full[i]), 1);
+            mbar_init(smem_u32(&sm.empty[i]), uint32_t(p.HG * WPH));
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == 0)
+        producer_warp<D>(&kmap, &vmap, p, sm, lane);
+    else
+        consumer_warp<D, NTW, WPH>(p, sm, warp - 1, lane);
+}
+
+// ------------------------------------------------------------------ merge
+// Combine the partial states of every sequence that a chunk boundary split:
+// M = max m_c, L = sum l_c 2^(m_c - M), out = sum acc_c 2^(m_c - M) / L
+// ("07 -- Inference" section 5.3; m is kept in the log2 domain). Sequences
+// with no token write zeros.
+__global__ void __launch_bounds__(256)
+    paged_decode_merge_kernel(const DecodeParams p, int D, int grid)
+{
+    const int s = blockIdx.x, hg = blockIdx.y;
+    const int nb_total = p.seq_start[p.S];
+    const int64_t F = int64_t(p.n_hg) * nb_total;
+    const int64_t fs = int64_t(hg) * nb_total + p.seq_start[s];
+    const int64_t fe = int64_t(hg) * nb_total + p.seq_start[s + 1];
+    const int n_el = p.HG * p.rows * D;
+
+    auto out_index = [&](int e, int &hl, int &row, int &d) -> int64_t {
+        hl = e / (p.rows * D);
+        const int rem = e - hl * p.rows * D;
+        row = rem / D;
+        d = rem - row * D;
+        const int j = row / p.G, gq = row - j * p.G;
+        const int kvh = hg * p.HG + hl;
+        return ((int64_t(s) * p.nq + j) * p.Hq + int64_t(kvh) * p.G + gq) * D + d;
+    };
+
+    if (fe == fs) {
+        for (int e = threadIdx.x; e < n_el; e += blockDim.x) {
+            int hl, row, d;
+            const int64_t o = out_index(e, hl, row, d);
+            if (p.out_f32)
+                static_cast<float *>(p.out)[o] = 0.f;
+            else
+                static_cast<__nv_bfloat16 *>(p.out)[o] = __float2bfloat16_rn(0.f);
+        }
+        return;
+    }
+    // chunk c covers [c*F/grid, (c+1)*F/grid); chunk_of(f) = ceil((f+1)*grid/F) - 1
+    const int64_t cb = ((fs + 1) * grid + F - 1) / F - 1;
+    const int64_t ce = (fe * grid + F - 1) / F - 1;
+    if (cb == ce)
+        return;  // finished in place by the main kernel
+    const bool cb_first = (cb * F / grid) == fs;  // sequence opens chunk cb
+
+    // With fewer units than CTAs some chunks are empty; they hold no partial.
+    auto empty_chunk = [&](int64_t c) { return c * F / grid == (c + 1) * F / grid; };
+    for (int e = threadIdx.x; e < n_el; e += blockDim.x) {
+        int hl, row, d;
+        const int64_t o = out_index(e, hl, row, d);
+        float M = -INFINITY;
+        for (int64_t c = cb; c <= ce; ++c) {
+            if (empty_chunk(c))
+                continue;
+            const int slot = (c == cb && !cb_first) ? 1 : 0;
+            const int64_t cell = (c * 2 + slot) * p.HG + hl;
+            M = fmaxf(M, p.ml[(cell * p.rows_pad + row) * 2]);
+        }
+        float L = 0.f, a = 0.f;
+        if (M != -INFINITY) {
+            for (int64_t c = cb; c <= ce; ++c) {
+                if (empty_chunk(c))
+                    continue;
+                const int slot = (c == cb && !cb_first) ? 1 : 0;
+                const int64_t cell = (c * 2 + slot) * p.HG + hl;
+                const float m = p.ml[(cell * p.rows_pad + row) * 2];
+                if (m == -INFINITY)
+                    continue;
+                const float f = ex2(m - M);
+                L += p.ml[(cell * p.rows_pad + row) * 2 + 1] * f;
+                a += p.part[(cell * p.rows_pad + row) * D + d] * f;
+            }
+        }
+        const float v = L > 0.f ? a / L : 0.f;
+        if (p.out_f32)
+            static_cast<float *>(p.out)[o] = v;
+        else
+            static_cast<__nv_bfloat16 *>(p.out)[o] = __float2bfloat16_rn(v);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int opt_ctas,
+                int opt_stages, int smem_optin, DecodePlan *pl)
+{
+    if (S < 1 || nq < 1 || Hkv < 1 || Hq % Hkv != 0 || (D != 64 && D != 128) || MB < 1)
+        return -1;
+    DecodePlan P{};
+    P.D = D;
+    P.G = Hq / Hkv;
+    P.rows = P.G * nq;
+    if (P.rows > kMaxRows)
+        return -1;
+    const int nt_total = (P.rows + 7) / 8;
+    if (nt_total <= 2) {
+        P.wph = 1;
+        P.ntw = nt_total;
+    } else {
+        P.wph = 2;
+        P.ntw = 2;
+    }
+    P.rows_pad = P.wph * P.ntw * 8;
+    const int max_hg = kMaxConsumerWarps / P.wph;
+    P.HG = 1;
+    for (int h = std::min(max_hg, Hkv); h >= 1; --h)
+        if (Hkv % h == 0) {
+            P.HG = h;
+            break;
+        }
+    P.n_hg = Hkv / P.HG;
+    P.threads = 32 * (1 + P.HG * P.wph);
+    P.stage_bytes = 2 * P.HG * (D / 64) * kTileBytes;
+    const int per_stage = P.stage_bytes + int(sizeof(StageHdr)) + 16;
+    int max_st = (smem_optin - 1024) / per_stage;
+    if (max_st > 8)
+        max_st = 8;
+    if (max_st < 2)
+        return -1;
+    P.nst = opt_stages > 0 ? std::min(std::max(opt_stages, 2), max_st) : max_st;
+    P.smem = 1024 + size_t(P.nst) * per_stage;
+    const int grid_cap = opt_ctas > 0 ? opt_ctas : num_sms;
+    if (grid_cap < 1)
+        return -1;
+    const int64_t f_max = int64_t(P.n_hg) * S * MB;
+    P.grid = int(std::min<int64_t>(grid_cap, f_max));
+    P.off_seq = 256;
+    P.off_ml = P.off_seq + round_up(size_t(S + 1) * 4, 256);
+    const size_t cells = size_t(grid_cap) * 2 * P.HG * P.rows_pad;
+    P.off_part = P.off_ml + round_up(cells * 2 * 4, 256);
+    P.ws_bytes = P.off_part + round_up(cells * size_t(D) * 4, 256);
+    *pl = P;
+    return 0;
+}
+
+template <int D, int NTW, int WPH>
+static cudaError_t launch_one(const DecodePlan &pl, const DecodeParams &p, const CUtensorMap &kmap,
+                              const CUtensorMap &vmap, cudaStream_t stream, cudaEvent_t ev_before,
+                              cudaEvent_t ev_after)
+{
+    auto kern = paged_decode_kernel<D, NTW, WPH>;
+    static int configured_smem[64] = {0};  // per device ordinal
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 64 && configured_smem[dev] < int(pl.smem)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(pl.smem));
+        if (e != cudaSuccess)
+            return e;
+        configured_smem[dev] = int(pl.smem);
+    }
+    if (ev_before && (e = cudaEventRecord(ev_before, stream)) != cudaSuccess)
+        return e;
+    kern<<<pl.grid, pl.threads, pl.smem, stream>>>(kmap, vmap, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    if (ev_after && (e = cudaEventRecord(ev_after, stream)) != cudaSuccess)
+        return e;
+    dim3 mg(p.S, p.n_hg);
+    paged_decode_merge_kernel<<<mg, 256, 0, stream>>>(p, D, pl.grid);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const DecodePlan &pl, const DecodeParams &p, const CUtensorMap &kmap,
+                          const CUtensorMap &vmap, cudaStream_t stream, cudaEvent_t eb,
+                          cudaEvent_t ea)
+{
+    if (pl.D == 64) {
+        if (pl.wph == 2)
+            return launch_one<64, 2, 2>(pl, p, kmap, vmap, stream, eb, ea);
+        if (pl.ntw == 2)
+            return launch_one<64, 2, 1>(pl, p, kmap, vmap, stream, eb, ea);
+        return launch_one<64, 1, 1>(pl, p, kmap, vmap, stream, eb, ea);
+    }
+    if (pl.wph == 2)
+        return launch_one<128, 2, 2>(pl, p, kmap, vmap, stream, eb, ea);
+    if (pl.ntw == 2)
+        return launch_one<128, 2, 1>(pl, p, kmap, vmap, stream, eb, ea);
+    return launch_one<128, 1, 1>(pl, p, kmap, vmap, stream, eb, ea);
+}
+
+}  // namespace pkv

@@ -1,0 +1,72 @@
+// pkv_internal.h -- shapes shared by the host API and the kernels of libpkv.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+constexpr int kBlockSize = 16;          // tokens per physical block
+constexpr int kTileBytes = 16 * 128;    // one (head, 64-column half) tile: 16 rows x 128 B
+constexpr int kMaxRows = 32;            // query rows per kv head: G * n_query_per_seq
+constexpr int kMaxConsumerWarps = 8;
+constexpr int kThreadsMax = 32 * (1 + kMaxConsumerWarps);
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded waits: 2 s
+
+// device error word codes (workspace offset 0)
+enum : uint32_t {
+    kErrConsumerWait = 1u,  // a consumer warp gave up waiting for a stage
+    kErrProducerWait = 2u,  // the producer gave up waiting for a free stage
+    kErrDrainWait = 4u,     // a copy did not land while unwinding
+    kErrBadBlock = 8u       // a block-table entry outside [0, num_blocks) (read as zeros)
+};
+
+// Split of the work of one call (computed on the host from the shapes).
+struct DecodePlan {
+    int D;           // head_dim
+    int G;           // query heads per kv head
+    int rows;        // G * nq: query rows per kv head
+    int wph;         // consumer warps per kv head (1 or 2)
+    int ntw;         // 8-row n-tiles per consumer warp
+    int rows_pad;    // wph * ntw * 8
+    int HG;          // kv heads per head group (one CTA streams one group)
+    int n_hg;        // Hkv / HG
+    int threads;     // 32 * (1 + HG * wph)
+    int stage_bytes; // K + V of one 16-token block for HG heads
+    int nst;         // pipeline stages
+    int grid;        // persistent CTAs
+    size_t smem;     // dynamic shared memory bytes
+    // workspace layout (byte offsets)
+    size_t off_seq, off_ml, off_part, ws_bytes;
+};
+
+struct DecodeParams {
+    const uint16_t *q;
+    void *out;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    int32_t *seq_start;    // workspace: [S + 1] block prefix sums (written by CTA 0)
+    float *ml;             // workspace: [grid][2][HG][rows_pad][2]  (m, l)
+    float *part;           // workspace: [grid][2][HG][rows_pad][D]  unnormalised acc
+    uint32_t *err;         // workspace word 0
+    int64_t num_blocks;
+    int S, MB, nq, Hq, Hkv, G, rows, rows_pad, HG, n_hg, out_f32;
+    int stage_bytes, nst;
+    float scale_log2;      // scale * log2(e)
+};
+
+int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int opt_ctas,
+                int opt_stages, int smem_optin, DecodePlan *plan);
+
+// ev_before/ev_after (may be null) are recorded around the main kernel only.
+cudaError_t launch_decode(const DecodePlan &plan, const DecodeParams &p, const CUtensorMap &kmap,
+                          const CUtensorMap &vmap, cudaStream_t stream, cudaEvent_t ev_before,
+                          cudaEvent_t ev_after);
+
+cudaError_t launch_kv_append(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                             int64_t n_new, void *k_cache, void *v_cache, int64_t num_blocks,
+                             int num_kv_heads, int head_dim, cudaStream_t stream);
+
+}  // namespace pkv

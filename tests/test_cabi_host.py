@@ -1,0 +1,130 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol, and
+rejects invalid arguments on the host before any device work."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_101_gb300 as pkv
+from paged_kv_cache_101_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+           if f.endswith(".h")]
+
+OK, NULL, SHAPE, DTYPE, ALIGN, RANGE, WORKSPACE, CUDA, UNSUP = range(9)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return pkv.lib()
+
+
+def declared_functions():
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(pkv_[a-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("pkv_kv_append", "pkv_paged_decode_attention", "pkv_workspace_size",
+                     "pkv_status_string"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared but not exported"
+        assert n in pkv.SIGNATURES, f"{n} has no Python binding"
+
+
+def test_status_strings_and_version(lib):
+    for s in range(9):
+        assert pkv.status_string(s)
+    assert pkv.status_string(99) == "unknown status"
+    assert lib.pkv_version() >= 100
+
+
+def test_options(lib):
+    assert pkv.set_option(pkv.PKV_OPT_NUM_CTAS, 7) == 0
+    assert pkv.set_option(pkv.PKV_OPT_NUM_CTAS, 0) == 7
+    assert pkv.set_option(pkv.PKV_OPT_STAGES, 3) == 0
+    assert pkv.set_option(pkv.PKV_OPT_STAGES, 0) == 3
+    assert pkv.set_option(42, 1) == -1
+    assert pkv.set_option(pkv.PKV_OPT_NUM_CTAS, -5) == -1
+
+
+A = 0x10000  # a 64 KiB-aligned dummy address: never dereferenced on these paths
+
+
+def append(lib, k=A, v=A, slots=A, n=4, kc=A, vc=A, nb=8, hkv=2, d=64):
+    return lib.pkv_kv_append(k, v, slots, n, kc, vc, nb, hkv, d, None)
+
+
+def test_append_validation(lib):
+    assert append(lib, n=0) == OK                      # empty step: no-op
+    assert append(lib, k=None) == NULL
+    assert append(lib, slots=None) == NULL
+    assert append(lib, n=-1) == SHAPE
+    assert append(lib, nb=0) == SHAPE
+    assert append(lib, hkv=0) == SHAPE
+    assert append(lib, d=60) == UNSUP                   # rows move in 16-byte vectors
+    assert append(lib, d=2048) == RANGE
+    assert append(lib, k=A + 8) == ALIGN
+    assert append(lib, vc=A + 2) == ALIGN
+    assert append(lib, slots=A + 4) == ALIGN
+
+
+def attn(lib, q=A, k=A, v=A, nb=64, bt=A, mb=8, cl=A, S=4, nq=1, hq=8, hkv=2, d=64,
+         scale=0.125, out=A, dt=0, ws=A, wsb=1 << 30):
+    return lib.pkv_paged_decode_attention(q, k, v, nb, bt, mb, cl, S, nq, hq, hkv, d, scale,
+                                          out, dt, ws, wsb, None)
+
+
+def test_attention_validation(lib):
+    assert attn(lib, S=0) == OK                         # empty batch: no-op
+    assert attn(lib, q=None) == NULL
+    assert attn(lib, bt=None) == NULL
+    assert attn(lib, cl=None) == NULL
+    assert attn(lib, out=None) == NULL
+    assert attn(lib, ws=None) == WORKSPACE
+    assert attn(lib, S=-1) == SHAPE
+    assert attn(lib, hq=6, hkv=4) == SHAPE              # heads not a multiple of kv heads
+    assert attn(lib, nb=0) == SHAPE
+    assert attn(lib, mb=0) == SHAPE
+    assert attn(lib, nq=0) == SHAPE
+    assert attn(lib, nq=5) == UNSUP
+    assert attn(lib, d=96) == UNSUP
+    assert attn(lib, d=256) == UNSUP
+    assert attn(lib, hq=64, hkv=1, nq=1) == UNSUP       # 64 query rows per kv head
+    assert attn(lib, hq=32, hkv=2, nq=4) == UNSUP       # 16*4 = 64 rows per kv head
+    assert attn(lib, dt=2) == DTYPE
+    assert attn(lib, q=A + 8) == ALIGN
+    assert attn(lib, out=A + 4) == ALIGN
+    assert attn(lib, ws=A + 16) == ALIGN
+    assert attn(lib, bt=A + 2) == ALIGN
+    assert attn(lib, mb=1 << 27) == RANGE
+
+
+def test_workspace_size_rejects_bad_geometry(lib):
+    assert lib.pkv_workspace_size(4, 5, 8, 2, 64) == 0
+    assert lib.pkv_workspace_size(4, 1, 8, 3, 64) == 0
+    assert lib.pkv_workspace_size(4, 1, 8, 2, 80) == 0
+    assert lib.pkv_workspace_size(0, 1, 8, 2, 64) == 256
+
+
+def test_product_path_has_no_cpu_fallback(monkeypatch, tmp_path):
+    """With the library missing, the binding raises instead of computing anything."""
+    monkeypatch.setattr(pkv, "_lib", None)
+    monkeypatch.setattr(pkv, "LIBRARY_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        pkv.lib()

@@ -1,0 +1,248 @@
+"""GPU parity: the sm_103a library against the fp64 oracle on the same seeded inputs.
+
+kv_append is compared bit for bit on the whole pool; attention element by
+element within |err| <= 2e-3 + 1e-2 |ref| (bf16 output) -- on every output for
+the small cases, on sampled (sequence, kv head) pairs for the five full-size
+workloads, which run in the launch configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import paged_kv_cache_101_gb300 as pkv
+import workloads as W
+from gpu_helpers import (ATOL, DeviceStep, bf16_host, compare, rows_of, sample_pairs, to_f64)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def o():
+    return oracle.Oracle()
+
+
+@pytest.fixture(autouse=True)
+def _defaults():
+    pkv.set_option(pkv.PKV_OPT_NUM_CTAS, 0)
+    pkv.set_option(pkv.PKV_OPT_STAGES, 0)
+    yield
+    pkv.set_option(pkv.PKV_OPT_NUM_CTAS, 0)
+    pkv.set_option(pkv.PKV_OPT_STAGES, 0)
+
+
+def run_small(o, w, out_dtype=None, check_pool=True):
+    d = DeviceStep(w, torch, out_dtype=out_dtype)
+    ref, k_ref, v_ref = o.step(w)
+    d.step()
+    torch.cuda.synchronize()
+    if check_pool:
+        assert np.array_equal(bf16_host(d.k_cache), k_ref)
+        assert np.array_equal(bf16_host(d.v_cache), v_ref)
+    got = to_f64(d.out)
+    stats = compare(got, ref, what=w.name)
+    assert pkv.workspace_error(pkv.workspace(d.q.device, 0)) == 0
+    return got, ref, stats
+
+
+# --------------------------------------------------------------- kv_append
+@pytest.mark.parametrize("name", ["tiny", "spec_verify"])
+def test_append_bit_exact_named(o, name):
+    w = W.make_workload(name, keep_full=True)
+    d = DeviceStep(w, torch)
+    d.append()
+    torch.cuda.synchronize()
+    k_ref, v_ref = o.kv_append(w.k_new, w.v_new, w.slot_mapping, w.k_cache, w.v_cache)
+    assert np.array_equal(bf16_host(d.k_cache), k_ref)
+    assert np.array_equal(bf16_host(d.v_cache), v_ref)
+    assert np.array_equal(k_ref, w.k_full) and np.array_equal(v_ref, w.v_full)
+
+
+def test_append_padding_and_out_of_pool_slots(o):
+    w = W.make_custom(3, 2, 8, 2, 64, [5, 17, 40], seed=70)
+    slots = w.slot_mapping.copy()
+    slots[0] = -1                          # padding
+    slots[3] = w.num_blocks * 16 + 5       # past the pool: skipped
+    d = DeviceStep(w, torch)
+    d.slots = torch.from_numpy(slots).cuda()
+    d.append()
+    torch.cuda.synchronize()
+    k_ref, v_ref = o.kv_append(w.k_new, w.v_new, slots, w.k_cache, w.v_cache)
+    assert np.array_equal(bf16_host(d.k_cache), k_ref)
+    assert np.array_equal(bf16_host(d.v_cache), v_ref)
+
+
+@pytest.mark.parametrize("hkv,dim", [(1, 8), (3, 40), (8, 128), (2, 64)])
+def test_append_shapes(o, hkv, dim):
+    rng = np.random.default_rng(hkv * 1000 + dim)
+    NB, n = 9, 37
+    pool = W.f32_to_bf16_bits(rng.standard_normal((NB, 16, hkv, dim), dtype=np.float32))
+    kn = W.f32_to_bf16_bits(rng.standard_normal((n, hkv, dim), dtype=np.float32))
+    vn = W.f32_to_bf16_bits(rng.standard_normal((n, hkv, dim), dtype=np.float32))
+    slots = rng.choice(NB * 16, size=n, replace=False).astype(np.int64)
+    from gpu_helpers import bf16_dev
+    kc, vc = bf16_dev(pool, torch), bf16_dev(pool, torch)
+    pkv.kv_append(bf16_dev(kn, torch), bf16_dev(vn, torch), torch.from_numpy(slots).cuda(), kc, vc)
+    torch.cuda.synchronize()
+    k_ref, v_ref = o.kv_append(kn, vn, slots, pool, pool)
+    assert np.array_equal(bf16_host(kc), k_ref) and np.array_equal(bf16_host(vc), v_ref)
+
+
+def test_append_empty():
+    w = W.make_custom(2, 1, 8, 2, 64, [3, 4], seed=71)
+    d = DeviceStep(w, torch)
+    e = torch.zeros((0, 2, 64), dtype=torch.bfloat16, device="cuda")
+    pkv.kv_append(e, e, torch.zeros(0, dtype=torch.int64, device="cuda"), d.k_cache, d.v_cache)
+    torch.cuda.synchronize()
+    assert np.array_equal(bf16_host(d.k_cache), w.k_cache)
+
+
+# --------------------------------------------------------------- attention, small
+def test_tiny_full(o):
+    w = W.make_workload("tiny")
+    run_small(o, w)
+
+
+@pytest.mark.parametrize("G,nq,D", [(1, 1, 64), (4, 1, 128), (8, 1, 128), (2, 4, 64),
+                                    (4, 4, 128), (8, 4, 128), (8, 2, 64), (3, 3, 128),
+                                    (16, 2, 128), (32, 1, 64), (5, 1, 128)])
+def test_gqa_nq_dims(o, G, nq, D):
+    Hkv = 2
+    T = [nq, nq + 1, 15, 16, 17, 31, 32, 33, 100, 257]
+    w = W.make_custom(len(T), nq, G * Hkv, Hkv, D, T, seed=100 + 7 * G + nq + D)
+    run_small(o, w)
+
+
+def test_every_length_mod_16(o):
+    T = list(range(1, 49)) + [63, 64, 65, 127, 128, 129, 511, 512, 513]
+    w = W.make_custom(len(T), 1, 8, 2, 128, T, seed=80)
+    run_small(o, w)
+
+
+def test_nq4_lengths(o):
+    T = list(range(4, 40))
+    w = W.make_custom(len(T), 4, 16, 2, 128, T, seed=81)
+    run_small(o, w)
+
+
+def test_fp32_output_strict(o):
+    w = W.make_custom(6, 2, 16, 4, 128, [2, 33, 190, 600, 17, 1000], seed=82)
+    got, ref, (max_abs, max_rel) = run_small(o, w, out_dtype=torch.float32)
+    assert max_abs <= ATOL
+    assert max_rel <= 1e-2
+
+
+def test_shared_prefix_small(o):
+    sh = np.array([True, False, True, True, False, True, True])
+    w = W.make_custom(7, 1, 16, 2, 128, [600, 40, 513, 700, 90, 1025, 530], seed=83,
+                      shared=sh, prefix_tokens=512)
+    run_small(o, w)
+
+
+@pytest.mark.parametrize("ctas", [1, 2, 7, 64, 300, 1000])
+def test_split_grid_invariance(o, ctas):
+    """Any persistent-grid size gives the definition (within rounding)."""
+    pkv.set_option(pkv.PKV_OPT_NUM_CTAS, ctas)
+    T = [3000, 20, 2, 777, 4096, 129]
+    w = W.make_custom(len(T), 2, 16, 4, 128, T, seed=84)
+    run_small(o, w)
+
+
+@pytest.mark.parametrize("stages", [2, 3, 5, 8])
+def test_pipeline_depths(o, stages):
+    pkv.set_option(pkv.PKV_OPT_STAGES, stages)
+    T = [400, 3, 1500, 64]
+    w = W.make_custom(len(T), 1, 8, 2, 64, T, seed=85)
+    run_small(o, w)
+
+
+def test_long_sequences_many_partitions(o):
+    pkv.set_option(pkv.PKV_OPT_NUM_CTAS, 152)
+    w = W.make_custom(2, 1, 8, 1, 128, [70000, 33333], seed=86)
+    run_small(o, w)
+
+
+def test_zero_and_short_contexts(o):
+    """T = 0 gives zeros; rows that see no token (T < nq) give zeros."""
+    w = W.make_custom(4, 3, 8, 2, 64, [3, 9, 40, 5], seed=87)
+    d = DeviceStep(w, torch)
+    d.append()
+    lens = w.context_lens.copy()
+    lens[1] = 0
+    lens[3] = 2   # fewer tokens than queries: query 0 sees nothing
+    d.lens = torch.from_numpy(lens).cuda()
+    d.attend()
+    torch.cuda.synchronize()
+    k, v = o.kv_append(w.k_new, w.v_new, w.slot_mapping, w.k_cache, w.v_cache)
+    ref = o.paged_attention(w.q, k, v, w.block_tables, lens, 3, w.scale)
+    got = to_f64(d.out)
+    compare(got, ref, what="zero/short")
+    assert np.all(got[3:6] == 0) and np.all(got[9] == 0)
+
+
+def test_deterministic(o):
+    w = W.make_custom(5, 2, 16, 2, 128, [900, 33, 4000, 2, 260], seed=88)
+    d = DeviceStep(w, torch)
+    d.step()
+    a = d.out.clone()
+    d.attend()
+    torch.cuda.synchronize()
+    assert torch.equal(a, d.out)
+
+
+def test_out_of_pool_block_id_is_flagged(o):
+    """A table entry past the pool reads zeros and sets the error word; no fault."""
+    w = W.make_custom(2, 1, 8, 2, 64, [40, 20], seed=89)
+    d = DeviceStep(w, torch)
+    d.append()
+    tables = w.block_tables.copy()
+    tables[0, 1] = w.num_blocks + 3
+    d.tables = torch.from_numpy(tables).cuda()
+    ws = torch.zeros(pkv.workspace_size(2, 1, 8, 2, 64), dtype=torch.uint8, device="cuda")
+    d.attend(ws=ws)
+    torch.cuda.synchronize()
+    assert pkv.workspace_error(ws) == 8
+    assert np.isfinite(to_f64(d.out)).all()
+
+
+# --------------------------------------------------------------- full-size workloads
+@pytest.mark.parametrize("name", W.WORKLOAD_ORDER)
+def test_named_workload_full_size(o, name):
+    w = W.make_workload(name)
+    d = DeviceStep(w, torch)
+    k_ref, v_ref = o.kv_append(w.k_new, w.v_new, w.slot_mapping, w.k_cache, w.v_cache)
+    d.step()
+    torch.cuda.synchronize()
+    assert np.array_equal(bf16_host(d.k_cache), k_ref), "append not bit-exact"
+    assert np.array_equal(bf16_host(d.v_cache), v_ref), "append not bit-exact"
+    got = to_f64(d.out)
+    assert np.isfinite(got).all()
+    if name == "tiny":
+        mask = np.ones((w.num_seqs, w.num_kv_heads), dtype=bool)
+    else:
+        mask = sample_pairs(w, seed=W.WORKLOAD_ORDER.index(name))
+    ref = o.paged_attention(w.q, k_ref, v_ref, w.block_tables, w.context_lens,
+                            w.n_query_per_seq, w.scale, pair_mask=mask)
+    r, h = rows_of(mask, w)
+    max_abs, max_rel = compare(got[r, h], ref[r, h], what=name)
+    print(f"{name}: pairs={int(mask.sum())} max_abs={max_abs:.2e} max_rel={max_rel:.2e}")
+    assert pkv.workspace_error(pkv.workspace(d.q.device, 0)) == 0
+
+
+@pytest.mark.parametrize("ctas", [0, 300])
+def test_stale_workspace_is_never_read(o, ctas):
+    """Partials left by other calls (here: NaN bytes) must not reach the output,
+    with more CTAs than work units (empty chunks) and with fewer."""
+    pkv.set_option(pkv.PKV_OPT_NUM_CTAS, ctas)
+    T = [1, 2, 15, 16, 17, 31, 32, 33, 100, 257]
+    w = W.make_custom(len(T), 1, 4, 2, 64, T, seed=90)
+    d = DeviceStep(w, torch)
+    ws = torch.full((pkv.workspace_size(len(T), 1, 4, 2, 64),), 0xFF, dtype=torch.uint8,
+                    device="cuda")
+    ws[:256] = 0
+    d.append()
+    d.attend(ws=ws)
+    torch.cuda.synchronize()
+    ref, _, _ = o.step(w)
+    compare(to_f64(d.out), ref, what="stale workspace")
+    assert pkv.workspace_error(ws) == 0

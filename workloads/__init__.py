@@ -19,9 +19,9 @@ last block's free slots) without masking shows up as NaN in its output.
 
 Seeding: every stream (lengths, pool permutation, prefix choice, queries, and
 the K/V values of each sequence) draws from its own ``numpy`` PCG64 generator
-spawned from ``SeedSequence(seed)``; the K/V values of sequence ``s`` come from
-the key ``(seed, 7, s)`` so a workload is identical whatever the number of
-worker threads.
+spawned from ``SeedSequence(seed)``; the K/V values of sequence ``s`` come in 4096-token
+chunks from the keys ``(seed, 7, s, chunk)`` so a workload is identical whatever
+the number of worker threads.
 """
 from __future__ import annotations
 
@@ -37,6 +37,9 @@ BLOCK_SIZE = 16
 # A bf16 quiet-NaN pattern that marks pool slots holding no token.
 SENTINEL_BF16 = np.uint16(0x7FC1)
 
+# Tokens per generator chunk of a sequence's K/V values (a multiple of 16).
+CHUNK_TOKENS = 4096
+
 # Stream ids inside one workload's SeedSequence.
 _S_LENS, _S_PERM, _S_SHARE, _S_Q, _S_KV = 1, 2, 3, 4, 7
 
@@ -48,8 +51,12 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """
     x = np.ascontiguousarray(x, dtype=np.float32)
     u = x.view(np.uint32)
-    u += ((u >> 16) & np.uint32(1)) + np.uint32(0x7FFF)
-    return (u >> 16).astype(np.uint16)
+    t = np.right_shift(u, 16)
+    np.bitwise_and(t, 1, out=t)
+    t += np.uint32(0x7FFF)
+    u += t
+    # little endian: the upper 16 bits of each word are the odd uint16 lanes
+    return np.ascontiguousarray(u.view(np.uint16)[..., 1::2]).reshape(u.shape)
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
@@ -193,6 +200,7 @@ def make_custom(S: int, nq: int, Hq: int, Hkv: int, D: int, context_lens: Sequen
     T = np.asarray(context_lens, dtype=np.int64).reshape(-1)
     assert T.shape[0] == S and S >= 0
     assert Hq % Hkv == 0 and D % 8 == 0 and nq >= 1
+    assert S == 0 or T.min() >= nq, "every sequence holds at least its nq new tokens"
     if shared is None:
         shared = np.zeros(S, dtype=bool)
     shared = np.asarray(shared, dtype=bool)
@@ -260,30 +268,41 @@ def make_custom(S: int, nq: int, Hq: int, Hkv: int, D: int, context_lens: Sequen
 
     dense_k = [None] * S if keep_dense else None
     dense_v = [None] * S if keep_dense else None
+    if keep_dense:
+        for s in range(S):
+            dense_k[s] = np.empty((int(T[s]), Hkv, D), dtype=np.uint16)
+            dense_v[s] = np.empty((int(T[s]), Hkv, D), dtype=np.uint16)
+            if shared[s]:
+                dense_k[s][:prefix_tokens] = pk
+                dense_v[s][:prefix_tokens] = pv
 
-    def fill(s):
-        r = _rng(seed, _S_KV, s)
+    # a sequence's own tokens come in chunks of CHUNK_TOKENS, each from the
+    # generator keyed (seed, 7, s, chunk): identical whatever the thread count
+    tasks = []
+    for s in range(S):
         start = n_prefix * BLOCK_SIZE if shared[s] else 0
         n = int(T[s]) - start
+        for c in range(0, max(n, 0), CHUNK_TOKENS):
+            tasks.append((s, start, c, min(CHUNK_TOKENS, n - c)))
+
+    def fill(task):
+        s, start, c, n = task
+        r = _rng(seed, _S_KV, s, c // CHUNK_TOKENS)
         kv = gen("k", s, (n, Hkv, D), r)
         vv = gen("v", s, (n, Hkv, D), r)
-        scatter(k_full, kv, tables[s], start)
-        scatter(v_full, vv, tables[s], start)
+        scatter(k_full, kv, tables[s], start + c)
+        scatter(v_full, vv, tables[s], start + c)
         if keep_dense:
-            if start:
-                dense_k[s] = np.concatenate([pk, kv])
-                dense_v[s] = np.concatenate([pv, vv])
-            else:
-                dense_k[s] = kv
-                dense_v[s] = vv
+            dense_k[s][start + c: start + c + n] = kv
+            dense_v[s][start + c: start + c + n] = vv
 
     nthreads = threads or min(16, os.cpu_count() or 1)
-    if nthreads > 1 and S > 1:
+    if nthreads > 1 and len(tasks) > 1:
         with ThreadPoolExecutor(nthreads) as ex:
-            list(ex.map(fill, range(S)))
+            list(ex.map(fill, tasks))
     else:
-        for s in range(S):
-            fill(s)
+        for t in tasks:
+            fill(t)
 
     q = gen("q", -1, (S * nq, Hq, D), _rng(seed, _S_Q))
 
