@@ -156,6 +156,47 @@ pkv_status pkv_paged_decode_attention(const void *q, const void *k_cache, const 
                                       float scale, void *out, int32_t out_dtype, void *workspace,
                                       size_t workspace_bytes, void *stream);
 
+/*
+ * pkv_paged_decode_attention_static -- pkv_paged_decode_attention without a
+ * caller-provided workspace, for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart: this is a packaging variant, not a step of
+ * the method. Some callers of this library cannot call cudaMalloc (or any
+ * allocator): plugins hosted by a framework that owns all device memory and
+ * hands its plugins no allocator, and serving loops whose device memory is
+ * fixed when they start (cudaMalloc/cudaFree synchronise the device and
+ * fragment the pool, so such loops forbid them after start-up). This entry point
+ * allocates nothing -- no cudaMalloc, cudaFree or allocating library routine --
+ * and the caller still passes every input and output buffer.
+ *
+ * Arguments, results and errors are those of pkv_paged_decode_attention
+ * without `workspace`/`workspace_bytes`. The scratch instead lives in one
+ * static device array of 32 MiB (32 * 2^20 bytes), which every GPU that loads
+ * the library's module holding it keeps until the process exits (with CUDA's
+ * default lazy module loading: from this entry point's first call on that
+ * GPU). A geometry whose scratch (pkv_workspace_size) exceeds 32 MiB returns
+ * PKV_ERR_WORKSPACE before anything is enqueued; on a 152-SM GB300 every
+ * supported geometry (up to 32 query rows per kv head) needs at most ~21 MiB
+ * plus 4 bytes per sequence.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ * first call before any stream capture. Each call clears the array's 4-byte
+ * device error word (a cudaMemsetAsync on `stream`) before its kernels; the
+ * kernels write every other byte they read. All calls share the one array and
+ * it keeps the last call's contents: calls that overlap on the GPU (on
+ * different streams, or from several threads) race on it and give
+ * unspecified results. Serialise them, e.g. on one stream.
+ */
+pkv_status pkv_paged_decode_attention_static(const void *q, const void *k_cache,
+                                             const void *v_cache, int64_t num_blocks,
+                                             const int32_t *block_tables,
+                                             int32_t max_blocks_per_seq,
+                                             const int32_t *context_lens, int32_t num_seqs,
+                                             int32_t n_query_per_seq, int32_t num_q_heads,
+                                             int32_t num_kv_heads, int32_t head_dim, float scale,
+                                             void *out, int32_t out_dtype, void *stream);
+
 /* Text for a status code (static storage; never NULL). */
 const char *pkv_status_string(int32_t status);
 

@@ -39,6 +39,8 @@ SIGNATURES = {
     "pkv_set_option": ([_I32, _I32], _I32),
     "pkv_version": ([], _I32),
     "pkv_set_profiling_events": ([_P, _P], None),
+    "pkv_paged_decode_attention_static": ([_P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _I32,
+                                           _I32, _F, _P, _I32, _P], ctypes.c_int),
 }
 
 _lib = None
@@ -194,4 +196,36 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, n_qu
         ws.numel(), _stream_handle(q.device))
     if st != PKV_OK:
         raise PkvError("pkv_paged_decode_attention", st)
+    return out
+
+
+def paged_decode_attention_static(q, k_cache, v_cache, block_tables, context_lens,
+                                  n_query_per_seq, scale, out):
+    """``paged_decode_attention`` for callers that cannot allocate device memory: the
+    scratch is the library's static 32 MiB device array, shared by every call (so
+    calls must not overlap on the GPU)."""
+    torch = _torch()
+    _check(q, "q", torch.bfloat16, 3)
+    _check(k_cache, "k_cache", torch.bfloat16, 4)
+    _check(v_cache, "v_cache", torch.bfloat16, 4)
+    _check(block_tables, "block_tables", torch.int32, 2)
+    _check(context_lens, "context_lens", torch.int32, 1)
+    if out.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("out must be bfloat16 or float32")
+    _check(out, "out", out.dtype, 3)
+    NB, bs, Hkv, D = k_cache.shape
+    S = context_lens.shape[0]
+    nq = int(n_query_per_seq)
+    Hq = q.shape[1]
+    if bs != BLOCK_SIZE or v_cache.shape != k_cache.shape:
+        raise ValueError("pools must be [num_blocks, 16, Hkv, D] and equal in shape")
+    if q.shape != (S * nq, Hq, D) or out.shape != q.shape or block_tables.shape[0] != S:
+        raise ValueError("q/out must be [num_seqs * n_query_per_seq, Hq, D], tables [num_seqs, MB]")
+    st = lib().pkv_paged_decode_attention_static(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), NB, block_tables.data_ptr(),
+        block_tables.shape[1], context_lens.data_ptr(), S, nq, Hq, Hkv, D, float(scale),
+        out.data_ptr(), PKV_FP32 if out.dtype == torch.float32 else PKV_BF16,
+        _stream_handle(q.device))
+    if st != PKV_OK:
+        raise PkvError("pkv_paged_decode_attention_static", st)
     return out

@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIBRARY = os.path.join(PKG, "libpkv.so")
-SOURCES = ["api.cu", "kv_append.cu", "paged_decode.cu"]
+SOURCES = ["api.cu", "kv_append.cu", "paged_decode.cu", "static_scratch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
