@@ -207,9 +207,17 @@ const char *pkv_status_string(int32_t status);
  *                        result up to fp32 rounding order.
  *   PKV_OPT_STAGES       pipeline depth (K/V stages in shared memory); 0 = as
  *                        many as fit (default), else clamped to [2, 8].
- * Returns the previous value, or -1 for an unknown option or a negative value.
+ *   PKV_OPT_HEADS_PER_CTA cap on the kv heads one CTA streams together (each
+ *                        stage holds one 16-token block of that many heads);
+ *                        0 = up to 8 (default).
+ *   PKV_OPT_TMA_BOX      0 = one TMA box per block when the driver accepts the
+ *                        tensor map, else one per (head, 64-column half) tile
+ *                        (default); 1 = always per tile; 2 = always per block
+ *                        (PKV_ERR_UNSUPPORTED if the driver refuses the map).
+ * All settings give the same result up to fp32 rounding order.
+ * Returns the previous value, or -1 for an unknown option or an invalid value.
  */
-enum { PKV_OPT_NUM_CTAS = 1, PKV_OPT_STAGES = 2 };
+enum { PKV_OPT_NUM_CTAS = 1, PKV_OPT_STAGES = 2, PKV_OPT_HEADS_PER_CTA = 3, PKV_OPT_TMA_BOX = 4 };
 int32_t pkv_set_option(int32_t option, int32_t value);
 
 /*
@@ -221,6 +229,18 @@ int32_t pkv_set_option(int32_t option, int32_t value);
  * owned by the caller and must belong to the stream's device.
  */
 void pkv_set_profiling_events(void *before, void *after);
+
+/*
+ * pkv_set_trace_buffer -- per-CTA timeline of the attention kernel (process-
+ * wide; NULL turns it off). When set, every later pkv_paged_decode_attention
+ * call whose grid fits writes, for each CTA c, 8 uint64 words at
+ * device_buffer[8c ..]: [0] entry, [1] first K/V copy issued, [2] first stage
+ * consumed, [3] last copy issued, [4] last stage consumed (ns of the GPU's
+ * global timer), [5] 16-token blocks streamed, [6] sequence segments started
+ * (added to the existing value), [7] SM id. The caller zeroes the buffer
+ * before a call; a buffer smaller than grid*64 bytes disables the trace.
+ */
+void pkv_set_trace_buffer(void *device_buffer, size_t bytes);
 
 /* Library version as an integer (major*10000 + minor*100 + patch). */
 int32_t pkv_version(void);

@@ -24,7 +24,7 @@ LIBRARY_PATH = os.path.join(_HERE, "libpkv.so")
 
 PKV_OK = 0
 PKV_BF16, PKV_FP32 = 0, 1
-PKV_OPT_NUM_CTAS, PKV_OPT_STAGES = 1, 2
+PKV_OPT_NUM_CTAS, PKV_OPT_STAGES, PKV_OPT_HEADS_PER_CTA, PKV_OPT_TMA_BOX = 1, 2, 3, 4
 BLOCK_SIZE = 16
 
 # function name -> (argtypes, restype); mirrors include/pkv.h
@@ -39,6 +39,7 @@ SIGNATURES = {
     "pkv_set_option": ([_I32, _I32], _I32),
     "pkv_version": ([], _I32),
     "pkv_set_profiling_events": ([_P, _P], None),
+    "pkv_set_trace_buffer": ([_P, _SZ], None),
     "pkv_paged_decode_attention_static": ([_P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _I32,
                                            _I32, _F, _P, _I32, _P], ctypes.c_int),
 }
@@ -92,6 +93,16 @@ def set_profiling_events(before, after):
             ev.record()  # torch creates the underlying event lazily
     lib().pkv_set_profiling_events(ctypes.c_void_p(before.cuda_event),
                                    ctypes.c_void_p(after.cuda_event))
+
+
+def set_trace_buffer(buf):
+    """Per-CTA timeline of later attention calls into a zeroed uint64 CUDA tensor
+    (8 words per CTA: see include/pkv.h); None turns it off."""
+    if buf is None:
+        lib().pkv_set_trace_buffer(None, 0)
+    else:
+        lib().pkv_set_trace_buffer(ctypes.c_void_p(buf.data_ptr()),
+                                   buf.numel() * buf.element_size())
 
 
 def _torch():

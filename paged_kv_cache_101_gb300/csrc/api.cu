@@ -17,8 +17,12 @@ namespace {
 
 int32_t g_opt_num_ctas = 0;
 int32_t g_opt_stages = 0;
+int32_t g_opt_heads = 0;
+int32_t g_opt_box = 0;
 cudaEvent_t g_ev_before = nullptr;
 cudaEvent_t g_ev_after = nullptr;
+void *g_trace = nullptr;
+size_t g_trace_bytes = 0;
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -90,16 +94,35 @@ CUresult encode_pool(CUtensorMap *map, const void *base, int64_t num_blocks, int
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// The same pool seen as (64, 16, D/64, Hkv, num_blocks): token before half and
+// head, so one box (64, 16, D/64, hg, 1) brings a whole block of hg heads and
+// lands in shared memory as [head][half][token][64], the layout the tile boxes
+// build. Returns non-success if the driver refuses this stride order.
+CUresult encode_pool_block(CUtensorMap *map, const void *base, int64_t num_blocks, int Hkv, int D,
+                           int hg)
+{
+    const cuuint64_t dims[5] = {64, 16, cuuint64_t(D / 64), cuuint64_t(Hkv),
+                                cuuint64_t(num_blocks)};
+    const cuuint64_t strides[4] = {cuuint64_t(Hkv) * D * 2, 128, cuuint64_t(D) * 2,
+                                   cuuint64_t(16) * Hkv * D * 2};
+    const cuuint32_t box[5] = {64, 16, cuuint32_t(D / 64), cuuint32_t(hg), 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 struct MapEntry {
     const void *base = nullptr;
     int64_t nb = 0;
-    int hkv = 0, d = 0, dev = -1;
+    int hkv = 0, d = 0, dev = -1, kind = 0;  // kind 0: tile boxes, else heads per box
     CUtensorMap map;
 };
 MapEntry g_maps[16];
 int g_map_next = 0;
 
-cudaError_t pool_map(const void *base, int64_t nb, int Hkv, int D, CUtensorMap *out)
+// kind 0: tile-box map; kind hg > 0: whole-block map with hg heads per box.
+cudaError_t pool_map(const void *base, int64_t nb, int Hkv, int D, int kind, CUtensorMap *out)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -110,13 +133,16 @@ cudaError_t pool_map(const void *base, int64_t nb, int Hkv, int D, CUtensorMap *
         return e;
     std::lock_guard<std::mutex> lk(g_mu);
     for (auto &m : g_maps)
-        if (m.base == base && m.nb == nb && m.hkv == Hkv && m.d == D && m.dev == dev) {
+        if (m.base == base && m.nb == nb && m.hkv == Hkv && m.d == D && m.dev == dev &&
+            m.kind == kind) {
             *out = m.map;
             return cudaSuccess;
         }
     MapEntry &m = g_maps[g_map_next];
     g_map_next = (g_map_next + 1) % 16;
-    if (encode_pool(&m.map, base, nb, Hkv, D) != CUDA_SUCCESS) {
+    const CUresult r = kind == 0 ? encode_pool(&m.map, base, nb, Hkv, D)
+                                 : encode_pool_block(&m.map, base, nb, Hkv, D, kind);
+    if (r != CUDA_SUCCESS) {
         m.base = nullptr;
         return cudaErrorInvalidValue;
     }
@@ -125,6 +151,7 @@ cudaError_t pool_map(const void *base, int64_t nb, int Hkv, int D, CUtensorMap *
     m.hkv = Hkv;
     m.d = D;
     m.dev = dev;
+    m.kind = kind;
     *out = m.map;
     return cudaSuccess;
 }
@@ -167,6 +194,12 @@ const char *pkv_status_string(int32_t status)
 
 int32_t pkv_version(void) { return 100; }
 
+void pkv_set_trace_buffer(void *device_buffer, size_t bytes)
+{
+    g_trace = device_buffer;
+    g_trace_bytes = device_buffer ? bytes : 0;
+}
+
 void pkv_set_profiling_events(void *before, void *after)
 {
     if (before && after) {
@@ -190,6 +223,16 @@ int32_t pkv_set_option(int32_t option, int32_t value)
     case PKV_OPT_STAGES:
         prev = g_opt_stages;
         g_opt_stages = value;
+        return prev;
+    case PKV_OPT_HEADS_PER_CTA:
+        prev = g_opt_heads;
+        g_opt_heads = value;
+        return prev;
+    case PKV_OPT_TMA_BOX:
+        if (value > 2)
+            return -1;
+        prev = g_opt_box;
+        g_opt_box = value;
         return prev;
     default:
         return -1;
@@ -232,7 +275,8 @@ size_t pkv_workspace_size(int32_t num_seqs, int32_t n_query_per_seq, int32_t num
         return 0;
     pkv::DecodePlan pl;
     if (pkv::plan_decode(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim, 1,
-                         d.num_sms, g_opt_num_ctas, g_opt_stages, d.smem_optin, &pl) != 0)
+                         d.num_sms, g_opt_num_ctas, g_opt_stages, g_opt_heads, d.smem_optin,
+                         &pl) != 0)
         return 0;
     return pl.ws_bytes;
 }
@@ -271,15 +315,28 @@ pkv_status pkv_paged_decode_attention(const void *q, const void *k_cache, const 
     pkv::DecodePlan pl;
     if (pkv::plan_decode(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim,
                          max_blocks_per_seq, d.num_sms, g_opt_num_ctas, g_opt_stages,
-                         d.smem_optin, &pl) != 0)
+                         g_opt_heads, d.smem_optin, &pl) != 0)
         return PKV_ERR_UNSUPPORTED;
     if (workspace_bytes < pl.ws_bytes)
         return PKV_ERR_WORKSPACE;
+    uint64_t *trace = nullptr;
+    if (g_trace && g_trace_bytes >= size_t(pl.grid) * pkv::kTraceWords * 8 &&
+        aligned(g_trace, 8))
+        trace = static_cast<uint64_t *>(g_trace);
 
     CUtensorMap kmap, vmap;
-    if (pool_map(k_cache, num_blocks, num_kv_heads, head_dim, &kmap) != cudaSuccess ||
-        pool_map(v_cache, num_blocks, num_kv_heads, head_dim, &vmap) != cudaSuccess)
-        return PKV_ERR_CUDA;
+    int whole_box = 0;
+    if (g_opt_box != 1 &&
+        pool_map(k_cache, num_blocks, num_kv_heads, head_dim, pl.HG, &kmap) == cudaSuccess &&
+        pool_map(v_cache, num_blocks, num_kv_heads, head_dim, pl.HG, &vmap) == cudaSuccess)
+        whole_box = 1;
+    if (!whole_box) {
+        if (g_opt_box == 2)
+            return PKV_ERR_UNSUPPORTED;  // whole-block boxes requested but refused
+        if (pool_map(k_cache, num_blocks, num_kv_heads, head_dim, 0, &kmap) != cudaSuccess ||
+            pool_map(v_cache, num_blocks, num_kv_heads, head_dim, 0, &vmap) != cudaSuccess)
+            return PKV_ERR_CUDA;
+    }
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     pkv::DecodeParams p;
@@ -289,6 +346,7 @@ pkv_status pkv_paged_decode_attention(const void *q, const void *k_cache, const 
     p.block_tables = block_tables;
     p.context_lens = context_lens;
     p.err = reinterpret_cast<uint32_t *>(ws);
+    p.trace = trace;
     p.seq_start = reinterpret_cast<int32_t *>(ws + pl.off_seq);
     p.ml = reinterpret_cast<float *>(ws + pl.off_ml);
     p.part = reinterpret_cast<float *>(ws + pl.off_part);
@@ -306,6 +364,7 @@ pkv_status pkv_paged_decode_attention(const void *q, const void *k_cache, const 
     p.out_f32 = out_dtype == PKV_FP32;
     p.stage_bytes = pl.stage_bytes;
     p.nst = pl.nst;
+    p.whole_box = whole_box;
     p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
     cudaError_t e = pkv::launch_decode(pl, p, kmap, vmap, static_cast<cudaStream_t>(stream),
                                        g_ev_before, g_ev_after);

@@ -20,6 +20,10 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4 *__restrict_
                                                         uint4 *__restrict__ v_cache,
                                                         int64_t total_slots, int row_vec)
 {
+    // a dependent launched with programmatic serialization (the attention
+    // kernel) may start its prologue now; it waits for this grid's completion
+    // before it reads anything from global memory
+    asm volatile("griddepcontrol.launch_dependents;");
     const int64_t i = blockIdx.x;
     const int64_t slot = __ldg(slot_mapping + i);
     if (slot < 0 || slot >= total_slots)

@@ -200,15 +200,24 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
                 const uint32_t kdst = smem_u32(sm.stages + size_t(st) * p.stage_bytes);
                 const uint32_t vdst = kdst + uint32_t(p.HG * NH * kTileBytes);
                 const int h0 = hg * p.HG;
-                for (int hl = 0; hl < p.HG; ++hl) {
+                if (p.whole_box) {
+                    // map dims (d, token, half, head, block): one box = HG heads x 16 rows
+                    tma_load_5d_hint(kdst, kmap, bar, 0, 0, 0, h0, phys, pol);
+                    tma_load_5d_hint(vdst, vmap, bar, 0, 0, 0, h0, phys, pol);
+                } else {
+                    // map dims (d, half, head, token, block): one box = one (head, half) tile
+                    for (int hl = 0; hl < p.HG; ++hl) {
 #pragma unroll
-                    for (int hf = 0; hf < NH; ++hf) {
-                        const uint32_t off = uint32_t((hl * NH + hf) * kTileBytes);
-                        tma_load_5d_hint(kdst + off, kmap, bar, 0, hf, h0 + hl, 0, phys, pol);
-                        tma_load_5d_hint(vdst + off, vmap, bar, 0, hf, h0 + hl, 0, phys, pol);
+                        for (int hf = 0; hf < NH; ++hf) {
+                            const uint32_t off = uint32_t((hl * NH + hf) * kTileBytes);
+                            tma_load_5d_hint(kdst + off, kmap, bar, 0, hf, h0 + hl, 0, phys, pol);
+                            tma_load_5d_hint(vdst + off, vmap, bar, 0, hf, h0 + hl, 0, phys, pol);
+                        }
                     }
                 }
             }
+            if (p.trace && lane == 0 && issued == 0)
+                p.trace[blockIdx.x * kTraceWords + 1] = global_timer_ns();
             __syncwarp();
             ++issued;
             if (++st == uint32_t(p.nst)) {
@@ -245,6 +254,10 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
         if (ok && lane == 0) {
             sm.hdr[st].flags = F_END;
             mbar_arrive(smem_u32(&sm.full[st]));
+            if (p.trace) {
+                p.trace[blockIdx.x * kTraceWords + 3] = global_timer_ns();
+                p.trace[blockIdx.x * kTraceWords + 5] = issued;
+            }
         }
     }
     if (!ok && lane == 0) {
@@ -308,6 +321,15 @@ __device__ void consumer_warp(const DecodeParams &p, const Smem &sm, int cw, int
             return;
         }
         const StageHdr h = sm.hdr[st];
+        if (p.trace && cw == 0 && lane == 0) {
+            uint64_t *tr = p.trace + blockIdx.x * kTraceWords;
+            if (h.flags & F_END)
+                tr[4] = global_timer_ns();
+            else if (tr[2] == 0)
+                tr[2] = global_timer_ns();
+            if (h.flags & F_FIRST)
+                tr[6] += 1;
+        }
         if (h.flags & F_END)
             return;
         const int kvh = h.hg * p.HG + hl;
@@ -349,13 +371,14 @@ __device__ void consumer_warp(const DecodeParams &p, const Smem &sm, int cw, int
         const uint32_t kb = stage_base + st * uint32_t(p.stage_bytes) + uint32_t(hl * NH * kTileBytes);
         const uint32_t vb = kb + uint32_t(p.HG * NH * kTileBytes);  // same head in the V half
 
-        // ---- scores S^T[token][row] for the block's 16 tokens
-        float sc[NTW][4];
+        // ---- scores S^T[token][row] for the block's 16 tokens (two accumulation
+        //      chains, even and odd k-steps, to halve the dependent-mma latency)
+        float sc[NTW][4], sc2[NTW][4];
 #pragma unroll
         for (int n = 0; n < NTW; ++n)
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-                sc[n][e] = 0.f;
+                sc[n][e] = sc2[n][e] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
             const int chunk = 2 * ks + k_cadd;
@@ -364,9 +387,18 @@ __device__ void consumer_warp(const DecodeParams &p, const Smem &sm, int cw, int
             uint32_t a[4];
             ldsm_x4(addr, a);
 #pragma unroll
-            for (int n = 0; n < NTW; ++n)
-                mma_bf16_16816(sc[n], a, qf[ks][n][0], qf[ks][n][1]);
+            for (int n = 0; n < NTW; ++n) {
+                if (ks & 1)
+                    mma_bf16_16816(sc2[n], a, qf[ks][n][0], qf[ks][n][1]);
+                else
+                    mma_bf16_16816(sc[n], a, qf[ks][n][0], qf[ks][n][1]);
+            }
         }
+#pragma unroll
+        for (int n = 0; n < NTW; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                sc[n][e] += sc2[n][e];
 
         // ---- scale (log2 domain) and causal / tail mask
         const int t0 = h.b * kBlockSize;
@@ -384,8 +416,11 @@ __device__ void consumer_warp(const DecodeParams &p, const Smem &sm, int cw, int
                 sc[n][e] = x;
             }
 
-        // ---- online softmax (rows 2tq, 2tq+1 of each n-tile live in this lane)
-        float corr[NTW][2];
+        // ---- online softmax (rows 2tq, 2tq+1 of each n-tile live in this lane).
+        //      The accumulator is rescaled only when some row's running max grew
+        //      (otherwise every factor would be exactly 1).
+        float bmax[NTW][2];
+        bool grew = false;
 #pragma unroll
         for (int n = 0; n < NTW; ++n)
 #pragma unroll
@@ -394,24 +429,41 @@ __device__ void consumer_warp(const DecodeParams &p, const Smem &sm, int cw, int
                 bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
                 bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
                 bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
-                const float mn = fmaxf(m_r[n][r], bm);
-                const float mu = (mn == -INFINITY) ? 0.f : mn;
-                corr[n][r] = ex2(m_r[n][r] - mu);
-                m_r[n][r] = mn;
+                bmax[n][r] = bm;
+                grew |= bm > m_r[n][r];
+            }
+        if (__any_sync(0xffffffffu, grew)) {
+            float corr[NTW][2];
+#pragma unroll
+            for (int n = 0; n < NTW; ++n)
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float mn = fmaxf(m_r[n][r], bmax[n][r]);
+                    const float mu = (mn == -INFINITY) ? 0.f : mn;
+                    corr[n][r] = ex2(m_r[n][r] - mu);
+                    m_r[n][r] = mn;
+                    l_r[n][r] *= corr[n][r];
+                }
+#pragma unroll
+            for (int i = 0; i < MT; ++i)
+#pragma unroll
+                for (int n = 0; n < NTW; ++n) {
+                    acc[i][n][0] *= corr[n][0];
+                    acc[i][n][1] *= corr[n][1];
+                    acc[i][n][2] *= corr[n][0];
+                    acc[i][n][3] *= corr[n][1];
+                }
+        }
+#pragma unroll
+        for (int n = 0; n < NTW; ++n)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const float mu = (m_r[n][r] == -INFINITY) ? 0.f : m_r[n][r];
                 const float p0 = ex2(sc[n][r] - mu);
                 const float p1 = ex2(sc[n][r + 2] - mu);
-                l_r[n][r] = l_r[n][r] * corr[n][r] + (p0 + p1);
+                l_r[n][r] += p0 + p1;
                 sc[n][r] = p0;
                 sc[n][r + 2] = p1;
-            }
-#pragma unroll
-        for (int i = 0; i < MT; ++i)
-#pragma unroll
-            for (int n = 0; n < NTW; ++n) {
-                acc[i][n][0] *= corr[n][0];
-                acc[i][n][1] *= corr[n][1];
-                acc[i][n][2] *= corr[n][0];
-                acc[i][n][3] *= corr[n][1];
             }
 
         // ---- P = hi + lo (bf16 each), transposed into mma B fragments
@@ -551,7 +603,19 @@ __global__ void __launch_bounds__(kThreadsMax, 1)
         }
         fence_mbar_init();
     }
+    // This grid may be launched while the previous kernel on the stream (e.g.
+    // the KV append writing the pool) still runs: wait for it to complete and
+    // its writes to be visible before reading any global memory.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (p.trace && threadIdx.x == 0) {
+        uint32_t smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        p.trace[blockIdx.x * kTraceWords + 0] = global_timer_ns();
+        p.trace[blockIdx.x * kTraceWords + 7] = smid;
+    }
     __syncthreads();
+    // let the merge grid be scheduled now; it waits for this grid's completion
+    asm volatile("griddepcontrol.launch_dependents;");
     if (warp == 0)
         producer_warp<D>(&kmap, &vmap, p, sm, lane);
     else
@@ -563,35 +627,54 @@ __global__ void __launch_bounds__(kThreadsMax, 1)
 // M = max m_c, L = sum l_c 2^(m_c - M), out = sum acc_c 2^(m_c - M) / L
 // ("07 -- Inference" section 5.3; m is kept in the log2 domain). Sequences
 // with no token write zeros.
+//
+// One warp per output row (sequence, head group, kv head, query row); lane i
+// owns head dims 4i..4i+3. Launched as a programmatic dependent of the main
+// kernel: it is scheduled while that kernel runs and waits (griddepcontrol)
+// for it to finish before reading the workspace.
 __global__ void __launch_bounds__(256)
     paged_decode_merge_kernel(const DecodeParams p, int D, int grid)
 {
-    const int s = blockIdx.x, hg = blockIdx.y;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int64_t wid = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    const int64_t total = int64_t(p.S) * p.n_hg * p.HG * p.rows;
+    if (wid >= total)
+        return;
+    int64_t w = wid;
+    const int row = int(w % p.rows);
+    w /= p.rows;
+    const int hl = int(w % p.HG);
+    w /= p.HG;
+    const int hg = int(w % p.n_hg);
+    const int s = int(w / p.n_hg);
+
+    const int j = row / p.G, gq = row - j * p.G;
+    const int kvh = hg * p.HG + hl;
+    const int64_t o = ((int64_t(s) * p.nq + j) * p.Hq + int64_t(kvh) * p.G + gq) * D;
+    const bool has_d = lane * 4 < D;
+
+    auto store4 = [&](float4 v) {
+        if (!has_d)
+            return;
+        if (p.out_f32) {
+            *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + o + lane * 4) = v;
+        } else {
+            __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+            __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+            uint2 u;
+            u.x = *reinterpret_cast<uint32_t *>(&a);
+            u.y = *reinterpret_cast<uint32_t *>(&b);
+            *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.out) + o + lane * 4) = u;
+        }
+    };
+
     const int nb_total = p.seq_start[p.S];
     const int64_t F = int64_t(p.n_hg) * nb_total;
     const int64_t fs = int64_t(hg) * nb_total + p.seq_start[s];
     const int64_t fe = int64_t(hg) * nb_total + p.seq_start[s + 1];
-    const int n_el = p.HG * p.rows * D;
-
-    auto out_index = [&](int e, int &hl, int &row, int &d) -> int64_t {
-        hl = e / (p.rows * D);
-        const int rem = e - hl * p.rows * D;
-        row = rem / D;
-        d = rem - row * D;
-        const int j = row / p.G, gq = row - j * p.G;
-        const int kvh = hg * p.HG + hl;
-        return ((int64_t(s) * p.nq + j) * p.Hq + int64_t(kvh) * p.G + gq) * D + d;
-    };
-
     if (fe == fs) {
-        for (int e = threadIdx.x; e < n_el; e += blockDim.x) {
-            int hl, row, d;
-            const int64_t o = out_index(e, hl, row, d);
-            if (p.out_f32)
-                static_cast<float *>(p.out)[o] = 0.f;
-            else
-                static_cast<__nv_bfloat16 *>(p.out)[o] = __float2bfloat16_rn(0.f);
-        }
+        store4(make_float4(0.f, 0.f, 0.f, 0.f));
         return;
     }
     // chunk c covers [c*F/grid, (c+1)*F/grid); chunk_of(f) = ceil((f+1)*grid/F) - 1
@@ -599,49 +682,60 @@ __global__ void __launch_bounds__(256)
     const int64_t ce = (fe * grid + F - 1) / F - 1;
     if (cb == ce)
         return;  // finished in place by the main kernel
-    const bool cb_first = (cb * F / grid) == fs;  // sequence opens chunk cb
+    const bool cb_first = (cb * F / grid) == fs;  // the sequence opens chunk cb
 
     // With fewer units than CTAs some chunks are empty; they hold no partial.
-    auto empty_chunk = [&](int64_t c) { return c * F / grid == (c + 1) * F / grid; };
-    for (int e = threadIdx.x; e < n_el; e += blockDim.x) {
-        int hl, row, d;
-        const int64_t o = out_index(e, hl, row, d);
-        float M = -INFINITY;
-        for (int64_t c = cb; c <= ce; ++c) {
-            if (empty_chunk(c))
-                continue;
-            const int slot = (c == cb && !cb_first) ? 1 : 0;
-            const int64_t cell = (c * 2 + slot) * p.HG + hl;
-            M = fmaxf(M, p.ml[(cell * p.rows_pad + row) * 2]);
+    auto cell_of = [&](int64_t c) -> int64_t {
+        if (c * F / grid == (c + 1) * F / grid)
+            return -1;
+        const int slot = (c == cb && !cb_first) ? 1 : 0;
+        return ((c * 2 + slot) * p.HG + hl) * p.rows_pad + row;
+    };
+
+    // M over the covering chunks, 32 chunks per round (one per lane)
+    float M = -INFINITY;
+    for (int64_t c0 = cb; c0 <= ce; c0 += 32) {
+        const int64_t c = c0 + lane;
+        if (c <= ce) {
+            const int64_t cell = cell_of(c);
+            if (cell >= 0)
+                M = fmaxf(M, p.ml[cell * 2]);
         }
-        float L = 0.f, a = 0.f;
-        if (M != -INFINITY) {
-            for (int64_t c = cb; c <= ce; ++c) {
-                if (empty_chunk(c))
-                    continue;
-                const int slot = (c == cb && !cb_first) ? 1 : 0;
-                const int64_t cell = (c * 2 + slot) * p.HG + hl;
-                const float m = p.ml[(cell * p.rows_pad + row) * 2];
-                if (m == -INFINITY)
-                    continue;
-                const float f = ex2(m - M);
-                L += p.ml[(cell * p.rows_pad + row) * 2 + 1] * f;
-                a += p.part[(cell * p.rows_pad + row) * D + d] * f;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+
+    float L = 0.f;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+        for (int64_t c = cb; c <= ce; ++c) {
+            const int64_t cell = cell_of(c);
+            if (cell < 0)
+                continue;
+            const float m = p.ml[cell * 2];
+            if (m == -INFINITY)
+                continue;
+            const float f = ex2(m - M);
+            L += p.ml[cell * 2 + 1] * f;
+            if (has_d) {
+                const float4 v = *reinterpret_cast<const float4 *>(p.part + cell * D + lane * 4);
+                a.x += v.x * f;
+                a.y += v.y * f;
+                a.z += v.z * f;
+                a.w += v.w * f;
             }
         }
-        const float v = L > 0.f ? a / L : 0.f;
-        if (p.out_f32)
-            static_cast<float *>(p.out)[o] = v;
-        else
-            static_cast<__nv_bfloat16 *>(p.out)[o] = __float2bfloat16_rn(v);
     }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    store4(make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv));
 }
 
 // ------------------------------------------------------------------ host side
 static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int opt_ctas,
-                int opt_stages, int smem_optin, DecodePlan *pl)
+                int opt_stages, int opt_heads, int smem_optin, DecodePlan *pl)
 {
     if (S < 1 || nq < 1 || Hkv < 1 || Hq % Hkv != 0 || (D != 64 && D != 128) || MB < 1)
         return -1;
@@ -660,7 +754,9 @@ int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int 
         P.ntw = 2;
     }
     P.rows_pad = P.wph * P.ntw * 8;
-    const int max_hg = kMaxConsumerWarps / P.wph;
+    int max_hg = kMaxConsumerWarps / P.wph;
+    if (opt_heads > 0 && opt_heads < max_hg)
+        max_hg = opt_heads;
     P.HG = 1;
     for (int h = std::min(max_hg, Hkv); h >= 1; --h)
         if (Hkv % h == 0) {
@@ -711,14 +807,43 @@ static cudaError_t launch_one(const DecodePlan &pl, const DecodeParams &p, const
     }
     if (ev_before && (e = cudaEventRecord(ev_before, stream)) != cudaSuccess)
         return e;
-    kern<<<pl.grid, pl.threads, pl.smem, stream>>>(kmap, vmap, p);
+    {
+        // programmatic serialization: the kernel's prologue may overlap the tail
+        // of the previous kernel; it waits (griddepcontrol.wait) before any read
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(unsigned(pl.grid));
+        cfg.blockDim = dim3(unsigned(pl.threads));
+        cfg.dynamicSmemBytes = pl.smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, kmap, vmap, p);
+        if (e != cudaSuccess)
+            return e;
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
     if (ev_after && (e = cudaEventRecord(ev_after, stream)) != cudaSuccess)
         return e;
-    dim3 mg(p.S, p.n_hg);
-    paged_decode_merge_kernel<<<mg, 256, 0, stream>>>(p, D, pl.grid);
+    // merge: one warp per output row, launched as a programmatic dependent
+    const int64_t warps = int64_t(p.S) * p.n_hg * p.HG * p.rows;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned((warps + 7) / 8));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, paged_decode_merge_kernel, p, int(D), int(pl.grid));
+    if (e != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 

@@ -14,6 +14,9 @@ constexpr int kMaxRows = 32;            // query rows per kv head: G * n_query_p
 constexpr int kMaxConsumerWarps = 8;
 constexpr int kThreadsMax = 32 * (1 + kMaxConsumerWarps);
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded waits: 2 s
+// per-CTA trace words: entry, first TMA issued, first stage consumed, last TMA
+// issued, last stage consumed (ns, %globaltimer), units, segments, SM id
+constexpr int kTraceWords = 8;
 
 // device error word codes (workspace offset 0)
 enum : uint32_t {
@@ -36,6 +39,7 @@ struct DecodePlan {
     int threads;     // 32 * (1 + HG * wph)
     int stage_bytes; // K + V of one 16-token block for HG heads
     int nst;         // pipeline stages
+    int whole_box;   // 1: one TMA box per block for K (and V) of all HG heads
     int grid;        // persistent CTAs
     size_t smem;     // dynamic shared memory bytes
     // workspace layout (byte offsets)
@@ -51,14 +55,16 @@ struct DecodeParams {
     float *ml;             // workspace: [grid][2][HG][rows_pad][2]  (m, l)
     float *part;           // workspace: [grid][2][HG][rows_pad][D]  unnormalised acc
     uint32_t *err;         // workspace word 0
+    uint64_t *trace;       // optional per-CTA timeline [grid][kTraceWords] (null: off)
     int64_t num_blocks;
     int S, MB, nq, Hq, Hkv, G, rows, rows_pad, HG, n_hg, out_f32;
     int stage_bytes, nst;
+    int whole_box;         // 1: the tensor maps box a whole block (HG heads) at once
     float scale_log2;      // scale * log2(e)
 };
 
 int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int opt_ctas,
-                int opt_stages, int smem_optin, DecodePlan *plan);
+                int opt_stages, int opt_heads, int smem_optin, DecodePlan *plan);
 
 // ev_before/ev_after (may be null) are recorded around the main kernel only.
 cudaError_t launch_decode(const DecodePlan &plan, const DecodeParams &p, const CUtensorMap &kmap,

@@ -22,13 +22,17 @@ def o():
     return oracle.Oracle()
 
 
+OPTIONS = (pkv.PKV_OPT_NUM_CTAS, pkv.PKV_OPT_STAGES, pkv.PKV_OPT_HEADS_PER_CTA,
+           pkv.PKV_OPT_TMA_BOX)
+
+
 @pytest.fixture(autouse=True)
 def _defaults():
-    pkv.set_option(pkv.PKV_OPT_NUM_CTAS, 0)
-    pkv.set_option(pkv.PKV_OPT_STAGES, 0)
+    for opt in OPTIONS:
+        pkv.set_option(opt, 0)
     yield
-    pkv.set_option(pkv.PKV_OPT_NUM_CTAS, 0)
-    pkv.set_option(pkv.PKV_OPT_STAGES, 0)
+    for opt in OPTIONS:
+        pkv.set_option(opt, 0)
 
 
 def run_small(o, w, out_dtype=None, check_pool=True):
@@ -246,3 +250,21 @@ def test_stale_workspace_is_never_read(o, ctas):
     ref, _, _ = o.step(w)
     compare(to_f64(d.out), ref, what="stale workspace")
     assert pkv.workspace_error(ws) == 0
+
+
+@pytest.mark.parametrize("box", [1, 2])
+@pytest.mark.parametrize("heads", [1, 2, 4, 8])
+def test_tma_box_modes_and_head_groups(o, box, heads):
+    """Per-tile and whole-block TMA boxes, for every head-group size."""
+    pkv.set_option(pkv.PKV_OPT_TMA_BOX, box)
+    pkv.set_option(pkv.PKV_OPT_HEADS_PER_CTA, heads)
+    T = [700, 17, 1, 2048, 333]
+    w = W.make_custom(len(T), 1, 32, 8, 128, T, seed=91 + heads)
+    try:
+        run_small(o, w)
+    except pkv.PkvError as e:
+        if box == 2 and e.status == 8:
+            pytest.skip("driver refuses the whole-block tensor map")
+        raise
+    w = W.make_custom(4, 4, 16, 2, 64, [4, 90, 257, 31], seed=95 + heads)
+    run_small(o, w)
