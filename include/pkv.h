@@ -140,12 +140,18 @@ size_t pkv_workspace_size(int32_t num_seqs, int32_t n_query_per_seq, int32_t num
  *   out            device, [num_seqs*n_query_per_seq][num_q_heads][head_dim] of
  *                  out_dtype (PKV_BF16 rounds to nearest even), 16-byte aligned.
  *   workspace      device, >= pkv_workspace_size(...) bytes, 256-byte aligned,
- *                  ZERO-FILLED before its first use. Its first 4 bytes are a
- *                  sticky device error word: a kernel that gives up on a wait
- *                  (never expected; a bounded wait guards against a hang)
- *                  stores a nonzero code there and returns early. The library
- *                  never clears it. Calls sharing a workspace must be ordered
- *                  on one stream (or otherwise serialised).
+ *                  ZERO-FILLED before its first use; every call leaves the
+ *                  counters it uses at zero again, so one workspace serves any
+ *                  sequence of calls (of any shapes that fit it). It holds a
+ *                  256-byte header, the block prefix sums and the split-K
+ *                  partial states (m, l, acc) per cell (a fixed slice of the
+ *                  batch's blocks). Its first 4
+ *                  bytes are a sticky device error word: a kernel that gives up
+ *                  on a wait (never expected; a bounded wait guards against a
+ *                  hang) ORs a nonzero code there and returns early; zero the
+ *                  workspace again after such a call. Calls sharing a
+ *                  workspace must be ordered on one stream (or otherwise
+ *                  serialised).
  *   num_seqs == 0  is a no-op returning PKV_OK.
  */
 pkv_status pkv_paged_decode_attention(const void *q, const void *k_cache, const void *v_cache,
@@ -181,9 +187,9 @@ pkv_status pkv_paged_decode_attention(const void *q, const void *k_cache, const 
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and keeps it; make that
- * first call before any stream capture. Each call clears the array's 4-byte
- * device error word (a cudaMemsetAsync on `stream`) before its kernels; the
- * kernels write every other byte they read. All calls share the one array and
+ * first call before any stream capture. Each call clears the array's
+ * 256-byte header (device error word, work counters; one cudaMemsetAsync on
+ * `stream`) before its kernels; they write every other byte they read. All calls share the one array and
  * it keeps the last call's contents: calls that overlap on the GPU (on
  * different streams, or from several threads) race on it and give
  * unspecified results. Serialise them, e.g. on one stream.
@@ -233,12 +239,13 @@ void pkv_set_profiling_events(void *before, void *after);
 /*
  * pkv_set_trace_buffer -- per-CTA timeline of the attention kernel (process-
  * wide; NULL turns it off). When set, every later pkv_paged_decode_attention
- * call whose grid fits writes, for each CTA c, 8 uint64 words at
- * device_buffer[8c ..]: [0] entry, [1] first K/V copy issued, [2] first stage
+ * call whose grid fits writes, for each CTA c, 16 uint64 words at
+ * device_buffer[16c ..]: [0] entry, [1] first K/V copy issued, [2] first stage
  * consumed, [3] last copy issued, [4] last stage consumed (ns of the GPU's
- * global timer), [5] 16-token blocks streamed, [6] sequence segments started
- * (added to the existing value), [7] SM id. The caller zeroes the buffer
- * before a call; a buffer smaller than grid*64 bytes disables the trace.
+ * global timer), [5] 16-token blocks streamed, [6] sequence segments
+ * started, [7] SM id; the counters add to the existing values; [8..15]
+ * are reserved. The caller zeroes the buffer before a call; a
+ * buffer smaller than grid*128 bytes disables the trace.
  */
 void pkv_set_trace_buffer(void *device_buffer, size_t bytes);
 

@@ -174,6 +174,28 @@ pkv_status check_geometry(int32_t num_seqs, int32_t nq, int32_t Hq, int32_t Hkv,
 
 }  // namespace
 
+namespace pkv {
+
+// Leading workspace bytes that must be zero when a call starts (the header:
+// device error word and work counters); 0 if the geometry is unsupported.
+size_t workspace_zero_prefix(int32_t num_seqs, int32_t n_query_per_seq, int32_t num_q_heads,
+                             int32_t num_kv_heads, int32_t head_dim)
+{
+    if (check_geometry(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim) != PKV_OK ||
+        num_seqs < 1)
+        return 0;
+    DeviceInfo d;
+    if (device_info(&d) != cudaSuccess)
+        return 0;
+    DecodePlan pl;
+    if (plan_decode(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim, 1, d.num_sms,
+                    g_opt_num_ctas, g_opt_stages, g_opt_heads, d.smem_optin, &pl) != 0)
+        return 0;
+    return kWsHeaderBytes;
+}
+
+}  // namespace pkv
+
 extern "C" {
 
 const char *pkv_status_string(int32_t status)
@@ -345,11 +367,11 @@ pkv_status pkv_paged_decode_attention(const void *q, const void *k_cache, const 
     p.out = out;
     p.block_tables = block_tables;
     p.context_lens = context_lens;
-    p.err = reinterpret_cast<uint32_t *>(ws);
-    p.trace = trace;
+    p.ws = reinterpret_cast<uint32_t *>(ws);
     p.seq_start = reinterpret_cast<int32_t *>(ws + pl.off_seq);
     p.ml = reinterpret_cast<float *>(ws + pl.off_ml);
     p.part = reinterpret_cast<float *>(ws + pl.off_part);
+    p.trace = trace;
     p.num_blocks = num_blocks;
     p.S = num_seqs;
     p.MB = max_blocks_per_seq;
@@ -365,6 +387,10 @@ pkv_status pkv_paged_decode_attention(const void *q, const void *k_cache, const 
     p.stage_bytes = pl.stage_bytes;
     p.nst = pl.nst;
     p.whole_box = whole_box;
+    p.ncw = pl.HG * pl.wph;
+    p.tickets_max = pl.tickets_max;
+    p.ticket_div = 8;
+    p.ticket_units = 4;
     p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
     cudaError_t e = pkv::launch_decode(pl, p, kmap, vmap, static_cast<cudaStream_t>(stream),
                                        g_ev_before, g_ev_after);

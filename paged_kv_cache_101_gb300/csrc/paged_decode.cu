@@ -10,14 +10,17 @@
 //
 // How (GB300 design, not the pages' kernel):
 //  * Work space. Per head group (HG kv heads), the blocks of all sequences are
-//    laid end to end: unit u = hg * NB_total + block_prefix[s] + b. The
-//    persistent grid cuts this flat space into equal contiguous chunks, one per
-//    CTA, so every CTA streams the same number of 16-token blocks whatever the
-//    length mix (short and long sequences both fill all SMs). A sequence cut by
-//    a chunk boundary leaves a partial (m, l, acc) per CTA in the workspace; the
-//    merge kernel combines them. Sequences inside one chunk are finished in
-//    place (normalised output written directly).
-//  * Staging. Warp 0 is the producer: it walks its chunk, reads block-table
+//    laid end to end: unit u = hg * NB_total + block_prefix[s] + b. This flat
+//    space is cut into fixed cells: one equal contiguous chunk per CTA of the
+//    persistent grid, optionally followed by a tail of smaller tickets that
+//    CTAs claim dynamically once their chunk is done (so SMs that stream faster
+//    take more of the tail). Cell boundaries depend only on the sizes, never on
+//    which CTA runs a cell, so results are deterministic.
+//  * Split-K. A sequence inside one cell is finished in place (normalised
+//    output). A sequence cut by cell boundaries leaves one partial (m, l, acc)
+//    per cell in the workspace; a small merge kernel, launched as a
+//    programmatic dependent, combines them (same rescaling rule).
+//  * Staging. Warp 0 is the producer: it walks its cells, reads block-table
 //    entries 32 at a time (one coalesced load), and for each block issues TMA
 //    tensor loads of K and V for its HG heads into a ring of shared-memory
 //    stages (128-byte swizzle, mbarrier completion with byte counts). Stages are
@@ -49,10 +52,54 @@ struct StageHdr {
     int32_t T;      // context length (clamped)
     int32_t hg;     // head group
     int32_t flags;  // F_*
-    int32_t slot;   // partial slot for a split sequence's segment (0: chunk's first)
-    int32_t pad0, pad1;
+    int32_t slot;   // partial slot: 0 if the segment opens its cell, else 1
+    int32_t cell;   // cell holding this block
+    int32_t fs;     // flat index of the sequence's first unit (head group included)
 };
 enum : int32_t { F_FIRST = 1, F_LAST = 2, F_DIRECT = 4, F_END = 8 };
+
+// The fixed partition of the flat unit space [0, F): cells 0..G-1 split
+// [0, F1) evenly (cell c is CTA c's chunk); cells G..G+NT-1 split [F1, F) evenly
+// (tickets, claimed dynamically).
+struct Cells {
+    int64_t F, F1, F2;
+    int32_t G, NT;
+
+    __device__ __forceinline__ int64_t start(int64_t k) const
+    {
+        return k <= G ? k * F1 / G : F1 + (k - G) * F2 / NT;
+    }
+    __device__ __forceinline__ bool empty(int64_t k) const { return start(k) == start(k + 1); }
+    // the cell holding unit f (0 <= f < F)
+    __device__ __forceinline__ int64_t cell_of(int64_t f) const
+    {
+        if (f < F1)
+            return ((f + 1) * G + F1 - 1) / F1 - 1;
+        return G + ((f - F1 + 1) * NT + F2 - 1) / F2 - 1;
+    }
+};
+
+// The cells of a call: G static chunks, then up to tickets_max tickets over the
+// last F / ticket_div units. A function of the sizes only (the merge kernel
+// rebuilds the same cells).
+__device__ __forceinline__ Cells make_cells(const DecodeParams &p, int nb_total, int grid)
+{
+    Cells C;
+    C.F = int64_t(p.n_hg) * nb_total;
+    C.G = grid;
+    C.NT = 0;
+    C.F2 = 0;
+    if (p.tickets_max > 0 && p.ticket_div > 0) {
+        const int64_t f2 = C.F / p.ticket_div;
+        const int64_t nt = f2 / (p.ticket_units > 0 ? p.ticket_units : 1);
+        if (nt > 0) {
+            C.NT = int(nt < p.tickets_max ? nt : p.tickets_max);
+            C.F2 = f2;
+        }
+    }
+    C.F1 = C.F - C.F2;
+    return C;
+}
 
 __device__ __forceinline__ int seq_tokens(const DecodeParams &p, int s)
 {
@@ -72,6 +119,7 @@ struct Smem {
     StageHdr *hdr;
     uint64_t *full;
     uint64_t *empty;
+    Cells *cells;
 };
 
 __device__ __forceinline__ Smem carve(uint8_t *raw, const DecodeParams &p)
@@ -83,7 +131,25 @@ __device__ __forceinline__ Smem carve(uint8_t *raw, const DecodeParams &p)
     s.hdr = reinterpret_cast<StageHdr *>(base + size_t(p.nst) * p.stage_bytes);
     s.full = reinterpret_cast<uint64_t *>(s.hdr + p.nst);
     s.empty = s.full + p.nst;
+    s.cells = reinterpret_cast<Cells *>(s.empty + p.nst);
     return s;
+}
+
+// Write zeros to every output row of sequence s (it has no token).
+__device__ void zero_sequence(const DecodeParams &p, int D, int s)
+{
+    const int64_t row_elems = int64_t(p.Hq) * D;
+    const int64_t first = int64_t(s) * p.nq * row_elems;
+    const int64_t n = int64_t(p.nq) * row_elems;
+    if (p.out_f32) {
+        float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + first);
+        for (int64_t i = 0; i < n / 4; ++i)
+            o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+        uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + first);
+        for (int64_t i = 0; i < n / 8; ++i)
+            o[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
 }
 
 // ------------------------------------------------------------------ producer
@@ -111,6 +177,7 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
     const int base = incl - local;
     const int nb_total = __shfl_sync(FULLMASK, incl, 31);
     if (blockIdx.x == 0) {
+        // block prefix sums for the merge kernel
         int run = base;
         for (int s = s_lo; s < s_hi; ++s) {
             p.seq_start[s] = run;
@@ -120,127 +187,164 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
             p.seq_start[S] = nb_total;
     }
 
-    const int64_t F = int64_t(p.n_hg) * nb_total;
-    const int64_t f0 = int64_t(blockIdx.x) * F / gridDim.x;
-    const int64_t f1 = int64_t(blockIdx.x + 1) * F / gridDim.x;
+    const Cells C = make_cells(p, nb_total, int(gridDim.x));
+    if (lane == 0)
+        *sm.cells = C;  // published to the consumers by the first stage's arrive
 
     uint32_t st = 0, phase = 0;  // ring position of the next stage to fill
     uint32_t issued = 0;         // stages filled so far
     bool ok = true;
+    const uint64_t pol = policy_evict_first();
 
-    if (f0 < f1) {
-        // ---- locate the first unit of this chunk
-        int hg = int(f0 / nb_total);
-        const int r0 = int(f0 - int64_t(hg) * nb_total);
-        const unsigned own = __ballot_sync(FULLMASK, local > 0 && r0 >= base && r0 < base + local);
-        const int src = __ffs(own) - 1;
-        int s_f = 0, b_f = 0;
-        if (lane == src) {
-            int run = base;
-            for (int s = s_lo; s < s_hi; ++s) {
-                const int nb = seq_blocks(p, s);
-                if (r0 < run + nb) {
-                    s_f = s;
-                    b_f = r0 - run;
-                    break;
-                }
-                run += nb;
-            }
-        }
-        int s = __shfl_sync(FULLMASK, s_f, src);
-        int b = __shfl_sync(FULLMASK, b_f, src);
-        int T = seq_tokens(p, s);
-        int nb = (T + kBlockSize - 1) / kBlockSize;
-        int seg_b0 = b;
-        bool chunk_first = true;
-        int bt_base = -(1 << 30);
-        int bt_val = 0;
-        const uint64_t pol = policy_evict_first();
-
-        for (int64_t u = f0; u < f1; ++u) {
-            if (b < bt_base || b >= bt_base + 32) {
-                bt_base = b;
-                const int idx = b + lane;
-                bt_val = idx < nb ? __ldg(p.block_tables + int64_t(s) * p.MB + idx) : 0;
-            }
-            int phys = __shfl_sync(FULLMASK, bt_val, b - bt_base);
-            if (phys < 0 || int64_t(phys) >= p.num_blocks) {
-                // outside the pool: flag it; the TMA box past the tensor's end reads zeros
-                if (lane == 0)
-                    atomicOr(p.err, kErrBadBlock);
-                phys = int(p.num_blocks < 0x7fffffff ? p.num_blocks : 0x7fffffff);
-            }
-            if (issued >= uint32_t(p.nst)) {
-                int w_ok = 1;
-                if (lane == 0)
-                    w_ok = mbar_wait(smem_u32(&sm.empty[st]), phase ^ 1u, kWaitLimitNs);
-                w_ok = __shfl_sync(FULLMASK, w_ok, 0);
-                if (!w_ok) {
-                    ok = false;
-                    break;
+    int64_t cell = blockIdx.x;       // phase 1: this CTA's own chunk
+    int claim = -1;                  // lane 0: a ticket claimed ahead
+    bool claimed = false;
+    for (;;) {
+        const int64_t a = C.start(cell), e = C.start(cell + 1);
+        // locate unit f: head group, sequence, block within it, flat start of the sequence
+        auto locate = [&](int64_t f, int &hg_o, int &s_o, int &b_o, int64_t &fs_o) {
+            hg_o = int(f / nb_total);
+            const int r0 = int(f - int64_t(hg_o) * nb_total);
+            const unsigned own =
+                __ballot_sync(FULLMASK, local > 0 && r0 >= base && r0 < base + local);
+            const int src = __ffs(own) - 1;
+            int s_f = 0, b_f = 0, pre_f = 0;
+            if (lane == src) {
+                int run = base;
+                for (int s = s_lo; s < s_hi; ++s) {
+                    const int nb = seq_blocks(p, s);
+                    if (r0 < run + nb) {
+                        s_f = s;
+                        b_f = r0 - run;
+                        pre_f = run;
+                        break;
+                    }
+                    run += nb;
                 }
             }
-            const bool first = (u == f0) || (b == 0);
-            if (first)
-                seg_b0 = b;
-            const bool last = (u == f1 - 1) || (b == nb - 1);
-            int flags = (first ? F_FIRST : 0) | (last ? F_LAST : 0);
-            if (last && seg_b0 == 0 && b == nb - 1)
-                flags |= F_DIRECT;
-            if (lane == 0) {
-                StageHdr *h = &sm.hdr[st];
-                h->s = s;
-                h->b = b;
-                h->T = T;
-                h->hg = hg;
-                h->flags = flags;
-                h->slot = chunk_first ? 0 : 1;
-                const uint32_t bar = smem_u32(&sm.full[st]);
-                mbar_arrive_expect_tx(bar, uint32_t(p.stage_bytes));
-                const uint32_t kdst = smem_u32(sm.stages + size_t(st) * p.stage_bytes);
-                const uint32_t vdst = kdst + uint32_t(p.HG * NH * kTileBytes);
-                const int h0 = hg * p.HG;
-                if (p.whole_box) {
-                    // map dims (d, token, half, head, block): one box = HG heads x 16 rows
-                    tma_load_5d_hint(kdst, kmap, bar, 0, 0, 0, h0, phys, pol);
-                    tma_load_5d_hint(vdst, vmap, bar, 0, 0, 0, h0, phys, pol);
-                } else {
-                    // map dims (d, half, head, token, block): one box = one (head, half) tile
-                    for (int hl = 0; hl < p.HG; ++hl) {
+            s_o = __shfl_sync(FULLMASK, s_f, src);
+            b_o = __shfl_sync(FULLMASK, b_f, src);
+            fs_o = int64_t(hg_o) * nb_total + __shfl_sync(FULLMASK, pre_f, src);
+        };
+        if (a < e) {
+            int hg, s, b;
+            int64_t fs;
+            locate(a, hg, s, b, fs);
+            int T = seq_tokens(p, s);
+            int nb = (T + kBlockSize - 1) / kBlockSize;
+            int seg_b0 = b;
+            bool cell_first = true;
+            int bt_base = -(1 << 30);
+            int bt_val = 0;
+
+            for (int64_t u = a; u < e; ++u) {
+                if (b < bt_base || b >= bt_base + 32) {
+                    bt_base = b;
+                    const int idx = b + lane;
+                    bt_val = idx < nb ? __ldg(p.block_tables + int64_t(s) * p.MB + idx) : 0;
+                }
+                int phys = __shfl_sync(FULLMASK, bt_val, b - bt_base);
+                if (phys < 0 || int64_t(phys) >= p.num_blocks) {
+                    // outside the pool: flag it; the TMA box past the tensor's end reads zeros
+                    if (lane == 0)
+                        atomicOr(p.ws + kWsErr, kErrBadBlock);
+                    phys = int(p.num_blocks < 0x7fffffff ? p.num_blocks : 0x7fffffff);
+                }
+                // claim the next ticket while the last few stages of this cell stream
+                if (C.NT > 0 && !claimed && e - u <= 2) {
+                    if (lane == 0)
+                        claim = int(atomicAdd(p.ws + kWsTicket, 1u));
+                    claimed = true;
+                }
+                if (issued >= uint32_t(p.nst)) {
+                    int w_ok = 1;
+                    if (lane == 0)
+                        w_ok = mbar_wait(smem_u32(&sm.empty[st]), phase ^ 1u, kWaitLimitNs);
+                    w_ok = __shfl_sync(FULLMASK, w_ok, 0);
+                    if (!w_ok) {
+                        ok = false;
+                        break;
+                    }
+                }
+                const bool first = (u == a) || (b == 0);
+                if (first)
+                    seg_b0 = b;
+                const bool last = (u == e - 1) || (b == nb - 1);
+                int flags = (first ? F_FIRST : 0) | (last ? F_LAST : 0);
+                if (last && seg_b0 == 0 && b == nb - 1)
+                    flags |= F_DIRECT;
+                if (lane == 0) {
+                    StageHdr *h = &sm.hdr[st];
+                    h->s = s;
+                    h->b = b;
+                    h->T = T;
+                    h->hg = hg;
+                    h->flags = flags;
+                    h->slot = cell_first ? 0 : 1;  // 0: the segment opens the cell
+                    h->cell = int(cell);
+                    h->fs = int(fs);
+                    const uint32_t bar = smem_u32(&sm.full[st]);
+                    mbar_arrive_expect_tx(bar, uint32_t(p.stage_bytes));
+                    const uint32_t kdst = smem_u32(sm.stages + size_t(st) * p.stage_bytes);
+                    const uint32_t vdst = kdst + uint32_t(p.HG * NH * kTileBytes);
+                    const int h0 = hg * p.HG;
+                    if (p.whole_box) {
+                        // map dims (d, token, half, head, block): one box = HG heads x 16 rows
+                        tma_load_5d_hint(kdst, kmap, bar, 0, 0, 0, h0, phys, pol);
+                        tma_load_5d_hint(vdst, vmap, bar, 0, 0, 0, h0, phys, pol);
+                    } else {
+                        // map dims (d, half, head, token, block): one box = one (head, half) tile
+                        for (int hl = 0; hl < p.HG; ++hl) {
 #pragma unroll
-                        for (int hf = 0; hf < NH; ++hf) {
-                            const uint32_t off = uint32_t((hl * NH + hf) * kTileBytes);
-                            tma_load_5d_hint(kdst + off, kmap, bar, 0, hf, h0 + hl, 0, phys, pol);
-                            tma_load_5d_hint(vdst + off, vmap, bar, 0, hf, h0 + hl, 0, phys, pol);
+                            for (int hf = 0; hf < NH; ++hf) {
+                                const uint32_t off = uint32_t((hl * NH + hf) * kTileBytes);
+                                tma_load_5d_hint(kdst + off, kmap, bar, 0, hf, h0 + hl, 0, phys,
+                                                 pol);
+                                tma_load_5d_hint(vdst + off, vmap, bar, 0, hf, h0 + hl, 0, phys,
+                                                 pol);
+                            }
                         }
                     }
+                    if (p.trace && issued == 0)
+                        p.trace[blockIdx.x * kTraceWords + 1] = global_timer_ns();
+                }
+                __syncwarp();
+                ++issued;
+                if (++st == uint32_t(p.nst)) {
+                    st = 0;
+                    phase ^= 1u;
+                }
+                if (last)
+                    cell_first = false;
+                // advance to the next unit
+                ++b;
+                if (b == nb && u + 1 < e) {
+                    do {
+                        fs += nb;
+                        if (++s == S) {
+                            s = 0;
+                            ++hg;
+                        }
+                        T = seq_tokens(p, s);
+                        nb = (T + kBlockSize - 1) / kBlockSize;
+                    } while (nb == 0);
+                    b = 0;
+                    bt_base = -(1 << 30);
                 }
             }
-            if (p.trace && lane == 0 && issued == 0)
-                p.trace[blockIdx.x * kTraceWords + 1] = global_timer_ns();
-            __syncwarp();
-            ++issued;
-            if (++st == uint32_t(p.nst)) {
-                st = 0;
-                phase ^= 1u;
-            }
-            if (last)
-                chunk_first = false;
-            // advance to the next unit
-            ++b;
-            if (b == nb && u + 1 < f1) {
-                do {
-                    if (++s == S) {
-                        s = 0;
-                        ++hg;
-                    }
-                    T = seq_tokens(p, s);
-                    nb = (T + kBlockSize - 1) / kBlockSize;
-                } while (nb == 0);
-                b = 0;
-                bt_base = -(1 << 30);
-            }
+            if (!ok)
+                break;
         }
+        // ---- the next cell: a ticket
+        if (C.NT == 0)
+            break;
+        if (!claimed && lane == 0)
+            claim = int(atomicAdd(p.ws + kWsTicket, 1u));
+        const int t = __shfl_sync(FULLMASK, claim, 0);
+        claimed = false;
+        if (t >= C.NT)
+            break;
+        cell = int64_t(C.G) + t;
     }
 
     if (ok) {
@@ -260,8 +364,15 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
             }
         }
     }
+    if (lane == 0) {
+        // the last CTA to finish claiming resets the ticket counters for the next call
+        if (atomicAdd(p.ws + kWsDone, 1u) == gridDim.x - 1) {
+            atomicExch(p.ws + kWsTicket, 0u);
+            atomicExch(p.ws + kWsDone, 0u);
+        }
+    }
     if (!ok && lane == 0) {
-        atomicOr(p.err, kErrProducerWait);
+        atomicOr(p.ws + kWsErr, kErrProducerWait);
         // wait (bounded) for every copy this warp may still have in flight
         const uint32_t n = issued < uint32_t(p.nst) ? issued : uint32_t(p.nst);
         for (uint32_t k = 0; k < n; ++k) {
@@ -276,7 +387,7 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
                 }
             }
             if (!mbar_wait(smem_u32(&sm.full[ps]), pp, kWaitLimitNs))
-                atomicOr(p.err, kErrDrainWait);
+                atomicOr(p.ws + kWsErr, kErrDrainWait);
         }
     }
 }
@@ -312,12 +423,33 @@ __device__ void consumer_warp(const DecodeParams &p, const Smem &sm, int cw, int
             jrow[n][r] = j < p.nq ? j : p.nq - 1;
         }
 
+    // running state of the current segment
+    auto reset_state = [&]() {
+#pragma unroll
+        for (int n = 0; n < NTW; ++n) {
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks)
+                qf[ks][n][0] = qf[ks][n][1] = 0u;
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                m_r[n][r] = -INFINITY;
+                l_r[n][r] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < MT; ++i)
+#pragma unroll
+            for (int n = 0; n < NTW; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    acc[i][n][e] = 0.f;
+    };
     const uint32_t stage_base = smem_u32(sm.stages);
     uint32_t st = 0, phase = 0;
     for (;;) {
         if (!mbar_wait(smem_u32(&sm.full[st]), phase, kWaitLimitNs)) {
             if (lane == 0)
-                atomicOr(p.err, kErrConsumerWait);
+                atomicOr(p.ws + kWsErr, kErrConsumerWait);
             return;
         }
         const StageHdr h = sm.hdr[st];
@@ -331,10 +463,12 @@ __device__ void consumer_warp(const DecodeParams &p, const Smem &sm, int cw, int
                 tr[6] += 1;
         }
         if (h.flags & F_END)
-            return;
+            break;
         const int kvh = h.hg * p.HG + hl;
 
         if (h.flags & F_FIRST) {
+            // a new segment: fresh running state and its query rows
+            reset_state();
 #pragma unroll
             for (int n = 0; n < NTW; ++n) {
                 const int row = (rh * NTW + n) * 8 + g;
@@ -348,24 +482,8 @@ __device__ void consumer_warp(const DecodeParams &p, const Smem &sm, int cw, int
                         qf[ks][n][0] = __ldg(qrow + ks * 8 + tq);
                         qf[ks][n][1] = __ldg(qrow + ks * 8 + 4 + tq);
                     }
-                } else {
-#pragma unroll
-                    for (int ks = 0; ks < KS; ++ks)
-                        qf[ks][n][0] = qf[ks][n][1] = 0u;
-                }
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    m_r[n][r] = -INFINITY;
-                    l_r[n][r] = 0.f;
                 }
             }
-#pragma unroll
-            for (int i = 0; i < MT; ++i)
-#pragma unroll
-                for (int n = 0; n < NTW; ++n)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        acc[i][n][e] = 0.f;
         }
 
         const uint32_t kb = stage_base + st * uint32_t(p.stage_bytes) + uint32_t(hl * NH * kTileBytes);
@@ -561,7 +679,8 @@ __device__ void consumer_warp(const DecodeParams &p, const Smem &sm, int cw, int
                         }
                     }
             } else {
-                const int64_t cell = (int64_t(blockIdx.x) * 2 + h.slot) * p.HG + hl;
+                // partial of this cell; then arrive, and merge if the sequence is complete
+                const int64_t cellbase = (int64_t(h.cell) * 2 + h.slot) * p.HG + hl;
 #pragma unroll
                 for (int n = 0; n < NTW; ++n)
 #pragma unroll
@@ -569,14 +688,14 @@ __device__ void consumer_warp(const DecodeParams &p, const Smem &sm, int cw, int
                         const int row = (rh * NTW + n) * 8 + 2 * tq + r;
                         if (row >= p.rows)
                             continue;
-                        float *pa = p.part + (cell * p.rows_pad + row) * D;
+                        float *pa = p.part + (cellbase * p.rows + row) * D;
 #pragma unroll
                         for (int i = 0; i < MT; ++i) {
                             pa[16 * i + g] = acc[i][n][r];
                             pa[16 * i + 8 + g] = acc[i][n][r + 2];
                         }
                         if (g == 0) {
-                            float *ml = p.ml + (cell * p.rows_pad + row) * 2;
+                            float *ml = p.ml + (cellbase * p.rows + row) * 2;
                             ml[0] = m_r[n][r];
                             ml[1] = lf[n][r];
                         }
@@ -584,6 +703,7 @@ __device__ void consumer_warp(const DecodeParams &p, const Smem &sm, int cw, int
             }
         }
     }
+
 }
 
 template <int D, int NTW, int WPH>
@@ -614,8 +734,6 @@ __global__ void __launch_bounds__(kThreadsMax, 1)
         p.trace[blockIdx.x * kTraceWords + 7] = smid;
     }
     __syncthreads();
-    // let the merge grid be scheduled now; it waits for this grid's completion
-    asm volatile("griddepcontrol.launch_dependents;");
     if (warp == 0)
         producer_warp<D>(&kmap, &vmap, p, sm, lane);
     else
@@ -623,112 +741,126 @@ __global__ void __launch_bounds__(kThreadsMax, 1)
 }
 
 // ------------------------------------------------------------------ merge
-// Combine the partial states of every sequence that a chunk boundary split:
-// M = max m_c, L = sum l_c 2^(m_c - M), out = sum acc_c 2^(m_c - M) / L
-// ("07 -- Inference" section 5.3; m is kept in the log2 domain). Sequences
-// with no token write zeros.
-//
-// One warp per output row (sequence, head group, kv head, query row); lane i
-// owns head dims 4i..4i+3. Launched as a programmatic dependent of the main
-// kernel: it is scheduled while that kernel runs and waits (griddepcontrol)
-// for it to finish before reading the workspace.
+// Combine the partials of every sequence that cell boundaries split:
+// M = max m_k, L = sum l_k 2^(m_k - M), out = sum acc_k 2^(m_k - M) / L
+// over the cells k the sequence spans ("07 -- Inference" section 5.3; m in the
+// log2 domain), folded in groups of CG cells with the same rescaling rule.
+// Sequences with no token get zeros. One CTA per (sequence, head group); a
+// warp takes RPW output rows at a time, lane i dims 4i..4i+3, and issues all
+// loads of a group (m, l, acc of RPW rows x CG cells) before using any, so a
+// group costs one memory round trip. Launched as a programmatic dependent of
+// the main kernel: it waits (griddepcontrol) for it to finish.
+template <int D>
 __global__ void __launch_bounds__(256)
-    paged_decode_merge_kernel(const DecodeParams p, int D, int grid)
+    paged_decode_merge_kernel(const DecodeParams p, int grid)
 {
+    constexpr int RPW = 4, CG = 4;
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int64_t wid = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    const int64_t total = int64_t(p.S) * p.n_hg * p.HG * p.rows;
-    if (wid >= total)
-        return;
-    int64_t w = wid;
-    const int row = int(w % p.rows);
-    w /= p.rows;
-    const int hl = int(w % p.HG);
-    w /= p.HG;
-    const int hg = int(w % p.n_hg);
-    const int s = int(w / p.n_hg);
-
-    const int j = row / p.G, gq = row - j * p.G;
-    const int kvh = hg * p.HG + hl;
-    const int64_t o = ((int64_t(s) * p.nq + j) * p.Hq + int64_t(kvh) * p.G + gq) * D;
+    const int s = blockIdx.x, hg = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    const int nb_total = __ldcg(p.seq_start + p.S);
+    const Cells C = make_cells(p, nb_total, grid);
+    const int64_t fs = int64_t(hg) * nb_total + __ldcg(p.seq_start + s);
+    const int64_t fe = int64_t(hg) * nb_total + __ldcg(p.seq_start + s + 1);
+    const int nrows = p.HG * p.rows;  // output rows of this (sequence, head group)
     const bool has_d = lane * 4 < D;
 
-    auto store4 = [&](float4 v) {
-        if (!has_d)
-            return;
+    auto out_offset = [&](int r) -> int64_t {  // r = hl * rows + row
+        const int hl = r / p.rows, row = r - hl * p.rows;
+        const int j = row / p.G, gq = row - j * p.G;
+        return ((int64_t(s) * p.nq + j) * p.Hq + int64_t(hg * p.HG + hl) * p.G + gq) * D +
+               lane * 4;
+    };
+    auto store = [&](int64_t o, float4 v) {
         if (p.out_f32) {
-            *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + o + lane * 4) = v;
+            *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + o) = v;
         } else {
-            __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
-            __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+            __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
             uint2 u;
-            u.x = *reinterpret_cast<uint32_t *>(&a);
-            u.y = *reinterpret_cast<uint32_t *>(&b);
-            *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.out) + o + lane * 4) = u;
+            u.x = *reinterpret_cast<uint32_t *>(&lo);
+            u.y = *reinterpret_cast<uint32_t *>(&hi);
+            *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.out) + o) = u;
         }
     };
 
-    const int nb_total = p.seq_start[p.S];
-    const int64_t F = int64_t(p.n_hg) * nb_total;
-    const int64_t fs = int64_t(hg) * nb_total + p.seq_start[s];
-    const int64_t fe = int64_t(hg) * nb_total + p.seq_start[s + 1];
-    if (fe == fs) {
-        store4(make_float4(0.f, 0.f, 0.f, 0.f));
+    if (fe == fs) {  // no token: zeros
+        for (int r = warp; r < nrows; r += nwarps)
+            if (has_d)
+                store(out_offset(r), make_float4(0.f, 0.f, 0.f, 0.f));
         return;
     }
-    // chunk c covers [c*F/grid, (c+1)*F/grid); chunk_of(f) = ceil((f+1)*grid/F) - 1
-    const int64_t cb = ((fs + 1) * grid + F - 1) / F - 1;
-    const int64_t ce = (fe * grid + F - 1) / F - 1;
-    if (cb == ce)
+    const int64_t kb = C.cell_of(fs), ke = C.cell_of(fe - 1);
+    if (kb == ke)
         return;  // finished in place by the main kernel
-    const bool cb_first = (cb * F / grid) == fs;  // the sequence opens chunk cb
 
-    // With fewer units than CTAs some chunks are empty; they hold no partial.
-    auto cell_of = [&](int64_t c) -> int64_t {
-        if (c * F / grid == (c + 1) * F / grid)
-            return -1;
-        const int slot = (c == cb && !cb_first) ? 1 : 0;
-        return ((c * 2 + slot) * p.HG + hl) * p.rows_pad + row;
-    };
-
-    // M over the covering chunks, 32 chunks per round (one per lane)
-    float M = -INFINITY;
-    for (int64_t c0 = cb; c0 <= ce; c0 += 32) {
-        const int64_t c = c0 + lane;
-        if (c <= ce) {
-            const int64_t cell = cell_of(c);
-            if (cell >= 0)
-                M = fmaxf(M, p.ml[cell * 2]);
-        }
-    }
+    for (int r0 = warp * RPW; r0 < nrows; r0 += nwarps * RPW) {
+        float Mr[RPW], Lr[RPW];
+        float4 ar[RPW];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-
-    float L = 0.f;
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -INFINITY) {
-        for (int64_t c = cb; c <= ce; ++c) {
-            const int64_t cell = cell_of(c);
-            if (cell < 0)
-                continue;
-            const float m = p.ml[cell * 2];
-            if (m == -INFINITY)
-                continue;
-            const float f = ex2(m - M);
-            L += p.ml[cell * 2 + 1] * f;
-            if (has_d) {
-                const float4 v = *reinterpret_cast<const float4 *>(p.part + cell * D + lane * 4);
-                a.x += v.x * f;
-                a.y += v.y * f;
-                a.z += v.z * f;
-                a.w += v.w * f;
+        for (int i = 0; i < RPW; ++i) {
+            Mr[i] = -INFINITY;
+            Lr[i] = 0.f;
+            ar[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        for (int64_t k0 = kb; k0 <= ke; k0 += CG) {
+            float mc[CG][RPW], lc[CG][RPW];
+            float4 vc[CG][RPW];
+#pragma unroll
+            for (int c = 0; c < CG; ++c) {
+                const int64_t k = k0 + c;
+                int64_t cb = -1;  // (cell, slot) base index
+                if (k <= ke && !C.empty(k))
+                    cb = (k * 2 + (C.start(k) >= fs ? 0 : 1)) * p.HG;
+#pragma unroll
+                for (int i = 0; i < RPW; ++i) {
+                    const int r = r0 + i;
+                    const bool ok = cb >= 0 && r < nrows;
+                    const int64_t idx = cb * p.rows + r;  // (cell, slot, hl, row)
+                    mc[c][i] = ok ? __ldcg(p.ml + idx * 2) : -INFINITY;
+                    lc[c][i] = ok ? __ldcg(p.ml + idx * 2 + 1) : 0.f;
+                    vc[c][i] = (ok && has_d)
+                                   ? __ldcg(reinterpret_cast<const float4 *>(p.part + idx * D) + lane)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < RPW; ++i) {
+                float gm = Mr[i];
+#pragma unroll
+                for (int c = 0; c < CG; ++c)
+                    gm = fmaxf(gm, mc[c][i]);
+                if (gm == -INFINITY)
+                    continue;  // nothing seen yet for this row
+                const float so = ex2(Mr[i] - gm);  // 0 while Mr is -inf
+                Lr[i] *= so;
+                ar[i].x *= so;
+                ar[i].y *= so;
+                ar[i].z *= so;
+                ar[i].w *= so;
+#pragma unroll
+                for (int c = 0; c < CG; ++c) {
+                    const float f = ex2(mc[c][i] - gm);  // 0 for an absent cell
+                    Lr[i] += lc[c][i] * f;
+                    ar[i].x += vc[c][i].x * f;
+                    ar[i].y += vc[c][i].y * f;
+                    ar[i].z += vc[c][i].z * f;
+                    ar[i].w += vc[c][i].w * f;
+                }
+                Mr[i] = gm;
             }
         }
+        if (!has_d)
+            continue;
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) {
+            if (r0 + i >= nrows)
+                break;
+            const float inv = Lr[i] > 0.f ? 1.f / Lr[i] : 0.f;
+            store(out_offset(r0 + i),
+                  make_float4(ar[i].x * inv, ar[i].y * inv, ar[i].z * inv, ar[i].w * inv));
+        }
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    store4(make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv));
 }
 
 // ------------------------------------------------------------------ host side
@@ -767,23 +899,25 @@ int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int 
     P.threads = 32 * (1 + P.HG * P.wph);
     P.stage_bytes = 2 * P.HG * (D / 64) * kTileBytes;
     const int per_stage = P.stage_bytes + int(sizeof(StageHdr)) + 16;
-    int max_st = (smem_optin - 1024) / per_stage;
+    const int fixed = 1024 + int(sizeof(Cells)) + 64;
+    int max_st = (smem_optin - fixed) / per_stage;
     if (max_st > 8)
         max_st = 8;
     if (max_st < 2)
         return -1;
     P.nst = opt_stages > 0 ? std::min(std::max(opt_stages, 2), max_st) : max_st;
-    P.smem = 1024 + size_t(P.nst) * per_stage;
+    P.smem = size_t(fixed) + size_t(P.nst) * per_stage;
     const int grid_cap = opt_ctas > 0 ? opt_ctas : num_sms;
-    if (grid_cap < 1)
+    if (grid_cap < 1 || grid_cap > 16384)
         return -1;
     const int64_t f_max = int64_t(P.n_hg) * S * MB;
     P.grid = int(std::min<int64_t>(grid_cap, f_max));
-    P.off_seq = 256;
+    P.tickets_max = 0;
+    const size_t cells = size_t(grid_cap) + size_t(P.tickets_max);
+    P.off_seq = kWsHeaderBytes;
     P.off_ml = P.off_seq + round_up(size_t(S + 1) * 4, 256);
-    const size_t cells = size_t(grid_cap) * 2 * P.HG * P.rows_pad;
-    P.off_part = P.off_ml + round_up(cells * 2 * 4, 256);
-    P.ws_bytes = P.off_part + round_up(cells * size_t(D) * 4, 256);
+    P.off_part = P.off_ml + round_up(cells * 2 * P.HG * P.rows * 2 * 4, 256);
+    P.ws_bytes = P.off_part + round_up(cells * 2 * P.HG * P.rows * size_t(D) * 4, 256);
     *pl = P;
     return 0;
 }
@@ -807,41 +941,35 @@ static cudaError_t launch_one(const DecodePlan &pl, const DecodeParams &p, const
     }
     if (ev_before && (e = cudaEventRecord(ev_before, stream)) != cudaSuccess)
         return e;
-    {
-        // programmatic serialization: the kernel's prologue may overlap the tail
-        // of the previous kernel; it waits (griddepcontrol.wait) before any read
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(unsigned(pl.grid));
-        cfg.blockDim = dim3(unsigned(pl.threads));
-        cfg.dynamicSmemBytes = pl.smem;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, kern, kmap, vmap, p);
-        if (e != cudaSuccess)
-            return e;
-    }
-    e = cudaGetLastError();
-    if (e != cudaSuccess)
-        return e;
-    if (ev_after && (e = cudaEventRecord(ev_after, stream)) != cudaSuccess)
-        return e;
-    // merge: one warp per output row, launched as a programmatic dependent
-    const int64_t warps = int64_t(p.S) * p.n_hg * p.HG * p.rows;
+    // programmatic serialization: the kernel's prologue may overlap the tail of
+    // the previous kernel; it waits (griddepcontrol.wait) before any read
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned((warps + 7) / 8));
-    cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = 0;
+    cfg.gridDim = dim3(unsigned(pl.grid));
+    cfg.blockDim = dim3(unsigned(pl.threads));
+    cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, paged_decode_merge_kernel, p, int(D), int(pl.grid));
+    e = cudaLaunchKernelEx(&cfg, kern, kmap, vmap, p);
+    if (e != cudaSuccess)
+        return e;
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    if (ev_after && (e = cudaEventRecord(ev_after, stream)) != cudaSuccess)
+        return e;
+    // the merge: one CTA per (sequence, head group), a programmatic dependent
+    cudaLaunchConfig_t mcfg = {};
+    mcfg.gridDim = dim3(unsigned(p.S), unsigned(p.n_hg));
+    mcfg.blockDim = dim3(256);
+    mcfg.dynamicSmemBytes = 0;
+    mcfg.stream = stream;
+    mcfg.attrs = attr;
+    mcfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&mcfg, paged_decode_merge_kernel<D>, p, int(pl.grid));
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();

@@ -12,11 +12,13 @@ constexpr int kBlockSize = 16;          // tokens per physical block
 constexpr int kTileBytes = 16 * 128;    // one (head, 64-column half) tile: 16 rows x 128 B
 constexpr int kMaxRows = 32;            // query rows per kv head: G * n_query_per_seq
 constexpr int kMaxConsumerWarps = 8;
+// warp 0 produces, warps 1..ncw consume
 constexpr int kThreadsMax = 32 * (1 + kMaxConsumerWarps);
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded waits: 2 s
 // per-CTA trace words: entry, first TMA issued, first stage consumed, last TMA
-// issued, last stage consumed (ns, %globaltimer), units, segments, SM id
-constexpr int kTraceWords = 8;
+// issued, last stage consumed (ns, %globaltimer), units, segments, SM id,
+// 8 spare
+constexpr int kTraceWords = 16;
 
 // device error word codes (workspace offset 0)
 enum : uint32_t {
@@ -41,35 +43,45 @@ struct DecodePlan {
     int nst;         // pipeline stages
     int whole_box;   // 1: one TMA box per block for K (and V) of all HG heads
     int grid;        // persistent CTAs
+    int tickets_max; // cap on dynamically claimed tickets (0: static chunks only)
     size_t smem;     // dynamic shared memory bytes
     // workspace layout (byte offsets)
     size_t off_seq, off_ml, off_part, ws_bytes;
 };
 
+// Workspace header words (uint32 at byte offset 4*i).
+enum { kWsErr = 0, kWsTicket = 2, kWsDone = 3, kWsHeaderBytes = 256 };
 struct DecodeParams {
     const uint16_t *q;
     void *out;
     const int32_t *block_tables;
     const int32_t *context_lens;
-    int32_t *seq_start;    // workspace: [S + 1] block prefix sums (written by CTA 0)
-    float *ml;             // workspace: [grid][2][HG][rows_pad][2]  (m, l)
-    float *part;           // workspace: [grid][2][HG][rows_pad][D]  unnormalised acc
-    uint32_t *err;         // workspace word 0
+    uint32_t *ws;          // workspace header: error word, ticket and done counters
+    int32_t *seq_start;    // [S + 1] block prefix sums (written by CTA 0 for the merge)
+    float *ml;             // [cells][2][HG][rows] (m, l) partial states
+    float *part;           // [cells][2][HG][rows][D] unnormalised partial acc
     uint64_t *trace;       // optional per-CTA timeline [grid][kTraceWords] (null: off)
     int64_t num_blocks;
     int S, MB, nq, Hq, Hkv, G, rows, rows_pad, HG, n_hg, out_f32;
     int stage_bytes, nst;
     int whole_box;         // 1: the tensor maps box a whole block (HG heads) at once
+    int ncw;               // consumer warps per CTA (HG * wph)
+    int tickets_max;       // dynamic tickets: at most this many (0: none)
+    int ticket_div;        // the last F / ticket_div units go to tickets
+    int ticket_units;      // at least this many units per ticket
     float scale_log2;      // scale * log2(e)
 };
 
 int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int opt_ctas,
                 int opt_stages, int opt_heads, int smem_optin, DecodePlan *plan);
 
-// ev_before/ev_after (may be null) are recorded around the main kernel only.
+// ev_before/ev_after (may be null) are recorded around the kernel.
 cudaError_t launch_decode(const DecodePlan &plan, const DecodeParams &p, const CUtensorMap &kmap,
                           const CUtensorMap &vmap, cudaStream_t stream, cudaEvent_t ev_before,
                           cudaEvent_t ev_after);
+
+size_t workspace_zero_prefix(int32_t num_seqs, int32_t n_query_per_seq, int32_t num_q_heads,
+                             int32_t num_kv_heads, int32_t head_dim);
 
 cudaError_t launch_kv_append(const void *k_new, const void *v_new, const int64_t *slot_mapping,
                              int64_t n_new, void *k_cache, void *v_cache, int64_t num_blocks,

@@ -78,9 +78,13 @@ extern "C" pkv_status pkv_paged_decode_attention_static(
     void *scratch = static_scratch_address();
     if (scratch == nullptr)
         return PKV_ERR_CUDA;
-    // Only the 4-byte device error word must start at zero; every other byte of
-    // the scratch is written by the kernels before it is read.
-    if (cudaMemsetAsync(scratch, 0, 4, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    // The header (device error word, work counters) must start at zero; every
+    // other byte of the scratch is written by the kernels before it is read.
+    const size_t zero = pkv::workspace_zero_prefix(num_seqs, n_query_per_seq, num_q_heads,
+                                                   num_kv_heads, head_dim);
+    if (zero == 0 || zero > kStaticScratchBytes)
+        return PKV_ERR_CUDA;
+    if (cudaMemsetAsync(scratch, 0, zero, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return PKV_ERR_CUDA;
     return pkv_paged_decode_attention(q, k_cache, v_cache, num_blocks, block_tables,
                                       max_blocks_per_seq, context_lens, num_seqs, n_query_per_seq,

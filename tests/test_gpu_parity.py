@@ -235,20 +235,25 @@ def test_named_workload_full_size(o, name):
 
 @pytest.mark.parametrize("ctas", [0, 300])
 def test_stale_workspace_is_never_read(o, ctas):
-    """Partials left by other calls (here: NaN bytes) must not reach the output,
-    with more CTAs than work units (empty chunks) and with fewer."""
+    """Partials left in the workspace by a call of another shape must not reach
+    the output, with more CTAs than work units (empty cells) and with fewer."""
     pkv.set_option(pkv.PKV_OPT_NUM_CTAS, ctas)
     T = [1, 2, 15, 16, 17, 31, 32, 33, 100, 257]
     w = W.make_custom(len(T), 1, 4, 2, 64, T, seed=90)
+    other = W.make_custom(6, 2, 16, 2, 64, [900, 3000, 70, 1200, 5, 2500], seed=93)
+    n = max(pkv.workspace_size(len(T), 1, 4, 2, 64), pkv.workspace_size(6, 2, 16, 2, 64))
+    ws = torch.zeros((n,), dtype=torch.uint8, device="cuda")
+    d0 = DeviceStep(other, torch)
+    d0.append()
+    d0.attend(ws=ws)          # leaves its partial states behind
     d = DeviceStep(w, torch)
-    ws = torch.full((pkv.workspace_size(len(T), 1, 4, 2, 64),), 0xFF, dtype=torch.uint8,
-                    device="cuda")
-    ws[:256] = 0
     d.append()
     d.attend(ws=ws)
     torch.cuda.synchronize()
     ref, _, _ = o.step(w)
     compare(to_f64(d.out), ref, what="stale workspace")
+    ref0, _, _ = o.step(other)
+    compare(to_f64(d0.out), ref0, what="first call")
     assert pkv.workspace_error(ws) == 0
 
 

@@ -55,9 +55,10 @@ def test_static_scratch_matches_workspace_entry_point(lib, name):
 
 
 def test_static_scratch_refuses_oversized_geometry(lib):
-    w = W.make_workload("tiny")
+    # 32 query rows per kv head and 1000 CTAs: ~130 MiB of split-K scratch
+    w = W.make_custom(4, 4, 64, 8, 128, [40, 50, 60, 70], seed=7)
     d = DeviceStep(w, torch)
-    prev = pkv.set_option(pkv.PKV_OPT_NUM_CTAS, 20000)   # scratch grows with the grid
+    prev = pkv.set_option(pkv.PKV_OPT_NUM_CTAS, 1000)    # scratch grows with the grid
     try:
         out = torch.zeros_like(d.out)
         assert static_call(lib, d, out) == 6             # PKV_ERR_WORKSPACE
