@@ -220,10 +220,16 @@ const char *pkv_status_string(int32_t status);
  *                        tensor map, else one per (head, 64-column half) tile
  *                        (default); 1 = always per tile; 2 = always per block
  *                        (PKV_ERR_UNSUPPORTED if the driver refuses the map).
+ *   PKV_OPT_TAIL         0 or 1 = no dynamic tail (default); n >= 2 = the last
+ *                        1/n of the work goes out as dynamically claimed
+ *                        tickets to the CTAs that finish their static share
+ *                        first. Ticket boundaries depend on the sizes only, so
+ *                        results stay deterministic.
  * All settings give the same result up to fp32 rounding order.
  * Returns the previous value, or -1 for an unknown option or an invalid value.
  */
-enum { PKV_OPT_NUM_CTAS = 1, PKV_OPT_STAGES = 2, PKV_OPT_HEADS_PER_CTA = 3, PKV_OPT_TMA_BOX = 4 };
+enum { PKV_OPT_NUM_CTAS = 1, PKV_OPT_STAGES = 2, PKV_OPT_HEADS_PER_CTA = 3, PKV_OPT_TMA_BOX = 4,
+       PKV_OPT_TAIL = 5 };
 int32_t pkv_set_option(int32_t option, int32_t value);
 
 /*

@@ -19,6 +19,7 @@ int32_t g_opt_num_ctas = 0;
 int32_t g_opt_stages = 0;
 int32_t g_opt_heads = 0;
 int32_t g_opt_box = 0;
+int32_t g_opt_tail = 0;
 cudaEvent_t g_ev_before = nullptr;
 cudaEvent_t g_ev_after = nullptr;
 void *g_trace = nullptr;
@@ -189,7 +190,7 @@ size_t workspace_zero_prefix(int32_t num_seqs, int32_t n_query_per_seq, int32_t 
         return 0;
     DecodePlan pl;
     if (plan_decode(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim, 1, d.num_sms,
-                    g_opt_num_ctas, g_opt_stages, g_opt_heads, d.smem_optin, &pl) != 0)
+                    g_opt_num_ctas, g_opt_stages, g_opt_heads, g_opt_tail, d.smem_optin, &pl) != 0)
         return 0;
     return kWsHeaderBytes;
 }
@@ -250,6 +251,10 @@ int32_t pkv_set_option(int32_t option, int32_t value)
         prev = g_opt_heads;
         g_opt_heads = value;
         return prev;
+    case PKV_OPT_TAIL:
+        prev = g_opt_tail;
+        g_opt_tail = value;
+        return prev;
     case PKV_OPT_TMA_BOX:
         if (value > 2)
             return -1;
@@ -297,7 +302,7 @@ size_t pkv_workspace_size(int32_t num_seqs, int32_t n_query_per_seq, int32_t num
         return 0;
     pkv::DecodePlan pl;
     if (pkv::plan_decode(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim, 1,
-                         d.num_sms, g_opt_num_ctas, g_opt_stages, g_opt_heads, d.smem_optin,
+                         d.num_sms, g_opt_num_ctas, g_opt_stages, g_opt_heads, g_opt_tail, d.smem_optin,
                          &pl) != 0)
         return 0;
     return pl.ws_bytes;
@@ -337,7 +342,7 @@ pkv_status pkv_paged_decode_attention(const void *q, const void *k_cache, const 
     pkv::DecodePlan pl;
     if (pkv::plan_decode(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim,
                          max_blocks_per_seq, d.num_sms, g_opt_num_ctas, g_opt_stages,
-                         g_opt_heads, d.smem_optin, &pl) != 0)
+                         g_opt_heads, g_opt_tail, d.smem_optin, &pl) != 0)
         return PKV_ERR_UNSUPPORTED;
     if (workspace_bytes < pl.ws_bytes)
         return PKV_ERR_WORKSPACE;
@@ -389,7 +394,7 @@ pkv_status pkv_paged_decode_attention(const void *q, const void *k_cache, const 
     p.whole_box = whole_box;
     p.ncw = pl.HG * pl.wph;
     p.tickets_max = pl.tickets_max;
-    p.ticket_div = 8;
+    p.ticket_div = pl.tail_div;
     p.ticket_units = 4;
     p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
     cudaError_t e = pkv::launch_decode(pl, p, kmap, vmap, static_cast<cudaStream_t>(stream),

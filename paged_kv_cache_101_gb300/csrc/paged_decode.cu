@@ -867,7 +867,7 @@ __global__ void __launch_bounds__(256)
 static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int opt_ctas,
-                int opt_stages, int opt_heads, int smem_optin, DecodePlan *pl)
+                int opt_stages, int opt_heads, int opt_tail, int smem_optin, DecodePlan *pl)
 {
     if (S < 1 || nq < 1 || Hkv < 1 || Hq % Hkv != 0 || (D != 64 && D != 128) || MB < 1)
         return -1;
@@ -912,7 +912,12 @@ int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int 
         return -1;
     const int64_t f_max = int64_t(P.n_hg) * S * MB;
     P.grid = int(std::min<int64_t>(grid_cap, f_max));
-    P.tickets_max = 0;
+    // Optional dynamic tail: the last 1/tail_div of the units go out as tickets
+    // to the CTAs that finish their chunk first (per-SM streaming rates differ
+    // by a few percent). Off by default: the extra cells cost the merge more
+    // than the balance gains. Never with many query rows per kv head.
+    P.tail_div = opt_tail <= 1 ? 0 : opt_tail;
+    P.tickets_max = (P.tail_div > 0 && P.rows <= 16) ? 2 * grid_cap : 0;
     const size_t cells = size_t(grid_cap) + size_t(P.tickets_max);
     P.off_seq = kWsHeaderBytes;
     P.off_ml = P.off_seq + round_up(size_t(S + 1) * 4, 256);

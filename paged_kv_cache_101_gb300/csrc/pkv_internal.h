@@ -44,6 +44,7 @@ struct DecodePlan {
     int whole_box;   // 1: one TMA box per block for K (and V) of all HG heads
     int grid;        // persistent CTAs
     int tickets_max; // cap on dynamically claimed tickets (0: static chunks only)
+    int tail_div;    // the last 1/tail_div of the units go out as tickets (0: none)
     size_t smem;     // dynamic shared memory bytes
     // workspace layout (byte offsets)
     size_t off_seq, off_ml, off_part, ws_bytes;
@@ -73,7 +74,7 @@ struct DecodeParams {
 };
 
 int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int opt_ctas,
-                int opt_stages, int opt_heads, int smem_optin, DecodePlan *plan);
+                int opt_stages, int opt_heads, int opt_tail, int smem_optin, DecodePlan *plan);
 
 // ev_before/ev_after (may be null) are recorded around the kernel.
 cudaError_t launch_decode(const DecodePlan &plan, const DecodeParams &p, const CUtensorMap &kmap,

@@ -23,7 +23,7 @@ def o():
 
 
 OPTIONS = (pkv.PKV_OPT_NUM_CTAS, pkv.PKV_OPT_STAGES, pkv.PKV_OPT_HEADS_PER_CTA,
-           pkv.PKV_OPT_TMA_BOX)
+           pkv.PKV_OPT_TMA_BOX, pkv.PKV_OPT_TAIL)
 
 
 @pytest.fixture(autouse=True)
@@ -273,3 +273,33 @@ def test_tma_box_modes_and_head_groups(o, box, heads):
         raise
     w = W.make_custom(4, 4, 16, 2, 64, [4, 90, 257, 31], seed=95 + heads)
     run_small(o, w)
+
+
+@pytest.mark.parametrize("tail", [1, 2, 8, 64])
+@pytest.mark.parametrize("ctas", [0, 7, 300])
+def test_dynamic_tail_tickets(o, tail, ctas):
+    """Static chunks plus dynamically claimed tickets give the definition."""
+    pkv.set_option(pkv.PKV_OPT_TAIL, tail)
+    pkv.set_option(pkv.PKV_OPT_NUM_CTAS, ctas)
+    T = [3000, 20, 2, 777, 4096, 129, 1, 16, 17, 2500]
+    w = W.make_custom(len(T), 1, 16, 4, 128, T, seed=97 + tail)
+    run_small(o, w)
+    w = W.make_custom(4, 2, 8, 1, 64, [9000, 33, 5000, 2], seed=98)
+    run_small(o, w)
+
+
+def test_tickets_repeat_deterministically(o):
+    """With tickets, repeated calls reuse the self-resetting counters and give
+    bit-identical results."""
+    T = [3000, 20, 2, 777, 4096, 129, 1, 16, 17, 2500] * 4
+    w = W.make_custom(len(T), 1, 32, 8, 128, T, seed=99)
+    d = DeviceStep(w, torch)
+    d.step()
+    first = d.out.clone()
+    for _ in range(5):
+        d.attend()
+    torch.cuda.synchronize()
+    assert torch.equal(first, d.out)
+    ref, _, _ = o.step(w)
+    compare(to_f64(d.out), ref, what="tickets repeated")
+    assert pkv.workspace_error(pkv.workspace(d.q.device, 0)) == 0
