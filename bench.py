@@ -43,7 +43,12 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM traffic (read + write bytes per launch) of the main attention kernel from
 # one ncu capture, keyed by workload; valid only while the kernel source hashes
 # to `source_sha256` (otherwise the bench reports traffic = null).
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    "llama3_8b_decode": {
+        "bytes": 582048000 + 3930112,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "7a9657a7b653b5d0973a25dc8cbd898837a06cb57b0be6b70d30d55c5e10f916",
+    },
+}
 
 
 def kernel_source_sha() -> str:
@@ -377,7 +382,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=W.WORKLOAD_ORDER)
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
