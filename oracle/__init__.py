@@ -7,7 +7,9 @@ library, and the CUDA library never imports it.
 Parity status of every function here: pinned (see the ``tests/test_oracle_*``
 files: dense library attention, block-id permutation invariance, softmax weight
 sums, shared prefix == copied prefix, closed forms, the block-table diagram of
-"07 -- Inference" section 2.2, and the merge algebra of section 5.3).
+"07 -- Inference" section 2.2, and the merge algebra of section 5.3; block copy:
+the copy-on-write worked example of "ML Interview Prep, Lesson 13" and read-back
+of every sequence's tokens through a simulated pool, in ``tests/test_block_manager_oracle.py``).
 """
 from __future__ import annotations
 
@@ -44,6 +46,8 @@ def _bind(lib):
     i32, i64 = ctypes.c_int32, ctypes.c_int64
     lib.oracle_kv_append.argtypes = [P, P, P, i64, P, P, i64, i32, i32, i32]
     lib.oracle_kv_append.restype = ctypes.c_int
+    lib.oracle_copy_blocks.argtypes = [P, P, i64, i32, i32, i32, P, P, i64]
+    lib.oracle_copy_blocks.restype = ctypes.c_int
     common = [P, P, P, i64, i32, P, i32, P, i32, i32, i32, i32, i32, ctypes.c_float]
     lib.oracle_paged_attention.argtypes = common + [P, P, i32]
     lib.oracle_paged_attention.restype = ctypes.c_int
@@ -99,6 +103,21 @@ class Oracle:
                                        _ptr(k_cache), _ptr(v_cache), NB, bs, Hkv, D)
         if st not in (0, -1):
             raise RuntimeError(f"oracle_kv_append failed: {st}")
+        return k_cache, v_cache
+
+    def copy_blocks(self, k_cache, v_cache, src, dst):
+        """Copy whole blocks src[i] -> dst[i] in (copies of) the pools, in order."""
+        k_cache = np.array(k_cache, dtype=np.uint16, copy=True, order="C")
+        v_cache = np.array(v_cache, dtype=np.uint16, copy=True, order="C")
+        NB, bs, Hkv, D = k_cache.shape
+        src = _c(src, np.int32)
+        dst = _c(dst, np.int32)
+        if src.shape != dst.shape:
+            raise ValueError("src and dst differ in length")
+        st = self.lib.oracle_copy_blocks(_ptr(k_cache), _ptr(v_cache), NB, bs, Hkv, D,
+                                         _ptr(src), _ptr(dst), src.size)
+        if st not in (0, -1):
+            raise RuntimeError(f"oracle_copy_blocks failed: {st}")
         return k_cache, v_cache
 
     def _common(self, q, k_cache, v_cache, block_tables, context_lens, nq, scale):

@@ -31,6 +31,12 @@
  *    "ML Interview Prep, Lesson 13", section 3.3). A row that sees no token
  *    (T < nq) is defined as all zeros.
  *
+ *  - Copy-on-write block copy ("ML Interview Prep, Lesson 13", section 3.5
+ *    "Sharing": before a sequence writes into a block whose reference count is
+ *    above 1 it gets a private copy): for each (src, dst) pair, in order, all
+ *    16 token rows of physical block src are copied to block dst, in K and in
+ *    V. A pair naming a block outside the pool copies nothing.
+ *
  *  - Split and merge ("07 -- Inference", section 5.3 FlashDecoding): a token
  *    range gives a partial (m, l, acc) with m = max score, l = sum exp(x - m),
  *    acc = sum exp(x - m) V; partials merge with the same rescaling rule as the
@@ -38,7 +44,9 @@
  *    so the tests can check the merge rule against it.
  *
  * Parity: pinned (dense library attention, permutation invariance, weight sums,
- * shared == copied, closed forms, the page's block-table diagram, merge algebra).
+ * shared == copied, closed forms, the page's block-table diagram, merge algebra;
+ * block copy: the copy-on-write worked example and read-back of every
+ * sequence's logical tokens through a simulated pool).
  */
 #include <math.h>
 #include <stdint.h>
@@ -78,6 +86,26 @@ int oracle_kv_append(const uint16_t *k_new, const uint16_t *v_new,
         for (int64_t e = 0; e < row; ++e) {
             k_cache[dst + e] = k_new[i * row + e];
             v_cache[dst + e] = v_new[i * row + e];
+        }
+    }
+    return bad ? -1 : 0;
+}
+
+int oracle_copy_blocks(uint16_t *k_cache, uint16_t *v_cache, int64_t num_blocks,
+                       int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                       const int32_t *src, const int32_t *dst, int64_t n_pairs)
+{
+    const int64_t blk = (int64_t)block_size * num_kv_heads * head_dim; /* elements per block */
+    int bad = 0;
+    for (int64_t i = 0; i < n_pairs; ++i) {
+        const int64_t a = src[i], b = dst[i];
+        if (a < 0 || a >= num_blocks || b < 0 || b >= num_blocks) {
+            bad = 1;
+            continue;
+        }
+        for (int64_t e = 0; e < blk; ++e) {
+            k_cache[b * blk + e] = k_cache[a * blk + e];
+            v_cache[b * blk + e] = v_cache[a * blk + e];
         }
     }
     return bad ? -1 : 0;
