@@ -45,8 +45,12 @@ FALLBACK_HBM_GBS = 6800.0
 # to `source_sha256` (otherwise the bench reports traffic = null).
 NCU_TRAFFIC = {
     "llama3_8b_decode": {
-        "bytes": 582048000 + 3930112,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "7a9657a7b653b5d0973a25dc8cbd898837a06cb57b0be6b70d30d55c5e10f916",
+        "bytes": 582002688 + 3782144,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "acaf26dc30a9fe6106b0f788f2eb288a93b71a51937f73effa1bcf73f1bd3d39",
+    },
+    "spec_verify": {
+        "bytes": 1417726000 + 5026304,
+        "source_sha256": "acaf26dc30a9fe6106b0f788f2eb288a93b71a51937f73effa1bcf73f1bd3d39",
     },
 }
 

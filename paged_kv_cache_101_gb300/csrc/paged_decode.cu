@@ -25,14 +25,20 @@
 //    tensor loads of K and V for its HG heads into a ring of shared-memory
 //    stages (128-byte swizzle, mbarrier completion with byte counts). Stages are
 //    recycled through "empty" mbarriers the consumers arrive on.
-//  * Math. One or two consumer warps per kv head. Scores S^T = K.Q^T use bf16
-//    mma.sync m16n8k16 with M = the block's 16 tokens, N = 8 query rows, K =
-//    16 head dims (fp32 accumulate). The online softmax runs on the fragments
-//    (warp shuffles across the 8 token lanes). P is split into bf16 hi + lo
-//    parts (P = hi + lo to 2^-16) and transposed in registers with movmatrix,
-//    then O^T += V^T.P^T with V^T fragments from ldmatrix.trans. Rows of a
-//    sequence's last block past T_s are masked in the scores and zeroed in the
-//    V fragments, so stale or NaN pool contents never reach the output.
+//  * Math. One or two consumer warps per kv head, bf16 mma.sync m16n8k16 with
+//    fp32 accumulation, two orientations chosen by the query rows per kv head:
+//    - up to 8 rows (one warp per head): S^T = K.Q^T with M = the block's 16
+//      tokens, N = 8 rows, K = 16 head dims, so no mma work goes to padding
+//      rows. The online softmax runs on the fragments (shuffles across the 8
+//      token lanes); P is transposed in registers with movmatrix and
+//      O^T += V^T.P^T takes V^T fragments from ldmatrix.trans.
+//    - 9 to 32 rows (16 rows per warp): S = Q.K^T with M = 16 rows, N = 8
+//      tokens, so the score fragments are the A operand of O += P.V as they
+//      stand (no transposes), row reductions take two shuffles and outputs
+//      leave as pairs.
+//    In both, P is split into bf16 hi + lo parts (P = hi + lo to 2^-16). Rows
+//    of a sequence's last block past T_s are masked in the scores and zeroed
+//    in the V fragments, so stale or NaN pool contents never reach the output.
 //  * Safety. Every mbarrier wait is bounded (2 s of %globaltimer); on timeout
 //    the warp records a code in the workspace error word and unwinds; the
 //    producer waits (bounded) for its own TMA copies before leaving. TMA reads
@@ -392,15 +398,18 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
     }
 }
 
-// ------------------------------------------------------------------ consumer
-template <int D, int NTW, int WPH>
-__device__ void consumer_warp(const DecodeParams &p, const Smem &sm, int cw, int lane)
+// ------------------------------------------------------------------ consumers
+// Consumer for warps that own at most 8 query rows (G*nq <= 8): scores in the
+// tokens x rows orientation (M = the block's 16 tokens, N = 8 rows, K = 16
+// dims), so a single n-tile covers the rows and no mma work is spent on
+// padding rows; lane holds rows 2tq, 2tq+1.
+template <int D>
+__device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, int lane)
 {
     constexpr int NH = D / 64;  // 64-column halves per head row
     constexpr int KS = D / 16;  // k-steps of the score mma
     constexpr int MT = D / 16;  // 16-dim m-tiles of the PV mma
-    const int hl = cw / WPH;    // kv head within the group
-    const int rh = cw % WPH;    // which n-tiles of the head's rows
+    const int hl = cw;          // kv head within the group (one warp per head)
     const int g = lane >> 2, tq = lane & 3;
 
     // ldmatrix row addresses inside a (head, half) tile: [16 tokens][8 x 16 B], 128B swizzle
@@ -410,39 +419,31 @@ __device__ void consumer_warp(const DecodeParams &p, const Smem &sm, int cw, int
     const int v_cadd = (lane >> 3) & 1;
     const int sw = lane & 7;  // == k_tok & 7 == v_tok & 7
 
-    float acc[MT][NTW][4];
-    uint32_t qf[KS][NTW][2];
-    float m_r[NTW][2], l_r[NTW][2];
-    int jrow[NTW][2];  // query index j of this lane's two score rows per n-tile
+    float acc[MT][4];
+    uint32_t qf[KS][2];
+    float m_r[2], l_r[2];
+    int jrow[2];  // query index j of this lane's two score rows
 #pragma unroll
-    for (int n = 0; n < NTW; ++n)
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int row = (rh * NTW + n) * 8 + 2 * tq + r;
-            const int j = row / p.G;
-            jrow[n][r] = j < p.nq ? j : p.nq - 1;
-        }
+    for (int r = 0; r < 2; ++r) {
+        const int j = (2 * tq + r) / p.G;
+        jrow[r] = j < p.nq ? j : p.nq - 1;
+    }
 
     // running state of the current segment
     auto reset_state = [&]() {
 #pragma unroll
-        for (int n = 0; n < NTW; ++n) {
+        for (int ks = 0; ks < KS; ++ks)
+            qf[ks][0] = qf[ks][1] = 0u;
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks)
-                qf[ks][n][0] = qf[ks][n][1] = 0u;
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                m_r[n][r] = -INFINITY;
-                l_r[n][r] = 0.f;
-            }
+        for (int r = 0; r < 2; ++r) {
+            m_r[r] = -INFINITY;
+            l_r[r] = 0.f;
         }
 #pragma unroll
         for (int i = 0; i < MT; ++i)
 #pragma unroll
-            for (int n = 0; n < NTW; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    acc[i][n][e] = 0.f;
+            for (int e = 0; e < 4; ++e)
+                acc[i][e] = 0.f;
     };
     const uint32_t stage_base = smem_u32(sm.stages);
     uint32_t st = 0, phase = 0;
@@ -469,19 +470,15 @@ __device__ void consumer_warp(const DecodeParams &p, const Smem &sm, int cw, int
         if (h.flags & F_FIRST) {
             // a new segment: fresh running state and its query rows
             reset_state();
+            if (g < p.rows) {
+                const int j = g / p.G;
+                const int gq = g - j * p.G;
+                const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+                    p.q + ((int64_t(h.s) * p.nq + j) * p.Hq + int64_t(kvh) * p.G + gq) * D);
 #pragma unroll
-            for (int n = 0; n < NTW; ++n) {
-                const int row = (rh * NTW + n) * 8 + g;
-                if (row < p.rows) {
-                    const int j = row / p.G;
-                    const int gq = row - j * p.G;
-                    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-                        p.q + ((int64_t(h.s) * p.nq + j) * p.Hq + int64_t(kvh) * p.G + gq) * D);
-#pragma unroll
-                    for (int ks = 0; ks < KS; ++ks) {
-                        qf[ks][n][0] = __ldg(qrow + ks * 8 + tq);
-                        qf[ks][n][1] = __ldg(qrow + ks * 8 + 4 + tq);
-                    }
+                for (int ks = 0; ks < KS; ++ks) {
+                    qf[ks][0] = __ldg(qrow + ks * 8 + tq);
+                    qf[ks][1] = __ldg(qrow + ks * 8 + 4 + tq);
                 }
             }
         }
@@ -491,12 +488,10 @@ __device__ void consumer_warp(const DecodeParams &p, const Smem &sm, int cw, int
 
         // ---- scores S^T[token][row] for the block's 16 tokens (two accumulation
         //      chains, even and odd k-steps, to halve the dependent-mma latency)
-        float sc[NTW][4], sc2[NTW][4];
+        float sc[4], sc2[4];
 #pragma unroll
-        for (int n = 0; n < NTW; ++n)
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                sc[n][e] = sc2[n][e] = 0.f;
+        for (int e = 0; e < 4; ++e)
+            sc[e] = sc2[e] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
             const int chunk = 2 * ks + k_cadd;
@@ -504,100 +499,82 @@ __device__ void consumer_warp(const DecodeParams &p, const Smem &sm, int cw, int
                                                 (((chunk & 7) ^ sw) << 4));
             uint32_t a[4];
             ldsm_x4(addr, a);
-#pragma unroll
-            for (int n = 0; n < NTW; ++n) {
-                if (ks & 1)
-                    mma_bf16_16816(sc2[n], a, qf[ks][n][0], qf[ks][n][1]);
-                else
-                    mma_bf16_16816(sc[n], a, qf[ks][n][0], qf[ks][n][1]);
-            }
+            if (ks & 1)
+                mma_bf16_16816(sc2, a, qf[ks][0], qf[ks][1]);
+            else
+                mma_bf16_16816(sc, a, qf[ks][0], qf[ks][1]);
         }
 #pragma unroll
-        for (int n = 0; n < NTW; ++n)
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                sc[n][e] += sc2[n][e];
+        for (int e = 0; e < 4; ++e)
+            sc[e] += sc2[e];
 
         // ---- scale (log2 domain) and causal / tail mask
         const int t0 = h.b * kBlockSize;
         const bool need_mask = (t0 + kBlockSize - 1) > (h.T - p.nq);
 #pragma unroll
-        for (int n = 0; n < NTW; ++n)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float x = sc[n][e] * p.scale_log2;
-                if (need_mask) {
-                    const int tok = t0 + g + ((e >> 1) << 3);
-                    const int lim = h.T - p.nq + jrow[n][e & 1];
-                    x = tok > lim ? -INFINITY : x;
-                }
-                sc[n][e] = x;
+        for (int e = 0; e < 4; ++e) {
+            float x = sc[e] * p.scale_log2;
+            if (need_mask) {
+                const int tok = t0 + g + ((e >> 1) << 3);
+                const int lim = h.T - p.nq + jrow[e & 1];
+                x = tok > lim ? -INFINITY : x;
             }
+            sc[e] = x;
+        }
 
-        // ---- online softmax (rows 2tq, 2tq+1 of each n-tile live in this lane).
-        //      The accumulator is rescaled only when some row's running max grew
+        // ---- online softmax (rows 2tq, 2tq+1 live in this lane). The
+        //      accumulator is rescaled only when some row's running max grew
         //      (otherwise every factor would be exactly 1).
-        float bmax[NTW][2];
+        float bmax[2];
         bool grew = false;
 #pragma unroll
-        for (int n = 0; n < NTW; ++n)
+        for (int r = 0; r < 2; ++r) {
+            float bm = fmaxf(sc[r], sc[r + 2]);
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+            bmax[r] = bm;
+            grew |= bm > m_r[r];
+        }
+        if (__any_sync(0xffffffffu, grew)) {
+            float corr[2];
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                float bm = fmaxf(sc[n][r], sc[n][r + 2]);
-                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
-                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
-                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
-                bmax[n][r] = bm;
-                grew |= bm > m_r[n][r];
+                const float mn = fmaxf(m_r[r], bmax[r]);
+                const float mu = (mn == -INFINITY) ? 0.f : mn;
+                corr[r] = ex2(m_r[r] - mu);
+                m_r[r] = mn;
+                l_r[r] *= corr[r];
             }
-        if (__any_sync(0xffffffffu, grew)) {
-            float corr[NTW][2];
 #pragma unroll
-            for (int n = 0; n < NTW; ++n)
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    const float mn = fmaxf(m_r[n][r], bmax[n][r]);
-                    const float mu = (mn == -INFINITY) ? 0.f : mn;
-                    corr[n][r] = ex2(m_r[n][r] - mu);
-                    m_r[n][r] = mn;
-                    l_r[n][r] *= corr[n][r];
-                }
-#pragma unroll
-            for (int i = 0; i < MT; ++i)
-#pragma unroll
-                for (int n = 0; n < NTW; ++n) {
-                    acc[i][n][0] *= corr[n][0];
-                    acc[i][n][1] *= corr[n][1];
-                    acc[i][n][2] *= corr[n][0];
-                    acc[i][n][3] *= corr[n][1];
-                }
+            for (int i = 0; i < MT; ++i) {
+                acc[i][0] *= corr[0];
+                acc[i][1] *= corr[1];
+                acc[i][2] *= corr[0];
+                acc[i][3] *= corr[1];
+            }
         }
 #pragma unroll
-        for (int n = 0; n < NTW; ++n)
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const float mu = (m_r[n][r] == -INFINITY) ? 0.f : m_r[n][r];
-                const float p0 = ex2(sc[n][r] - mu);
-                const float p1 = ex2(sc[n][r + 2] - mu);
-                l_r[n][r] += p0 + p1;
-                sc[n][r] = p0;
-                sc[n][r + 2] = p1;
-            }
+        for (int r = 0; r < 2; ++r) {
+            const float mu = (m_r[r] == -INFINITY) ? 0.f : m_r[r];
+            const float p0 = ex2(sc[r] - mu);
+            const float p1 = ex2(sc[r + 2] - mu);
+            l_r[r] += p0 + p1;
+            sc[r] = p0;
+            sc[r + 2] = p1;
+        }
 
         // ---- P = hi + lo (bf16 each), transposed into mma B fragments
-        uint32_t bh[NTW][2], bl[NTW][2];
-#pragma unroll
-        for (int n = 0; n < NTW; ++n) {
-            const uint32_t h01 = pack_bf16x2(sc[n][0], sc[n][1]);
-            const uint32_t h23 = pack_bf16x2(sc[n][2], sc[n][3]);
-            const uint32_t l01 =
-                pack_bf16x2(sc[n][0] - bf16lo_f32(h01), sc[n][1] - bf16hi_f32(h01));
-            const uint32_t l23 =
-                pack_bf16x2(sc[n][2] - bf16lo_f32(h23), sc[n][3] - bf16hi_f32(h23));
-            bh[n][0] = movmatrix_trans(h01);
-            bh[n][1] = movmatrix_trans(h23);
-            bl[n][0] = movmatrix_trans(l01);
-            bl[n][1] = movmatrix_trans(l23);
+        uint32_t bh[2], bl[2];
+        {
+            const uint32_t h01 = pack_bf16x2(sc[0], sc[1]);
+            const uint32_t h23 = pack_bf16x2(sc[2], sc[3]);
+            const uint32_t l01 = pack_bf16x2(sc[0] - bf16lo_f32(h01), sc[1] - bf16hi_f32(h01));
+            const uint32_t l23 = pack_bf16x2(sc[2] - bf16lo_f32(h23), sc[3] - bf16hi_f32(h23));
+            bh[0] = movmatrix_trans(h01);
+            bh[1] = movmatrix_trans(h23);
+            bl[0] = movmatrix_trans(l01);
+            bl[1] = movmatrix_trans(l23);
         }
 
         // ---- V rows past the context (stale or NaN slots) are zeroed
@@ -621,11 +598,8 @@ __device__ void consumer_warp(const DecodeParams &p, const Smem &sm, int cw, int
             a[1] &= mlo;
             a[2] &= mhi;
             a[3] &= mhi;
-#pragma unroll
-            for (int n = 0; n < NTW; ++n) {
-                mma_bf16_16816(acc[i][n], a, bh[n][0], bh[n][1]);
-                mma_bf16_16816(acc[i][n], a, bl[n][0], bl[n][1]);
-            }
+            mma_bf16_16816(acc[i], a, bh[0], bh[1]);
+            mma_bf16_16816(acc[i], a, bl[0], bl[1]);
         }
 
         // the stage's shared memory is no longer needed: hand it back
@@ -639,71 +613,353 @@ __device__ void consumer_warp(const DecodeParams &p, const Smem &sm, int cw, int
 
         if (h.flags & F_LAST) {
             // ---- finish the segment: full row sums, then output or partial
-            float lf[NTW][2];
+            float lf[2];
 #pragma unroll
-            for (int n = 0; n < NTW; ++n)
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    float v = l_r[n][r];
-                    v += __shfl_xor_sync(0xffffffffu, v, 4);
-                    v += __shfl_xor_sync(0xffffffffu, v, 8);
-                    v += __shfl_xor_sync(0xffffffffu, v, 16);
-                    lf[n][r] = v;
-                }
+            for (int r = 0; r < 2; ++r) {
+                float v = l_r[r];
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                v += __shfl_xor_sync(0xffffffffu, v, 8);
+                v += __shfl_xor_sync(0xffffffffu, v, 16);
+                lf[r] = v;
+            }
             if (h.flags & F_DIRECT) {
 #pragma unroll
-                for (int n = 0; n < NTW; ++n)
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        const int row = (rh * NTW + n) * 8 + 2 * tq + r;
-                        if (row >= p.rows)
-                            continue;
-                        const int j = row / p.G;
-                        const int gq = row - j * p.G;
-                        const int64_t o = ((int64_t(h.s) * p.nq + j) * p.Hq + int64_t(kvh) * p.G + gq) * D;
-                        const float inv = lf[n][r] > 0.f ? 1.f / lf[n][r] : 0.f;
-                        if (p.out_f32) {
-                            float *out = static_cast<float *>(p.out) + o;
-#pragma unroll
-                            for (int i = 0; i < MT; ++i) {
-                                out[16 * i + g] = acc[i][n][r] * inv;
-                                out[16 * i + 8 + g] = acc[i][n][r + 2] * inv;
-                            }
-                        } else {
-                            __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out) + o;
-#pragma unroll
-                            for (int i = 0; i < MT; ++i) {
-                                out[16 * i + g] = __float2bfloat16_rn(acc[i][n][r] * inv);
-                                out[16 * i + 8 + g] = __float2bfloat16_rn(acc[i][n][r + 2] * inv);
-                            }
-                        }
-                    }
-            } else {
-                // partial of this cell; then arrive, and merge if the sequence is complete
-                const int64_t cellbase = (int64_t(h.cell) * 2 + h.slot) * p.HG + hl;
-#pragma unroll
-                for (int n = 0; n < NTW; ++n)
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        const int row = (rh * NTW + n) * 8 + 2 * tq + r;
-                        if (row >= p.rows)
-                            continue;
-                        float *pa = p.part + (cellbase * p.rows + row) * D;
+                for (int r = 0; r < 2; ++r) {
+                    const int row = 2 * tq + r;
+                    if (row >= p.rows)
+                        continue;
+                    const int j = row / p.G;
+                    const int gq = row - j * p.G;
+                    const int64_t o = ((int64_t(h.s) * p.nq + j) * p.Hq + int64_t(kvh) * p.G + gq) * D;
+                    const float inv = lf[r] > 0.f ? 1.f / lf[r] : 0.f;
+                    if (p.out_f32) {
+                        float *out = static_cast<float *>(p.out) + o;
 #pragma unroll
                         for (int i = 0; i < MT; ++i) {
-                            pa[16 * i + g] = acc[i][n][r];
-                            pa[16 * i + 8 + g] = acc[i][n][r + 2];
+                            out[16 * i + g] = acc[i][r] * inv;
+                            out[16 * i + 8 + g] = acc[i][r + 2] * inv;
                         }
-                        if (g == 0) {
-                            float *ml = p.ml + (cellbase * p.rows + row) * 2;
-                            ml[0] = m_r[n][r];
-                            ml[1] = lf[n][r];
+                    } else {
+                        __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out) + o;
+#pragma unroll
+                        for (int i = 0; i < MT; ++i) {
+                            out[16 * i + g] = __float2bfloat16_rn(acc[i][r] * inv);
+                            out[16 * i + 8 + g] = __float2bfloat16_rn(acc[i][r + 2] * inv);
                         }
                     }
+                }
+            } else {
+                // partial (m, l, acc) of this cell for the merge kernel
+                const int64_t cellbase = (int64_t(h.cell) * 2 + h.slot) * p.HG + hl;
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int row = 2 * tq + r;
+                    if (row >= p.rows)
+                        continue;
+                    float *pa = p.part + (cellbase * p.rows + row) * D;
+#pragma unroll
+                    for (int i = 0; i < MT; ++i) {
+                        pa[16 * i + g] = acc[i][r];
+                        pa[16 * i + 8 + g] = acc[i][r + 2];
+                    }
+                    if (g == 0) {
+                        float *ml = p.ml + (cellbase * p.rows + row) * 2;
+                        ml[0] = m_r[r];
+                        ml[1] = lf[r];
+                    }
+                }
             }
         }
     }
+}
 
+// Consumer for warps that own 16 query rows (G*nq > 8): scores in the
+// rows x tokens orientation (M = the warp's 16 rows, N = 8 tokens, K = 16 dims),
+// so the score fragments are directly the A operand of the PV mma and each lane
+// holds two rows (g, g+8): no register transposes, two-shuffle row reductions,
+// pairwise output stores. Same pipeline, masking, hi/lo split of P and lazy
+// rescale as the 8-row consumer.
+template <int D, int WPH>
+__device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw, int lane)
+{
+    constexpr int NH = D / 64;  // 64-column halves per head row
+    constexpr int KS = D / 16;  // k-steps of the score mma
+    constexpr int ND = D / 8;   // 8-dim n-tiles of the output
+    const int hl = cw / WPH;    // kv head within the group
+    const int r0 = (cw % WPH) * 16;
+    const int g = lane >> 2, tq = lane & 3;
+
+    // ldmatrix rows inside a (head, half) tile [16 tokens][8 x 16 B], 128B swizzle
+    const int mi = lane >> 3;
+    const int k_tok = (lane & 7) + ((mi >> 1) << 3);  // K: tokens 0-7 | 8-15, chunks c | c+1
+    const int k_cadd = mi & 1;
+    const int v_tok = (lane & 7) + ((mi & 1) << 3);   // V: tokens 0-7 | 8-15, chunks c | c+1
+    const int v_cadd = mi >> 1;
+    const int sw = lane & 7;
+
+    float acc[ND][4];
+    uint32_t qa[KS][4];
+    float m_r[2], l_r[2];
+    int jr[2];
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        const int j = (r0 + g + 8 * rr) / p.G;
+        jr[rr] = j < p.nq ? j : p.nq - 1;
+    }
+    auto reset_state = [&]() {
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                qa[ks][e] = 0u;
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            m_r[rr] = -INFINITY;
+            l_r[rr] = 0.f;
+        }
+#pragma unroll
+        for (int n = 0; n < ND; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                acc[n][e] = 0.f;
+    };
+
+    const uint32_t stage_base = smem_u32(sm.stages);
+    uint32_t st = 0, phase = 0;
+    for (;;) {
+        if (!mbar_wait(smem_u32(&sm.full[st]), phase, kWaitLimitNs)) {
+            if (lane == 0)
+                atomicOr(p.ws + kWsErr, kErrConsumerWait);
+            return;
+        }
+        const StageHdr h = sm.hdr[st];
+        if (p.trace && cw == 0 && lane == 0) {
+            uint64_t *tr = p.trace + blockIdx.x * kTraceWords;
+            if (h.flags & F_END)
+                tr[4] = global_timer_ns();
+            else if (tr[2] == 0)
+                tr[2] = global_timer_ns();
+            if (h.flags & F_FIRST)
+                tr[6] += 1;
+        }
+        if (h.flags & F_END)
+            break;
+        const int kvh = h.hg * p.HG + hl;
+
+        if (h.flags & F_FIRST) {
+            reset_state();
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int row = r0 + g + 8 * rr;
+                if (row < p.rows) {
+                    const int j = row / p.G;
+                    const int gq = row - j * p.G;
+                    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+                        p.q + ((int64_t(h.s) * p.nq + j) * p.Hq + int64_t(kvh) * p.G + gq) * D);
+#pragma unroll
+                    for (int ks = 0; ks < KS; ++ks) {
+                        qa[ks][rr] = __ldg(qrow + ks * 8 + tq);          // dims 16ks+2tq..
+                        qa[ks][2 + rr] = __ldg(qrow + ks * 8 + 4 + tq);  // dims 16ks+8+2tq..
+                    }
+                }
+            }
+        }
+
+        const uint32_t kb = stage_base + st * uint32_t(p.stage_bytes) + uint32_t(hl * NH * kTileBytes);
+        const uint32_t vb = kb + uint32_t(p.HG * NH * kTileBytes);  // same head in the V half
+
+        // ---- scores S[row][token]: n-tile 0 = tokens 0-7, n-tile 1 = tokens 8-15
+        float sc[2][4], sc2[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                sc[n][e] = sc2[n][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const int chunk = 2 * ks + k_cadd;
+            const uint32_t addr = kb + uint32_t((chunk >> 3) * kTileBytes + k_tok * 128 +
+                                                (((chunk & 7) ^ sw) << 4));
+            uint32_t b[4];
+            ldsm_x4(addr, b);
+            const uint32_t a[4] = {qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]};
+            if (ks & 1) {
+                mma_bf16_16816(sc2[0], a, b[0], b[1]);
+                mma_bf16_16816(sc2[1], a, b[2], b[3]);
+            } else {
+                mma_bf16_16816(sc[0], a, b[0], b[1]);
+                mma_bf16_16816(sc[1], a, b[2], b[3]);
+            }
+        }
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                sc[n][e] += sc2[n][e];
+
+        // ---- scale (log2 domain) and causal / tail mask
+        const int t0 = h.b * kBlockSize;
+        const bool need_mask = (t0 + kBlockSize - 1) > (h.T - p.nq);
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float x = sc[n][e] * p.scale_log2;
+                if (need_mask) {
+                    const int tok = t0 + 8 * n + 2 * tq + (e & 1);
+                    const int lim = h.T - p.nq + jr[e >> 1];
+                    x = tok > lim ? -INFINITY : x;
+                }
+                sc[n][e] = x;
+            }
+
+        // ---- online softmax over the lane's two rows (g: e = 0,1; g+8: e = 2,3)
+        float bmax[2];
+        bool grew = false;
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            float bm = fmaxf(fmaxf(sc[0][2 * rr], sc[0][2 * rr + 1]),
+                             fmaxf(sc[1][2 * rr], sc[1][2 * rr + 1]));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+            bmax[rr] = bm;
+            grew |= bm > m_r[rr];
+        }
+        if (__any_sync(0xffffffffu, grew)) {
+            float corr[2];
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const float mn = fmaxf(m_r[rr], bmax[rr]);
+                const float mu = (mn == -INFINITY) ? 0.f : mn;
+                corr[rr] = ex2(m_r[rr] - mu);
+                m_r[rr] = mn;
+                l_r[rr] *= corr[rr];
+            }
+#pragma unroll
+            for (int n = 0; n < ND; ++n) {
+                acc[n][0] *= corr[0];
+                acc[n][1] *= corr[0];
+                acc[n][2] *= corr[1];
+                acc[n][3] *= corr[1];
+            }
+        }
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const float mu = (m_r[rr] == -INFINITY) ? 0.f : m_r[rr];
+            float sum = 0.f;
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int e = 2 * rr; e < 2 * rr + 2; ++e) {
+                    const float pv = ex2(sc[n][e] - mu);
+                    sc[n][e] = pv;
+                    sum += pv;
+                }
+            l_r[rr] += sum;
+        }
+
+        // ---- P (16 rows x 16 tokens) as the A operand, split into bf16 hi + lo
+        uint32_t ph[4], plo[4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const float x0 = sc[n][2 * rr], x1 = sc[n][2 * rr + 1];
+                const uint32_t hi = pack_bf16x2(x0, x1);
+                ph[2 * n + rr] = hi;  // a0 = (g, 0-7), a1 = (g+8, 0-7), a2 = (g, 8-15), a3 = (g+8, 8-15)
+                plo[2 * n + rr] = pack_bf16x2(x0 - bf16lo_f32(hi), x1 - bf16hi_f32(hi));
+            }
+
+        // ---- V rows past the context (stale or NaN slots) are zeroed
+        uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+        const int vc = h.T - t0;
+        if (vc < kBlockSize) {
+            const int k0 = 2 * tq;
+            mlo = (k0 < vc ? 0x0000ffffu : 0u) | (k0 + 1 < vc ? 0xffff0000u : 0u);
+            mhi = (k0 + 8 < vc ? 0x0000ffffu : 0u) | (k0 + 9 < vc ? 0xffff0000u : 0u);
+        }
+
+        // ---- O[row][d] += P[row][tok] . V[tok][d]
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) {
+            const int chunk = 2 * i + v_cadd;
+            const uint32_t addr = vb + uint32_t((chunk >> 3) * kTileBytes + v_tok * 128 +
+                                                (((chunk & 7) ^ sw) << 4));
+            uint32_t b[4];
+            ldsm_x4_trans(addr, b);
+            b[0] &= mlo;
+            b[1] &= mhi;
+            b[2] &= mlo;
+            b[3] &= mhi;
+            mma_bf16_16816(acc[2 * i], ph, b[0], b[1]);
+            mma_bf16_16816(acc[2 * i], plo, b[0], b[1]);
+            mma_bf16_16816(acc[2 * i + 1], ph, b[2], b[3]);
+            mma_bf16_16816(acc[2 * i + 1], plo, b[2], b[3]);
+        }
+
+        // the stage's shared memory is no longer needed: hand it back
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_u32(&sm.empty[st]));
+        if (++st == uint32_t(p.nst)) {
+            st = 0;
+            phase ^= 1u;
+        }
+
+        if (h.flags & F_LAST) {
+            float lf[2];
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                float v = l_r[rr];
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                lf[rr] = v;
+            }
+            if (h.flags & F_DIRECT) {
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int row = r0 + g + 8 * rr;
+                    if (row >= p.rows)
+                        continue;
+                    const int j = row / p.G;
+                    const int gq = row - j * p.G;
+                    const int64_t o = ((int64_t(h.s) * p.nq + j) * p.Hq + int64_t(kvh) * p.G + gq) * D;
+                    const float inv = lf[rr] > 0.f ? 1.f / lf[rr] : 0.f;
+                    if (p.out_f32) {
+                        float *out = static_cast<float *>(p.out) + o;
+#pragma unroll
+                        for (int n = 0; n < ND; ++n)
+                            *reinterpret_cast<float2 *>(out + 8 * n + 2 * tq) =
+                                make_float2(acc[n][2 * rr] * inv, acc[n][2 * rr + 1] * inv);
+                    } else {
+                        __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out) + o;
+#pragma unroll
+                        for (int n = 0; n < ND; ++n)
+                            *reinterpret_cast<__nv_bfloat162 *>(out + 8 * n + 2 * tq) =
+                                __floats2bfloat162_rn(acc[n][2 * rr] * inv, acc[n][2 * rr + 1] * inv);
+                    }
+                }
+            } else {
+                const int64_t cellbase = (int64_t(h.cell) * 2 + h.slot) * p.HG + hl;
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int row = r0 + g + 8 * rr;
+                    if (row >= p.rows)
+                        continue;
+                    float *pa = p.part + (cellbase * p.rows + row) * D;
+#pragma unroll
+                    for (int n = 0; n < ND; ++n)
+                        *reinterpret_cast<float2 *>(pa + 8 * n + 2 * tq) =
+                            make_float2(acc[n][2 * rr], acc[n][2 * rr + 1]);
+                    if (tq == 0) {
+                        float *ml = p.ml + (cellbase * p.rows + row) * 2;
+                        ml[0] = m_r[rr];
+                        ml[1] = lf[rr];
+                    }
+                }
+            }
+        }
+    }
 }
 
 template <int D, int NTW, int WPH>
@@ -711,6 +967,7 @@ __global__ void __launch_bounds__(kThreadsMax, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const DecodeParams p)
 {
+    static_assert(NTW == 2 || WPH == 1, "8-row warps each own a whole kv head");
     extern __shared__ uint8_t smem_raw[];
     const Smem sm = carve(smem_raw, p);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -734,10 +991,14 @@ __global__ void __launch_bounds__(kThreadsMax, 1)
         p.trace[blockIdx.x * kTraceWords + 7] = smid;
     }
     __syncthreads();
-    if (warp == 0)
+    if (warp == 0) {
         producer_warp<D>(&kmap, &vmap, p, sm, lane);
-    else
-        consumer_warp<D, NTW, WPH>(p, sm, warp - 1, lane);
+    } else {
+        if constexpr (NTW == 2)
+            consumer_warp_m16<D, WPH>(p, sm, warp - 1, lane);
+        else
+            consumer_warp_m8<D>(p, sm, warp - 1, lane);
+    }
 }
 
 // ------------------------------------------------------------------ merge
