@@ -1,6 +1,7 @@
 """Benchmark of one paged decode step (KV append + paged decode attention) on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl pkv|reference]
+    python bench.py --op copy_blocks [--pairs P] [--workload NAME]   # copy-on-write copy alone
 
 Prints ONE JSON line (rank 0). A step is the whole hot path over one batch:
 ``kv_append`` of the step's new tokens, then ``paged_decode_attention`` (main
@@ -302,6 +303,127 @@ def run_pkv(args, rank, world, dist):
     return res
 
 
+# ------------------------------------------------------------------ copy-on-write copy
+COPY_METRIC = "copy-on-write block copy GB/s (bytes read + written)"
+
+
+def run_copy(args, rank, world, dist):
+    """Time pkv_copy_blocks alone: `--pairs` block pairs of the workload's geometry
+    (16 tokens x Hkv x D bf16 in K and V per block), disjoint sources and
+    destinations drawn by a seeded permutation of a pool twice that size."""
+    import torch
+
+    import oracle as O
+    import paged_kv_cache_101_gb300 as pkv
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    geo = W.WORKLOADS[args.workload]
+    Hkv, D = geo["Hkv"], geo["D"]
+    P = int(args.pairs)
+    NB = 2 * P + 64
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234)
+    k_cache = torch.randint(-(1 << 15), 1 << 15, (NB, 16, Hkv, D), dtype=torch.int16, device=dev,
+                            generator=g).view(torch.bfloat16)
+    v_cache = torch.randint(-(1 << 15), 1 << 15, (NB, 16, Hkv, D), dtype=torch.int16, device=dev,
+                            generator=g).view(torch.bfloat16)
+    perm = np.random.default_rng(1234).permutation(NB).astype(np.int32)
+    src = torch.from_numpy(perm[:P].copy()).to(dev)
+    dst = torch.from_numpy(perm[P:2 * P].copy()).to(dev)
+    block_bytes = 2 * 16 * Hkv * D * 2            # K + V of one block
+    step_bytes = 2 * P * block_bytes              # read and written
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        pkv.copy_blocks(k_cache, v_cache, src, dst)
+    torch.cuda.synchronize()
+    K = args.steps
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        ev_s[i].record()
+        pkv.copy_blocks(k_cache, v_cache, src, dst)
+        ev_e[i].record()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = sum(a.elapsed_time(b) for a, b in zip(ev_s, ev_e)) / K
+
+    # end to end: the pairs come from pinned host memory each step (as a block
+    # manager hands them out), the pool stays on the device; 4 bytes read back
+    h_src = src.cpu().pin_memory()
+    h_dst = dst.cpu().pin_memory()
+    h_probe = torch.empty(2, dtype=torch.int16).pin_memory()
+    Ke = max(1, min(K, 200))
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    for i in range(Ke):
+        flush.zero_()
+        e_s[i].record()
+        src.copy_(h_src, non_blocking=True)
+        dst.copy_(h_dst, non_blocking=True)
+        pkv.copy_blocks(k_cache, v_cache, src, dst)
+        h_probe.copy_(k_cache.view(torch.int16)[int(perm[P]), 0, 0, :2], non_blocking=True)
+        e_e[i].record()
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e_s, e_e)) / Ke
+    if dist is not None:
+        t = torch.tensor([ms, e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = (float(x) for x in t.tolist())
+
+    peak, peak_kind = measured_peaks()
+    achieved = step_bytes / (ms * 1e-3) / 1e9
+    res = {
+        "metric": COPY_METRIC, "value": round(world * achieved, 2), "unit": "GB/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 6),
+        "us_per_step": round(ms * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 (bit copy)",
+        "data": "synthetic (seeded random bf16 bit patterns; 512 MiB L2 flush between steps)",
+        "config": {"workload": f"copy_blocks {P} pairs, {args.workload} geometry",
+                   "num_kv_heads": Hkv, "head_dim": D, "pairs": P, "num_blocks": NB,
+                   "bytes_per_step": step_bytes, "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "copy_blocks_kernel",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_kind} hbm_gbs (burst)", "traffic": None,
+                     "kernel_us": round(ms * 1e3, 3), "algorithmic_bytes_per_launch": step_bytes},
+        "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 6), "h2d_bytes_per_step": 8 * P,
+                "d2h_bytes_per_step": 4,
+                "path": "pinned host pairs -> H2D -> copy_blocks -> D2H probe"},
+        "gpu_launches": K,
+    }
+    if clk is not None:
+        res["clocks"] = clk
+    if rank == 0 and not args.no_cpu_baseline:
+        # the oracle's block copy on a bounded sample of the pairs
+        o = O.Oracle()
+        sp = min(P, 512)
+        kh = np.zeros((2 * sp + 64, 16, Hkv, D), dtype=np.uint16)
+        vh = kh.copy()
+        t0 = time.perf_counter()
+        n = 0
+        while time.perf_counter() - t0 < args.cpu_seconds / 5 or n == 0:
+            kh, vh = o.copy_blocks(kh, vh, np.arange(sp), np.arange(sp, 2 * sp))
+            n += 1
+        el = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": round(n * 2 * sp * block_bytes / el / 1e9, 4),
+                               "unit": "GB/s", "cores": 1, "kind": "oracle",
+                               "sample": f"{n} copies of {sp} pairs in {el:.1f} s (one thread; "
+                                         f"each call also copies the pools once)"}
+    return res
+
+
 # ------------------------------------------------------------------ oracle (CPU)
 def oracle_sample(w, budget_s: float, threads: int):
     """Time the fp64 oracle on whole decode steps of ``w`` for about budget_s seconds
@@ -398,6 +520,10 @@ def main():
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="step", choices=["step", "copy_blocks"],
+                    help="step: append + attention (the headline); copy_blocks: the "
+                         "copy-on-write block copy alone")
+    ap.add_argument("--pairs", type=int, default=4096, help="block pairs per copy_blocks step")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -416,6 +542,13 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         td.init_process_group("nccl")
         dist = td
+    if args.op == "copy_blocks":
+        res = run_copy(args, rank, world, dist)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
     res = run_pkv(args, rank, world, dist)
     if rank == 0:
         if not args.no_cpu_baseline:

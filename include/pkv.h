@@ -10,6 +10,10 @@
  *                                sequence over the pool, through per-sequence
  *                                block tables.
  *
+ * When sequences share blocks, pkv_copy_blocks first gives a writer its
+ * private copy of a shared block (copy-on-write). The host-side block
+ * manager that decides slots, tables and copies is in pkv_block_manager.h.
+ *
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - Pointers named as device buffers must point to memory of the current
@@ -50,7 +54,9 @@ typedef enum pkv_status {
     PKV_ERR_RANGE = 5,       /* a size is beyond what the library supports     */
     PKV_ERR_WORKSPACE = 6,   /* workspace missing or smaller than required     */
     PKV_ERR_CUDA = 7,        /* a CUDA runtime/driver call or launch failed    */
-    PKV_ERR_UNSUPPORTED = 8  /* a valid shape this build has no kernel for     */
+    PKV_ERR_UNSUPPORTED = 8, /* a valid shape this build has no kernel for     */
+    PKV_ERR_NO_BLOCKS = 9,   /* block manager: not enough free blocks          */
+    PKV_ERR_SEQUENCE = 10    /* block manager: unknown or duplicate sequence id */
 } pkv_status;
 
 typedef enum pkv_dtype {
@@ -88,6 +94,35 @@ pkv_status pkv_kv_append(const void *k_new, const void *v_new,
                          const int64_t *slot_mapping, int64_t n_new,
                          void *k_cache, void *v_cache, int64_t num_blocks,
                          int32_t num_kv_heads, int32_t head_dim, void *stream);
+
+/*
+ * pkv_copy_blocks -- copy whole physical blocks of the pool (copy-on-write).
+ *
+ * Passage: "ML Interview Prep, Lesson 13" section 3.5 "Sharing" (before a
+ * sequence writes into a block whose reference count is above 1 it gets a
+ * private copy, and the shared block's count drops by one) and "LLM Serving:
+ * Continuous Batching & PagedAttention" section 4.2 (copy-on-write prefix
+ * sharing). The host block manager (pkv_block_manager.h) decides the pairs;
+ * this call moves the bytes: for every i in [0, num_pairs),
+ *     k_cache[block_dst[i]][:] = k_cache[block_src[i]][:]   (all 16 token rows,
+ *     v_cache[block_dst[i]][:] = v_cache[block_src[i]][:]    every kv head)
+ * bit-exact. Enqueue it before the pkv_kv_append of the same step: the append
+ * may write into a source block (its last sharer writes in place).
+ *
+ *   k_cache,v_cache device pool as described above, 16-byte aligned.
+ *   block_src, block_dst device, int32 [num_pairs], 4-byte aligned. A pair
+ *                  naming a block outside [0, num_blocks), or with src == dst,
+ *                  is skipped (no write, no fault). The destinations must be
+ *                  distinct and no destination may be another pair's source
+ *                  (the pairs of one block-manager step always are); otherwise
+ *                  the result is unspecified.
+ *   head_dim       a multiple of 8, <= 1024 (16-byte vectors), as for the append.
+ *   num_pairs == 0 is a no-op returning PKV_OK.
+ */
+pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, int64_t num_blocks,
+                           int32_t num_kv_heads, int32_t head_dim,
+                           const int32_t *block_src, const int32_t *block_dst,
+                           int32_t num_pairs, void *stream);
 
 /*
  * pkv_workspace_size -- bytes of device workspace pkv_paged_decode_attention

@@ -7,6 +7,8 @@ PyTorch fallback: if the library is missing, every call raises.
     kv_append(k_new, v_new, slot_mapping, k_cache, v_cache)
     paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens,
                            n_query_per_seq, scale, out)
+    copy_blocks(k_cache, v_cache, src, dst)      # copy-on-write, on the device
+    BlockManager(num_blocks)                     # host: tables, counts, forks
 
 Tensors are torch CUDA tensors on the current device: bf16 K/V/Q laid out as
 ``include/pkv.h`` describes (pools ``[num_blocks, 16, num_kv_heads, head_dim]``),
@@ -23,6 +25,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIBRARY_PATH = os.path.join(_HERE, "libpkv.so")
 
 PKV_OK = 0
+PKV_ERR_NO_BLOCKS, PKV_ERR_SEQUENCE = 9, 10
 PKV_BF16, PKV_FP32 = 0, 1
 PKV_OPT_NUM_CTAS, PKV_OPT_STAGES, PKV_OPT_HEADS_PER_CTA, PKV_OPT_TMA_BOX, PKV_OPT_TAIL = 1, 2, 3, 4, 5
 BLOCK_SIZE = 16
@@ -42,6 +45,22 @@ SIGNATURES = {
     "pkv_set_trace_buffer": ([_P, _SZ], None),
     "pkv_paged_decode_attention_static": ([_P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _I32,
                                            _I32, _F, _P, _I32, _P], ctypes.c_int),
+    "pkv_copy_blocks": ([_P, _P, _I64, _I32, _I32, _P, _P, _I32, _P], ctypes.c_int),
+    # host block manager (include/pkv_block_manager.h)
+    "pkv_bm_create": ([_I64], _P),
+    "pkv_bm_destroy": ([_P], None),
+    "pkv_bm_num_free": ([_P], _I64),
+    "pkv_bm_num_blocks": ([_P], _I64),
+    "pkv_bm_num_sequences": ([_P], _I64),
+    "pkv_bm_refcount": ([_P, _I64], _I32),
+    "pkv_bm_add_sequence": ([_P, _I64, _I64], ctypes.c_int),
+    "pkv_bm_fork": ([_P, _I64, _I64], ctypes.c_int),
+    "pkv_bm_free_sequence": ([_P, _I64], ctypes.c_int),
+    "pkv_bm_append": ([_P, _P, _I32, _I32, _P, _P, _P, _P], ctypes.c_int),
+    "pkv_bm_sequence_length": ([_P, _I64], _I64),
+    "pkv_bm_sequence_blocks": ([_P, _I64, _P, _I64], _I64),
+    "pkv_bm_block_tables": ([_P, _P, _I32, _P, _I32, _P], ctypes.c_int),
+    "pkv_bm_check": ([_P], _I32),
 }
 
 _lib = None
@@ -148,6 +167,124 @@ def kv_append(k_new, v_new, slot_mapping, k_cache, v_cache):
                              _stream_handle(k_cache.device))
     if st != PKV_OK:
         raise PkvError("pkv_kv_append", st)
+
+
+def copy_blocks(k_cache, v_cache, src, dst):
+    """Copy whole blocks ``src[i] -> dst[i]`` (int32 CUDA tensors) in both pools."""
+    torch = _torch()
+    _check(k_cache, "k_cache", torch.bfloat16, 4)
+    _check(v_cache, "v_cache", torch.bfloat16, 4)
+    _check(src, "src", torch.int32, 1)
+    _check(dst, "dst", torch.int32, 1)
+    NB, bs, Hkv, D = k_cache.shape
+    if bs != BLOCK_SIZE or v_cache.shape != k_cache.shape:
+        raise ValueError("pools must be [num_blocks, 16, Hkv, D] and equal in shape")
+    if src.shape != dst.shape:
+        raise ValueError("src and dst must have the same length")
+    st = lib().pkv_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(), NB, Hkv, D,
+                               src.data_ptr(), dst.data_ptr(), src.shape[0],
+                               _stream_handle(k_cache.device))
+    if st != PKV_OK:
+        raise PkvError("pkv_copy_blocks", st)
+
+
+class BlockManager:
+    """Host-side block manager of a pool (free list, block tables, reference
+    counts, forks, copy-on-write); a thin face of ``pkv_bm_*``."""
+
+    def __init__(self, num_blocks: int):
+        self._h = lib().pkv_bm_create(int(num_blocks))
+        if not self._h:
+            raise PkvError("pkv_bm_create", 2)
+        self.num_blocks = int(num_blocks)
+
+    def close(self):
+        if self._h:
+            lib().pkv_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _call(self, name, *args):
+        st = getattr(lib(), name)(self._h, *args)
+        if st != PKV_OK:
+            raise PkvError(name, st)
+
+    def num_free(self) -> int:
+        return int(lib().pkv_bm_num_free(self._h))
+
+    def num_sequences(self) -> int:
+        return int(lib().pkv_bm_num_sequences(self._h))
+
+    def ref(self, block: int) -> int:
+        return int(lib().pkv_bm_refcount(self._h, int(block)))
+
+    def add_sequence(self, seq: int, n_tokens: int) -> bool:
+        """False when the free blocks do not suffice (nothing changes)."""
+        st = lib().pkv_bm_add_sequence(self._h, int(seq), int(n_tokens))
+        if st == PKV_ERR_NO_BLOCKS:
+            return False
+        if st != PKV_OK:
+            raise PkvError("pkv_bm_add_sequence", st)
+        return True
+
+    def fork(self, parent: int, child: int) -> None:
+        self._call("pkv_bm_fork", int(parent), int(child))
+
+    def free(self, seq: int) -> None:
+        self._call("pkv_bm_free_sequence", int(seq))
+
+    def append_batch(self, seqs, n_per_seq: int = 1):
+        """``(slots, copies)`` for n tokens of each sequence, or None (no change)
+        when the free blocks do not suffice; slots is an int64 array, copies a
+        list of (src, dst) block pairs."""
+        import numpy as np
+        ids = np.ascontiguousarray(seqs, dtype=np.int64)
+        k = ids.size
+        slots = np.empty(k * int(n_per_seq), dtype=np.int64)
+        src = np.empty(max(k, 1), dtype=np.int32)
+        dst = np.empty(max(k, 1), dtype=np.int32)
+        nc = ctypes.c_int32(0)
+        st = lib().pkv_bm_append(self._h, ids.ctypes.data, k, int(n_per_seq), slots.ctypes.data,
+                                 src.ctypes.data, dst.ctypes.data, ctypes.byref(nc))
+        if st == PKV_ERR_NO_BLOCKS:
+            return None
+        if st != PKV_OK:
+            raise PkvError("pkv_bm_append", st)
+        return slots, [(int(src[i]), int(dst[i])) for i in range(nc.value)]
+
+    def length(self, seq: int) -> int:
+        n = int(lib().pkv_bm_sequence_length(self._h, int(seq)))
+        if n < 0:
+            raise PkvError("pkv_bm_sequence_length", PKV_ERR_SEQUENCE)
+        return n
+
+    def table(self, seq: int) -> list:
+        import numpy as np
+        n = int(lib().pkv_bm_sequence_blocks(self._h, int(seq), None, 0))
+        if n < 0:
+            raise PkvError("pkv_bm_sequence_blocks", PKV_ERR_SEQUENCE)
+        out = np.empty(max(n, 1), dtype=np.int32)
+        lib().pkv_bm_sequence_blocks(self._h, int(seq), out.ctypes.data, n)
+        return [int(b) for b in out[:n]]
+
+    def block_tables(self, seqs, max_blocks_per_seq: int):
+        """int32 ``[len(seqs), max_blocks_per_seq]`` (padded with -1) and int32 lengths."""
+        import numpy as np
+        ids = np.ascontiguousarray(seqs, dtype=np.int64)
+        tables = np.empty((ids.size, max(int(max_blocks_per_seq), 1)), dtype=np.int32)
+        lens = np.empty(max(ids.size, 1), dtype=np.int32)
+        self._call("pkv_bm_block_tables", ids.ctypes.data, ids.size, tables.ctypes.data,
+                   int(max_blocks_per_seq), lens.ctypes.data)
+        return tables[:, :int(max_blocks_per_seq)], lens[:ids.size]
+
+    def check(self) -> int:
+        """0 when the manager's own state is consistent (see pkv_bm_check)."""
+        return int(lib().pkv_bm_check(self._h))
 
 
 def workspace_size(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim) -> int:

@@ -16,7 +16,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIBRARY = os.path.join(PKG, "libpkv.so")
-SOURCES = ["api.cu", "kv_append.cu", "paged_decode.cu", "static_scratch.cu"]
+SOURCES = ["api.cu", "kv_append.cu", "copy_blocks.cu", "paged_decode.cu", "static_scratch.cu",
+           "block_manager.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -48,7 +49,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     objs = []
     cmds = []
     for src in SOURCES:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
         objs.append(obj)
         cmds.append([nvcc(), *_flags(extra_flags), "-c", os.path.join(CSRC, src), "-o", obj])
 

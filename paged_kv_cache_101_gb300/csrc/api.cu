@@ -13,6 +13,13 @@
 #include "pkv.h"
 #include "pkv_internal.h"
 
+namespace pkv {
+// copy_blocks.cu
+cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, int64_t num_blocks, int num_kv_heads,
+                               int head_dim, const int32_t *src, const int32_t *dst,
+                               int num_pairs, cudaStream_t stream);
+}  // namespace pkv
+
 namespace {
 
 int32_t g_opt_num_ctas = 0;
@@ -211,6 +218,8 @@ const char *pkv_status_string(int32_t status)
     case PKV_ERR_WORKSPACE: return "workspace missing or too small";
     case PKV_ERR_CUDA: return "a CUDA call or kernel launch failed";
     case PKV_ERR_UNSUPPORTED: return "no kernel for this (valid) shape";
+    case PKV_ERR_NO_BLOCKS: return "not enough free blocks in the pool";
+    case PKV_ERR_SEQUENCE: return "unknown or duplicate sequence id";
     default: return "unknown status";
     }
 }
@@ -287,6 +296,29 @@ pkv_status pkv_kv_append(const void *k_new, const void *v_new, const int64_t *sl
     cudaError_t e = pkv::launch_kv_append(k_new, v_new, slot_mapping, n_new, k_cache, v_cache,
                                           num_blocks, num_kv_heads, head_dim,
                                           static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, int64_t num_blocks,
+                           int32_t num_kv_heads, int32_t head_dim, const int32_t *block_src,
+                           const int32_t *block_dst, int32_t num_pairs, void *stream)
+{
+    if (num_pairs < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 1)
+        return PKV_ERR_SHAPE;
+    if (num_pairs == 0)
+        return PKV_OK;
+    if (!k_cache || !v_cache || !block_src || !block_dst)
+        return PKV_ERR_NULL;
+    if (head_dim % 8 != 0)
+        return PKV_ERR_UNSUPPORTED;
+    if (head_dim > 1024 || num_kv_heads > 1024 || num_blocks > (int64_t(1) << 40))
+        return PKV_ERR_RANGE;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(block_src, 4) ||
+        !aligned(block_dst, 4))
+        return PKV_ERR_ALIGN;
+    cudaError_t e = pkv::launch_copy_blocks(k_cache, v_cache, num_blocks, num_kv_heads, head_dim,
+                                            block_src, block_dst, num_pairs,
+                                            static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

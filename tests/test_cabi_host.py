@@ -13,7 +13,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
            if f.endswith(".h")]
 
-OK, NULL, SHAPE, DTYPE, ALIGN, RANGE, WORKSPACE, CUDA, UNSUP = range(9)
+OK, NULL, SHAPE, DTYPE, ALIGN, RANGE, WORKSPACE, CUDA, UNSUP, NO_BLOCKS, SEQUENCE = range(11)
 
 
 @pytest.fixture(scope="module")
@@ -35,7 +35,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for required in ("pkv_kv_append", "pkv_paged_decode_attention", "pkv_workspace_size",
-                     "pkv_status_string"):
+                     "pkv_status_string", "pkv_copy_blocks", "pkv_bm_create", "pkv_bm_append",
+                     "pkv_bm_block_tables"):
         assert required in names
 
 
@@ -48,8 +49,8 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    for s in range(9):
-        assert pkv.status_string(s)
+    for s in range(11):
+        assert pkv.status_string(s) and pkv.status_string(s) != "unknown status"
     assert pkv.status_string(99) == "unknown status"
     assert lib.pkv_version() >= 100
 
@@ -82,6 +83,23 @@ def test_append_validation(lib):
     assert append(lib, k=A + 8) == ALIGN
     assert append(lib, vc=A + 2) == ALIGN
     assert append(lib, slots=A + 4) == ALIGN
+
+
+def copyb(lib, k=A, v=A, nb=8, hkv=2, d=64, src=A, dst=A, n=3):
+    return lib.pkv_copy_blocks(k, v, nb, hkv, d, src, dst, n, None)
+
+
+def test_copy_blocks_validation(lib):
+    assert copyb(lib, n=0) == OK                        # nothing to copy: no-op
+    assert copyb(lib, k=None) == NULL
+    assert copyb(lib, dst=None) == NULL
+    assert copyb(lib, n=-1) == SHAPE
+    assert copyb(lib, nb=0) == SHAPE
+    assert copyb(lib, hkv=0) == SHAPE
+    assert copyb(lib, d=12) == UNSUP
+    assert copyb(lib, d=2048) == RANGE
+    assert copyb(lib, v=A + 8) == ALIGN
+    assert copyb(lib, src=A + 2) == ALIGN
 
 
 def attn(lib, q=A, k=A, v=A, nb=64, bt=A, mb=8, cl=A, S=4, nq=1, hq=8, hkv=2, d=64,
