@@ -48,6 +48,15 @@ def _bind(lib):
     lib.oracle_kv_append.restype = ctypes.c_int
     lib.oracle_copy_blocks.argtypes = [P, P, i64, i32, i32, i32, P, P, i64]
     lib.oracle_copy_blocks.restype = ctypes.c_int
+    lib.oracle_e4m3_encode_array.argtypes = [P, i64, P]
+    lib.oracle_e4m3_encode_array.restype = None
+    lib.oracle_e4m3_decode_array.argtypes = [P, i64, P]
+    lib.oracle_e4m3_decode_array.restype = None
+    lib.oracle_kv_append_fp8.argtypes = [P, P, P, i64, P, P, i64, i32, i32, i32, P, P]
+    lib.oracle_kv_append_fp8.restype = ctypes.c_int
+    lib.oracle_paged_attention_fp8.argtypes = [P, P, P, i64, i32, P, i32, P, i32, i32, i32, i32,
+                                               i32, ctypes.c_float, P, P, P, P, i32]
+    lib.oracle_paged_attention_fp8.restype = ctypes.c_int
     common = [P, P, P, i64, i32, P, i32, P, i32, i32, i32, i32, i32, ctypes.c_float]
     lib.oracle_paged_attention.argtypes = common + [P, P, i32]
     lib.oracle_paged_attention.restype = ctypes.c_int
@@ -119,6 +128,64 @@ class Oracle:
         if st not in (0, -1):
             raise RuntimeError(f"oracle_copy_blocks failed: {st}")
         return k_cache, v_cache
+
+    # ---- FP8 (E4M3) KV cache
+    def e4m3_encode(self, x) -> np.ndarray:
+        """uint8 E4M3 codes of float32 values (nearest, ties to even, saturating)."""
+        x = _c(x, np.float32)
+        out = np.empty(x.shape, dtype=np.uint8)
+        self.lib.oracle_e4m3_encode_array(_ptr(x), x.size, _ptr(out))
+        return out
+
+    def e4m3_decode(self, c) -> np.ndarray:
+        c = _c(c, np.uint8)
+        out = np.empty(c.shape, dtype=np.float64)
+        self.lib.oracle_e4m3_decode_array(_ptr(c), c.size, _ptr(out))
+        return out
+
+    def kv_append_fp8(self, k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale):
+        """Quantise the new bf16 rows into (copies of) the uint8 pools."""
+        k_cache = np.array(k_cache, dtype=np.uint8, copy=True, order="C")
+        v_cache = np.array(v_cache, dtype=np.uint8, copy=True, order="C")
+        NB, bs, Hkv, D = k_cache.shape
+        k_new = _c(k_new, np.uint16)
+        v_new = _c(v_new, np.uint16)
+        slots = _c(slot_mapping, np.int64)
+        ks = _c(k_scale, np.float32)
+        vs = _c(v_scale, np.float32)
+        assert ks.size == Hkv and vs.size == Hkv
+        st = self.lib.oracle_kv_append_fp8(_ptr(k_new), _ptr(v_new), _ptr(slots), slots.size,
+                                           _ptr(k_cache), _ptr(v_cache), NB, bs, Hkv, D,
+                                           _ptr(ks), _ptr(vs))
+        if st not in (0, -1):
+            raise RuntimeError(f"oracle_kv_append_fp8 failed: {st}")
+        return k_cache, v_cache
+
+    def paged_attention_fp8(self, q, k_cache, v_cache, block_tables, context_lens,
+                            n_query_per_seq, scale, k_scale, v_scale, pair_mask=None,
+                            threads: int = 0) -> np.ndarray:
+        q = _c(q, np.uint16)
+        k_cache = _c(k_cache, np.uint8)
+        v_cache = _c(v_cache, np.uint8)
+        bt = _c(block_tables, np.int32)
+        cl = _c(context_lens, np.int32)
+        ks = _c(k_scale, np.float32)
+        vs = _c(v_scale, np.float32)
+        NB, bs, Hkv, D = k_cache.shape
+        S = cl.shape[0]
+        Hq = q.shape[1]
+        MB = bt.shape[1] if bt.ndim == 2 else 1
+        out = np.full((S * n_query_per_seq, Hq, D), np.nan, dtype=np.float64)
+        pm = None
+        if pair_mask is not None:
+            pm = _c(np.asarray(pair_mask).reshape(S, Hkv), np.uint8)
+        st = self.lib.oracle_paged_attention_fp8(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), NB, bs, _ptr(bt), MB, _ptr(cl), S,
+            int(n_query_per_seq), Hq, Hkv, D, ctypes.c_float(float(np.float32(scale))),
+            _ptr(ks), _ptr(vs), _ptr(pm) if pm is not None else None, _ptr(out), int(threads))
+        if st != 0:
+            raise ValueError(f"oracle_paged_attention_fp8: invalid input (status {st})")
+        return out
 
     def _common(self, q, k_cache, v_cache, block_tables, context_lens, nq, scale):
         q = _c(q, np.uint16)

@@ -391,3 +391,183 @@ int oracle_num_threads(void)
     return 1;
 #endif
 }
+
+/* ------------------------------------------------------------------------
+ * FP8 (E4M3) KV cache.
+ *
+ * "ML Interview Prep, Lesson 13", section 3.7 (an fp8 or int8 KV cache stores
+ * keys and values in 8 bits while the matmuls still run at 16 bits: twice the
+ * tokens in memory, half the KV read time) and "07 -- Inference", section 4.3
+ * (E4M3 for inference, largest magnitude 448; per-tensor, per-channel or
+ * per-block scales). Reading: one float scale per kv head for K and one for V;
+ * a stored code c of head h stands for decode(c) * scale[h].
+ *
+ * E4M3 ("fn" variant of the OCP 8-bit floating point format): sign bit,
+ * 4 exponent bits with bias 7, 3 mantissa bits. Exponent field 0 holds the
+ * subnormals m * 2^-9; S.1111.111 is NaN; there are no infinities, so the
+ * largest finite magnitude is 1.75 * 2^8 = 448.
+ * ---------------------------------------------------------------------- */
+
+double oracle_e4m3_decode(uint8_t c)
+{
+    const int e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    const double v = (e == 0) ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+    return (c & 0x80) ? -v : v;
+}
+
+/* Nearest E4M3 value, ties to the even code; magnitudes whose rounded value
+ * exceeds 448 (and infinities) give 448 with the sign kept; NaN gives 0x7F. */
+uint8_t oracle_e4m3_encode(float x)
+{
+    if (isnan(x))
+        return 0x7F;
+    const uint8_t sgn = signbit(x) ? 0x80 : 0x00;
+    const double a = fabs((double)x);
+    if (isinf(a))
+        return sgn | 0x7E;
+    int k;
+    frexp(a, &k); /* a = f * 2^k, f in [0.5, 1): floor(log2 a) = k - 1 */
+    int E = k - 1;
+    if (a == 0.0 || E < -6) {
+        /* subnormal range: grid step 2^-9; the code is the step count (8 = 2^-6) */
+        const double n = nearbyint(ldexp(a, 9));
+        return sgn | (uint8_t)n;
+    }
+    double n = nearbyint(ldexp(a, 3 - E)); /* 8 .. 16 steps of 2^(E-3) */
+    if (n == 16.0) {
+        E += 1;
+        n = 8.0;
+    }
+    const int field = E + 7;
+    if (field > 15 || (field == 15 && n - 8.0 > 6.0))
+        return sgn | 0x7E; /* beyond 448: saturate */
+    return sgn | (uint8_t)((field << 3) | (int)(n - 8.0));
+}
+
+/* The fp8 append: for every new token i with slot >= 0 and every kv head h,
+ * code = encode(k_new / k_scale[h]) (bf16 widened to float, divided in float
+ * with round-to-nearest), stored at block slot/16, offset slot%16; V likewise. */
+int oracle_kv_append_fp8(const uint16_t *k_new, const uint16_t *v_new,
+                         const int64_t *slot_mapping, int64_t n_new,
+                         uint8_t *k_cache, uint8_t *v_cache, int64_t num_blocks,
+                         int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                         const float *k_scale, const float *v_scale)
+{
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    int bad = 0;
+    for (int64_t i = 0; i < n_new; ++i) {
+        const int64_t slot = slot_mapping[i];
+        if (slot < 0)
+            continue;
+        const int64_t blk = slot / block_size;
+        const int64_t off = slot % block_size;
+        if (blk >= num_blocks) {
+            bad = 1;
+            continue;
+        }
+        for (int32_t h = 0; h < num_kv_heads; ++h) {
+            for (int32_t d = 0; d < head_dim; ++d) {
+                const int64_t src = i * row + (int64_t)h * head_dim + d;
+                const int64_t dst = (blk * block_size + off) * row + (int64_t)h * head_dim + d;
+                const float kx = (float)bf16_to_double(k_new[src]);
+                const float vx = (float)bf16_to_double(v_new[src]);
+                k_cache[dst] = oracle_e4m3_encode(kx / k_scale[h]);
+                v_cache[dst] = oracle_e4m3_encode(vx / v_scale[h]);
+            }
+        }
+    }
+    return bad ? -1 : 0;
+}
+
+/* Attention over the fp8 pool: the gathered K/V are decode(code) * scale[h] in
+ * fp64; everything after the gather is the bf16 definition above. */
+int oracle_paged_attention_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                               int64_t num_blocks, int32_t block_size,
+                               const int32_t *block_tables, int32_t max_blocks_per_seq,
+                               const int32_t *context_lens, int32_t num_seqs,
+                               int32_t n_query_per_seq, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_dim, float scale,
+                               const float *k_scale, const float *v_scale,
+                               const uint8_t *pair_mask, double *out, int32_t num_threads)
+{
+    if (check_shapes(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim, block_size))
+        return -2;
+    const int32_t group = num_q_heads / num_kv_heads;
+    const int64_t npairs = (int64_t)num_seqs * num_kv_heads;
+    int status = 0;
+#ifdef _OPENMP
+    if (num_threads > 0)
+        omp_set_num_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t pair = 0; pair < npairs; ++pair) {
+        const int32_t s = (int32_t)(pair / num_kv_heads);
+        const int32_t h = (int32_t)(pair % num_kv_heads);
+        if (pair_mask && !pair_mask[pair])
+            continue;
+        const int32_t T = eff_len(context_lens, s, max_blocks_per_seq, block_size);
+        double *K = (double *)malloc(sizeof(double) * ((size_t)T * head_dim + 1));
+        double *V = (double *)malloc(sizeof(double) * ((size_t)T * head_dim + 1));
+        double *w = (double *)malloc(sizeof(double) * ((size_t)T + 1));
+        double *qrow = (double *)malloc(sizeof(double) * (size_t)head_dim);
+        const int32_t *table = block_tables + (int64_t)s * max_blocks_per_seq;
+        int bad = 0;
+        for (int32_t t = 0; t < T && !bad; ++t) {
+            const int64_t phys = table[t / block_size];
+            if (phys < 0 || phys >= num_blocks) {
+                bad = 1;
+                break;
+            }
+            const int64_t base =
+                ((phys * block_size + t % block_size) * num_kv_heads + h) * (int64_t)head_dim;
+            for (int32_t d = 0; d < head_dim; ++d) {
+                K[(int64_t)t * head_dim + d] = oracle_e4m3_decode(k_cache[base + d]) * k_scale[h];
+                V[(int64_t)t * head_dim + d] = oracle_e4m3_decode(v_cache[base + d]) * v_scale[h];
+            }
+        }
+        if (bad) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            status = -1;
+        }
+        for (int32_t j = 0; j < n_query_per_seq && !bad; ++j) {
+            const int32_t lim = T - n_query_per_seq + j;
+            for (int32_t g = 0; g < group; ++g) {
+                const int32_t qh = h * group + g;
+                const int64_t row = ((int64_t)s * n_query_per_seq + j) * num_q_heads + qh;
+                double *o = out + row * head_dim;
+                for (int32_t d = 0; d < head_dim; ++d)
+                    o[d] = 0.0;
+                if (lim < 0 || T == 0)
+                    continue;
+                for (int32_t d = 0; d < head_dim; ++d)
+                    qrow[d] = bf16_to_double(q[row * head_dim + d]);
+                row_weights(qrow, K, T, lim, head_dim, (double)scale, w);
+                for (int32_t t = 0; t <= lim && t < T; ++t)
+                    for (int32_t d = 0; d < head_dim; ++d)
+                        o[d] += w[t] * V[(int64_t)t * head_dim + d];
+            }
+        }
+        free(K);
+        free(V);
+        free(w);
+        free(qrow);
+    }
+    return status;
+}
+
+/* Element-wise helpers for the tests. */
+void oracle_e4m3_encode_array(const float *x, int64_t n, uint8_t *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_e4m3_encode(x[i]);
+}
+
+void oracle_e4m3_decode_array(const uint8_t *c, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_e4m3_decode(c[i]);
+}

@@ -42,6 +42,8 @@ CHUNK_TOKENS = 4096
 
 # Stream ids inside one workload's SeedSequence.
 _S_LENS, _S_PERM, _S_SHARE, _S_Q, _S_KV = 1, 2, 3, 4, 7
+_S_FP8 = 11
+E4M3_NAN = np.uint8(0x7F)  # the E4M3 code S.1111.111 is NaN
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -392,3 +394,33 @@ def unshare_prefix(w: Workload) -> Workload:
     out.prefix_blocks = np.zeros(0, dtype=np.int32)
     out.k_full = out.v_full = None
     return out
+
+
+# ----------------------------------------------------------------------------
+# FP8 (E4M3) pools standing in for a workload's bf16 pools
+# ----------------------------------------------------------------------------
+def fp8_pools(w: Workload, seed: Optional[int] = None):
+    """uint8 code pools of the same shape as ``w``'s pools, and per-kv-head scales.
+
+    Every slot that holds a token gets a random E4M3 code with an exponent field
+    in 1..10 (magnitudes 2^-6 .. 15, i.e. 0.004 .. 3.75 after a scale near 1/4),
+    any mantissa and either sign; slots without a token (and this step's new
+    slots, which the append fills) hold the NaN code. Codes are drawn as bit
+    fields: no value is encoded here. Scales: K 0.25 * (1 + h/16), V
+    0.3 * (1 + h/32) for kv head h (float32). Returns (k8, v8, k_scale, v_scale).
+    """
+    rng = _rng(w.seed if seed is None else seed, _S_FP8)
+
+    def codes(pool):
+        r = rng.integers(0, 256, size=pool.shape, dtype=np.uint8)
+        field = (((r >> 3) & np.uint8(15)) % np.uint8(10)) + np.uint8(1)
+        c = (r & np.uint8(0x87)) | (field << np.uint8(3))
+        c[pool == SENTINEL_BF16] = E4M3_NAN
+        return c
+
+    k8 = codes(w.k_cache)
+    v8 = codes(w.v_cache)
+    h = np.arange(w.num_kv_heads, dtype=np.float32)
+    k_scale = (np.float32(0.25) * (np.float32(1) + h / np.float32(16))).astype(np.float32)
+    v_scale = (np.float32(0.3) * (np.float32(1) + h / np.float32(32))).astype(np.float32)
+    return k8, v8, k_scale, v_scale
