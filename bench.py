@@ -141,8 +141,17 @@ def run_pkv(args, rank, world, dist):
     def up(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
 
+    fp8 = args.kv_dtype == "fp8"
     q = up(w.q)
-    k_cache, v_cache = up(w.k_cache), up(w.v_cache)
+    if fp8:
+        k8, v8, ks_h, vs_h = W.fp8_pools(w)
+        k_cache = torch.from_numpy(k8).to(dev)
+        v_cache = torch.from_numpy(v8).to(dev)
+        k_scale = torch.from_numpy(ks_h).to(dev)
+        v_scale = torch.from_numpy(vs_h).to(dev)
+        del k8, v8
+    else:
+        k_cache, v_cache = up(w.k_cache), up(w.v_cache)
     k_new, v_new = up(w.k_new), up(w.v_new)
     slots = torch.from_numpy(w.slot_mapping).to(dev)
     tables = torch.from_numpy(w.block_tables).to(dev)
@@ -152,15 +161,22 @@ def run_pkv(args, rank, world, dist):
                                                 w.num_kv_heads, w.head_dim))
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    attn_bytes = R.workload_bytes(w, unique=True)
-    attn_bytes_logical = R.workload_bytes(w, unique=False)
-    app_bytes = R.append_bytes(int(w.slot_mapping.size), w.num_kv_heads, w.head_dim)
+    eb = 1 if fp8 else 2
+    attn_bytes = R.workload_bytes(w, unique=True, kv_bytes_per_element=eb)
+    attn_bytes_logical = R.workload_bytes(w, unique=False, kv_bytes_per_element=eb)
+    app_bytes = R.append_bytes(int(w.slot_mapping.size), w.num_kv_heads, w.head_dim,
+                               kv_bytes_per_element=eb)
     step_bytes = attn_bytes + app_bytes
 
     def step():
-        pkv.kv_append(k_new, v_new, slots, k_cache, v_cache)
-        pkv.paged_decode_attention(q, k_cache, v_cache, tables, lens, w.n_query_per_seq,
-                                   w.scale, out, ws=ws)
+        if fp8:
+            pkv.kv_append_fp8(k_new, v_new, slots, k_cache, v_cache, k_scale, v_scale)
+            pkv.paged_decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, tables, lens,
+                                           w.n_query_per_seq, w.scale, out, ws=ws)
+        else:
+            pkv.kv_append(k_new, v_new, slots, k_cache, v_cache)
+            pkv.paged_decode_attention(q, k_cache, v_cache, tables, lens, w.n_query_per_seq,
+                                       w.scale, out, ws=ws)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -253,7 +269,7 @@ def run_pkv(args, rank, world, dist):
     peak, peak_kind = measured_peaks()
     achieved = attn_bytes / (kern_mean * 1e-3) / 1e9
     traffic = None
-    nt = NCU_TRAFFIC.get(args.workload)
+    nt = NCU_TRAFFIC.get(args.workload + ("/fp8" if fp8 else ""))
     if nt and nt.get("source_sha256") == kernel_source_sha():
         traffic = nt["bytes"]
     value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
@@ -269,18 +285,21 @@ def run_pkv(args, rank, world, dist):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) bf16 K/V/Q; pools in HBM; inputs > L2 and a 512 MiB "
-                "L2 flush between timed steps)",
+        "dtype": "bf16 (E4M3 KV cache, f16 products)" if fp8 else "bf16",
+        "data": ("synthetic (seeded random E4M3 code pools with per-head scales, N(0,1) bf16 "
+                 "Q and new rows; " if fp8 else "synthetic (seeded N(0,1) bf16 K/V/Q; ") +
+                "pools in HBM; inputs > L2 and a 512 MiB L2 flush between timed steps)",
         "config": {
-            "workload": args.workload,
+            "workload": args.workload + (" (fp8 KV cache)" if fp8 else ""),
+            "kv_dtype": args.kv_dtype,
             "num_seqs": w.num_seqs, "n_query_per_seq": w.n_query_per_seq,
             "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
             "head_dim": w.head_dim, "block_size": 16,
             "context_tokens": int(w.context_lens.sum()),
             "num_blocks": w.num_blocks, "parallelism": f"replicas x{world}",
             "l2": "flushed between timed steps (512 MiB memset, untimed)",
-            "step": "kv_append + paged_decode_attention (main + merge kernels)",
+            "step": ("kv_append_fp8 + paged_decode_attention_fp8" if fp8 else
+                     "kv_append + paged_decode_attention") + " (main + merge kernels)",
             "bytes_per_step": step_bytes, "attention_bytes_unique": attn_bytes,
             "attention_bytes_logical": attn_bytes_logical,
         },
@@ -425,18 +444,34 @@ def run_copy(args, rank, world, dist):
 
 
 # ------------------------------------------------------------------ oracle (CPU)
-def oracle_sample(w, budget_s: float, threads: int):
-    """Time the fp64 oracle on whole decode steps of ``w`` for about budget_s seconds
-    (at least one pass). Returns (GB/s of algorithmic bytes, passes, seconds)."""
+def oracle_step_fn(w, kv_dtype: str, threads: int):
+    """One whole decode step of the fp64 oracle on ``w`` (bf16 or E4M3 pools) and its
+    algorithmic bytes."""
     import oracle as O
 
     o = O.Oracle()
-    step_bytes = R.workload_bytes(w, unique=True) + R.append_bytes(
-        int(w.slot_mapping.size), w.num_kv_heads, w.head_dim)
+    eb = 1 if kv_dtype == "fp8" else 2
+    step_bytes = R.workload_bytes(w, unique=True, kv_bytes_per_element=eb) + R.append_bytes(
+        int(w.slot_mapping.size), w.num_kv_heads, w.head_dim, kv_bytes_per_element=eb)
+    if kv_dtype != "fp8":
+        return (lambda: o.step(w, threads=threads)), step_bytes
+    k8, v8, ks, vs = W.fp8_pools(w)
+
+    def step():
+        k, v = o.kv_append_fp8(w.k_new, w.v_new, w.slot_mapping, k8, v8, ks, vs)
+        o.paged_attention_fp8(w.q, k, v, w.block_tables, w.context_lens, w.n_query_per_seq,
+                              w.scale, ks, vs, threads=threads)
+    return step, step_bytes
+
+
+def oracle_sample(w, budget_s: float, threads: int, kv_dtype: str = "bf16"):
+    """Time the fp64 oracle on whole decode steps of ``w`` for about budget_s seconds
+    (at least one pass). Returns (GB/s of algorithmic bytes, passes, seconds)."""
+    step_fn, step_bytes = oracle_step_fn(w, kv_dtype, threads)
     t0 = time.perf_counter()
     passes = 0
     while True:
-        o.step(w, threads=threads)
+        step_fn()
         passes += 1
         el = time.perf_counter() - t0
         if el >= budget_s or el * (passes + 1) / passes > 3 * budget_s:
@@ -475,25 +510,22 @@ CPU_SAMPLE_SEQS = {"tiny": 4, "llama3_8b_decode": 64, "llama3_70b_mix": 64, "lon
 def cpu_baseline(args):
     threads = host_cores()
     w, desc = sample_workload(args.workload, CPU_SAMPLE_SEQS.get(args.workload, 8))
-    gbs, passes, el = oracle_sample(w, args.cpu_seconds, threads)
+    gbs, passes, el = oracle_sample(w, args.cpu_seconds, threads, args.kv_dtype)
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{desc} of {args.workload}, {passes} full decode step(s) (append + "
-                      f"fp64 attention), {el:.1f} s on {threads} threads"}
+            "sample": f"{desc} of {args.workload} ({args.kv_dtype} KV), {passes} full decode "
+                      f"step(s) (append + fp64 attention), {el:.1f} s on {threads} threads"}
 
 
 def run_reference(args):
     threads = host_cores()
     w, desc = sample_workload(args.workload, CPU_SAMPLE_SEQS.get(args.workload, 8))
-    import oracle as O
-    o = O.Oracle()
-    step_bytes = R.workload_bytes(w, unique=True) + R.append_bytes(
-        int(w.slot_mapping.size), w.num_kv_heads, w.head_dim)
+    step_fn, step_bytes = oracle_step_fn(w, args.kv_dtype, threads)
     for _ in range(args.warmup):
-        o.step(w, threads=threads)
+        step_fn()
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        o.step(w, threads=threads)
+        step_fn()
         times.append(time.perf_counter() - t0)
     ms = 1e3 * sum(times) / len(times)
     value = step_bytes / (ms * 1e-3) / 1e9
@@ -502,7 +534,9 @@ def run_reference(args):
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) bf16 inputs)",
-        "config": {"workload": args.workload, "sample": desc},
+        "config": {"workload": args.workload + (" (fp8 KV cache)" if args.kv_dtype == "fp8"
+                                                else ""),
+                   "kv_dtype": args.kv_dtype, "sample": desc},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle",
                          "sample": f"{desc} of {args.workload}; each step = append + fp64 attention"},
@@ -524,6 +558,8 @@ def main():
                     help="step: append + attention (the headline); copy_blocks: the "
                          "copy-on-write block copy alone")
     ap.add_argument("--pairs", type=int, default=4096, help="block pairs per copy_blocks step")
+    ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
+                    help="KV pool element type (fp8 = E4M3 codes with per-head scales)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

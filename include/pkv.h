@@ -198,6 +198,54 @@ pkv_status pkv_paged_decode_attention(const void *q, const void *k_cache, const 
                                       size_t workspace_bytes, void *stream);
 
 /*
+ * FP8 (E4M3) pools -- the same two operations on a cache stored in 8 bits.
+ *
+ * Passages: "ML Interview Prep, Lesson 13" section 3.7 (an fp8 KV cache stores
+ * keys and values in 8 bits while the matmuls run at 16 bits: twice the tokens
+ * in memory, half the KV bytes read per step) and "07 -- Inference" section
+ * 4.3 (E4M3 for inference, largest magnitude 448; per-tensor, per-channel or
+ * per-block scales). Here each kv head h has one float scale for K and one for
+ * V: a stored code c stands for e4m3(c) * scale[h].
+ *
+ * Pools: k_cache, v_cache are uint8 [num_blocks][16][num_kv_heads][head_dim]
+ * of E4M3 codes (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no
+ * infinities; S.1111.111 is NaN), 16-byte aligned. k_scale, v_scale: device
+ * float [num_kv_heads], 4-byte aligned, finite and nonzero.
+ *
+ * pkv_kv_append_fp8 -- for every i with slot_mapping[i] >= 0 and every head h:
+ *     k_cache[slot/16][slot%16][h][d] = E4M3(k_new[i][h][d] / k_scale[h])
+ * (the quotient in float, round to nearest; then the nearest E4M3 value, ties
+ * to even, magnitudes beyond 448 saturate to 448, NaN stays NaN); V likewise.
+ * Bit-exact. Other arguments, limits and errors as pkv_kv_append (head_dim a
+ * multiple of 8; caches 8-byte aligned at least).
+ *
+ * pkv_paged_decode_attention_fp8 -- pkv_paged_decode_attention over E4M3
+ * pools: K_s[t] = e4m3(code) * k_scale[h], V likewise, everything else as
+ * there (causality, GQA, output layout and dtype, workspace, errors; the
+ * workspace size is pkv_workspace_size's). head_dim must be 128
+ * (PKV_ERR_UNSUPPORTED otherwise). The kernels dequantise exactly to fp16 and
+ * multiply in fp16 with fp32 accumulation: q is rounded to fp16 (|q| must stay
+ * below 65504) and the softmax weights P are rounded to fp16 (relative error
+ * <= 2^-12) before the PV product. Against the fp64 definition on the
+ * dequantised pool the result is within |err| <= 2e-3 + 1e-2*|ref| for the
+ * bf16 output.
+ */
+pkv_status pkv_kv_append_fp8(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                             int64_t n_new, void *k_cache, void *v_cache, int64_t num_blocks,
+                             int32_t num_kv_heads, int32_t head_dim, const float *k_scale,
+                             const float *v_scale, void *stream);
+
+pkv_status pkv_paged_decode_attention_fp8(const void *q, const void *k_cache, const void *v_cache,
+                                          int64_t num_blocks, const float *k_scale,
+                                          const float *v_scale, const int32_t *block_tables,
+                                          int32_t max_blocks_per_seq,
+                                          const int32_t *context_lens, int32_t num_seqs,
+                                          int32_t n_query_per_seq, int32_t num_q_heads,
+                                          int32_t num_kv_heads, int32_t head_dim, float scale,
+                                          void *out, int32_t out_dtype, void *workspace,
+                                          size_t workspace_bytes, void *stream);
+
+/*
  * pkv_paged_decode_attention_static -- pkv_paged_decode_attention without a
  * caller-provided workspace, for callers that cannot allocate device memory.
  *

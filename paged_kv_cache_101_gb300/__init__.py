@@ -46,6 +46,9 @@ SIGNATURES = {
     "pkv_paged_decode_attention_static": ([_P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _I32,
                                            _I32, _F, _P, _I32, _P], ctypes.c_int),
     "pkv_copy_blocks": ([_P, _P, _I64, _I32, _I32, _P, _P, _I32, _P], ctypes.c_int),
+    "pkv_kv_append_fp8": ([_P, _P, _P, _I64, _P, _P, _I64, _I32, _I32, _P, _P, _P], ctypes.c_int),
+    "pkv_paged_decode_attention_fp8": ([_P, _P, _P, _I64, _P, _P, _P, _I32, _P, _I32, _I32, _I32,
+                                        _I32, _I32, _F, _P, _I32, _P, _SZ, _P], ctypes.c_int),
     # host block manager (include/pkv_block_manager.h)
     "pkv_bm_create": ([_I64], _P),
     "pkv_bm_destroy": ([_P], None),
@@ -167,6 +170,68 @@ def kv_append(k_new, v_new, slot_mapping, k_cache, v_cache):
                              _stream_handle(k_cache.device))
     if st != PKV_OK:
         raise PkvError("pkv_kv_append", st)
+
+
+def _check_fp8_pools(k_cache, v_cache, k_scale, v_scale):
+    torch = _torch()
+    _check(k_cache, "k_cache", torch.uint8, 4)
+    _check(v_cache, "v_cache", torch.uint8, 4)
+    _check(k_scale, "k_scale", torch.float32, 1)
+    _check(v_scale, "v_scale", torch.float32, 1)
+    NB, bs, Hkv, D = k_cache.shape
+    if bs != BLOCK_SIZE or v_cache.shape != k_cache.shape:
+        raise ValueError("pools must be [num_blocks, 16, Hkv, D] and equal in shape")
+    if k_scale.shape != (Hkv,) or v_scale.shape != (Hkv,):
+        raise ValueError("k_scale / v_scale must hold one float per kv head")
+    return NB, Hkv, D
+
+
+def kv_append_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale):
+    """Quantise bf16 rows ``[n_new, Hkv, D]`` into E4M3 (uint8) pools with per-head scales."""
+    torch = _torch()
+    _check(k_new, "k_new", torch.bfloat16, 3)
+    _check(v_new, "v_new", torch.bfloat16, 3)
+    _check(slot_mapping, "slot_mapping", torch.int64, 1)
+    NB, Hkv, D = _check_fp8_pools(k_cache, v_cache, k_scale, v_scale)
+    n = slot_mapping.shape[0]
+    if k_new.shape != (n, Hkv, D) or v_new.shape != (n, Hkv, D):
+        raise ValueError("k_new/v_new must be [n_new, Hkv, D] matching the pool")
+    st = lib().pkv_kv_append_fp8(k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(), n,
+                                 k_cache.data_ptr(), v_cache.data_ptr(), NB, Hkv, D,
+                                 k_scale.data_ptr(), v_scale.data_ptr(),
+                                 _stream_handle(k_cache.device))
+    if st != PKV_OK:
+        raise PkvError("pkv_kv_append_fp8", st)
+
+
+def paged_decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                               context_lens, n_query_per_seq, scale, out, ws=None):
+    """Decode attention over E4M3 (uint8) pools with per-head scales; writes ``out``."""
+    torch = _torch()
+    _check(q, "q", torch.bfloat16, 3)
+    NB, Hkv, D = _check_fp8_pools(k_cache, v_cache, k_scale, v_scale)
+    _check(block_tables, "block_tables", torch.int32, 2)
+    _check(context_lens, "context_lens", torch.int32, 1)
+    if out.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("out must be bfloat16 or float32")
+    _check(out, "out", out.dtype, 3)
+    S = context_lens.shape[0]
+    nq = int(n_query_per_seq)
+    Hq = q.shape[1]
+    if q.shape != (S * nq, Hq, D) or out.shape != q.shape or block_tables.shape[0] != S:
+        raise ValueError("q/out must be [num_seqs * n_query_per_seq, Hq, D], tables [num_seqs, MB]")
+    need = workspace_size(S, nq, Hq, Hkv, D)
+    if ws is None:
+        ws = workspace(q.device, need)
+    st = lib().pkv_paged_decode_attention_fp8(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), NB, k_scale.data_ptr(),
+        v_scale.data_ptr(), block_tables.data_ptr(), block_tables.shape[1],
+        context_lens.data_ptr(), S, nq, Hq, Hkv, D, float(scale), out.data_ptr(),
+        PKV_FP32 if out.dtype == torch.float32 else PKV_BF16, ws.data_ptr(), ws.numel(),
+        _stream_handle(q.device))
+    if st != PKV_OK:
+        raise PkvError("pkv_paged_decode_attention_fp8", st)
+    return out
 
 
 def copy_blocks(k_cache, v_cache, src, dst):

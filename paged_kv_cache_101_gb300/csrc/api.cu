@@ -120,17 +120,44 @@ CUresult encode_pool_block(CUtensorMap *map, const void *base, int64_t num_block
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// E4M3 pools [num_blocks][16][Hkv][128] of uint8: a head row is one 128-byte
+// swizzle row. Tile boxes: (128, 1, Hkv, 16, num_blocks) with box (128,1,1,16,1);
+// whole-block boxes: (128, 16, 1, Hkv, num_blocks) with box (128,16,1,hg,1), so
+// shared memory holds [head][token][128 B] either way.
+CUresult encode_pool_fp8(CUtensorMap *map, const void *base, int64_t num_blocks, int Hkv, int hg)
+{
+    const cuuint64_t row = 128, tok = cuuint64_t(Hkv) * 128, blk = 16 * tok;
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    if (hg == 0) {
+        const cuuint64_t dims[5] = {128, 1, cuuint64_t(Hkv), 16, cuuint64_t(num_blocks)};
+        const cuuint64_t strides[4] = {row, row, tok, blk};
+        const cuuint32_t box[5] = {128, 1, 1, 16, 1};
+        return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void *>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    const cuuint64_t dims[5] = {128, 16, 1, cuuint64_t(Hkv), cuuint64_t(num_blocks)};
+    const cuuint64_t strides[4] = {tok, row, row, blk};
+    const cuuint32_t box[5] = {128, 16, 1, cuuint32_t(hg), 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 struct MapEntry {
     const void *base = nullptr;
     int64_t nb = 0;
     int hkv = 0, d = 0, dev = -1, kind = 0;  // kind 0: tile boxes, else heads per box
+    int kv8 = 0;
     CUtensorMap map;
 };
 MapEntry g_maps[16];
 int g_map_next = 0;
 
 // kind 0: tile-box map; kind hg > 0: whole-block map with hg heads per box.
-cudaError_t pool_map(const void *base, int64_t nb, int Hkv, int D, int kind, CUtensorMap *out)
+cudaError_t pool_map(const void *base, int64_t nb, int Hkv, int D, int kind, int kv8,
+                     CUtensorMap *out)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -142,14 +169,15 @@ cudaError_t pool_map(const void *base, int64_t nb, int Hkv, int D, int kind, CUt
     std::lock_guard<std::mutex> lk(g_mu);
     for (auto &m : g_maps)
         if (m.base == base && m.nb == nb && m.hkv == Hkv && m.d == D && m.dev == dev &&
-            m.kind == kind) {
+            m.kind == kind && m.kv8 == kv8) {
             *out = m.map;
             return cudaSuccess;
         }
     MapEntry &m = g_maps[g_map_next];
     g_map_next = (g_map_next + 1) % 16;
-    const CUresult r = kind == 0 ? encode_pool(&m.map, base, nb, Hkv, D)
-                                 : encode_pool_block(&m.map, base, nb, Hkv, D, kind);
+    const CUresult r = kv8         ? encode_pool_fp8(&m.map, base, nb, Hkv, kind)
+                       : kind == 0 ? encode_pool(&m.map, base, nb, Hkv, D)
+                                   : encode_pool_block(&m.map, base, nb, Hkv, D, kind);
     if (r != CUDA_SUCCESS) {
         m.base = nullptr;
         return cudaErrorInvalidValue;
@@ -158,6 +186,7 @@ cudaError_t pool_map(const void *base, int64_t nb, int Hkv, int D, int kind, CUt
     m.nb = nb;
     m.hkv = Hkv;
     m.d = D;
+    m.kv8 = kv8;
     m.dev = dev;
     m.kind = kind;
     *out = m.map;
@@ -197,7 +226,8 @@ size_t workspace_zero_prefix(int32_t num_seqs, int32_t n_query_per_seq, int32_t 
         return 0;
     DecodePlan pl;
     if (plan_decode(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim, 1, d.num_sms,
-                    g_opt_num_ctas, g_opt_stages, g_opt_heads, g_opt_tail, d.smem_optin, &pl) != 0)
+                    g_opt_num_ctas, g_opt_stages, g_opt_heads, g_opt_tail, d.smem_optin, 0,
+                    &pl) != 0)
         return 0;
     return kWsHeaderBytes;
 }
@@ -335,22 +365,29 @@ size_t pkv_workspace_size(int32_t num_seqs, int32_t n_query_per_seq, int32_t num
     pkv::DecodePlan pl;
     if (pkv::plan_decode(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim, 1,
                          d.num_sms, g_opt_num_ctas, g_opt_stages, g_opt_heads, g_opt_tail, d.smem_optin,
-                         &pl) != 0)
+                         0, &pl) != 0)
         return 0;
     return pl.ws_bytes;
 }
 
-pkv_status pkv_paged_decode_attention(const void *q, const void *k_cache, const void *v_cache,
-                                      int64_t num_blocks, const int32_t *block_tables,
-                                      int32_t max_blocks_per_seq, const int32_t *context_lens,
-                                      int32_t num_seqs, int32_t n_query_per_seq,
-                                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                                      float scale, void *out, int32_t out_dtype, void *workspace,
-                                      size_t workspace_bytes, void *stream)
+}  // extern "C"
+
+namespace {
+
+// The attention call for bf16 (kv8 = 0) or E4M3 (kv8 = 1, with scales) pools.
+pkv_status attention(const void *q, const void *k_cache, const void *v_cache, int64_t num_blocks,
+                     int kv8, const float *k_scale, const float *v_scale,
+                     const int32_t *block_tables, int32_t max_blocks_per_seq,
+                     const int32_t *context_lens, int32_t num_seqs, int32_t n_query_per_seq,
+                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, float scale,
+                     void *out, int32_t out_dtype, void *workspace, size_t workspace_bytes,
+                     void *stream)
 {
     pkv_status st = check_geometry(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim);
     if (st != PKV_OK)
         return st;
+    if (kv8 && head_dim != 128)
+        return PKV_ERR_UNSUPPORTED;
     if (num_blocks < 1 || max_blocks_per_seq < 1)
         return PKV_ERR_SHAPE;
     if (out_dtype != PKV_BF16 && out_dtype != PKV_FP32)
@@ -359,10 +396,14 @@ pkv_status pkv_paged_decode_attention(const void *q, const void *k_cache, const 
         return PKV_OK;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
         return PKV_ERR_NULL;
+    if (kv8 && (!k_scale || !v_scale))
+        return PKV_ERR_NULL;
     if (!workspace)
         return PKV_ERR_WORKSPACE;
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
         !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(workspace, 256))
+        return PKV_ERR_ALIGN;
+    if (kv8 && (!aligned(k_scale, 4) || !aligned(v_scale, 4)))
         return PKV_ERR_ALIGN;
     if (max_blocks_per_seq > (1 << 26) || num_blocks > 0x7fffffffLL || num_seqs > (1 << 24) ||
         num_kv_heads > 65535)
@@ -374,7 +415,7 @@ pkv_status pkv_paged_decode_attention(const void *q, const void *k_cache, const 
     pkv::DecodePlan pl;
     if (pkv::plan_decode(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim,
                          max_blocks_per_seq, d.num_sms, g_opt_num_ctas, g_opt_stages,
-                         g_opt_heads, g_opt_tail, d.smem_optin, &pl) != 0)
+                         g_opt_heads, g_opt_tail, d.smem_optin, kv8, &pl) != 0)
         return PKV_ERR_UNSUPPORTED;
     if (workspace_bytes < pl.ws_bytes)
         return PKV_ERR_WORKSPACE;
@@ -386,14 +427,14 @@ pkv_status pkv_paged_decode_attention(const void *q, const void *k_cache, const 
     CUtensorMap kmap, vmap;
     int whole_box = 0;
     if (g_opt_box != 1 &&
-        pool_map(k_cache, num_blocks, num_kv_heads, head_dim, pl.HG, &kmap) == cudaSuccess &&
-        pool_map(v_cache, num_blocks, num_kv_heads, head_dim, pl.HG, &vmap) == cudaSuccess)
+        pool_map(k_cache, num_blocks, num_kv_heads, head_dim, pl.HG, kv8, &kmap) == cudaSuccess &&
+        pool_map(v_cache, num_blocks, num_kv_heads, head_dim, pl.HG, kv8, &vmap) == cudaSuccess)
         whole_box = 1;
     if (!whole_box) {
         if (g_opt_box == 2)
             return PKV_ERR_UNSUPPORTED;  // whole-block boxes requested but refused
-        if (pool_map(k_cache, num_blocks, num_kv_heads, head_dim, 0, &kmap) != cudaSuccess ||
-            pool_map(v_cache, num_blocks, num_kv_heads, head_dim, 0, &vmap) != cudaSuccess)
+        if (pool_map(k_cache, num_blocks, num_kv_heads, head_dim, 0, kv8, &kmap) != cudaSuccess ||
+            pool_map(v_cache, num_blocks, num_kv_heads, head_dim, 0, kv8, &vmap) != cudaSuccess)
             return PKV_ERR_CUDA;
     }
 
@@ -429,8 +470,70 @@ pkv_status pkv_paged_decode_attention(const void *q, const void *k_cache, const 
     p.ticket_div = pl.tail_div;
     p.ticket_units = 4;
     p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
     cudaError_t e = pkv::launch_decode(pl, p, kmap, vmap, static_cast<cudaStream_t>(stream),
                                        g_ev_before, g_ev_after);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_paged_decode_attention(const void *q, const void *k_cache, const void *v_cache,
+                                      int64_t num_blocks, const int32_t *block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                      int32_t num_seqs, int32_t n_query_per_seq,
+                                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                      float scale, void *out, int32_t out_dtype, void *workspace,
+                                      size_t workspace_bytes, void *stream)
+{
+    return attention(q, k_cache, v_cache, num_blocks, 0, nullptr, nullptr, block_tables,
+                     max_blocks_per_seq, context_lens, num_seqs, n_query_per_seq, num_q_heads,
+                     num_kv_heads, head_dim, scale, out, out_dtype, workspace, workspace_bytes,
+                     stream);
+}
+
+pkv_status pkv_paged_decode_attention_fp8(const void *q, const void *k_cache, const void *v_cache,
+                                          int64_t num_blocks, const float *k_scale,
+                                          const float *v_scale, const int32_t *block_tables,
+                                          int32_t max_blocks_per_seq,
+                                          const int32_t *context_lens, int32_t num_seqs,
+                                          int32_t n_query_per_seq, int32_t num_q_heads,
+                                          int32_t num_kv_heads, int32_t head_dim, float scale,
+                                          void *out, int32_t out_dtype, void *workspace,
+                                          size_t workspace_bytes, void *stream)
+{
+    return attention(q, k_cache, v_cache, num_blocks, 1, k_scale, v_scale, block_tables,
+                     max_blocks_per_seq, context_lens, num_seqs, n_query_per_seq, num_q_heads,
+                     num_kv_heads, head_dim, scale, out, out_dtype, workspace, workspace_bytes,
+                     stream);
+}
+
+pkv_status pkv_kv_append_fp8(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                             int64_t n_new, void *k_cache, void *v_cache, int64_t num_blocks,
+                             int32_t num_kv_heads, int32_t head_dim, const float *k_scale,
+                             const float *v_scale, void *stream)
+{
+    if (n_new < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 1)
+        return PKV_ERR_SHAPE;
+    if (n_new == 0)
+        return PKV_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale)
+        return PKV_ERR_NULL;
+    if (head_dim % 8 != 0)
+        return PKV_ERR_UNSUPPORTED;
+    if (head_dim > 1024 || num_kv_heads > 1024 || n_new > 0x7fffffffLL ||
+        num_blocks > (int64_t(1) << 40))
+        return PKV_ERR_RANGE;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 8) ||
+        !aligned(v_cache, 8) || !aligned(slot_mapping, 8) || !aligned(k_scale, 4) ||
+        !aligned(v_scale, 4))
+        return PKV_ERR_ALIGN;
+    cudaError_t e = pkv::launch_kv_append_fp8(k_new, v_new, slot_mapping, n_new, k_cache,
+                                              v_cache, num_blocks, num_kv_heads, head_dim,
+                                              k_scale, v_scale, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -159,11 +159,11 @@ __device__ void zero_sequence(const DecodeParams &p, int D, int s)
 }
 
 // ------------------------------------------------------------------ producer
-template <int D>
+template <int D, bool KV8>
 __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
                               const DecodeParams &p, const Smem &sm, int lane)
 {
-    constexpr int NH = D / 64;
+    constexpr int NH = KV8 ? 1 : D / 64;  // 16-row x 128-byte tiles per head
     const unsigned FULLMASK = 0xffffffffu;
     const int S = p.S;
 
@@ -403,10 +403,11 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
 // tokens x rows orientation (M = the block's 16 tokens, N = 8 rows, K = 16
 // dims), so a single n-tile covers the rows and no mma work is spent on
 // padding rows; lane holds rows 2tq, 2tq+1.
-template <int D>
+template <int D, bool KV8>
 __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, int lane)
 {
-    constexpr int NH = D / 64;  // 64-column halves per head row
+    // bf16: a head row is D/64 tiles of 64 columns; E4M3: one 128-byte tile
+    constexpr int NH = KV8 ? 1 : D / 64;
     constexpr int KS = D / 16;  // k-steps of the score mma
     constexpr int MT = D / 16;  // 16-dim m-tiles of the PV mma
     const int hl = cw;          // kv head within the group (one warp per head)
@@ -422,6 +423,8 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
     float acc[MT][4];
     uint32_t qf[KS][2];
     float m_r[2], l_r[2];
+    // E4M3: K's scale folds into the score scale, V's into the output
+    float qscale = p.scale_log2, vscale = 1.f;
     int jrow[2];  // query index j of this lane's two score rows
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
@@ -470,6 +473,10 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
         if (h.flags & F_FIRST) {
             // a new segment: fresh running state and its query rows
             reset_state();
+            if constexpr (KV8) {
+                qscale = p.scale_log2 * __ldg(p.k_scale + kvh);
+                vscale = __ldg(p.v_scale + kvh);
+            }
             if (g < p.rows) {
                 const int j = g / p.G;
                 const int gq = g - j * p.G;
@@ -477,8 +484,16 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
                     p.q + ((int64_t(h.s) * p.nq + j) * p.Hq + int64_t(kvh) * p.G + gq) * D);
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
-                    qf[ks][0] = __ldg(qrow + ks * 8 + tq);
-                    qf[ks][1] = __ldg(qrow + ks * 8 + 4 + tq);
+                    if constexpr (KV8) {
+                        // k-step ks = 16-byte chunk ks of the E4M3 row; lane tq holds
+                        // dims 16ks+4tq .. +3 (k indices 2tq, 2tq+1 and 2tq+8, 2tq+9)
+                        const uint2 w = __ldg(reinterpret_cast<const uint2 *>(qrow) + ks * 4 + tq);
+                        qf[ks][0] = bf16x2_to_f16x2(w.x);
+                        qf[ks][1] = bf16x2_to_f16x2(w.y);
+                    } else {
+                        qf[ks][0] = __ldg(qrow + ks * 8 + tq);
+                        qf[ks][1] = __ldg(qrow + ks * 8 + 4 + tq);
+                    }
                 }
             }
         }
@@ -492,17 +507,35 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
 #pragma unroll
         for (int e = 0; e < 4; ++e)
             sc[e] = sc2[e] = 0.f;
+        if constexpr (KV8) {
+            // one ldmatrix brings chunks 2i and 2i+1 of tokens 0-7 and 8-15; a lane
+            // gets 4 codes (dims 4tq..4tq+3 of its chunk) per matrix
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            const int chunk = 2 * ks + k_cadd;
-            const uint32_t addr = kb + uint32_t((chunk >> 3) * kTileBytes + k_tok * 128 +
-                                                (((chunk & 7) ^ sw) << 4));
-            uint32_t a[4];
-            ldsm_x4(addr, a);
-            if (ks & 1)
-                mma_bf16_16816(sc2, a, qf[ks][0], qf[ks][1]);
-            else
-                mma_bf16_16816(sc, a, qf[ks][0], qf[ks][1]);
+            for (int i = 0; i < KS / 2; ++i) {
+                const int chunk = 2 * i + k_cadd;
+                const uint32_t addr = kb + uint32_t(k_tok * 128 + ((chunk ^ sw) << 4));
+                uint32_t r[4];
+                ldsm_x4(addr, r);
+                const uint32_t a0[4] = {e4m3x2_to_f16x2(r[0]), e4m3x2_to_f16x2(r[1]),
+                                        e4m3x2_to_f16x2(r[0] >> 16), e4m3x2_to_f16x2(r[1] >> 16)};
+                const uint32_t a1[4] = {e4m3x2_to_f16x2(r[2]), e4m3x2_to_f16x2(r[3]),
+                                        e4m3x2_to_f16x2(r[2] >> 16), e4m3x2_to_f16x2(r[3] >> 16)};
+                mma_f16_16816(sc, a0, qf[2 * i][0], qf[2 * i][1]);
+                mma_f16_16816(sc2, a1, qf[2 * i + 1][0], qf[2 * i + 1][1]);
+            }
+        } else {
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const int chunk = 2 * ks + k_cadd;
+                const uint32_t addr = kb + uint32_t((chunk >> 3) * kTileBytes + k_tok * 128 +
+                                                    (((chunk & 7) ^ sw) << 4));
+                uint32_t a[4];
+                ldsm_x4(addr, a);
+                if (ks & 1)
+                    mma_bf16_16816(sc2, a, qf[ks][0], qf[ks][1]);
+                else
+                    mma_bf16_16816(sc, a, qf[ks][0], qf[ks][1]);
+            }
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e)
@@ -513,7 +546,7 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
         const bool need_mask = (t0 + kBlockSize - 1) > (h.T - p.nq);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            float x = sc[e] * p.scale_log2;
+            float x = sc[e] * qscale;
             if (need_mask) {
                 const int tok = t0 + g + ((e >> 1) << 3);
                 const int lim = h.T - p.nq + jrow[e & 1];
@@ -565,8 +598,13 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
         }
 
         // ---- P = hi + lo (bf16 each), transposed into mma B fragments
+        //      (E4M3: P in f16, a single part: relative error <= 2^-12)
         uint32_t bh[2], bl[2];
-        {
+        if constexpr (KV8) {
+            bh[0] = movmatrix_trans(pack_f16x2(sc[0], sc[1]));
+            bh[1] = movmatrix_trans(pack_f16x2(sc[2], sc[3]));
+            bl[0] = bl[1] = 0u;
+        } else {
             const uint32_t h01 = pack_bf16x2(sc[0], sc[1]);
             const uint32_t h23 = pack_bf16x2(sc[2], sc[3]);
             const uint32_t l01 = pack_bf16x2(sc[0] - bf16lo_f32(h01), sc[1] - bf16hi_f32(h01));
@@ -587,19 +625,42 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
         }
 
         // ---- O^T[d][row] += V^T[d][tok] . P^T[tok][row]
+        if constexpr (KV8) {
+            // ldmatrix.trans of chunks 2i, 2i+1 (tokens 0-7 and 8-15) gives a lane
+            // tokens 2tq, 2tq+1 of the code pair (dims 2g, 2g+1); bytes 0,2 form the
+            // even-dim m-tile 2i and bytes 1,3 the odd-dim m-tile 2i+1. In both,
+            // M-row g is dim 32i+2g(+1) and M-row g+8 is dim 32i+16+2g(+1).
 #pragma unroll
-        for (int i = 0; i < MT; ++i) {
-            const int chunk = 2 * i + v_cadd;
-            const uint32_t addr = vb + uint32_t((chunk >> 3) * kTileBytes + v_tok * 128 +
-                                                (((chunk & 7) ^ sw) << 4));
-            uint32_t a[4];
-            ldsm_x4_trans(addr, a);
-            a[0] &= mlo;
-            a[1] &= mlo;
-            a[2] &= mhi;
-            a[3] &= mhi;
-            mma_bf16_16816(acc[i], a, bh[0], bh[1]);
-            mma_bf16_16816(acc[i], a, bl[0], bl[1]);
+            for (int i = 0; i < MT / 2; ++i) {
+                const int chunk = 2 * i + v_cadd;
+                const uint32_t addr = vb + uint32_t(v_tok * 128 + ((chunk ^ sw) << 4));
+                uint32_t r[4];
+                ldsm_x4_trans(addr, r);
+                uint32_t ae[4], ao[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const uint32_t keep = m < 2 ? mlo : mhi;
+                    ae[m] = e4m3x2_to_f16x2(__byte_perm(r[m], 0u, 0x0020)) & keep;
+                    ao[m] = e4m3x2_to_f16x2(__byte_perm(r[m], 0u, 0x0031)) & keep;
+                }
+                mma_f16_16816(acc[2 * i], ae, bh[0], bh[1]);
+                mma_f16_16816(acc[2 * i + 1], ao, bh[0], bh[1]);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < MT; ++i) {
+                const int chunk = 2 * i + v_cadd;
+                const uint32_t addr = vb + uint32_t((chunk >> 3) * kTileBytes + v_tok * 128 +
+                                                    (((chunk & 7) ^ sw) << 4));
+                uint32_t a[4];
+                ldsm_x4_trans(addr, a);
+                a[0] &= mlo;
+                a[1] &= mlo;
+                a[2] &= mhi;
+                a[3] &= mhi;
+                mma_bf16_16816(acc[i], a, bh[0], bh[1]);
+                mma_bf16_16816(acc[i], a, bl[0], bl[1]);
+            }
         }
 
         // the stage's shared memory is no longer needed: hand it back
@@ -632,7 +693,27 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
                     const int gq = row - j * p.G;
                     const int64_t o = ((int64_t(h.s) * p.nq + j) * p.Hq + int64_t(kvh) * p.G + gq) * D;
                     const float inv = lf[r] > 0.f ? 1.f / lf[r] : 0.f;
-                    if (p.out_f32) {
+                    if constexpr (KV8) {
+                        const float f = inv * vscale;
+#pragma unroll
+                        for (int i = 0; i < MT / 2; ++i) {
+                            const int d0 = 32 * i + 2 * g;  // and d0 + 16 for M-rows g+8
+                            if (p.out_f32) {
+                                float *out = static_cast<float *>(p.out) + o;
+                                *reinterpret_cast<float2 *>(out + d0) =
+                                    make_float2(acc[2 * i][r] * f, acc[2 * i + 1][r] * f);
+                                *reinterpret_cast<float2 *>(out + d0 + 16) =
+                                    make_float2(acc[2 * i][r + 2] * f, acc[2 * i + 1][r + 2] * f);
+                            } else {
+                                __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out) + o;
+                                *reinterpret_cast<__nv_bfloat162 *>(out + d0) =
+                                    __floats2bfloat162_rn(acc[2 * i][r] * f, acc[2 * i + 1][r] * f);
+                                *reinterpret_cast<__nv_bfloat162 *>(out + d0 + 16) =
+                                    __floats2bfloat162_rn(acc[2 * i][r + 2] * f,
+                                                          acc[2 * i + 1][r + 2] * f);
+                            }
+                        }
+                    } else if (p.out_f32) {
                         float *out = static_cast<float *>(p.out) + o;
 #pragma unroll
                         for (int i = 0; i < MT; ++i) {
@@ -657,10 +738,21 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
                     if (row >= p.rows)
                         continue;
                     float *pa = p.part + (cellbase * p.rows + row) * D;
+                    if constexpr (KV8) {
 #pragma unroll
-                    for (int i = 0; i < MT; ++i) {
-                        pa[16 * i + g] = acc[i][r];
-                        pa[16 * i + 8 + g] = acc[i][r + 2];
+                        for (int i = 0; i < MT / 2; ++i) {
+                            const int d0 = 32 * i + 2 * g;
+                            *reinterpret_cast<float2 *>(pa + d0) =
+                                make_float2(acc[2 * i][r] * vscale, acc[2 * i + 1][r] * vscale);
+                            *reinterpret_cast<float2 *>(pa + d0 + 16) = make_float2(
+                                acc[2 * i][r + 2] * vscale, acc[2 * i + 1][r + 2] * vscale);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < MT; ++i) {
+                            pa[16 * i + g] = acc[i][r];
+                            pa[16 * i + 8 + g] = acc[i][r + 2];
+                        }
                     }
                     if (g == 0) {
                         float *ml = p.ml + (cellbase * p.rows + row) * 2;
@@ -679,10 +771,11 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
 // holds two rows (g, g+8): no register transposes, two-shuffle row reductions,
 // pairwise output stores. Same pipeline, masking, hi/lo split of P and lazy
 // rescale as the 8-row consumer.
-template <int D, int WPH>
+template <int D, int WPH, bool KV8>
 __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw, int lane)
 {
-    constexpr int NH = D / 64;  // 64-column halves per head row
+    // bf16: a head row is D/64 tiles of 64 columns; E4M3: one 128-byte tile
+    constexpr int NH = KV8 ? 1 : D / 64;
     constexpr int KS = D / 16;  // k-steps of the score mma
     constexpr int ND = D / 8;   // 8-dim n-tiles of the output
     const int hl = cw / WPH;    // kv head within the group
@@ -701,6 +794,8 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
     uint32_t qa[KS][4];
     float m_r[2], l_r[2];
     int jr[2];
+    // E4M3: K's scale folds into the score scale, V's into the output
+    float qscale = p.scale_log2, vscale = 1.f;
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
         const int j = (r0 + g + 8 * rr) / p.G;
@@ -748,6 +843,10 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
 
         if (h.flags & F_FIRST) {
             reset_state();
+            if constexpr (KV8) {
+                qscale = p.scale_log2 * __ldg(p.k_scale + kvh);
+                vscale = __ldg(p.v_scale + kvh);
+            }
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
                 const int row = r0 + g + 8 * rr;
@@ -758,8 +857,17 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
                         p.q + ((int64_t(h.s) * p.nq + j) * p.Hq + int64_t(kvh) * p.G + gq) * D);
 #pragma unroll
                     for (int ks = 0; ks < KS; ++ks) {
-                        qa[ks][rr] = __ldg(qrow + ks * 8 + tq);          // dims 16ks+2tq..
-                        qa[ks][2 + rr] = __ldg(qrow + ks * 8 + 4 + tq);  // dims 16ks+8+2tq..
+                        if constexpr (KV8) {
+                            // k-step ks = 16-byte chunk ks of the E4M3 row: dims 16ks+4tq,
+                            // +1 are k indices 2tq, 2tq+1; dims +2, +3 are 2tq+8, 2tq+9
+                            const uint2 w =
+                                __ldg(reinterpret_cast<const uint2 *>(qrow) + ks * 4 + tq);
+                            qa[ks][rr] = bf16x2_to_f16x2(w.x);
+                            qa[ks][2 + rr] = bf16x2_to_f16x2(w.y);
+                        } else {
+                            qa[ks][rr] = __ldg(qrow + ks * 8 + tq);          // dims 16ks+2tq..
+                            qa[ks][2 + rr] = __ldg(qrow + ks * 8 + 4 + tq);  // 16ks+8+2tq..
+                        }
                     }
                 }
             }
@@ -775,20 +883,38 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
 #pragma unroll
             for (int e = 0; e < 4; ++e)
                 sc[n][e] = sc2[n][e] = 0.f;
+        if constexpr (KV8) {
+            // matrices: tokens 0-7 / chunk 2i, tokens 0-7 / 2i+1, tokens 8-15 / 2i,
+            // tokens 8-15 / 2i+1; a lane gets dims 4tq..4tq+3 of token g
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            const int chunk = 2 * ks + k_cadd;
-            const uint32_t addr = kb + uint32_t((chunk >> 3) * kTileBytes + k_tok * 128 +
-                                                (((chunk & 7) ^ sw) << 4));
-            uint32_t b[4];
-            ldsm_x4(addr, b);
-            const uint32_t a[4] = {qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]};
-            if (ks & 1) {
-                mma_bf16_16816(sc2[0], a, b[0], b[1]);
-                mma_bf16_16816(sc2[1], a, b[2], b[3]);
-            } else {
-                mma_bf16_16816(sc[0], a, b[0], b[1]);
-                mma_bf16_16816(sc[1], a, b[2], b[3]);
+            for (int i = 0; i < KS / 2; ++i) {
+                const int chunk = 2 * i + k_cadd;
+                const uint32_t addr = kb + uint32_t(k_tok * 128 + ((chunk ^ sw) << 4));
+                uint32_t r[4];
+                ldsm_x4(addr, r);
+                mma_f16_16816(sc[0], qa[2 * i], e4m3x2_to_f16x2(r[0]), e4m3x2_to_f16x2(r[0] >> 16));
+                mma_f16_16816(sc[1], qa[2 * i], e4m3x2_to_f16x2(r[2]), e4m3x2_to_f16x2(r[2] >> 16));
+                mma_f16_16816(sc2[0], qa[2 * i + 1], e4m3x2_to_f16x2(r[1]),
+                              e4m3x2_to_f16x2(r[1] >> 16));
+                mma_f16_16816(sc2[1], qa[2 * i + 1], e4m3x2_to_f16x2(r[3]),
+                              e4m3x2_to_f16x2(r[3] >> 16));
+            }
+        } else {
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const int chunk = 2 * ks + k_cadd;
+                const uint32_t addr = kb + uint32_t((chunk >> 3) * kTileBytes + k_tok * 128 +
+                                                    (((chunk & 7) ^ sw) << 4));
+                uint32_t b[4];
+                ldsm_x4(addr, b);
+                const uint32_t a[4] = {qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]};
+                if (ks & 1) {
+                    mma_bf16_16816(sc2[0], a, b[0], b[1]);
+                    mma_bf16_16816(sc2[1], a, b[2], b[3]);
+                } else {
+                    mma_bf16_16816(sc[0], a, b[0], b[1]);
+                    mma_bf16_16816(sc[1], a, b[2], b[3]);
+                }
             }
         }
 #pragma unroll
@@ -804,7 +930,7 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
         for (int n = 0; n < 2; ++n)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                float x = sc[n][e] * p.scale_log2;
+                float x = sc[n][e] * qscale;
                 if (need_mask) {
                     const int tok = t0 + 8 * n + 2 * tq + (e & 1);
                     const int lim = h.T - p.nq + jr[e >> 1];
@@ -859,16 +985,25 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
         }
 
         // ---- P (16 rows x 16 tokens) as the A operand, split into bf16 hi + lo
+        //      (E4M3: P in f16, a single part: relative error <= 2^-12)
         uint32_t ph[4], plo[4];
+        if constexpr (KV8) {
 #pragma unroll
-        for (int n = 0; n < 2; ++n)
+            for (int n = 0; n < 2; ++n)
 #pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                const float x0 = sc[n][2 * rr], x1 = sc[n][2 * rr + 1];
-                const uint32_t hi = pack_bf16x2(x0, x1);
-                ph[2 * n + rr] = hi;  // a0 = (g, 0-7), a1 = (g+8, 0-7), a2 = (g, 8-15), a3 = (g+8, 8-15)
-                plo[2 * n + rr] = pack_bf16x2(x0 - bf16lo_f32(hi), x1 - bf16hi_f32(hi));
-            }
+                for (int rr = 0; rr < 2; ++rr)
+                    ph[2 * n + rr] = pack_f16x2(sc[n][2 * rr], sc[n][2 * rr + 1]);
+        } else {
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const float x0 = sc[n][2 * rr], x1 = sc[n][2 * rr + 1];
+                    const uint32_t hi = pack_bf16x2(x0, x1);
+                    ph[2 * n + rr] = hi;  // a0 = (g, 0-7), a1 = (g+8, 0-7), a2 = (g, 8-15), a3 = (g+8, 8-15)
+                    plo[2 * n + rr] = pack_bf16x2(x0 - bf16lo_f32(hi), x1 - bf16hi_f32(hi));
+                }
+        }
 
         // ---- V rows past the context (stale or NaN slots) are zeroed
         uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
@@ -880,21 +1015,45 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
         }
 
         // ---- O[row][d] += P[row][tok] . V[tok][d]
+        if constexpr (KV8) {
+            // ldmatrix.trans of chunks 2i, 2i+1 (tokens 0-7 and 8-15) gives a lane
+            // tokens 2tq, 2tq+1 of the code pair (dims 2g, 2g+1): bytes 0,2 make an
+            // n-tile of even dims, bytes 1,3 one of odd dims. n-tile 4i+2c+par holds
+            // dims 16(2i+c) + 2n + par for its columns n = 0..7.
 #pragma unroll
-        for (int i = 0; i < D / 16; ++i) {
-            const int chunk = 2 * i + v_cadd;
-            const uint32_t addr = vb + uint32_t((chunk >> 3) * kTileBytes + v_tok * 128 +
-                                                (((chunk & 7) ^ sw) << 4));
-            uint32_t b[4];
-            ldsm_x4_trans(addr, b);
-            b[0] &= mlo;
-            b[1] &= mhi;
-            b[2] &= mlo;
-            b[3] &= mhi;
-            mma_bf16_16816(acc[2 * i], ph, b[0], b[1]);
-            mma_bf16_16816(acc[2 * i], plo, b[0], b[1]);
-            mma_bf16_16816(acc[2 * i + 1], ph, b[2], b[3]);
-            mma_bf16_16816(acc[2 * i + 1], plo, b[2], b[3]);
+            for (int i = 0; i < D / 32; ++i) {
+                const int chunk = 2 * i + v_cadd;
+                const uint32_t addr = vb + uint32_t(v_tok * 128 + ((chunk ^ sw) << 4));
+                uint32_t r[4];
+                ldsm_x4_trans(addr, r);  // r0: tok 0-7 / 2i, r1: 8-15 / 2i, r2: 0-7 / 2i+1, r3
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const uint32_t lo_t = r[2 * c], hi_t = r[2 * c + 1];
+                    mma_f16_16816(acc[4 * i + 2 * c], ph,
+                                  e4m3x2_to_f16x2(__byte_perm(lo_t, 0u, 0x0020)) & mlo,
+                                  e4m3x2_to_f16x2(__byte_perm(hi_t, 0u, 0x0020)) & mhi);
+                    mma_f16_16816(acc[4 * i + 2 * c + 1], ph,
+                                  e4m3x2_to_f16x2(__byte_perm(lo_t, 0u, 0x0031)) & mlo,
+                                  e4m3x2_to_f16x2(__byte_perm(hi_t, 0u, 0x0031)) & mhi);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i) {
+                const int chunk = 2 * i + v_cadd;
+                const uint32_t addr = vb + uint32_t((chunk >> 3) * kTileBytes + v_tok * 128 +
+                                                    (((chunk & 7) ^ sw) << 4));
+                uint32_t b[4];
+                ldsm_x4_trans(addr, b);
+                b[0] &= mlo;
+                b[1] &= mhi;
+                b[2] &= mlo;
+                b[3] &= mhi;
+                mma_bf16_16816(acc[2 * i], ph, b[0], b[1]);
+                mma_bf16_16816(acc[2 * i], plo, b[0], b[1]);
+                mma_bf16_16816(acc[2 * i + 1], ph, b[2], b[3]);
+                mma_bf16_16816(acc[2 * i + 1], plo, b[2], b[3]);
+            }
         }
 
         // the stage's shared memory is no longer needed: hand it back
@@ -925,7 +1084,30 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
                     const int gq = row - j * p.G;
                     const int64_t o = ((int64_t(h.s) * p.nq + j) * p.Hq + int64_t(kvh) * p.G + gq) * D;
                     const float inv = lf[rr] > 0.f ? 1.f / lf[rr] : 0.f;
-                    if (p.out_f32) {
+                    if constexpr (KV8) {
+                        // chunk ch: dims 16ch + 4tq .. +3 from the even / odd n-tiles
+                        const float f = inv * vscale;
+#pragma unroll
+                        for (int ch = 0; ch < D / 16; ++ch) {
+                            const int te = 4 * (ch >> 1) + 2 * (ch & 1);
+                            const float x0 = acc[te][2 * rr] * f, x1 = acc[te + 1][2 * rr] * f;
+                            const float x2 = acc[te][2 * rr + 1] * f;
+                            const float x3 = acc[te + 1][2 * rr + 1] * f;
+                            if (p.out_f32) {
+                                *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + o +
+                                                            16 * ch + 4 * tq) =
+                                    make_float4(x0, x1, x2, x3);
+                            } else {
+                                const __nv_bfloat162 lo = __floats2bfloat162_rn(x0, x1);
+                                const __nv_bfloat162 hi = __floats2bfloat162_rn(x2, x3);
+                                uint2 w;
+                                w.x = *reinterpret_cast<const uint32_t *>(&lo);
+                                w.y = *reinterpret_cast<const uint32_t *>(&hi);
+                                *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.out) +
+                                                           o + 16 * ch + 4 * tq) = w;
+                            }
+                        }
+                    } else if (p.out_f32) {
                         float *out = static_cast<float *>(p.out) + o;
 #pragma unroll
                         for (int n = 0; n < ND; ++n)
@@ -947,10 +1129,20 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
                     if (row >= p.rows)
                         continue;
                     float *pa = p.part + (cellbase * p.rows + row) * D;
+                    if constexpr (KV8) {
 #pragma unroll
-                    for (int n = 0; n < ND; ++n)
-                        *reinterpret_cast<float2 *>(pa + 8 * n + 2 * tq) =
-                            make_float2(acc[n][2 * rr], acc[n][2 * rr + 1]);
+                        for (int ch = 0; ch < D / 16; ++ch) {
+                            const int te = 4 * (ch >> 1) + 2 * (ch & 1);
+                            *reinterpret_cast<float4 *>(pa + 16 * ch + 4 * tq) = make_float4(
+                                acc[te][2 * rr] * vscale, acc[te + 1][2 * rr] * vscale,
+                                acc[te][2 * rr + 1] * vscale, acc[te + 1][2 * rr + 1] * vscale);
+                        }
+                    } else {
+#pragma unroll
+                        for (int n = 0; n < ND; ++n)
+                            *reinterpret_cast<float2 *>(pa + 8 * n + 2 * tq) =
+                                make_float2(acc[n][2 * rr], acc[n][2 * rr + 1]);
+                    }
                     if (tq == 0) {
                         float *ml = p.ml + (cellbase * p.rows + row) * 2;
                         ml[0] = m_r[rr];
@@ -962,7 +1154,7 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
     }
 }
 
-template <int D, int NTW, int WPH>
+template <int D, int NTW, int WPH, bool KV8>
 __global__ void __launch_bounds__(kThreadsMax, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const DecodeParams p)
@@ -992,12 +1184,12 @@ __global__ void __launch_bounds__(kThreadsMax, 1)
     }
     __syncthreads();
     if (warp == 0) {
-        producer_warp<D>(&kmap, &vmap, p, sm, lane);
+        producer_warp<D, KV8>(&kmap, &vmap, p, sm, lane);
     } else {
         if constexpr (NTW == 2)
-            consumer_warp_m16<D, WPH>(p, sm, warp - 1, lane);
+            consumer_warp_m16<D, WPH, KV8>(p, sm, warp - 1, lane);
         else
-            consumer_warp_m8<D>(p, sm, warp - 1, lane);
+            consumer_warp_m8<D, KV8>(p, sm, warp - 1, lane);
     }
 }
 
@@ -1128,12 +1320,16 @@ __global__ void __launch_bounds__(256)
 static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int opt_ctas,
-                int opt_stages, int opt_heads, int opt_tail, int smem_optin, DecodePlan *pl)
+                int opt_stages, int opt_heads, int opt_tail, int smem_optin, int kv8,
+                DecodePlan *pl)
 {
     if (S < 1 || nq < 1 || Hkv < 1 || Hq % Hkv != 0 || (D != 64 && D != 128) || MB < 1)
         return -1;
+    if (kv8 && D != 128)
+        return -1;  // E4M3 rows are one 128-byte swizzle row
     DecodePlan P{};
     P.D = D;
+    P.kv8 = kv8 ? 1 : 0;
     P.G = Hq / Hkv;
     P.rows = P.G * nq;
     if (P.rows > kMaxRows)
@@ -1158,7 +1354,7 @@ int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int 
         }
     P.n_hg = Hkv / P.HG;
     P.threads = 32 * (1 + P.HG * P.wph);
-    P.stage_bytes = 2 * P.HG * (D / 64) * kTileBytes;
+    P.stage_bytes = 2 * P.HG * (P.kv8 ? 1 : D / 64) * kTileBytes;
     const int per_stage = P.stage_bytes + int(sizeof(StageHdr)) + 16;
     const int fixed = 1024 + int(sizeof(Cells)) + 64;
     int max_st = (smem_optin - fixed) / per_stage;
@@ -1188,12 +1384,12 @@ int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int 
     return 0;
 }
 
-template <int D, int NTW, int WPH>
+template <int D, int NTW, int WPH, bool KV8>
 static cudaError_t launch_one(const DecodePlan &pl, const DecodeParams &p, const CUtensorMap &kmap,
                               const CUtensorMap &vmap, cudaStream_t stream, cudaEvent_t ev_before,
                               cudaEvent_t ev_after)
 {
-    auto kern = paged_decode_kernel<D, NTW, WPH>;
+    auto kern = paged_decode_kernel<D, NTW, WPH, KV8>;
     static int configured_smem[64] = {0};  // per device ordinal
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1245,18 +1441,25 @@ cudaError_t launch_decode(const DecodePlan &pl, const DecodeParams &p, const CUt
                           const CUtensorMap &vmap, cudaStream_t stream, cudaEvent_t eb,
                           cudaEvent_t ea)
 {
+    if (pl.kv8) {  // E4M3 pools: D = 128 only
+        if (pl.wph == 2)
+            return launch_one<128, 2, 2, true>(pl, p, kmap, vmap, stream, eb, ea);
+        if (pl.ntw == 2)
+            return launch_one<128, 2, 1, true>(pl, p, kmap, vmap, stream, eb, ea);
+        return launch_one<128, 1, 1, true>(pl, p, kmap, vmap, stream, eb, ea);
+    }
     if (pl.D == 64) {
         if (pl.wph == 2)
-            return launch_one<64, 2, 2>(pl, p, kmap, vmap, stream, eb, ea);
+            return launch_one<64, 2, 2, false>(pl, p, kmap, vmap, stream, eb, ea);
         if (pl.ntw == 2)
-            return launch_one<64, 2, 1>(pl, p, kmap, vmap, stream, eb, ea);
-        return launch_one<64, 1, 1>(pl, p, kmap, vmap, stream, eb, ea);
+            return launch_one<64, 2, 1, false>(pl, p, kmap, vmap, stream, eb, ea);
+        return launch_one<64, 1, 1, false>(pl, p, kmap, vmap, stream, eb, ea);
     }
     if (pl.wph == 2)
-        return launch_one<128, 2, 2>(pl, p, kmap, vmap, stream, eb, ea);
+        return launch_one<128, 2, 2, false>(pl, p, kmap, vmap, stream, eb, ea);
     if (pl.ntw == 2)
-        return launch_one<128, 2, 1>(pl, p, kmap, vmap, stream, eb, ea);
-    return launch_one<128, 1, 1>(pl, p, kmap, vmap, stream, eb, ea);
+        return launch_one<128, 2, 1, false>(pl, p, kmap, vmap, stream, eb, ea);
+    return launch_one<128, 1, 1, false>(pl, p, kmap, vmap, stream, eb, ea);
 }
 
 }  // namespace pkv

@@ -145,6 +145,44 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// D += A * B, m16n8k16, f16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two floats -> packed f16x2 (round to nearest even); `lo` lands in bits 0..15.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// Two E4M3 codes (bits 0..7 and 8..15) -> f16x2 with the first in bits 0..15.
+// Exact: every E4M3 value (NaN included) is an f16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair)
+{
+    uint32_t d;
+    const uint16_t x = uint16_t(pair);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(x));
+    return d;
+}
+
+// Two floats -> two E4M3 codes, `lo` in bits 0..7: nearest, ties to even,
+// saturating to +-448 (NaN stays NaN).
+__device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi)
+{
+    uint16_t d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
 // Two floats -> packed bf16x2 (round to nearest even); `lo` lands in bits 0..15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
@@ -155,6 +193,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 
 __device__ __forceinline__ float bf16lo_f32(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16hi_f32(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
+
+// bf16x2 -> f16x2 (round to nearest; magnitudes beyond 65504 become infinite).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x)
+{
+    return pack_f16x2(bf16lo_f32(x), bf16hi_f32(x));
+}
 
 // 2^x (hardware approximation, |rel err| ~ 2^-22); 2^-inf = +0.
 __device__ __forceinline__ float ex2(float x)

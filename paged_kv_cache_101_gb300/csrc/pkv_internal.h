@@ -42,6 +42,7 @@ struct DecodePlan {
     int stage_bytes; // K + V of one 16-token block for HG heads
     int nst;         // pipeline stages
     int whole_box;   // 1: one TMA box per block for K (and V) of all HG heads
+    int kv8;         // 1: E4M3 pools (one 128-byte tile per head row), 0: bf16
     int grid;        // persistent CTAs
     int tickets_max; // cap on dynamically claimed tickets (0: static chunks only)
     int tail_div;    // the last 1/tail_div of the units go out as tickets (0: none)
@@ -71,10 +72,13 @@ struct DecodeParams {
     int ticket_div;        // the last F / ticket_div units go to tickets
     int ticket_units;      // at least this many units per ticket
     float scale_log2;      // scale * log2(e)
+    const float *k_scale;  // E4M3 pools: [Hkv] dequantisation scales (null for bf16)
+    const float *v_scale;
 };
 
 int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int opt_ctas,
-                int opt_stages, int opt_heads, int opt_tail, int smem_optin, DecodePlan *plan);
+                int opt_stages, int opt_heads, int opt_tail, int smem_optin, int kv8,
+                DecodePlan *plan);
 
 // ev_before/ev_after (may be null) are recorded around the kernel.
 cudaError_t launch_decode(const DecodePlan &plan, const DecodeParams &p, const CUtensorMap &kmap,
@@ -87,5 +91,12 @@ size_t workspace_zero_prefix(int32_t num_seqs, int32_t n_query_per_seq, int32_t 
 cudaError_t launch_kv_append(const void *k_new, const void *v_new, const int64_t *slot_mapping,
                              int64_t n_new, void *k_cache, void *v_cache, int64_t num_blocks,
                              int num_kv_heads, int head_dim, cudaStream_t stream);
+
+// E4M3 pools: quantise the new rows with per-kv-head scales.
+cudaError_t launch_kv_append_fp8(const void *k_new, const void *v_new,
+                                 const int64_t *slot_mapping, int64_t n_new, void *k_cache,
+                                 void *v_cache, int64_t num_blocks, int num_kv_heads,
+                                 int head_dim, const float *k_scale, const float *v_scale,
+                                 cudaStream_t stream);
 
 }  // namespace pkv

@@ -49,14 +49,18 @@ def waste_tokens(n: int, block_size: int = BLOCK_SIZE) -> int:
 def attention_bytes(context_lens: Sequence[int], n_query_per_seq: int, num_q_heads: int,
                     num_kv_heads: int, head_dim: int, out_bytes_per_element: int = 2,
                     shared_prefix_tokens: int = 0, n_sharers: int = 0,
-                    unique: bool = False) -> int:
-    """Algorithmic bytes of one ``paged_decode_attention`` call (bf16 Q/K/V)."""
+                    unique: bool = False, kv_bytes_per_element: int = 2) -> int:
+    """Algorithmic bytes of one ``paged_decode_attention`` call (bf16 Q and output;
+    K/V elements of ``kv_bytes_per_element``: 2 for bf16, 1 for E4M3 pools, whose
+    per-head scales add 8 bytes per kv head)."""
     T = np.asarray(context_lens, dtype=np.int64)
     S = int(T.size)
     tokens = int(T.sum())
     if unique and n_sharers > 1:
         tokens -= (n_sharers - 1) * int(shared_prefix_tokens)
-    kv = tokens * num_kv_heads * head_dim * 2 * 2
+    kv = tokens * num_kv_heads * head_dim * 2 * kv_bytes_per_element
+    if kv_bytes_per_element == 1:
+        kv += num_kv_heads * 8
     q = S * n_query_per_seq * num_q_heads * head_dim * 2
     out = S * n_query_per_seq * num_q_heads * head_dim * out_bytes_per_element
     table_entries = int(((T + BLOCK_SIZE - 1) // BLOCK_SIZE).sum())
@@ -66,9 +70,10 @@ def attention_bytes(context_lens: Sequence[int], n_query_per_seq: int, num_q_hea
     return kv + q + out + tables
 
 
-def append_bytes(n_new: int, num_kv_heads: int, head_dim: int) -> int:
-    """K and V of the new tokens read once and written once, plus the slot ids."""
-    return n_new * num_kv_heads * head_dim * 2 * 2 * 2 + n_new * 8
+def append_bytes(n_new: int, num_kv_heads: int, head_dim: int, kv_bytes_per_element: int = 2) -> int:
+    """K and V of the new tokens read once (bf16) and written once (at the pool's
+    element size), plus the slot ids."""
+    return n_new * num_kv_heads * head_dim * 2 * (2 + kv_bytes_per_element) + n_new * 8
 
 
 def attention_flops(context_lens: Sequence[int], n_query_per_seq: int, num_q_heads: int,
@@ -82,10 +87,12 @@ def attention_flops(context_lens: Sequence[int], n_query_per_seq: int, num_q_hea
     return 4 * head_dim * num_q_heads * visible
 
 
-def workload_bytes(w, unique: bool = True, out_bytes_per_element: int = 2) -> int:
+def workload_bytes(w, unique: bool = True, out_bytes_per_element: int = 2,
+                   kv_bytes_per_element: int = 2) -> int:
     """``attention_bytes`` of a ``workloads.Workload``."""
     n_sh = int(np.asarray(w.shared).sum())
     return attention_bytes(w.context_lens, w.n_query_per_seq, w.num_q_heads, w.num_kv_heads,
                            w.head_dim, out_bytes_per_element,
                            shared_prefix_tokens=w.meta.get("prefix_tokens", 0),
-                           n_sharers=n_sh, unique=unique)
+                           n_sharers=n_sh, unique=unique,
+                           kv_bytes_per_element=kv_bytes_per_element)

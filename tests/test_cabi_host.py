@@ -133,6 +133,28 @@ def test_attention_validation(lib):
     assert attn(lib, mb=1 << 27) == RANGE
 
 
+def attn8(lib, q=A, k=A, v=A, nb=64, ks=A, vs=A, bt=A, mb=8, cl=A, S=4, nq=1, hq=8, hkv=2,
+          d=128, scale=0.125, out=A, dt=0, ws=A, wsb=1 << 30):
+    return lib.pkv_paged_decode_attention_fp8(q, k, v, nb, ks, vs, bt, mb, cl, S, nq, hq, hkv,
+                                              d, scale, out, dt, ws, wsb, None)
+
+
+def test_fp8_validation(lib):
+    assert attn8(lib, S=0) == OK
+    assert attn8(lib, d=64) == UNSUP                    # E4M3 rows are one 128-byte row
+    assert attn8(lib, ks=None) == NULL
+    assert attn8(lib, vs=None) == NULL
+    assert attn8(lib, vs=A + 2) == ALIGN
+    assert attn8(lib, ws=None) == WORKSPACE
+    assert attn8(lib, nq=5) == UNSUP
+    ap = lib.pkv_kv_append_fp8
+    assert ap(A, A, A, 0, A, A, 8, 2, 64, A, A, None) == OK
+    assert ap(A, A, A, 4, A, A, 8, 2, 64, None, A, None) == NULL
+    assert ap(A, A, A, 4, A, A, 8, 2, 60, A, A, None) == UNSUP
+    assert ap(A, A, A, 4, A + 4, A, 8, 2, 64, A, A, None) == ALIGN
+    assert ap(A, A, A, -1, A, A, 8, 2, 64, A, A, None) == SHAPE
+
+
 def test_workspace_size_rejects_bad_geometry(lib):
     assert lib.pkv_workspace_size(4, 5, 8, 2, 64) == 0
     assert lib.pkv_workspace_size(4, 1, 8, 3, 64) == 0
