@@ -48,6 +48,9 @@ def _bind(lib):
     lib.oracle_kv_append.restype = ctypes.c_int
     lib.oracle_copy_blocks.argtypes = [P, P, i64, i32, i32, i32, P, P, i64]
     lib.oracle_copy_blocks.restype = ctypes.c_int
+    lib.oracle_paged_attention_varlen.argtypes = [P, P, P, i64, i32, P, i32, P, i32, P, P, P,
+                                                  i32, i32, i32, ctypes.c_float, P, i32]
+    lib.oracle_paged_attention_varlen.restype = ctypes.c_int
     lib.oracle_e4m3_encode_array.argtypes = [P, i64, P]
     lib.oracle_e4m3_encode_array.restype = None
     lib.oracle_e4m3_decode_array.argtypes = [P, i64, P]
@@ -128,6 +131,33 @@ class Oracle:
         if st not in (0, -1):
             raise RuntimeError(f"oracle_copy_blocks failed: {st}")
         return k_cache, v_cache
+
+    def paged_attention_varlen(self, q, k_cache, v_cache, block_tables, context_lens, q_start,
+                               scale, tree_mask=None, tree_len=None, threads: int = 0):
+        """fp64 ``[q_start[-1], Hq, D]``: per-sequence query counts, causal or tree masks."""
+        q = _c(q, np.uint16)
+        k_cache = _c(k_cache, np.uint16)
+        v_cache = _c(v_cache, np.uint16)
+        bt = _c(block_tables, np.int32)
+        cl = _c(context_lens, np.int32)
+        qs = _c(q_start, np.int32)
+        NB, bs, Hkv, D = k_cache.shape
+        S = cl.shape[0]
+        Hq = q.shape[1]
+        MB = bt.shape[1] if bt.ndim == 2 else 1
+        assert qs.shape == (S + 1,) and q.shape[0] >= qs[-1]
+        tm = tl = None
+        if tree_mask is not None:
+            tm = _c(tree_mask, np.uint32)
+            tl = _c(tree_len, np.int32)
+        out = np.zeros((int(qs[-1]), Hq, D), dtype=np.float64)
+        st = self.lib.oracle_paged_attention_varlen(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), NB, bs, _ptr(bt), MB, _ptr(cl), S, _ptr(qs),
+            _ptr(tm) if tm is not None else None, _ptr(tl) if tl is not None else None, Hq, Hkv,
+            D, ctypes.c_float(float(np.float32(scale))), _ptr(out), int(threads))
+        if st != 0:
+            raise ValueError(f"oracle_paged_attention_varlen: invalid input (status {st})")
+        return out
 
     # ---- FP8 (E4M3) KV cache
     def e4m3_encode(self, x) -> np.ndarray:

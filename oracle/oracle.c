@@ -571,3 +571,127 @@ void oracle_e4m3_decode_array(const uint8_t *c, int64_t n, double *out)
     for (int64_t i = 0; i < n; ++i)
         out[i] = oracle_e4m3_decode(c[i]);
 }
+
+/* ------------------------------------------------------------------------
+ * Variable query counts, tree masks (and chunked prefill through them).
+ *
+ * "Chapter 18", section 18.1.2 (tree-based speculative decoding: the target
+ * scores every node of a candidate tree in one pass, each node attending to
+ * its own ancestors) and "07 -- Inference", section 2.4 (chunked prefill: a
+ * prompt processed in chunks gives the same result as one prefill). Sequence s
+ * owns query rows q_start[s] .. q_start[s+1]-1 (q_len = their count) and T_s
+ * cached tokens including the new ones. Without masks query j sees positions
+ * 0 .. T_s - q_len + j (causal). With masks the last W = tree_len[s] positions
+ * form a window: query j sees every position before T_s - W, and window
+ * position i (absolute T_s - W + i) iff bit i of tree_mask[q_start[s] + j].
+ * A row that sees no position is all zeros.
+ * ---------------------------------------------------------------------- */
+
+/* Weights of one row over the visible positions (vis[t] != 0), others 0. */
+static void row_weights_visible(const double *qrow, const double *K, int32_t T,
+                                const uint8_t *vis, int32_t head_dim, double scale, double *w)
+{
+    double mx = -INFINITY;
+    for (int32_t t = 0; t < T; ++t) {
+        if (!vis[t]) {
+            w[t] = 0.0;
+            continue;
+        }
+        double dot = 0.0;
+        for (int32_t d = 0; d < head_dim; ++d)
+            dot += qrow[d] * K[(int64_t)t * head_dim + d];
+        w[t] = scale * dot;
+        if (w[t] > mx)
+            mx = w[t];
+    }
+    double z = 0.0;
+    for (int32_t t = 0; t < T; ++t)
+        if (vis[t]) {
+            w[t] = exp(w[t] - mx);
+            z += w[t];
+        }
+    for (int32_t t = 0; t < T; ++t)
+        if (vis[t])
+            w[t] /= z;
+}
+
+int oracle_paged_attention_varlen(const uint16_t *q, const uint16_t *k_cache,
+                                  const uint16_t *v_cache, int64_t num_blocks, int32_t block_size,
+                                  const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t *context_lens, int32_t num_seqs,
+                                  const int32_t *q_start, const uint32_t *tree_mask,
+                                  const int32_t *tree_len, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, float scale,
+                                  double *out, int32_t num_threads)
+{
+    if (check_shapes(num_seqs, 1, num_q_heads, num_kv_heads, head_dim, block_size))
+        return -2;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        if (q_start[s + 1] < q_start[s])
+            return -2;
+        if (tree_mask && (tree_len[s] < 0 || tree_len[s] > 32))
+            return -2;
+    }
+    const int32_t group = num_q_heads / num_kv_heads;
+    const int64_t npairs = (int64_t)num_seqs * num_kv_heads;
+    int status = 0;
+#ifdef _OPENMP
+    if (num_threads > 0)
+        omp_set_num_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t pair = 0; pair < npairs; ++pair) {
+        const int32_t s = (int32_t)(pair / num_kv_heads);
+        const int32_t h = (int32_t)(pair % num_kv_heads);
+        const int32_t T = eff_len(context_lens, s, max_blocks_per_seq, block_size);
+        const int32_t ql = q_start[s + 1] - q_start[s];
+        double *K = (double *)malloc(sizeof(double) * ((size_t)T * head_dim + 1));
+        double *V = (double *)malloc(sizeof(double) * ((size_t)T * head_dim + 1));
+        double *w = (double *)malloc(sizeof(double) * ((size_t)T + 1));
+        uint8_t *vis = (uint8_t *)malloc((size_t)T + 1);
+        double *qrow = (double *)malloc(sizeof(double) * (size_t)head_dim);
+        int bad = gather_kv(k_cache, v_cache, num_blocks, block_size,
+                            block_tables + (int64_t)s * max_blocks_per_seq, T,
+                            num_kv_heads, head_dim, h, K, V);
+        if (bad) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            status = -1;
+        }
+        for (int32_t j = 0; j < ql && !bad; ++j) {
+            const int64_t qr = (int64_t)q_start[s] + j; /* the query's row */
+            int any = 0;
+            for (int32_t t = 0; t < T; ++t) {
+                if (tree_mask) {
+                    const int32_t w0 = T - tree_len[s]; /* first window position */
+                    vis[t] = (uint8_t)(t < w0 || ((tree_mask[qr] >> (t - w0)) & 1u));
+                } else {
+                    vis[t] = (uint8_t)(t <= T - ql + j);
+                }
+                any |= vis[t];
+            }
+            for (int32_t g = 0; g < group; ++g) {
+                const int32_t qh = h * group + g;
+                double *o = out + (qr * num_q_heads + qh) * head_dim;
+                for (int32_t d = 0; d < head_dim; ++d)
+                    o[d] = 0.0;
+                if (!any)
+                    continue;
+                for (int32_t d = 0; d < head_dim; ++d)
+                    qrow[d] = bf16_to_double(q[(qr * num_q_heads + qh) * head_dim + d]);
+                row_weights_visible(qrow, K, T, vis, head_dim, (double)scale, w);
+                for (int32_t t = 0; t < T; ++t)
+                    if (vis[t])
+                        for (int32_t d = 0; d < head_dim; ++d)
+                            o[d] += w[t] * V[(int64_t)t * head_dim + d];
+            }
+        }
+        free(K);
+        free(V);
+        free(w);
+        free(vis);
+        free(qrow);
+    }
+    return status;
+}
