@@ -443,6 +443,137 @@ def run_copy(args, rank, world, dist):
     return res
 
 
+# ------------------------------------------------------------------ tree verification
+TREE_METRIC = "tree-verify attention GB/s (unique KV bytes); µs per step"
+
+
+def binary_tree_masks(levels: int):
+    """Ancestor-or-self bits of a complete binary tree, nodes in level order."""
+    masks = []
+    for node in range(2 ** levels - 1):
+        m, a = 0, node
+        while True:
+            m |= 1 << a
+            if a == 0:
+                break
+            a = (a - 1) // 2
+        masks.append(m)
+    return np.array(masks, dtype=np.uint32)
+
+
+def run_tree(args, rank, world, dist):
+    """Speculative tree verification on a workload's sequences: every sequence
+    appends a 15-node binary candidate tree (4 levels, branching 2) and scores all
+    nodes in one call; nodes see the cached context and their own ancestors.
+    The 15 rows of a sequence go out as runs of at most 32 / G queries."""
+    import torch
+
+    import paged_kv_cache_101_gb300 as pkv
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    base_lens = W.workload_lengths(args.workload)[0]
+    geo = W.WORKLOADS[args.workload]
+    Hq, Hkv, D = geo["Hq"], geo["Hkv"], geo["D"]
+    masks = binary_tree_masks(4)
+    n = masks.size
+    ctx = np.asarray(base_lens, dtype=np.int64) - geo["nq"]
+    T = (ctx + n).astype(np.int32)
+    w = W.make_custom(len(T), n, Hq, Hkv, D, T, seed=1234 + 17)
+    S = w.num_seqs
+    max_q = min(32 // (Hq // Hkv), n)
+    qs = (np.arange(S + 1) * n).astype(np.int32)
+    split = pkv.split_queries(qs, T, max_q, tree_len=np.full(S, n, np.int32))
+    V = split["table_row"].size
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+    q, k_cache, v_cache = up(w.q), up(w.k_cache), up(w.v_cache)
+    k_new, v_new = up(w.k_new), up(w.v_new)
+    slots = torch.from_numpy(w.slot_mapping).to(dev)
+    tables = torch.from_numpy(w.block_tables).to(dev)
+    v_lens, v_qs, v_tr = i32(split["context_lens"]), i32(split["q_start"]), i32(split["table_row"])
+    v_tl = i32(split["tree_len"])
+    tmask = torch.from_numpy(np.tile(masks, S).view(np.int32)).to(dev)
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    ws = pkv.workspace(dev, pkv.workspace_size(V, max_q, Hq, Hkv, D))
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    attn_bytes = R.attention_bytes(T, n, Hq, Hkv, D) + S * n * 4
+    step_bytes = attn_bytes + R.append_bytes(S * n, Hkv, D)
+
+    def step():
+        pkv.kv_append(k_new, v_new, slots, k_cache, v_cache)
+        pkv.paged_decode_attention_varlen(q, k_cache, v_cache, tables, v_lens, v_qs, max_q,
+                                          w.scale, out, tree_mask=tmask, tree_len=v_tl,
+                                          table_row=v_tr, ws=ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_k0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_k1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for ev in ev_k0 + ev_k1:
+        ev.record()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    HOOK = 4
+    for i in range(K):
+        flush.zero_()
+        if i % HOOK == 0:
+            pkv.set_profiling_events(ev_k0[i], ev_k1[i])
+        ev_s[i].record()
+        step()
+        ev_e[i].record()
+        if i % HOOK == 0:
+            pkv.set_profiling_events(None, None)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = sum(a.elapsed_time(b) for a, b in zip(ev_s, ev_e)) / K
+    kern = [ev_k0[i].elapsed_time(ev_k1[i]) for i in range(0, K, HOOK)]
+    kern_ms = sum(kern) / len(kern)
+    if dist is not None:
+        t = torch.tensor([ms, kern_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, kern_ms = (float(x) for x in t.tolist())
+    peak, peak_kind = measured_peaks()
+    achieved = attn_bytes / (kern_ms * 1e-3) / 1e9
+    res = {
+        "metric": TREE_METRIC, "value": round(world * step_bytes / (ms * 1e-3) / 1e9, 2),
+        "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(ms, 6), "us_per_step": round(ms * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16; 512 MiB L2 flush between steps)",
+        "config": {"workload": f"tree verify: {args.workload} lengths + 15-node binary tree",
+                   "num_seqs": S, "tree_nodes": n, "runs": V, "max_queries_per_run": max_q,
+                   "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": D,
+                   "context_tokens": int(T.sum()), "bytes_per_step": step_bytes,
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_kind} hbm_gbs (burst)", "traffic": None,
+                     "kernel_us": round(kern_ms * 1e3, 3), "algorithmic_bytes_per_launch": attn_bytes},
+        "gpu_launches": 3 * K,
+        "device_error_word": pkv.workspace_error(ws),
+    }
+    if clk is not None:
+        res["clocks"] = clk
+    return res
+
+
 # ------------------------------------------------------------------ oracle (CPU)
 def oracle_step_fn(w, kv_dtype: str, threads: int):
     """One whole decode step of the fp64 oracle on ``w`` (bf16 or E4M3 pools) and its
@@ -554,9 +685,10 @@ def main():
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="step", choices=["step", "copy_blocks"],
+    ap.add_argument("--op", default="step", choices=["step", "copy_blocks", "tree_verify"],
                     help="step: append + attention (the headline); copy_blocks: the "
-                         "copy-on-write block copy alone")
+                         "copy-on-write block copy alone; tree_verify: a 15-node candidate "
+                         "tree per sequence scored with tree masks")
     ap.add_argument("--pairs", type=int, default=4096, help="block pairs per copy_blocks step")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
                     help="KV pool element type (fp8 = E4M3 codes with per-head scales)")
@@ -578,8 +710,8 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         td.init_process_group("nccl")
         dist = td
-    if args.op == "copy_blocks":
-        res = run_copy(args, rank, world, dist)
+    if args.op in ("copy_blocks", "tree_verify"):
+        res = (run_copy if args.op == "copy_blocks" else run_tree)(args, rank, world, dist)
         if rank == 0:
             print(json.dumps(res), flush=True)
         if dist is not None:

@@ -127,7 +127,8 @@ pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, int64_t num_blocks,
 /*
  * pkv_workspace_size -- bytes of device workspace pkv_paged_decode_attention
  * needs for this geometry on the CURRENT CUDA device (the size depends on its
- * SM count). Returns 0 if the geometry is unsupported or no device is usable.
+ * SM count). n_query_per_seq may be up to 32 / (num_q_heads / num_kv_heads)
+ * (the max_q_len of pkv_paged_decode_attention_varlen). Returns 0 if the geometry is unsupported or no device is usable.
  * The workspace holds the split-K partial states (m, l, acc) that the merge
  * step combines, a per-sequence block prefix sum and a 4-byte device error
  * word at offset 0 (see pkv_paged_decode_attention).
@@ -196,6 +197,68 @@ pkv_status pkv_paged_decode_attention(const void *q, const void *k_cache, const 
                                       int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                       float scale, void *out, int32_t out_dtype, void *workspace,
                                       size_t workspace_bytes, void *stream);
+
+/*
+ * pkv_paged_decode_attention_varlen -- per-sequence query counts, optional
+ * tree masks, optional shared block-table rows.
+ *
+ * Passages: "Chapter 18" section 18.1.2 (tree-based speculative decoding: all
+ * candidate nodes are scored in one pass, each seeing its own ancestors) and
+ * section 18.2 (variable-length attention, no padding); "07 -- Inference"
+ * section 2.4 (chunked prefill: attending a prompt chunk by chunk gives the
+ * one-pass result).
+ *
+ * Sequence s owns query rows q_start[s] .. q_start[s+1]-1 of q and out
+ * (q_len_s of them, 0 <= q_len_s <= max_q_len) and T_s = context_lens[s]
+ * tokens read through block-table row table_row[s] (or s when table_row is
+ * NULL). Without masks query j sees positions 0 .. T_s - q_len_s + j (causal
+ * over the sequence's last q_len_s tokens). With masks the last
+ * W_s = tree_len[s] (0..32) positions form a window: query row r sees every
+ * position before T_s - W_s and window position i iff bit i of tree_mask[r].
+ * A row that sees nothing is zeros.
+ *
+ *   q, out          [total_q][num_q_heads][head_dim] (bf16 / out_dtype).
+ *   block_tables    device int32 [num_table_rows][max_blocks_per_seq].
+ *   table_row       device int32 [num_seqs] or NULL (then num_table_rows >= num_seqs).
+ *   context_lens    device int32 [num_seqs].
+ *   q_start         device int32 [num_seqs + 1], nondecreasing, q_start[num_seqs] <= total_q.
+ *   tree_mask       device uint32 [total_q] or NULL; tree_len device int32
+ *                   [num_seqs], given together with tree_mask.
+ *   max_q_len       >= 1 with (num_q_heads/num_kv_heads) * max_q_len <= 32 (the
+ *                   kernel's score rows per kv head; unlike the fixed-count call,
+ *                   more than 4 is allowed); the workspace is
+ *                   pkv_workspace_size(num_seqs, max_q_len, ...).
+ * Device values that break these rules (rows outside [0, total_q), more than
+ * max_q_len rows, a table row outside the tables) give that sequence no output
+ * and OR 16 into the workspace error word. Other arguments and errors as
+ * pkv_paged_decode_attention. Longer query runs go through pkv_split_queries.
+ */
+pkv_status pkv_paged_decode_attention_varlen(
+    const void *q, const void *k_cache, const void *v_cache, int64_t num_blocks,
+    const int32_t *block_tables, int32_t max_blocks_per_seq, int32_t num_table_rows,
+    const int32_t *table_row, const int32_t *context_lens, const int32_t *q_start,
+    const uint32_t *tree_mask, const int32_t *tree_len, int32_t num_seqs, int32_t max_q_len,
+    int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, float scale,
+    void *out, int32_t out_dtype, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * pkv_split_queries -- host arrays in and out: cut every sequence's query rows
+ * into runs of at most max_rows rows ("virtual sequences") for
+ * pkv_paged_decode_attention_varlen, so prefill chunks and large candidate
+ * trees fit its row limit. Run k of sequence s covers rows
+ * q_start[s] + k*max_rows .. (exclusive) min(q_start[s+1], ...), reads table row
+ * s, and keeps every row's visibility: without tree_len its context length is
+ * T_s - q_len_s + (its end row - q_start[s]) (causal); with tree_len its context
+ * is T_s and its window tree_len[s] (the rows keep their mask words).
+ * Sequences with no query row produce no run. Writes v_q_start[0..V],
+ * v_context_lens[0..V-1], v_table_row[0..V-1] and (with tree_len) v_tree_len;
+ * *num_virtual = V. PKV_ERR_RANGE (and *num_virtual = the V needed) when
+ * capacity < V; PKV_ERR_SHAPE for negative counts or max_rows < 1.
+ */
+pkv_status pkv_split_queries(const int32_t *q_start, const int32_t *context_lens,
+                             const int32_t *tree_len, int32_t num_seqs, int32_t max_rows,
+                             int32_t *v_q_start, int32_t *v_context_lens, int32_t *v_tree_len,
+                             int32_t *v_table_row, int32_t capacity, int32_t *num_virtual);
 
 /*
  * FP8 (E4M3) pools -- the same two operations on a cache stored in 8 bits.

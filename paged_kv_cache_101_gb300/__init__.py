@@ -46,6 +46,10 @@ SIGNATURES = {
     "pkv_paged_decode_attention_static": ([_P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _I32,
                                            _I32, _F, _P, _I32, _P], ctypes.c_int),
     "pkv_copy_blocks": ([_P, _P, _I64, _I32, _I32, _P, _P, _I32, _P], ctypes.c_int),
+    "pkv_paged_decode_attention_varlen": ([_P, _P, _P, _I64, _P, _I32, _I32, _P, _P, _P, _P, _P,
+                                           _I32, _I32, _I32, _I32, _I32, _I32, _F, _P, _I32, _P,
+                                           _SZ, _P], ctypes.c_int),
+    "pkv_split_queries": ([_P, _P, _P, _I32, _I32, _P, _P, _P, _P, _I32, _P], ctypes.c_int),
     "pkv_kv_append_fp8": ([_P, _P, _P, _I64, _P, _P, _I64, _I32, _I32, _P, _P, _P], ctypes.c_int),
     "pkv_paged_decode_attention_fp8": ([_P, _P, _P, _I64, _P, _P, _P, _I32, _P, _I32, _I32, _I32,
                                         _I32, _I32, _F, _P, _I32, _P, _SZ, _P], ctypes.c_int),
@@ -170,6 +174,87 @@ def kv_append(k_new, v_new, slot_mapping, k_cache, v_cache):
                              _stream_handle(k_cache.device))
     if st != PKV_OK:
         raise PkvError("pkv_kv_append", st)
+
+
+def split_queries(q_start, context_lens, max_rows, tree_len=None):
+    """Host: cut query runs into virtual sequences of at most ``max_rows`` rows
+    (see pkv_split_queries). Returns a dict of int32 numpy arrays: q_start
+    [V+1], context_lens [V], table_row [V] and, with tree_len, tree_len [V]."""
+    import numpy as np
+    qs = np.ascontiguousarray(q_start, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    S = cl.size
+    tl = None if tree_len is None else np.ascontiguousarray(tree_len, dtype=np.int32)
+    nv = ctypes.c_int32(0)
+    st = lib().pkv_split_queries(qs.ctypes.data, cl.ctypes.data,
+                                 tl.ctypes.data if tl is not None else None, S, int(max_rows),
+                                 None, None, None, None, 0, ctypes.byref(nv))
+    cap = nv.value
+    if st not in (PKV_OK, 5):
+        raise PkvError("pkv_split_queries", st)
+    vq = np.zeros(cap + 1, np.int32)
+    vc = np.zeros(max(cap, 1), np.int32)
+    vt = np.zeros(max(cap, 1), np.int32)
+    vr = np.zeros(max(cap, 1), np.int32)
+    st = lib().pkv_split_queries(qs.ctypes.data, cl.ctypes.data,
+                                 tl.ctypes.data if tl is not None else None, S, int(max_rows),
+                                 vq.ctypes.data, vc.ctypes.data, vt.ctypes.data, vr.ctypes.data,
+                                 cap, ctypes.byref(nv))
+    if st != PKV_OK:
+        raise PkvError("pkv_split_queries", st)
+    V = nv.value
+    out = dict(q_start=vq[:V + 1] if V else np.zeros(1, np.int32), context_lens=vc[:V],
+               table_row=vr[:V])
+    if tl is not None:
+        out["tree_len"] = vt[:V]
+    return out
+
+
+def paged_decode_attention_varlen(q, k_cache, v_cache, block_tables, context_lens, q_start,
+                                  max_q_len, scale, out, tree_mask=None, tree_len=None,
+                                  table_row=None, ws=None):
+    """Decode attention with per-sequence query counts (rows q_start[s] ..
+    q_start[s+1]-1 of q/out), optional tree masks (uint32 per row, with int32
+    windows tree_len) and optional block-table rows (table_row)."""
+    torch = _torch()
+    _check(q, "q", torch.bfloat16, 3)
+    _check(k_cache, "k_cache", torch.bfloat16, 4)
+    _check(v_cache, "v_cache", torch.bfloat16, 4)
+    _check(block_tables, "block_tables", torch.int32, 2)
+    _check(context_lens, "context_lens", torch.int32, 1)
+    _check(q_start, "q_start", torch.int32, 1)
+    if out.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("out must be bfloat16 or float32")
+    _check(out, "out", out.dtype, 3)
+    NB, bs, Hkv, D = k_cache.shape
+    if bs != BLOCK_SIZE or v_cache.shape != k_cache.shape:
+        raise ValueError("pools must be [num_blocks, 16, Hkv, D] and equal in shape")
+    S = context_lens.shape[0]
+    if q_start.shape[0] != S + 1 or out.shape != q.shape or q.shape[2] != D:
+        raise ValueError("q_start must have num_seqs + 1 entries; q and out [total_q, Hq, D]")
+    if (tree_mask is None) != (tree_len is None):
+        raise ValueError("tree_mask and tree_len come together")
+    if tree_mask is not None:
+        _check(tree_mask, "tree_mask", torch.int32, 1)   # uint32 bits stored as int32
+        _check(tree_len, "tree_len", torch.int32, 1)
+    if table_row is not None:
+        _check(table_row, "table_row", torch.int32, 1)
+    total_q, Hq = q.shape[0], q.shape[1]
+    need = workspace_size(S, int(max_q_len), Hq, Hkv, D)
+    if ws is None:
+        ws = workspace(q.device, need)
+    st = lib().pkv_paged_decode_attention_varlen(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), NB, block_tables.data_ptr(),
+        block_tables.shape[1], block_tables.shape[0],
+        table_row.data_ptr() if table_row is not None else None, context_lens.data_ptr(),
+        q_start.data_ptr(), tree_mask.data_ptr() if tree_mask is not None else None,
+        tree_len.data_ptr() if tree_len is not None else None, S, int(max_q_len), total_q, Hq,
+        Hkv, D, float(scale), out.data_ptr(),
+        PKV_FP32 if out.dtype == torch.float32 else PKV_BF16, ws.data_ptr(), ws.numel(),
+        _stream_handle(q.device))
+    if st != PKV_OK:
+        raise PkvError("pkv_paged_decode_attention_varlen", st)
+    return out
 
 
 def _check_fp8_pools(k_cache, v_cache, k_scale, v_scale):

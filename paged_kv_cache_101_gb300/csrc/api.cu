@@ -193,8 +193,11 @@ cudaError_t pool_map(const void *base, int64_t nb, int Hkv, int D, int kind, int
     return cudaSuccess;
 }
 
-// Host-side checks shared by the workspace query and the attention call.
-pkv_status check_geometry(int32_t num_seqs, int32_t nq, int32_t Hq, int32_t Hkv, int32_t D)
+// Host-side checks shared by the workspace query and the attention calls. The
+// fixed-count call takes 1..4 queries per sequence; the variable-count call any
+// count whose score rows (G per query) fit the kernel's 32 rows per kv head.
+pkv_status check_geometry(int32_t num_seqs, int32_t nq, int32_t Hq, int32_t Hkv, int32_t D,
+                          bool varlen = false)
 {
     if (num_seqs < 0 || nq < 1 || Hq < 1 || Hkv < 1)
         return PKV_ERR_SHAPE;
@@ -202,7 +205,7 @@ pkv_status check_geometry(int32_t num_seqs, int32_t nq, int32_t Hq, int32_t Hkv,
         return PKV_ERR_SHAPE;
     if (D != 64 && D != 128)
         return PKV_ERR_UNSUPPORTED;
-    if (nq > 4)
+    if (nq > 4 && !varlen)
         return PKV_ERR_UNSUPPORTED;
     if ((Hq / Hkv) * nq > pkv::kMaxRows)
         return PKV_ERR_UNSUPPORTED;
@@ -355,7 +358,8 @@ pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, int64_t num_blocks,
 size_t pkv_workspace_size(int32_t num_seqs, int32_t n_query_per_seq, int32_t num_q_heads,
                           int32_t num_kv_heads, int32_t head_dim)
 {
-    if (check_geometry(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim) != PKV_OK)
+    if (check_geometry(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim, true) !=
+        PKV_OK)
         return 0;
     if (num_seqs == 0)
         return 256;
@@ -374,16 +378,28 @@ size_t pkv_workspace_size(int32_t num_seqs, int32_t n_query_per_seq, int32_t num
 
 namespace {
 
-// The attention call for bf16 (kv8 = 0) or E4M3 (kv8 = 1, with scales) pools.
+// Variable query counts (all null / 0 for the fixed-count call).
+struct Varlen {
+    const int32_t *q_start = nullptr;
+    const uint32_t *tree_mask = nullptr;
+    const int32_t *tree_len = nullptr;
+    const int32_t *table_row = nullptr;
+    int32_t total_q = 0, table_rows = 0;
+};
+
+// The attention call for bf16 (kv8 = 0) or E4M3 (kv8 = 1, with scales) pools;
+// n_query_per_seq is the query count of every sequence, or with vl.q_start the
+// largest one.
 pkv_status attention(const void *q, const void *k_cache, const void *v_cache, int64_t num_blocks,
                      int kv8, const float *k_scale, const float *v_scale,
                      const int32_t *block_tables, int32_t max_blocks_per_seq,
                      const int32_t *context_lens, int32_t num_seqs, int32_t n_query_per_seq,
                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, float scale,
                      void *out, int32_t out_dtype, void *workspace, size_t workspace_bytes,
-                     void *stream)
+                     void *stream, const Varlen &vl = Varlen())
 {
-    pkv_status st = check_geometry(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim);
+    pkv_status st = check_geometry(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim,
+                                   vl.q_start != nullptr);
     if (st != PKV_OK)
         return st;
     if (kv8 && head_dim != 128)
@@ -472,6 +488,12 @@ pkv_status attention(const void *q, const void *k_cache, const void *v_cache, in
     p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
     p.k_scale = k_scale;
     p.v_scale = v_scale;
+    p.q_start = vl.q_start;
+    p.tree_mask = vl.tree_mask;
+    p.tree_len = vl.tree_len;
+    p.table_row = vl.table_row;
+    p.total_q = vl.q_start ? vl.total_q : num_seqs * n_query_per_seq;
+    p.table_rows = vl.table_row ? vl.table_rows : num_seqs;
     cudaError_t e = pkv::launch_decode(pl, p, kmap, vmap, static_cast<cudaStream_t>(stream),
                                        g_ev_before, g_ev_after);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
@@ -509,6 +531,36 @@ pkv_status pkv_paged_decode_attention_fp8(const void *q, const void *k_cache, co
                      max_blocks_per_seq, context_lens, num_seqs, n_query_per_seq, num_q_heads,
                      num_kv_heads, head_dim, scale, out, out_dtype, workspace, workspace_bytes,
                      stream);
+}
+
+pkv_status pkv_paged_decode_attention_varlen(
+    const void *q, const void *k_cache, const void *v_cache, int64_t num_blocks,
+    const int32_t *block_tables, int32_t max_blocks_per_seq, int32_t num_table_rows,
+    const int32_t *table_row, const int32_t *context_lens, const int32_t *q_start,
+    const uint32_t *tree_mask, const int32_t *tree_len, int32_t num_seqs, int32_t max_q_len,
+    int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, float scale,
+    void *out, int32_t out_dtype, void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (num_seqs > 0 && !q_start)
+        return PKV_ERR_NULL;
+    if ((tree_mask == nullptr) != (tree_len == nullptr))
+        return PKV_ERR_NULL;  // masks and their windows come together
+    if (total_q < 0 || num_table_rows < 0 || (table_row == nullptr && num_table_rows < num_seqs))
+        return PKV_ERR_SHAPE;
+    if ((q_start && !aligned(q_start, 4)) || (tree_mask && !aligned(tree_mask, 4)) ||
+        (tree_len && !aligned(tree_len, 4)) || (table_row && !aligned(table_row, 4)))
+        return PKV_ERR_ALIGN;
+    Varlen vl;
+    vl.q_start = q_start;
+    vl.tree_mask = tree_mask;
+    vl.tree_len = tree_len;
+    vl.table_row = table_row;
+    vl.total_q = total_q;
+    vl.table_rows = table_row ? num_table_rows : num_seqs;
+    return attention(q, k_cache, v_cache, num_blocks, 0, nullptr, nullptr, block_tables,
+                     max_blocks_per_seq, context_lens, num_seqs, max_q_len, num_q_heads,
+                     num_kv_heads, head_dim, scale, out, out_dtype, workspace, workspace_bytes,
+                     stream, vl);
 }
 
 pkv_status pkv_kv_append_fp8(const void *k_new, const void *v_new, const int64_t *slot_mapping,

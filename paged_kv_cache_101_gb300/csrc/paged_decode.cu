@@ -53,15 +53,17 @@
 namespace pkv {
 
 struct StageHdr {
-    int32_t s;      // sequence
+    int32_t q0;     // the sequence's first query row
     int32_t b;      // logical block within the sequence
     int32_t T;      // context length (clamped)
     int32_t hg;     // head group
     int32_t flags;  // F_*
     int32_t slot;   // partial slot: 0 if the segment opens its cell, else 1
     int32_t cell;   // cell holding this block
-    int32_t fs;     // flat index of the sequence's first unit (head group included)
+    int16_t ql;     // the sequence's query rows (G * ql score rows per kv head)
+    int16_t W;      // mask window: per-row masks rule the last W positions
 };
+static_assert(sizeof(StageHdr) == 32, "stage header: two 16-byte words");
 enum : int32_t { F_FIRST = 1, F_LAST = 2, F_DIRECT = 4, F_END = 8 };
 
 // The fixed partition of the flat unit space [0, F): cells 0..G-1 split
@@ -115,10 +117,54 @@ __device__ __forceinline__ int seq_tokens(const DecodeParams &p, int s)
     return T > cap ? cap : T;
 }
 
-__device__ __forceinline__ int seq_blocks(const DecodeParams &p, int s)
+// Per-sequence view of the inputs. Fixed query count: rows s*nq .. +nq, block
+// table row s, causal. Variable counts (q_start): rows q_start[s] ..
+// q_start[s+1]-1 (at most nq), table row table_row[s] (or s), and with tree
+// masks a window of tree_len[s] positions. Inconsistent device values (rows
+// outside [0, total_q), more rows than nq, a table row outside the tables)
+// leave the sequence without queries and set kErrBadQuery.
+struct SeqInfo {
+    int T;   // tokens (clamped to the table)
+    int nb;  // blocks to stream (0 if the sequence has no query rows)
+    int q0;  // first query row
+    int ql;  // query rows
+    int W;   // mask window (causal: ql)
+    int tr;  // block-table row
+};
+
+__device__ __forceinline__ SeqInfo seq_info(const DecodeParams &p, int s)
 {
-    return (seq_tokens(p, s) + kBlockSize - 1) / kBlockSize;
+    SeqInfo i;
+    i.T = seq_tokens(p, s);
+    i.q0 = s * p.nq;
+    i.ql = p.nq;
+    i.tr = s;
+    bool bad = false;
+    if (p.q_start) {
+        const int a = __ldg(p.q_start + s), e = __ldg(p.q_start + s + 1);
+        bad = a < 0 || e < a || e > p.total_q || e - a > p.nq;
+        i.q0 = a;
+        i.ql = bad ? 0 : e - a;
+    }
+    if (p.table_row) {
+        i.tr = __ldg(p.table_row + s);
+        if (i.tr < 0 || i.tr >= p.table_rows) {
+            bad = true;
+            i.ql = 0;
+        }
+    }
+    i.W = i.ql;
+    if (p.tree_mask) {
+        const int w = __ldg(p.tree_len + s);
+        i.W = w < 0 ? 0 : (w > 32 ? 32 : w);
+    }
+    if (bad)
+        atomicOr(p.ws + kWsErr, kErrBadQuery);
+    i.nb = i.ql > 0 ? (i.T + kBlockSize - 1) / kBlockSize : 0;
+    return i;
 }
+
+__device__ __forceinline__ int seq_blocks(const DecodeParams &p, int s) { return seq_info(p, s).nb; }
 
 struct Smem {
     uint8_t *stages;
@@ -139,23 +185,6 @@ __device__ __forceinline__ Smem carve(uint8_t *raw, const DecodeParams &p)
     s.empty = s.full + p.nst;
     s.cells = reinterpret_cast<Cells *>(s.empty + p.nst);
     return s;
-}
-
-// Write zeros to every output row of sequence s (it has no token).
-__device__ void zero_sequence(const DecodeParams &p, int D, int s)
-{
-    const int64_t row_elems = int64_t(p.Hq) * D;
-    const int64_t first = int64_t(s) * p.nq * row_elems;
-    const int64_t n = int64_t(p.nq) * row_elems;
-    if (p.out_f32) {
-        float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + first);
-        for (int64_t i = 0; i < n / 4; ++i)
-            o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    } else {
-        uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + first);
-        for (int64_t i = 0; i < n / 8; ++i)
-            o[i] = make_uint4(0u, 0u, 0u, 0u);
-    }
 }
 
 // ------------------------------------------------------------------ producer
@@ -207,14 +236,14 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
     bool claimed = false;
     for (;;) {
         const int64_t a = C.start(cell), e = C.start(cell + 1);
-        // locate unit f: head group, sequence, block within it, flat start of the sequence
-        auto locate = [&](int64_t f, int &hg_o, int &s_o, int &b_o, int64_t &fs_o) {
+        // locate unit f: head group, sequence and block within it
+        auto locate = [&](int64_t f, int &hg_o, int &s_o, int &b_o) {
             hg_o = int(f / nb_total);
             const int r0 = int(f - int64_t(hg_o) * nb_total);
             const unsigned own =
                 __ballot_sync(FULLMASK, local > 0 && r0 >= base && r0 < base + local);
             const int src = __ffs(own) - 1;
-            int s_f = 0, b_f = 0, pre_f = 0;
+            int s_f = 0, b_f = 0;
             if (lane == src) {
                 int run = base;
                 for (int s = s_lo; s < s_hi; ++s) {
@@ -222,7 +251,6 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
                     if (r0 < run + nb) {
                         s_f = s;
                         b_f = r0 - run;
-                        pre_f = run;
                         break;
                     }
                     run += nb;
@@ -230,14 +258,13 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
             }
             s_o = __shfl_sync(FULLMASK, s_f, src);
             b_o = __shfl_sync(FULLMASK, b_f, src);
-            fs_o = int64_t(hg_o) * nb_total + __shfl_sync(FULLMASK, pre_f, src);
         };
         if (a < e) {
             int hg, s, b;
-            int64_t fs;
-            locate(a, hg, s, b, fs);
-            int T = seq_tokens(p, s);
-            int nb = (T + kBlockSize - 1) / kBlockSize;
+            locate(a, hg, s, b);
+            SeqInfo si = seq_info(p, s);
+            int T = si.T;
+            int nb = si.nb;
             int seg_b0 = b;
             bool cell_first = true;
             int bt_base = -(1 << 30);
@@ -247,7 +274,7 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
                 if (b < bt_base || b >= bt_base + 32) {
                     bt_base = b;
                     const int idx = b + lane;
-                    bt_val = idx < nb ? __ldg(p.block_tables + int64_t(s) * p.MB + idx) : 0;
+                    bt_val = idx < nb ? __ldg(p.block_tables + int64_t(si.tr) * p.MB + idx) : 0;
                 }
                 int phys = __shfl_sync(FULLMASK, bt_val, b - bt_base);
                 if (phys < 0 || int64_t(phys) >= p.num_blocks) {
@@ -281,14 +308,15 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
                     flags |= F_DIRECT;
                 if (lane == 0) {
                     StageHdr *h = &sm.hdr[st];
-                    h->s = s;
+                    h->q0 = si.q0;
                     h->b = b;
                     h->T = T;
                     h->hg = hg;
                     h->flags = flags;
                     h->slot = cell_first ? 0 : 1;  // 0: the segment opens the cell
                     h->cell = int(cell);
-                    h->fs = int(fs);
+                    h->ql = int16_t(si.ql);
+                    h->W = int16_t(si.W);
                     const uint32_t bar = smem_u32(&sm.full[st]);
                     mbar_arrive_expect_tx(bar, uint32_t(p.stage_bytes));
                     const uint32_t kdst = smem_u32(sm.stages + size_t(st) * p.stage_bytes);
@@ -326,13 +354,13 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
                 ++b;
                 if (b == nb && u + 1 < e) {
                     do {
-                        fs += nb;
                         if (++s == S) {
                             s = 0;
                             ++hg;
                         }
-                        T = seq_tokens(p, s);
-                        nb = (T + kBlockSize - 1) / kBlockSize;
+                        si = seq_info(p, s);
+                        T = si.T;
+                        nb = si.nb;
                     } while (nb == 0);
                     b = 0;
                     bt_base = -(1 << 30);
@@ -425,12 +453,6 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
     float m_r[2], l_r[2];
     // E4M3: K's scale folds into the score scale, V's into the output
     float qscale = p.scale_log2, vscale = 1.f;
-    int jrow[2];  // query index j of this lane's two score rows
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const int j = (2 * tq + r) / p.G;
-        jrow[r] = j < p.nq ? j : p.nq - 1;
-    }
 
     // running state of the current segment
     auto reset_state = [&]() {
@@ -477,11 +499,11 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
                 qscale = p.scale_log2 * __ldg(p.k_scale + kvh);
                 vscale = __ldg(p.v_scale + kvh);
             }
-            if (g < p.rows) {
+            if (g < p.G * h.ql) {
                 const int j = g / p.G;
                 const int gq = g - j * p.G;
                 const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-                    p.q + ((int64_t(h.s) * p.nq + j) * p.Hq + int64_t(kvh) * p.G + gq) * D);
+                    p.q + ((int64_t(h.q0) + j) * p.Hq + int64_t(kvh) * p.G + gq) * D);
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
                     if constexpr (KV8) {
@@ -541,16 +563,33 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
         for (int e = 0; e < 4; ++e)
             sc[e] += sc2[e];
 
-        // ---- scale (log2 domain) and causal / tail mask
+        // ---- scale (log2 domain) and causal / tree / tail mask: positions
+        //      before the first maskable one are seen by every row
         const int t0 = h.b * kBlockSize;
-        const bool need_mask = (t0 + kBlockSize - 1) > (h.T - p.nq);
+        const int w0 = p.tree_mask ? h.T - h.W : h.T - h.ql + 1;
+        const bool need_mask = (t0 + kBlockSize - 1) >= w0;
+        // the lane's rows 2tq, 2tq+1: their query index (the last one for padding
+        // rows) and, with tree masks, their window bits (read only when needed)
+        int jrow[2] = {0, 0};
+        uint32_t tm[2] = {0u, 0u};
+        if (need_mask) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int j = (2 * tq + r) / p.G;
+                jrow[r] = j < h.ql ? j : h.ql - 1;
+                if (p.tree_mask && j < h.ql)
+                    tm[r] = __ldg(p.tree_mask + h.q0 + j);
+            }
+        }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             float x = sc[e] * qscale;
             if (need_mask) {
                 const int tok = t0 + g + ((e >> 1) << 3);
-                const int lim = h.T - p.nq + jrow[e & 1];
-                x = tok > lim ? -INFINITY : x;
+                const bool vis = p.tree_mask
+                                     ? (tok < w0 || (tok < h.T && ((tm[e & 1] >> (tok - w0)) & 1u)))
+                                     : tok <= h.T - h.ql + jrow[e & 1];
+                x = vis ? x : -INFINITY;
             }
             sc[e] = x;
         }
@@ -687,11 +726,11 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     const int row = 2 * tq + r;
-                    if (row >= p.rows)
+                    if (row >= p.G * h.ql)
                         continue;
                     const int j = row / p.G;
                     const int gq = row - j * p.G;
-                    const int64_t o = ((int64_t(h.s) * p.nq + j) * p.Hq + int64_t(kvh) * p.G + gq) * D;
+                    const int64_t o = ((int64_t(h.q0) + j) * p.Hq + int64_t(kvh) * p.G + gq) * D;
                     const float inv = lf[r] > 0.f ? 1.f / lf[r] : 0.f;
                     if constexpr (KV8) {
                         const float f = inv * vscale;
@@ -735,7 +774,7 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     const int row = 2 * tq + r;
-                    if (row >= p.rows)
+                    if (row >= p.G * h.ql)
                         continue;
                     float *pa = p.part + (cellbase * p.rows + row) * D;
                     if constexpr (KV8) {
@@ -793,14 +832,8 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
     float acc[ND][4];
     uint32_t qa[KS][4];
     float m_r[2], l_r[2];
-    int jr[2];
     // E4M3: K's scale folds into the score scale, V's into the output
     float qscale = p.scale_log2, vscale = 1.f;
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-        const int j = (r0 + g + 8 * rr) / p.G;
-        jr[rr] = j < p.nq ? j : p.nq - 1;
-    }
     auto reset_state = [&]() {
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks)
@@ -850,11 +883,11 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
                 const int row = r0 + g + 8 * rr;
-                if (row < p.rows) {
+                if (row < p.G * h.ql) {
                     const int j = row / p.G;
                     const int gq = row - j * p.G;
                     const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-                        p.q + ((int64_t(h.s) * p.nq + j) * p.Hq + int64_t(kvh) * p.G + gq) * D);
+                        p.q + ((int64_t(h.q0) + j) * p.Hq + int64_t(kvh) * p.G + gq) * D);
 #pragma unroll
                     for (int ks = 0; ks < KS; ++ks) {
                         if constexpr (KV8) {
@@ -923,9 +956,24 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
             for (int e = 0; e < 4; ++e)
                 sc[n][e] += sc2[n][e];
 
-        // ---- scale (log2 domain) and causal / tail mask
+        // ---- scale (log2 domain) and causal / tree / tail mask: positions
+        //      before the first maskable one are seen by every row
         const int t0 = h.b * kBlockSize;
-        const bool need_mask = (t0 + kBlockSize - 1) > (h.T - p.nq);
+        const int w0 = p.tree_mask ? h.T - h.W : h.T - h.ql + 1;
+        const bool need_mask = (t0 + kBlockSize - 1) >= w0;
+        // the lane's rows g, g+8: their query index (the last one for padding
+        // rows) and, with tree masks, their window bits (read only when needed)
+        int jr[2] = {0, 0};
+        uint32_t tm[2] = {0u, 0u};
+        if (need_mask) {
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int j = (r0 + g + 8 * rr) / p.G;
+                jr[rr] = j < h.ql ? j : h.ql - 1;
+                if (p.tree_mask && j < h.ql)
+                    tm[rr] = __ldg(p.tree_mask + h.q0 + j);
+            }
+        }
 #pragma unroll
         for (int n = 0; n < 2; ++n)
 #pragma unroll
@@ -933,8 +981,10 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
                 float x = sc[n][e] * qscale;
                 if (need_mask) {
                     const int tok = t0 + 8 * n + 2 * tq + (e & 1);
-                    const int lim = h.T - p.nq + jr[e >> 1];
-                    x = tok > lim ? -INFINITY : x;
+                    const bool vis =
+                        p.tree_mask ? (tok < w0 || (tok < h.T && ((tm[e >> 1] >> (tok - w0)) & 1u)))
+                                    : tok <= h.T - h.ql + jr[e >> 1];
+                    x = vis ? x : -INFINITY;
                 }
                 sc[n][e] = x;
             }
@@ -1078,11 +1128,11 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr) {
                     const int row = r0 + g + 8 * rr;
-                    if (row >= p.rows)
+                    if (row >= p.G * h.ql)
                         continue;
                     const int j = row / p.G;
                     const int gq = row - j * p.G;
-                    const int64_t o = ((int64_t(h.s) * p.nq + j) * p.Hq + int64_t(kvh) * p.G + gq) * D;
+                    const int64_t o = ((int64_t(h.q0) + j) * p.Hq + int64_t(kvh) * p.G + gq) * D;
                     const float inv = lf[rr] > 0.f ? 1.f / lf[rr] : 0.f;
                     if constexpr (KV8) {
                         // chunk ch: dims 16ch + 4tq .. +3 from the even / odd n-tiles
@@ -1126,7 +1176,7 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr) {
                     const int row = r0 + g + 8 * rr;
-                    if (row >= p.rows)
+                    if (row >= p.G * h.ql)
                         continue;
                     float *pa = p.part + (cellbase * p.rows + row) * D;
                     if constexpr (KV8) {
@@ -1215,14 +1265,16 @@ __global__ void __launch_bounds__(256)
     const Cells C = make_cells(p, nb_total, grid);
     const int64_t fs = int64_t(hg) * nb_total + __ldcg(p.seq_start + s);
     const int64_t fe = int64_t(hg) * nb_total + __ldcg(p.seq_start + s + 1);
-    const int nrows = p.HG * p.rows;  // output rows of this (sequence, head group)
+    const int nrows = p.HG * p.rows;  // partial rows of this (sequence, head group)
     const bool has_d = lane * 4 < D;
+    const SeqInfo si = seq_info(p, s);
+    const int vrows = p.G * si.ql;    // rows of each kv head with a query
 
+    auto valid = [&](int r) { return r - (r / p.rows) * p.rows < vrows; };
     auto out_offset = [&](int r) -> int64_t {  // r = hl * rows + row
         const int hl = r / p.rows, row = r - hl * p.rows;
         const int j = row / p.G, gq = row - j * p.G;
-        return ((int64_t(s) * p.nq + j) * p.Hq + int64_t(hg * p.HG + hl) * p.G + gq) * D +
-               lane * 4;
+        return ((int64_t(si.q0) + j) * p.Hq + int64_t(hg * p.HG + hl) * p.G + gq) * D + lane * 4;
     };
     auto store = [&](int64_t o, float4 v) {
         if (p.out_f32) {
@@ -1237,9 +1289,9 @@ __global__ void __launch_bounds__(256)
         }
     };
 
-    if (fe == fs) {  // no token: zeros
+    if (fe == fs) {  // no token (or no query rows): zeros
         for (int r = warp; r < nrows; r += nwarps)
-            if (has_d)
+            if (has_d && valid(r))
                 store(out_offset(r), make_float4(0.f, 0.f, 0.f, 0.f));
         return;
     }
@@ -1309,6 +1361,8 @@ __global__ void __launch_bounds__(256)
         for (int i = 0; i < RPW; ++i) {
             if (r0 + i >= nrows)
                 break;
+            if (!valid(r0 + i))
+                continue;
             const float inv = Lr[i] > 0.f ? 1.f / Lr[i] : 0.f;
             store(out_offset(r0 + i),
                   make_float4(ar[i].x * inv, ar[i].y * inv, ar[i].z * inv, ar[i].w * inv));

@@ -25,7 +25,8 @@ enum : uint32_t {
     kErrConsumerWait = 1u,  // a consumer warp gave up waiting for a stage
     kErrProducerWait = 2u,  // the producer gave up waiting for a free stage
     kErrDrainWait = 4u,     // a copy did not land while unwinding
-    kErrBadBlock = 8u       // a block-table entry outside [0, num_blocks) (read as zeros)
+    kErrBadBlock = 8u,      // a block-table entry outside [0, num_blocks) (read as zeros)
+    kErrBadQuery = 16u      // variable query counts: a sequence's rows or table row invalid
 };
 
 // Split of the work of one call (computed on the host from the shapes).
@@ -74,6 +75,13 @@ struct DecodeParams {
     float scale_log2;      // scale * log2(e)
     const float *k_scale;  // E4M3 pools: [Hkv] dequantisation scales (null for bf16)
     const float *v_scale;
+    // variable query counts (all null for a fixed n_query_per_seq = nq, causal):
+    const int32_t *q_start;     // [S + 1] first query row of each sequence
+    const uint32_t *tree_mask;  // [total_q] per-row visibility bits over the window
+    const int32_t *tree_len;    // [S] mask window (positions T - W .. T - 1)
+    const int32_t *table_row;   // [S] block-table row of each sequence
+    int total_q;                // rows of q and out
+    int table_rows;             // rows of block_tables
 };
 
 int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int opt_ctas,
