@@ -46,6 +46,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "pkv_common.cuh"
 #include "pkv_internal.h"
@@ -567,31 +568,32 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
         //      before the first maskable one are seen by every row
         const int t0 = h.b * kBlockSize;
         const int w0 = p.tree_mask ? h.T - h.W : h.T - h.ql + 1;
-        const bool need_mask = (t0 + kBlockSize - 1) >= w0;
-        // the lane's rows 2tq, 2tq+1: their query index (the last one for padding
-        // rows) and, with tree masks, their window bits (read only when needed)
-        int jrow[2] = {0, 0};
-        uint32_t tm[2] = {0u, 0u};
-        if (need_mask) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            sc[e] *= qscale;
+        if (__builtin_expect((t0 + kBlockSize - 1) >= w0, 0)) {
+            // a sequence's last block(s): the lane's rows 2tq, 2tq+1 (the last query
+            // index for padding rows) against the causal limit or their window bits
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                const int j = (2 * tq + r) / p.G;
-                jrow[r] = j < h.ql ? j : h.ql - 1;
-                if (p.tree_mask && j < h.ql)
-                    tm[r] = __ldg(p.tree_mask + h.q0 + j);
-            }
-        }
+                int j = (2 * tq + r) / p.G;
+                j = j < h.ql ? j : h.ql - 1;
+                if (p.tree_mask) {
+                    const uint32_t bits = (2 * tq + r) < p.G * h.ql ? __ldg(p.tree_mask + h.q0 + j) : 0u;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            float x = sc[e] * qscale;
-            if (need_mask) {
-                const int tok = t0 + g + ((e >> 1) << 3);
-                const bool vis = p.tree_mask
-                                     ? (tok < w0 || (tok < h.T && ((tm[e & 1] >> (tok - w0)) & 1u)))
-                                     : tok <= h.T - h.ql + jrow[e & 1];
-                x = vis ? x : -INFINITY;
+                    for (int hi = 0; hi < 2; ++hi) {
+                        const int tok = t0 + g + 8 * hi;
+                        const bool vis = tok < w0 || (tok < h.T && ((bits >> (tok - w0)) & 1u));
+                        if (!vis)
+                            sc[2 * hi + r] = -INFINITY;
+                    }
+                } else {
+#pragma unroll
+                    for (int hi = 0; hi < 2; ++hi)
+                        if (t0 + g + 8 * hi > h.T - h.ql + j)
+                            sc[2 * hi + r] = -INFINITY;
+                }
             }
-            sc[e] = x;
         }
 
         // ---- online softmax (rows 2tq, 2tq+1 live in this lane). The
@@ -663,46 +665,68 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
             mhi = (k0 + 8 < vc ? 0x0000ffffu : 0u) | (k0 + 9 < vc ? 0xffff0000u : 0u);
         }
 
-        // ---- O^T[d][row] += V^T[d][tok] . P^T[tok][row]
-        if constexpr (KV8) {
-            // ldmatrix.trans of chunks 2i, 2i+1 (tokens 0-7 and 8-15) gives a lane
-            // tokens 2tq, 2tq+1 of the code pair (dims 2g, 2g+1); bytes 0,2 form the
-            // even-dim m-tile 2i and bytes 1,3 the odd-dim m-tile 2i+1. In both,
-            // M-row g is dim 32i+2g(+1) and M-row g+8 is dim 32i+16+2g(+1).
+        // ---- O^T[d][row] += V^T[d][tok] . P^T[tok][row]; the masks are applied
+        //      in a sequence's last block only (MASKED = true)
+        auto pv = [&](auto masked) {
+            constexpr bool MASKED = decltype(masked)::value;
+            if constexpr (KV8) {
+                // ldmatrix.trans of chunks 2i, 2i+1 (tokens 0-7 and 8-15) gives a lane
+                // tokens 2tq, 2tq+1 of the code pair (dims 2g, 2g+1); bytes 0,2 form
+                // the even-dim m-tile 2i and bytes 1,3 the odd-dim m-tile 2i+1. In
+                // both, M-row g is dim 32i+2g(+1) and M-row g+8 is dim 32i+16+2g(+1).
 #pragma unroll
-            for (int i = 0; i < MT / 2; ++i) {
-                const int chunk = 2 * i + v_cadd;
-                const uint32_t addr = vb + uint32_t(v_tok * 128 + ((chunk ^ sw) << 4));
-                uint32_t r[4];
-                ldsm_x4_trans(addr, r);
-                uint32_t ae[4], ao[4];
+                for (int i = 0; i < MT / 2; ++i) {
+                    const int chunk = 2 * i + v_cadd;
+                    const uint32_t addr = vb + uint32_t(v_tok * 128 + ((chunk ^ sw) << 4));
+                    uint32_t r[4];
+                    ldsm_x4_trans(addr, r);
+                    uint32_t ae[4], ao[4];
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const uint32_t keep = m < 2 ? mlo : mhi;
-                    ae[m] = e4m3x2_to_f16x2(__byte_perm(r[m], 0u, 0x0020)) & keep;
-                    ao[m] = e4m3x2_to_f16x2(__byte_perm(r[m], 0u, 0x0031)) & keep;
+                    for (int m = 0; m < 4; ++m) {
+                        ae[m] = e4m3x2_to_f16x2(__byte_perm(r[m], 0u, 0x0020));
+                        ao[m] = e4m3x2_to_f16x2(__byte_perm(r[m], 0u, 0x0031));
+                        if constexpr (MASKED) {
+                            ae[m] &= m < 2 ? mlo : mhi;
+                            ao[m] &= m < 2 ? mlo : mhi;
+                        }
+                    }
+                    mma_f16_16816(acc[2 * i], ae, bh[0], bh[1]);
+                    mma_f16_16816(acc[2 * i + 1], ao, bh[0], bh[1]);
                 }
-                mma_f16_16816(acc[2 * i], ae, bh[0], bh[1]);
-                mma_f16_16816(acc[2 * i + 1], ao, bh[0], bh[1]);
-            }
-        } else {
+            } else {
 #pragma unroll
-            for (int i = 0; i < MT; ++i) {
-                const int chunk = 2 * i + v_cadd;
-                const uint32_t addr = vb + uint32_t((chunk >> 3) * kTileBytes + v_tok * 128 +
-                                                    (((chunk & 7) ^ sw) << 4));
-                uint32_t a[4];
-                ldsm_x4_trans(addr, a);
-                a[0] &= mlo;
-                a[1] &= mlo;
-                a[2] &= mhi;
-                a[3] &= mhi;
-                mma_bf16_16816(acc[i], a, bh[0], bh[1]);
-                mma_bf16_16816(acc[i], a, bl[0], bl[1]);
+                for (int i = 0; i < MT; ++i) {
+                    const int chunk = 2 * i + v_cadd;
+                    const uint32_t addr = vb + uint32_t((chunk >> 3) * kTileBytes + v_tok * 128 +
+                                                        (((chunk & 7) ^ sw) << 4));
+                    uint32_t a[4];
+                    ldsm_x4_trans(addr, a);
+                    if constexpr (MASKED) {
+                        a[0] &= mlo;
+                        a[1] &= mlo;
+                        a[2] &= mhi;
+                        a[3] &= mhi;
+                    }
+                    mma_bf16_16816(acc[i], a, bh[0], bh[1]);
+                    mma_bf16_16816(acc[i], a, bl[0], bl[1]);
+                }
             }
-        }
+        };
+        if (__builtin_expect(vc < kBlockSize, 0))
+            pv(std::true_type());
+        else
+            pv(std::false_type());
 
-        // the stage's shared memory is no longer needed: hand it back
+        // the epilogue's header fields are read now (not kept live through the
+        // stage); then the stage's shared memory goes back to the producer
+        int e_q0 = 0, e_rows = 0, e_cell = 0, e_slot = 0;
+        if (h.flags & F_LAST) {
+            const StageHdr *hp = &sm.hdr[st];
+            e_q0 = hp->q0;
+            e_rows = p.G * hp->ql;
+            e_cell = hp->cell;
+            e_slot = hp->slot;
+        }
         __syncwarp();
         if (lane == 0)
             mbar_arrive(smem_u32(&sm.empty[st]));
@@ -726,11 +750,11 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     const int row = 2 * tq + r;
-                    if (row >= p.G * h.ql)
+                    if (row >= e_rows)
                         continue;
                     const int j = row / p.G;
                     const int gq = row - j * p.G;
-                    const int64_t o = ((int64_t(h.q0) + j) * p.Hq + int64_t(kvh) * p.G + gq) * D;
+                    const int64_t o = ((int64_t(e_q0) + j) * p.Hq + int64_t(kvh) * p.G + gq) * D;
                     const float inv = lf[r] > 0.f ? 1.f / lf[r] : 0.f;
                     if constexpr (KV8) {
                         const float f = inv * vscale;
@@ -770,11 +794,11 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
                 }
             } else {
                 // partial (m, l, acc) of this cell for the merge kernel
-                const int64_t cellbase = (int64_t(h.cell) * 2 + h.slot) * p.HG + hl;
+                const int64_t cellbase = (int64_t(e_cell) * 2 + e_slot) * p.HG + hl;
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     const int row = 2 * tq + r;
-                    if (row >= p.G * h.ql)
+                    if (row >= e_rows)
                         continue;
                     float *pa = p.part + (cellbase * p.rows + row) * D;
                     if constexpr (KV8) {
@@ -960,34 +984,40 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
         //      before the first maskable one are seen by every row
         const int t0 = h.b * kBlockSize;
         const int w0 = p.tree_mask ? h.T - h.W : h.T - h.ql + 1;
-        const bool need_mask = (t0 + kBlockSize - 1) >= w0;
-        // the lane's rows g, g+8: their query index (the last one for padding
-        // rows) and, with tree masks, their window bits (read only when needed)
-        int jr[2] = {0, 0};
-        uint32_t tm[2] = {0u, 0u};
-        if (need_mask) {
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                const int j = (r0 + g + 8 * rr) / p.G;
-                jr[rr] = j < h.ql ? j : h.ql - 1;
-                if (p.tree_mask && j < h.ql)
-                    tm[rr] = __ldg(p.tree_mask + h.q0 + j);
-            }
-        }
 #pragma unroll
         for (int n = 0; n < 2; ++n)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float x = sc[n][e] * qscale;
-                if (need_mask) {
-                    const int tok = t0 + 8 * n + 2 * tq + (e & 1);
-                    const bool vis =
-                        p.tree_mask ? (tok < w0 || (tok < h.T && ((tm[e >> 1] >> (tok - w0)) & 1u)))
-                                    : tok <= h.T - h.ql + jr[e >> 1];
-                    x = vis ? x : -INFINITY;
+            for (int e = 0; e < 4; ++e)
+                sc[n][e] *= qscale;
+        if (__builtin_expect((t0 + kBlockSize - 1) >= w0, 0)) {
+            // a sequence's last block(s): the lane's rows g, g+8 (the last query index
+            // for padding rows) against the causal limit or their window bits
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int row = r0 + g + 8 * rr;
+                int j = row / p.G;
+                j = j < h.ql ? j : h.ql - 1;
+                if (p.tree_mask) {
+                    const uint32_t bits = row < p.G * h.ql ? __ldg(p.tree_mask + h.q0 + j) : 0u;
+#pragma unroll
+                    for (int n = 0; n < 2; ++n)
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            const int tok = t0 + 8 * n + 2 * tq + c;
+                            const bool vis = tok < w0 || (tok < h.T && ((bits >> (tok - w0)) & 1u));
+                            if (!vis)
+                                sc[n][2 * rr + c] = -INFINITY;
+                        }
+                } else {
+#pragma unroll
+                    for (int n = 0; n < 2; ++n)
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
+                            if (t0 + 8 * n + 2 * tq + c > h.T - h.ql + j)
+                                sc[n][2 * rr + c] = -INFINITY;
                 }
-                sc[n][e] = x;
             }
+        }
 
         // ---- online softmax over the lane's two rows (g: e = 0,1; g+8: e = 2,3)
         float bmax[2];
@@ -1064,49 +1094,74 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
             mhi = (k0 + 8 < vc ? 0x0000ffffu : 0u) | (k0 + 9 < vc ? 0xffff0000u : 0u);
         }
 
-        // ---- O[row][d] += P[row][tok] . V[tok][d]
-        if constexpr (KV8) {
-            // ldmatrix.trans of chunks 2i, 2i+1 (tokens 0-7 and 8-15) gives a lane
-            // tokens 2tq, 2tq+1 of the code pair (dims 2g, 2g+1): bytes 0,2 make an
-            // n-tile of even dims, bytes 1,3 one of odd dims. n-tile 4i+2c+par holds
-            // dims 16(2i+c) + 2n + par for its columns n = 0..7.
+        // ---- O[row][d] += P[row][tok] . V[tok][d]; the masks are applied in a
+        //      sequence's last block only (MASKED = true)
+        auto pv = [&](auto masked) {
+            constexpr bool MASKED = decltype(masked)::value;
+            if constexpr (KV8) {
+                // ldmatrix.trans of chunks 2i, 2i+1 (tokens 0-7 and 8-15) gives a lane
+                // tokens 2tq, 2tq+1 of the code pair (dims 2g, 2g+1): bytes 0,2 make
+                // an n-tile of even dims, bytes 1,3 one of odd dims. n-tile 4i+2c+par
+                // holds dims 16(2i+c) + 2n + par for its columns n = 0..7.
 #pragma unroll
-            for (int i = 0; i < D / 32; ++i) {
-                const int chunk = 2 * i + v_cadd;
-                const uint32_t addr = vb + uint32_t(v_tok * 128 + ((chunk ^ sw) << 4));
-                uint32_t r[4];
-                ldsm_x4_trans(addr, r);  // r0: tok 0-7 / 2i, r1: 8-15 / 2i, r2: 0-7 / 2i+1, r3
+                for (int i = 0; i < D / 32; ++i) {
+                    const int chunk = 2 * i + v_cadd;
+                    const uint32_t addr = vb + uint32_t(v_tok * 128 + ((chunk ^ sw) << 4));
+                    uint32_t r[4];
+                    ldsm_x4_trans(addr, r);  // r0: tok 0-7 / 2i, r1: 8-15 / 2i, r2, r3: 2i+1
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const uint32_t lo_t = r[2 * c], hi_t = r[2 * c + 1];
-                    mma_f16_16816(acc[4 * i + 2 * c], ph,
-                                  e4m3x2_to_f16x2(__byte_perm(lo_t, 0u, 0x0020)) & mlo,
-                                  e4m3x2_to_f16x2(__byte_perm(hi_t, 0u, 0x0020)) & mhi);
-                    mma_f16_16816(acc[4 * i + 2 * c + 1], ph,
-                                  e4m3x2_to_f16x2(__byte_perm(lo_t, 0u, 0x0031)) & mlo,
-                                  e4m3x2_to_f16x2(__byte_perm(hi_t, 0u, 0x0031)) & mhi);
+                    for (int c = 0; c < 2; ++c) {
+                        const uint32_t lo_t = r[2 * c], hi_t = r[2 * c + 1];
+                        uint32_t e0 = e4m3x2_to_f16x2(__byte_perm(lo_t, 0u, 0x0020));
+                        uint32_t e1 = e4m3x2_to_f16x2(__byte_perm(hi_t, 0u, 0x0020));
+                        uint32_t o0 = e4m3x2_to_f16x2(__byte_perm(lo_t, 0u, 0x0031));
+                        uint32_t o1 = e4m3x2_to_f16x2(__byte_perm(hi_t, 0u, 0x0031));
+                        if constexpr (MASKED) {
+                            e0 &= mlo;
+                            e1 &= mhi;
+                            o0 &= mlo;
+                            o1 &= mhi;
+                        }
+                        mma_f16_16816(acc[4 * i + 2 * c], ph, e0, e1);
+                        mma_f16_16816(acc[4 * i + 2 * c + 1], ph, o0, o1);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < D / 16; ++i) {
+                    const int chunk = 2 * i + v_cadd;
+                    const uint32_t addr = vb + uint32_t((chunk >> 3) * kTileBytes + v_tok * 128 +
+                                                        (((chunk & 7) ^ sw) << 4));
+                    uint32_t b[4];
+                    ldsm_x4_trans(addr, b);
+                    if constexpr (MASKED) {
+                        b[0] &= mlo;
+                        b[1] &= mhi;
+                        b[2] &= mlo;
+                        b[3] &= mhi;
+                    }
+                    mma_bf16_16816(acc[2 * i], ph, b[0], b[1]);
+                    mma_bf16_16816(acc[2 * i], plo, b[0], b[1]);
+                    mma_bf16_16816(acc[2 * i + 1], ph, b[2], b[3]);
+                    mma_bf16_16816(acc[2 * i + 1], plo, b[2], b[3]);
                 }
             }
-        } else {
-#pragma unroll
-            for (int i = 0; i < D / 16; ++i) {
-                const int chunk = 2 * i + v_cadd;
-                const uint32_t addr = vb + uint32_t((chunk >> 3) * kTileBytes + v_tok * 128 +
-                                                    (((chunk & 7) ^ sw) << 4));
-                uint32_t b[4];
-                ldsm_x4_trans(addr, b);
-                b[0] &= mlo;
-                b[1] &= mhi;
-                b[2] &= mlo;
-                b[3] &= mhi;
-                mma_bf16_16816(acc[2 * i], ph, b[0], b[1]);
-                mma_bf16_16816(acc[2 * i], plo, b[0], b[1]);
-                mma_bf16_16816(acc[2 * i + 1], ph, b[2], b[3]);
-                mma_bf16_16816(acc[2 * i + 1], plo, b[2], b[3]);
-            }
-        }
+        };
+        if (__builtin_expect(vc < kBlockSize, 0))
+            pv(std::true_type());
+        else
+            pv(std::false_type());
 
-        // the stage's shared memory is no longer needed: hand it back
+        // the epilogue's header fields are read now (not kept live through the
+        // stage); then the stage's shared memory goes back to the producer
+        int e_q0 = 0, e_rows = 0, e_cell = 0, e_slot = 0;
+        if (h.flags & F_LAST) {
+            const StageHdr *hp = &sm.hdr[st];
+            e_q0 = hp->q0;
+            e_rows = p.G * hp->ql;
+            e_cell = hp->cell;
+            e_slot = hp->slot;
+        }
         __syncwarp();
         if (lane == 0)
             mbar_arrive(smem_u32(&sm.empty[st]));
@@ -1128,11 +1183,11 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr) {
                     const int row = r0 + g + 8 * rr;
-                    if (row >= p.G * h.ql)
+                    if (row >= e_rows)
                         continue;
                     const int j = row / p.G;
                     const int gq = row - j * p.G;
-                    const int64_t o = ((int64_t(h.q0) + j) * p.Hq + int64_t(kvh) * p.G + gq) * D;
+                    const int64_t o = ((int64_t(e_q0) + j) * p.Hq + int64_t(kvh) * p.G + gq) * D;
                     const float inv = lf[rr] > 0.f ? 1.f / lf[rr] : 0.f;
                     if constexpr (KV8) {
                         // chunk ch: dims 16ch + 4tq .. +3 from the even / odd n-tiles
@@ -1172,11 +1227,11 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
                     }
                 }
             } else {
-                const int64_t cellbase = (int64_t(h.cell) * 2 + h.slot) * p.HG + hl;
+                const int64_t cellbase = (int64_t(e_cell) * 2 + e_slot) * p.HG + hl;
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr) {
                     const int row = r0 + g + 8 * rr;
-                    if (row >= p.G * h.ql)
+                    if (row >= e_rows)
                         continue;
                     float *pa = p.part + (cellbase * p.rows + row) * D;
                     if constexpr (KV8) {
