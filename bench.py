@@ -137,6 +137,9 @@ def run_pkv(args, rank, world, dist):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     w = W.make_workload(args.workload)
+    cascade = bool(args.cascade) and bool(w.shared.any())
+    if cascade:
+        w = W.sharers_first(w)  # the sharing sequences form one consecutive group
 
     def up(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
@@ -157,8 +160,15 @@ def run_pkv(args, rank, world, dist):
     tables = torch.from_numpy(w.block_tables).to(dev)
     lens = torch.from_numpy(w.context_lens).to(dev)
     out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
-    ws = pkv.workspace(dev, pkv.workspace_size(w.num_seqs, w.n_query_per_seq, w.num_q_heads,
-                                                w.num_kv_heads, w.head_dim))
+    if cascade:
+        M = int(w.shared.sum())
+        groups = torch.tensor([[0, M, w.meta["prefix_tokens"] // 16]], dtype=torch.int32,
+                              device=dev)
+        ws = pkv.workspace(dev, int(pkv.lib().pkv_workspace_size_cascade(
+            w.num_seqs, w.n_query_per_seq, w.num_q_heads, w.num_kv_heads, w.head_dim)))
+    else:
+        ws = pkv.workspace(dev, pkv.workspace_size(w.num_seqs, w.n_query_per_seq, w.num_q_heads,
+                                                    w.num_kv_heads, w.head_dim))
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     eb = 1 if fp8 else 2
@@ -173,6 +183,10 @@ def run_pkv(args, rank, world, dist):
             pkv.kv_append_fp8(k_new, v_new, slots, k_cache, v_cache, k_scale, v_scale)
             pkv.paged_decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, tables, lens,
                                            w.n_query_per_seq, w.scale, out, ws=ws)
+        elif cascade:
+            pkv.kv_append(k_new, v_new, slots, k_cache, v_cache)
+            pkv.paged_decode_attention_cascade(q, k_cache, v_cache, tables, lens,
+                                               w.n_query_per_seq, w.scale, out, groups, M, ws=ws)
         else:
             pkv.kv_append(k_new, v_new, slots, k_cache, v_cache)
             pkv.paged_decode_attention(q, k_cache, v_cache, tables, lens, w.n_query_per_seq,
@@ -269,7 +283,7 @@ def run_pkv(args, rank, world, dist):
     peak, peak_kind = measured_peaks()
     achieved = attn_bytes / (kern_mean * 1e-3) / 1e9
     traffic = None
-    nt = NCU_TRAFFIC.get(args.workload + ("/fp8" if fp8 else ""))
+    nt = NCU_TRAFFIC.get(args.workload + ("/fp8" if fp8 else "") + ("/cascade" if cascade else ""))
     if nt and nt.get("source_sha256") == kernel_source_sha():
         traffic = nt["bytes"]
     value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
@@ -290,7 +304,8 @@ def run_pkv(args, rank, world, dist):
                  "Q and new rows; " if fp8 else "synthetic (seeded N(0,1) bf16 K/V/Q; ") +
                 "pools in HBM; inputs > L2 and a 512 MiB L2 flush between timed steps)",
         "config": {
-            "workload": args.workload + (" (fp8 KV cache)" if fp8 else ""),
+            "workload": args.workload + (" (fp8 KV cache)" if fp8 else "") +
+                        (" (shared-prefix cascade)" if cascade else ""),
             "kv_dtype": args.kv_dtype,
             "num_seqs": w.num_seqs, "n_query_per_seq": w.n_query_per_seq,
             "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
@@ -304,7 +319,8 @@ def run_pkv(args, rank, world, dist):
             "attention_bytes_logical": attn_bytes_logical,
         },
         "roofline": {
-            "bound": "hbm", "kernel": "paged_decode_kernel",
+            "bound": "hbm",
+            "kernel": "paged_decode_kernel" + (" (prefix pass + main pass)" if cascade else ""),
             "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs (burst)",
             "traffic": traffic, "kernel_us": round(kern_mean * 1e3, 3),
@@ -314,7 +330,7 @@ def run_pkv(args, rank, world, dist):
                 "ms_per_step": round(e2e_ms, 6), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "path": "pinned host inputs -> H2D -> kv_append + attention -> D2H output"},
-        "gpu_launches": K * 3,
+        "gpu_launches": K * (4 if cascade else 3),
         "device_error_word": err,
     }
     if clk is not None:
@@ -574,6 +590,107 @@ def run_tree(args, rank, world, dist):
     return res
 
 
+# ------------------------------------------------------------------ shared system prompt
+PREFIX_METRIC = "shared-prompt decode attention GB/s (unique KV bytes); µs per step"
+
+
+def run_shared_prefix(args, rank, world, dist):
+    """Decode step of 256 sequences (8B-layer heads) that share a 4,096-token system
+    prompt, each with a private suffix of 16..511 tokens: the cascade (prompt
+    attended once per group row tile) against the plain call on the same inputs."""
+    import torch
+
+    import paged_kv_cache_101_gb300 as pkv
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    S, P_TOK = 256, 4096
+    rng = np.random.default_rng(1234 + 23)
+    lens = P_TOK + rng.integers(16, 512, size=S)
+    w = W.make_custom(S, 1, 32, 8, 128, lens, seed=1234 + 23, shared=np.ones(S, bool),
+                      prefix_tokens=P_TOK)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    q, k_cache, v_cache = up(w.q), up(w.k_cache), up(w.v_cache)
+    k_new, v_new = up(w.k_new), up(w.v_new)
+    slots = torch.from_numpy(w.slot_mapping).to(dev)
+    tables = torch.from_numpy(w.block_tables).to(dev)
+    lens_d = torch.from_numpy(w.context_lens).to(dev)
+    groups = torch.tensor([[0, S, P_TOK // 16]], dtype=torch.int32, device=dev)
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    ws = pkv.workspace(dev, int(pkv.lib().pkv_workspace_size_cascade(S, 1, 32, 8, 128)))
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    attn_bytes = R.workload_bytes(w, unique=True)
+    step_bytes = attn_bytes + R.append_bytes(S, 8, 128)
+
+    def step_cascade():
+        pkv.kv_append(k_new, v_new, slots, k_cache, v_cache)
+        pkv.paged_decode_attention_cascade(q, k_cache, v_cache, tables, lens_d, 1, w.scale, out,
+                                           groups, S, ws=ws)
+
+    def step_plain():
+        pkv.kv_append(k_new, v_new, slots, k_cache, v_cache)
+        pkv.paged_decode_attention(q, k_cache, v_cache, tables, lens_d, 1, w.scale, out, ws=ws)
+
+    def timed(step, K):
+        for _ in range(args.warmup):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+        for a, b in ev:
+            flush.zero_()
+            a.record()
+            step()
+            b.record()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / K
+
+    K = args.steps
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    if dist is not None:
+        dist.barrier()
+    ms = timed(step_cascade, K)
+    ms_plain = timed(step_plain, K)
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    if dist is not None:
+        t = torch.tensor([ms, ms_plain], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, ms_plain = (float(x) for x in t.tolist())
+    peak, peak_kind = measured_peaks()
+    res = {
+        "metric": PREFIX_METRIC, "value": round(world * step_bytes / (ms * 1e-3) / 1e9, 2),
+        "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(ms, 6), "us_per_step": round(ms * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16; 512 MiB L2 flush between steps)",
+        "config": {"workload": "256 sequences sharing a 4096-token system prompt, private "
+                               "suffixes U[16, 512), 8B-layer heads (32/8, d 128)",
+                   "context_tokens": int(w.context_lens.sum()), "bytes_per_step": step_bytes,
+                   "attention_bytes_unique": attn_bytes,
+                   "attention_bytes_logical": R.workload_bytes(w, unique=False),
+                   "parallelism": f"replicas x{world}"},
+        "plain_call": {"us_per_step": round(ms_plain * 1e3, 3),
+                       "value": round(world * step_bytes / (ms_plain * 1e-3) / 1e9, 2)},
+        "speedup_vs_plain": round(ms_plain / ms, 3),
+        "roofline": {"bound": "hbm", "kernel": "step (append + prefix pass + main + merge)",
+                     "achieved": round(step_bytes / (ms * 1e-3) / 1e9, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(step_bytes / (ms * 1e-3) / 1e9 / peak, 4),
+                     "peak_source": f"{peak_kind} hbm_gbs (burst)", "traffic": None},
+        "gpu_launches": 4 * K + 3 * K,
+        "device_error_word": pkv.workspace_error(ws),
+    }
+    if clk is not None:
+        res["clocks"] = clk
+    return res
+
+
 # ------------------------------------------------------------------ oracle (CPU)
 def oracle_step_fn(w, kv_dtype: str, threads: int):
     """One whole decode step of the fp64 oracle on ``w`` (bf16 or E4M3 pools) and its
@@ -685,11 +802,15 @@ def main():
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="step", choices=["step", "copy_blocks", "tree_verify"],
+    ap.add_argument("--op", default="step",
+                    choices=["step", "copy_blocks", "tree_verify", "shared_prefix"],
                     help="step: append + attention (the headline); copy_blocks: the "
                          "copy-on-write block copy alone; tree_verify: a 15-node candidate "
                          "tree per sequence scored with tree masks")
     ap.add_argument("--pairs", type=int, default=4096, help="block pairs per copy_blocks step")
+    ap.add_argument("--cascade", action="store_true",
+                    help="attend the workload's shared prefix once per group (its sharers "
+                         "moved to the front of the batch)")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
                     help="KV pool element type (fp8 = E4M3 codes with per-head scales)")
     args = ap.parse_args()
@@ -710,8 +831,10 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         td.init_process_group("nccl")
         dist = td
-    if args.op in ("copy_blocks", "tree_verify"):
-        res = (run_copy if args.op == "copy_blocks" else run_tree)(args, rank, world, dist)
+    if args.op in ("copy_blocks", "tree_verify", "shared_prefix"):
+        fn = {"copy_blocks": run_copy, "tree_verify": run_tree,
+              "shared_prefix": run_shared_prefix}[args.op]
+        res = fn(args, rank, world, dist)
         if rank == 0:
             print(json.dumps(res), flush=True)
         if dist is not None:

@@ -199,6 +199,50 @@ pkv_status pkv_paged_decode_attention(const void *q, const void *k_cache, const 
                                       size_t workspace_bytes, void *stream);
 
 /*
+ * pkv_paged_decode_attention_cascade -- pkv_paged_decode_attention for a batch
+ * whose sequences share prefixes, with each shared prefix attended once per
+ * group of sequences instead of once per sequence.
+ *
+ * Passages: "ML Interview Prep, Lesson 13" section 3.5 "Sharing" (parallel
+ * samples and a common system prompt share physical blocks) and "07 --
+ * Inference" section 5.3 (a partial (m, l, acc) over any token range merges
+ * exactly with the others by the online-softmax rescaling rule). The result is
+ * the same function as pkv_paged_decode_attention on the same inputs (within
+ * the same tolerance); only the work differs.
+ *
+ *   prefix_groups   device int32 [num_groups][3]: (first sequence, number of
+ *                   sequences, prefix blocks P). A group's sequences are
+ *                   consecutive in the batch, groups ascend by first sequence and
+ *                   do not overlap, and every member's block-table row starts with
+ *                   the same P physical ids (its first P blocks are the shared
+ *                   prefix); P <= max_blocks_per_seq.
+ *   max_group_seqs  host bound on the sequences of any group (it sizes the grid
+ *                   of the prefix pass).
+ *   workspace       >= pkv_workspace_size_cascade(...) bytes (zero-filled before
+ *                   first use, as for pkv_paged_decode_attention).
+ * A member whose query rows do not all see the whole prefix (16*P > T - nq) or
+ * whose context is the prefix alone is attended without the cascade; a group
+ * outside the batch or the tables is skipped and ORs 32 into the workspace
+ * error word. num_groups == 0 is the plain call. bf16 pools only.
+ *
+ * How: a prefix pass (one kv head per CTA; 128 score rows = 128/G members'
+ * queries per row tile) streams each group's prefix blocks once per row tile
+ * and leaves every member row's partial (m, l, acc); the main pass streams only
+ * the members' own blocks; the merge starts each member row from its prefix
+ * partial.
+ */
+size_t pkv_workspace_size_cascade(int32_t num_seqs, int32_t n_query_per_seq, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim);
+
+pkv_status pkv_paged_decode_attention_cascade(
+    const void *q, const void *k_cache, const void *v_cache, int64_t num_blocks,
+    const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+    int32_t num_seqs, int32_t n_query_per_seq, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_dim, float scale, const int32_t *prefix_groups, int32_t num_groups,
+    int32_t max_group_seqs, void *out, int32_t out_dtype, void *workspace,
+    size_t workspace_bytes, void *stream);
+
+/*
  * pkv_paged_decode_attention_varlen -- per-sequence query counts, optional
  * tree masks, optional shared block-table rows.
  *

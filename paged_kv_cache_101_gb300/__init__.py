@@ -49,6 +49,10 @@ SIGNATURES = {
     "pkv_paged_decode_attention_varlen": ([_P, _P, _P, _I64, _P, _I32, _I32, _P, _P, _P, _P, _P,
                                            _I32, _I32, _I32, _I32, _I32, _I32, _F, _P, _I32, _P,
                                            _SZ, _P], ctypes.c_int),
+    "pkv_workspace_size_cascade": ([_I32, _I32, _I32, _I32, _I32], _SZ),
+    "pkv_paged_decode_attention_cascade": ([_P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _I32,
+                                            _I32, _F, _P, _I32, _I32, _P, _I32, _P, _SZ, _P],
+                                           ctypes.c_int),
     "pkv_split_queries": ([_P, _P, _P, _I32, _I32, _P, _P, _P, _P, _I32, _P], ctypes.c_int),
     "pkv_kv_append_fp8": ([_P, _P, _P, _I64, _P, _P, _I64, _I32, _I32, _P, _P, _P], ctypes.c_int),
     "pkv_paged_decode_attention_fp8": ([_P, _P, _P, _I64, _P, _P, _P, _I32, _P, _I32, _I32, _I32,
@@ -174,6 +178,46 @@ def kv_append(k_new, v_new, slot_mapping, k_cache, v_cache):
                              _stream_handle(k_cache.device))
     if st != PKV_OK:
         raise PkvError("pkv_kv_append", st)
+
+
+def paged_decode_attention_cascade(q, k_cache, v_cache, block_tables, context_lens,
+                                   n_query_per_seq, scale, out, prefix_groups, max_group_seqs,
+                                   ws=None):
+    """``paged_decode_attention`` with shared prefixes attended once per group:
+    ``prefix_groups`` is an int32 CUDA tensor [num_groups, 3] of (first sequence,
+    sequences, prefix blocks), members consecutive, groups ascending."""
+    torch = _torch()
+    _check(q, "q", torch.bfloat16, 3)
+    _check(k_cache, "k_cache", torch.bfloat16, 4)
+    _check(v_cache, "v_cache", torch.bfloat16, 4)
+    _check(block_tables, "block_tables", torch.int32, 2)
+    _check(context_lens, "context_lens", torch.int32, 1)
+    _check(prefix_groups, "prefix_groups", torch.int32, 2)
+    if out.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("out must be bfloat16 or float32")
+    _check(out, "out", out.dtype, 3)
+    NB, bs, Hkv, D = k_cache.shape
+    if bs != BLOCK_SIZE or v_cache.shape != k_cache.shape:
+        raise ValueError("pools must be [num_blocks, 16, Hkv, D] and equal in shape")
+    if prefix_groups.shape[1] != 3:
+        raise ValueError("prefix_groups must be [num_groups, 3]")
+    S = context_lens.shape[0]
+    nq = int(n_query_per_seq)
+    Hq = q.shape[1]
+    if q.shape != (S * nq, Hq, D) or out.shape != q.shape or block_tables.shape[0] != S:
+        raise ValueError("q/out must be [num_seqs * n_query_per_seq, Hq, D], tables [num_seqs, MB]")
+    need = int(lib().pkv_workspace_size_cascade(S, nq, Hq, Hkv, D))
+    if ws is None:
+        ws = workspace(q.device, need)
+    st = lib().pkv_paged_decode_attention_cascade(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), NB, block_tables.data_ptr(),
+        block_tables.shape[1], context_lens.data_ptr(), S, nq, Hq, Hkv, D, float(scale),
+        prefix_groups.data_ptr(), prefix_groups.shape[0], int(max_group_seqs), out.data_ptr(),
+        PKV_FP32 if out.dtype == torch.float32 else PKV_BF16, ws.data_ptr(), ws.numel(),
+        _stream_handle(q.device))
+    if st != PKV_OK:
+        raise PkvError("pkv_paged_decode_attention_cascade", st)
+    return out
 
 
 def split_queries(q_start, context_lens, max_rows, tree_len=None):

@@ -378,6 +378,21 @@ size_t pkv_workspace_size(int32_t num_seqs, int32_t n_query_per_seq, int32_t num
 
 namespace {
 
+// Shared-prefix cascade (null / 0 without).
+struct Cascade {
+    const int32_t *groups = nullptr;  // device [num_groups][3]
+    int32_t num_groups = 0, max_group_seqs = 0;
+};
+
+// Bytes of the cascade's prefix partials: (m, l) and acc[D] per (prefix chunk,
+// query row, head), for up to kMaxPreChunks chunks.
+size_t prefix_region_bytes(int64_t total_q, int32_t Hq, int32_t D)
+{
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t rows = size_t(pkv::kMaxPreChunks) * size_t(total_q) * Hq;
+    return up(rows * 2 * 4) + up(rows * D * 4);
+}
+
 // Variable query counts (all null / 0 for the fixed-count call).
 struct Varlen {
     const int32_t *q_start = nullptr;
@@ -396,7 +411,7 @@ pkv_status attention(const void *q, const void *k_cache, const void *v_cache, in
                      const int32_t *context_lens, int32_t num_seqs, int32_t n_query_per_seq,
                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, float scale,
                      void *out, int32_t out_dtype, void *workspace, size_t workspace_bytes,
-                     void *stream, const Varlen &vl = Varlen())
+                     void *stream, const Varlen &vl = Varlen(), const Cascade &cc = Cascade())
 {
     pkv_status st = check_geometry(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim,
                                    vl.q_start != nullptr);
@@ -433,6 +448,23 @@ pkv_status attention(const void *q, const void *k_cache, const void *v_cache, in
                          max_blocks_per_seq, d.num_sms, g_opt_num_ctas, g_opt_stages,
                          g_opt_heads, g_opt_tail, d.smem_optin, kv8, &pl) != 0)
         return PKV_ERR_UNSUPPORTED;
+    // cascade: the prefix pass's plan and the prefix partials after the workspace
+    pkv::DecodePlan ppl{};
+    int pre_tiles = 0;
+    size_t off_pre = 0;
+    if (cc.groups) {
+        if (kv8 || vl.q_start)
+            return PKV_ERR_UNSUPPORTED;  // the cascade runs on bf16 pools, fixed counts
+        pre_tiles = pkv::plan_prefix(head_dim, num_q_heads / num_kv_heads, num_kv_heads,
+                                     cc.num_groups, cc.max_group_seqs, n_query_per_seq,
+                                     d.smem_optin, &ppl);
+        if (pre_tiles < 1)
+            return PKV_ERR_UNSUPPORTED;
+        off_pre = (pl.ws_bytes + 255) / 256 * 256;
+        const int64_t total_q = int64_t(num_seqs) * n_query_per_seq;
+        if (workspace_bytes < off_pre + prefix_region_bytes(total_q, num_q_heads, head_dim))
+            return PKV_ERR_WORKSPACE;
+    }
     if (workspace_bytes < pl.ws_bytes)
         return PKV_ERR_WORKSPACE;
     uint64_t *trace = nullptr;
@@ -494,8 +526,57 @@ pkv_status attention(const void *q, const void *k_cache, const void *v_cache, in
     p.table_row = vl.table_row;
     p.total_q = vl.q_start ? vl.total_q : num_seqs * n_query_per_seq;
     p.table_rows = vl.table_row ? vl.table_rows : num_seqs;
+    cudaEvent_t ev_b = g_ev_before;
+    if (cc.groups) {
+        const int64_t total_q = int64_t(num_seqs) * n_query_per_seq;
+        p.prefix_groups = cc.groups;
+        p.num_groups = cc.num_groups;
+        p.pre_ml = reinterpret_cast<float *>(ws + off_pre);
+        p.pre_acc = reinterpret_cast<float *>(
+            ws + off_pre +
+            (size_t(pkv::kMaxPreChunks) * total_q * num_q_heads * 2 * 4 + 255) / 256 * 256);
+        // cut each group's prefix into up to kMaxPreChunks block ranges so the prefix
+        // pass keeps about two CTAs per SM busy
+        const int64_t base_ctas = int64_t(ppl.grid);
+        int chunks = int((2 * int64_t(d.num_sms) + base_ctas - 1) / base_ctas);
+        chunks = chunks < 1 ? 1 : (chunks > pkv::kMaxPreChunks ? pkv::kMaxPreChunks : chunks);
+        p.pre_chunks = chunks;
+        ppl.grid = int(base_ctas * chunks);
+        // the prefix pass: one kv head per CTA; its own tensor maps (one head per box)
+        CUtensorMap pk, pv;
+        int pbox = 0;
+        if (g_opt_box != 1 &&
+            pool_map(k_cache, num_blocks, num_kv_heads, head_dim, 1, 0, &pk) == cudaSuccess &&
+            pool_map(v_cache, num_blocks, num_kv_heads, head_dim, 1, 0, &pv) == cudaSuccess)
+            pbox = 1;
+        if (!pbox &&
+            (pool_map(k_cache, num_blocks, num_kv_heads, head_dim, 0, 0, &pk) != cudaSuccess ||
+             pool_map(v_cache, num_blocks, num_kv_heads, head_dim, 0, 0, &pv) != cudaSuccess))
+            return PKV_ERR_CUDA;
+        pkv::DecodeParams pp = p;
+        pp.prefix_pass = 1;
+        pp.pre_tiles = pre_tiles;
+        pp.pre_chunks = p.pre_chunks;
+        pp.pre_qrows = 128 / (num_q_heads / num_kv_heads);
+        pp.rows = ppl.rows;
+        pp.rows_pad = ppl.rows_pad;
+        pp.HG = 1;
+        pp.n_hg = num_kv_heads;
+        pp.stage_bytes = ppl.stage_bytes;
+        pp.nst = ppl.nst;
+        pp.whole_box = pbox;
+        pp.ncw = 8;
+        pp.tickets_max = 0;
+        pp.ticket_div = 0;
+        pp.trace = nullptr;
+        cudaError_t e = pkv::launch_decode(ppl, pp, pk, pv, static_cast<cudaStream_t>(stream),
+                                           ev_b, nullptr);
+        if (e != cudaSuccess)
+            return PKV_ERR_CUDA;
+        ev_b = nullptr;  // the timing hook spans the prefix pass and the main kernel
+    }
     cudaError_t e = pkv::launch_decode(pl, p, kmap, vmap, static_cast<cudaStream_t>(stream),
-                                       g_ev_before, g_ev_after);
+                                       ev_b, g_ev_after);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
@@ -531,6 +612,45 @@ pkv_status pkv_paged_decode_attention_fp8(const void *q, const void *k_cache, co
                      max_blocks_per_seq, context_lens, num_seqs, n_query_per_seq, num_q_heads,
                      num_kv_heads, head_dim, scale, out, out_dtype, workspace, workspace_bytes,
                      stream);
+}
+
+size_t pkv_workspace_size_cascade(int32_t num_seqs, int32_t n_query_per_seq, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim)
+{
+    const size_t base = pkv_workspace_size(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads,
+                                           head_dim);
+    if (base == 0)
+        return 0;
+    return (base + 255) / 256 * 256 +
+           prefix_region_bytes(int64_t(num_seqs) * n_query_per_seq, num_q_heads, head_dim);
+}
+
+pkv_status pkv_paged_decode_attention_cascade(
+    const void *q, const void *k_cache, const void *v_cache, int64_t num_blocks,
+    const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+    int32_t num_seqs, int32_t n_query_per_seq, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_dim, float scale, const int32_t *prefix_groups, int32_t num_groups,
+    int32_t max_group_seqs, void *out, int32_t out_dtype, void *workspace,
+    size_t workspace_bytes, void *stream)
+{
+    if (num_groups < 0 || max_group_seqs < 0)
+        return PKV_ERR_SHAPE;
+    Cascade cc;
+    if (num_seqs > 0 && num_groups > 0 && max_group_seqs > 0) {
+        if (!prefix_groups)
+            return PKV_ERR_NULL;
+        if (!aligned(prefix_groups, 4))
+            return PKV_ERR_ALIGN;
+        if (int64_t(num_groups) > num_seqs || max_group_seqs > num_seqs)
+            return PKV_ERR_RANGE;
+        cc.groups = prefix_groups;
+        cc.num_groups = num_groups;
+        cc.max_group_seqs = max_group_seqs;
+    }
+    return attention(q, k_cache, v_cache, num_blocks, 0, nullptr, nullptr, block_tables,
+                     max_blocks_per_seq, context_lens, num_seqs, n_query_per_seq, num_q_heads,
+                     num_kv_heads, head_dim, scale, out, out_dtype, workspace, workspace_bytes,
+                     stream, Varlen(), cc);
 }
 
 pkv_status pkv_paged_decode_attention_varlen(

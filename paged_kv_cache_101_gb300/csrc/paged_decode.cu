@@ -46,6 +46,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <climits>
 #include <type_traits>
 
 #include "pkv_common.cuh"
@@ -65,7 +66,9 @@ struct StageHdr {
     int16_t W;      // mask window: per-row masks rule the last W positions
 };
 static_assert(sizeof(StageHdr) == 32, "stage header: two 16-byte words");
-enum : int32_t { F_FIRST = 1, F_LAST = 2, F_DIRECT = 4, F_END = 8 };
+// F_PREFIX: a stage of the cascade's prefix pass; F_PRE: the first stage of a
+// cascade member's own blocks, whose running state starts from its prefix partial
+enum : int32_t { F_FIRST = 1, F_LAST = 2, F_DIRECT = 4, F_END = 8, F_PREFIX = 16, F_PRE = 32 };
 
 // The fixed partition of the flat unit space [0, F): cells 0..G-1 split
 // [0, F1) evenly (cell c is CTA c's chunk); cells G..G+NT-1 split [F1, F) evenly
@@ -131,7 +134,27 @@ struct SeqInfo {
     int ql;  // query rows
     int W;   // mask window (causal: ql)
     int tr;  // block-table row
+    int b0;  // first block streamed: a cascade member's prefix is attended apart
 };
+
+// Cascade: the group holding sequence s (groups ascending by first sequence),
+// or -1. Each row of pre-computed groups is (first sequence, sequences, blocks).
+__device__ __forceinline__ int group_of(const DecodeParams &p, int s)
+{
+    int lo = 0, hi = p.num_groups - 1;
+    while (lo <= hi) {
+        const int mid = (lo + hi) >> 1;
+        const int f = __ldg(p.prefix_groups + 3 * mid);
+        if (s < f) {
+            hi = mid - 1;
+        } else if (s >= f + __ldg(p.prefix_groups + 3 * mid + 1)) {
+            lo = mid + 1;
+        } else {
+            return mid;
+        }
+    }
+    return -1;
+}
 
 __device__ __forceinline__ SeqInfo seq_info(const DecodeParams &p, int s)
 {
@@ -161,7 +184,23 @@ __device__ __forceinline__ SeqInfo seq_info(const DecodeParams &p, int s)
     }
     if (bad)
         atomicOr(p.ws + kWsErr, kErrBadQuery);
-    i.nb = i.ql > 0 ? (i.T + kBlockSize - 1) / kBlockSize : 0;
+    const int nb = i.ql > 0 ? (i.T + kBlockSize - 1) / kBlockSize : 0;
+    i.b0 = 0;
+    if (p.prefix_groups && nb > 0) {
+        // a member skips its group's prefix when every query row sees all of it
+        const int gi = group_of(p, s);
+        if (gi >= 0) {
+            // the same validity rule as the prefix pass: a group it skips is not
+            // skipped here either
+            const int f = __ldg(p.prefix_groups + 3 * gi);
+            const int cnt = __ldg(p.prefix_groups + 3 * gi + 1);
+            const int P = __ldg(p.prefix_groups + 3 * gi + 2);
+            const bool group_ok = f >= 0 && cnt >= 0 && f + cnt <= p.S && P >= 0 && P <= p.MB;
+            if (group_ok && P > 0 && P < nb && kBlockSize * P <= i.T - i.ql)
+                i.b0 = P;
+        }
+    }
+    i.nb = nb - i.b0;  // blocks streamed by the main pass
     return i;
 }
 
@@ -232,10 +271,111 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
     bool ok = true;
     const uint64_t pol = policy_evict_first();
 
+    // Fill the next stage with block `phys` (all HG heads of group hg) under the
+    // given header; waits for the stage to be free first. False if that wait
+    // gave up.
+    auto issue = [&](int phys, int q0, int ql, int W, int b, int T, int hg, int flags, int cellv,
+                     int slot) -> bool {
+        if (issued >= uint32_t(p.nst)) {
+            int w_ok = 1;
+            if (lane == 0)
+                w_ok = mbar_wait(smem_u32(&sm.empty[st]), phase ^ 1u, kWaitLimitNs);
+            if (!__shfl_sync(FULLMASK, w_ok, 0))
+                return false;
+        }
+        if (lane == 0) {
+            StageHdr *h = &sm.hdr[st];
+            h->q0 = q0;
+            h->b = b;
+            h->T = T;
+            h->hg = hg;
+            h->flags = flags;
+            h->slot = slot;
+            h->cell = cellv;
+            h->ql = int16_t(ql);
+            h->W = int16_t(W);
+            const uint32_t bar = smem_u32(&sm.full[st]);
+            mbar_arrive_expect_tx(bar, uint32_t(p.stage_bytes));
+            const uint32_t kdst = smem_u32(sm.stages + size_t(st) * p.stage_bytes);
+            const uint32_t vdst = kdst + uint32_t(p.HG * NH * kTileBytes);
+            const int h0 = hg * p.HG;
+            if (p.whole_box) {
+                // map dims (d, token, half, head, block): one box = HG heads x 16 rows
+                tma_load_5d_hint(kdst, kmap, bar, 0, 0, 0, h0, phys, pol);
+                tma_load_5d_hint(vdst, vmap, bar, 0, 0, 0, h0, phys, pol);
+            } else {
+                // map dims (d, half, head, token, block): one box = one (head, half) tile
+                for (int hl = 0; hl < p.HG; ++hl) {
+#pragma unroll
+                    for (int hf = 0; hf < NH; ++hf) {
+                        const uint32_t off = uint32_t((hl * NH + hf) * kTileBytes);
+                        tma_load_5d_hint(kdst + off, kmap, bar, 0, hf, h0 + hl, 0, phys, pol);
+                        tma_load_5d_hint(vdst + off, vmap, bar, 0, hf, h0 + hl, 0, phys, pol);
+                    }
+                }
+            }
+            if (p.trace && issued == 0)
+                p.trace[blockIdx.x * kTraceWords + 1] = global_timer_ns();
+        }
+        __syncwarp();
+        ++issued;
+        if (++st == uint32_t(p.nst)) {
+            st = 0;
+            phase ^= 1u;
+        }
+        return true;
+    };
+    // a block id outside the pool is flagged and read past the tensor's end (zeros)
+    auto checked = [&](int phys) -> int {
+        if (phys < 0 || int64_t(phys) >= p.num_blocks) {
+            if (lane == 0)
+                atomicOr(p.ws + kWsErr, kErrBadBlock);
+            phys = int(p.num_blocks < 0x7fffffff ? p.num_blocks : 0x7fffffff);
+        }
+        return phys;
+    };
+
     int64_t cell = blockIdx.x;       // phase 1: this CTA's own chunk
     int claim = -1;                  // lane 0: a ticket claimed ahead
     bool claimed = false;
-    for (;;) {
+    if (p.prefix_pass) {
+        // Cascade prefix pass: CTA = (group, row tile, kv head); it streams the
+        // group's prefix blocks once for the tile's query rows (up to 16 x 8 = 128
+        // score rows, one consumer warp per 16), read through the first member's
+        // table row, and leaves each row's partial over the prefix.
+        const int head = int(blockIdx.x) % p.n_hg;
+        const int rest = int(blockIdx.x) / p.n_hg;
+        const int c = rest % p.pre_chunks;  // block range c of the prefix
+        const int v = rest / p.pre_chunks;
+        const int gi = v / p.pre_tiles, t = v - gi * p.pre_tiles;
+        const int f = __ldg(p.prefix_groups + 3 * gi);
+        const int cnt = __ldg(p.prefix_groups + 3 * gi + 1);
+        int P = __ldg(p.prefix_groups + 3 * gi + 2);
+        const bool bad = f < 0 || cnt < 0 || f + cnt > S || P < 0 || P > p.MB;
+        if (bad && lane == 0)
+            atomicOr(p.ws + kWsErr, kErrBadGroup);
+        const int qrows = bad ? 0 : cnt * p.nq;
+        const int q0 = f * p.nq + t * p.pre_qrows;
+        int ql = qrows - t * p.pre_qrows;
+        ql = ql < 0 ? 0 : (ql > p.pre_qrows ? p.pre_qrows : ql);
+        if (ql == 0)
+            P = 0;
+        // blocks [c*P/C, (c+1)*P/C) of the prefix; the chunk index rides in `cell`
+        const int b_lo = c * P / p.pre_chunks, b_hi = (c + 1) * P / p.pre_chunks;
+        int bt_base = -(1 << 30), bt_val = 0;
+        for (int b = b_lo; b < b_hi && ok; ++b) {
+            if (b >= bt_base + 32) {
+                bt_base = b;
+                const int idx = b + lane;
+                bt_val = idx < b_hi ? __ldg(p.block_tables + int64_t(f) * p.MB + idx) : 0;
+            }
+            const int phys = checked(__shfl_sync(FULLMASK, bt_val, b - bt_base));
+            const int flags =
+                F_PREFIX | (b == b_lo ? F_FIRST : 0) | (b == b_hi - 1 ? F_LAST : 0);
+            ok = issue(phys, q0, ql, 0, b, P * kBlockSize, head, flags, c, 0);
+        }
+    }
+    for (; !p.prefix_pass;) {
         const int64_t a = C.start(cell), e = C.start(cell + 1);
         // locate unit f: head group, sequence and block within it
         auto locate = [&](int64_t f, int &hg_o, int &s_o, int &b_o) {
@@ -264,8 +404,8 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
             int hg, s, b;
             locate(a, hg, s, b);
             SeqInfo si = seq_info(p, s);
-            int T = si.T;
-            int nb = si.nb;
+            b += si.b0;                  // locate counts streamed blocks only
+            int b_end = si.b0 + si.nb;   // one past the sequence's last block
             int seg_b0 = b;
             bool cell_first = true;
             int bt_base = -(1 << 30);
@@ -275,95 +415,45 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
                 if (b < bt_base || b >= bt_base + 32) {
                     bt_base = b;
                     const int idx = b + lane;
-                    bt_val = idx < nb ? __ldg(p.block_tables + int64_t(si.tr) * p.MB + idx) : 0;
+                    bt_val = idx < b_end ? __ldg(p.block_tables + int64_t(si.tr) * p.MB + idx) : 0;
                 }
-                int phys = __shfl_sync(FULLMASK, bt_val, b - bt_base);
-                if (phys < 0 || int64_t(phys) >= p.num_blocks) {
-                    // outside the pool: flag it; the TMA box past the tensor's end reads zeros
-                    if (lane == 0)
-                        atomicOr(p.ws + kWsErr, kErrBadBlock);
-                    phys = int(p.num_blocks < 0x7fffffff ? p.num_blocks : 0x7fffffff);
-                }
+                const int phys = checked(__shfl_sync(FULLMASK, bt_val, b - bt_base));
                 // claim the next ticket while the last few stages of this cell stream
                 if (C.NT > 0 && !claimed && e - u <= 2) {
                     if (lane == 0)
                         claim = int(atomicAdd(p.ws + kWsTicket, 1u));
                     claimed = true;
                 }
-                if (issued >= uint32_t(p.nst)) {
-                    int w_ok = 1;
-                    if (lane == 0)
-                        w_ok = mbar_wait(smem_u32(&sm.empty[st]), phase ^ 1u, kWaitLimitNs);
-                    w_ok = __shfl_sync(FULLMASK, w_ok, 0);
-                    if (!w_ok) {
-                        ok = false;
-                        break;
-                    }
-                }
-                const bool first = (u == a) || (b == 0);
+                const bool first = (u == a) || (b == si.b0);
                 if (first)
                     seg_b0 = b;
-                const bool last = (u == e - 1) || (b == nb - 1);
+                const bool last = (u == e - 1) || (b == b_end - 1);
                 int flags = (first ? F_FIRST : 0) | (last ? F_LAST : 0);
-                if (last && seg_b0 == 0 && b == nb - 1)
+                // a cascade member's own blocks continue from its prefix partial
+                if (first && si.b0 > 0 && b == si.b0)
+                    flags |= F_PRE;
+                // a whole sequence in one cell is finished in place
+                if (last && seg_b0 == si.b0 && b == b_end - 1)
                     flags |= F_DIRECT;
-                if (lane == 0) {
-                    StageHdr *h = &sm.hdr[st];
-                    h->q0 = si.q0;
-                    h->b = b;
-                    h->T = T;
-                    h->hg = hg;
-                    h->flags = flags;
-                    h->slot = cell_first ? 0 : 1;  // 0: the segment opens the cell
-                    h->cell = int(cell);
-                    h->ql = int16_t(si.ql);
-                    h->W = int16_t(si.W);
-                    const uint32_t bar = smem_u32(&sm.full[st]);
-                    mbar_arrive_expect_tx(bar, uint32_t(p.stage_bytes));
-                    const uint32_t kdst = smem_u32(sm.stages + size_t(st) * p.stage_bytes);
-                    const uint32_t vdst = kdst + uint32_t(p.HG * NH * kTileBytes);
-                    const int h0 = hg * p.HG;
-                    if (p.whole_box) {
-                        // map dims (d, token, half, head, block): one box = HG heads x 16 rows
-                        tma_load_5d_hint(kdst, kmap, bar, 0, 0, 0, h0, phys, pol);
-                        tma_load_5d_hint(vdst, vmap, bar, 0, 0, 0, h0, phys, pol);
-                    } else {
-                        // map dims (d, half, head, token, block): one box = one (head, half) tile
-                        for (int hl = 0; hl < p.HG; ++hl) {
-#pragma unroll
-                            for (int hf = 0; hf < NH; ++hf) {
-                                const uint32_t off = uint32_t((hl * NH + hf) * kTileBytes);
-                                tma_load_5d_hint(kdst + off, kmap, bar, 0, hf, h0 + hl, 0, phys,
-                                                 pol);
-                                tma_load_5d_hint(vdst + off, vmap, bar, 0, hf, h0 + hl, 0, phys,
-                                                 pol);
-                            }
-                        }
-                    }
-                    if (p.trace && issued == 0)
-                        p.trace[blockIdx.x * kTraceWords + 1] = global_timer_ns();
-                }
-                __syncwarp();
-                ++issued;
-                if (++st == uint32_t(p.nst)) {
-                    st = 0;
-                    phase ^= 1u;
+                if (!issue(phys, si.q0, si.ql, si.W, b, si.T, hg, flags, int(cell),
+                           cell_first ? 0 : 1)) {
+                    ok = false;
+                    break;
                 }
                 if (last)
                     cell_first = false;
                 // advance to the next unit
                 ++b;
-                if (b == nb && u + 1 < e) {
+                if (b == b_end && u + 1 < e) {
                     do {
                         if (++s == S) {
                             s = 0;
                             ++hg;
                         }
                         si = seq_info(p, s);
-                        T = si.T;
-                        nb = si.nb;
-                    } while (nb == 0);
-                    b = 0;
+                    } while (si.nb == 0);
+                    b = si.b0;
+                    b_end = si.b0 + si.nb;
                     bt_base = -(1 << 30);
                 }
             }
@@ -499,6 +589,41 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
             if constexpr (KV8) {
                 qscale = p.scale_log2 * __ldg(p.k_scale + kvh);
                 vscale = __ldg(p.v_scale + kvh);
+            }
+            if constexpr (!KV8) {
+                if (h.flags & F_PRE) {
+                    // cascade member: continue from the prefix pass's (m, l, acc) of
+                    // the lane's rows 2tq, 2tq+1 (l on one lane of the row's reduction)
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const int row = 2 * tq + r;
+                        if (row >= p.G * h.ql)
+                            continue;
+                        const int j = row / p.G;
+                        const int64_t pi0 =
+                            (int64_t(h.q0) + j) * p.Hq + int64_t(kvh) * p.G + (row - j * p.G);
+                        const int P = h.b;  // the member's first own block = prefix blocks
+                        float M = -INFINITY, L = 0.f;
+                        for (int c = 0; c < p.pre_chunks; ++c) {
+                            if ((c + 1) * P / p.pre_chunks == c * P / p.pre_chunks)
+                                continue;  // an empty block range left no partial
+                            const int64_t pi = int64_t(c) * p.total_q * p.Hq + pi0;
+                            const float mc = __ldcg(p.pre_ml + pi * 2);
+                            const float Mn = fmaxf(M, mc);
+                            const float so = ex2(M - Mn), sn = ex2(mc - Mn);
+                            L = L * so + __ldcg(p.pre_ml + pi * 2 + 1) * sn;
+#pragma unroll
+                            for (int i = 0; i < MT; ++i) {
+                                acc[i][r] = acc[i][r] * so + __ldcg(p.pre_acc + pi * D + 16 * i + g) * sn;
+                                acc[i][r + 2] =
+                                    acc[i][r + 2] * so + __ldcg(p.pre_acc + pi * D + 16 * i + 8 + g) * sn;
+                            }
+                            M = Mn;
+                        }
+                        m_r[r] = M;
+                        l_r[r] = g == 0 ? L : 0.f;
+                    }
+                }
             }
             if (g < p.G * h.ql) {
                 const int j = g / p.G;
@@ -843,6 +968,8 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
     constexpr int ND = D / 8;   // 8-dim n-tiles of the output
     const int hl = cw / WPH;    // kv head within the group
     const int r0 = (cw % WPH) * 16;
+    // only the 8-warp instance runs the cascade's prefix pass
+    constexpr bool kPrefixPass = (WPH == 8);
     const int g = lane >> 2, tq = lane & 3;
 
     // ldmatrix rows inside a (head, half) tile [16 tokens][8 x 16 B], 128B swizzle
@@ -903,6 +1030,42 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
             if constexpr (KV8) {
                 qscale = p.scale_log2 * __ldg(p.k_scale + kvh);
                 vscale = __ldg(p.v_scale + kvh);
+            }
+            if constexpr (!KV8 && !kPrefixPass) {
+                if (h.flags & F_PRE) {
+                    // cascade member: continue from the prefix pass's (m, l, acc) of
+                    // the lane's rows g, g+8 (l on one lane of the row's reduction)
+#pragma unroll
+                    for (int rr = 0; rr < 2; ++rr) {
+                        const int row = r0 + g + 8 * rr;
+                        if (row >= p.G * h.ql)
+                            continue;
+                        const int j = row / p.G;
+                        const int64_t pi0 =
+                            (int64_t(h.q0) + j) * p.Hq + int64_t(kvh) * p.G + (row - j * p.G);
+                        const int P = h.b;  // the member's first own block = prefix blocks
+                        float M = -INFINITY, L = 0.f;
+                        for (int c = 0; c < p.pre_chunks; ++c) {
+                            if ((c + 1) * P / p.pre_chunks == c * P / p.pre_chunks)
+                                continue;  // an empty block range left no partial
+                            const int64_t pi = int64_t(c) * p.total_q * p.Hq + pi0;
+                            const float mc = __ldcg(p.pre_ml + pi * 2);
+                            const float Mn = fmaxf(M, mc);
+                            const float so = ex2(M - Mn), sn = ex2(mc - Mn);
+                            L = L * so + __ldcg(p.pre_ml + pi * 2 + 1) * sn;
+#pragma unroll
+                            for (int n = 0; n < ND; ++n) {
+                                const float2 v = __ldcg(reinterpret_cast<const float2 *>(
+                                    p.pre_acc + pi * D + 8 * n + 2 * tq));
+                                acc[n][2 * rr] = acc[n][2 * rr] * so + v.x * sn;
+                                acc[n][2 * rr + 1] = acc[n][2 * rr + 1] * so + v.y * sn;
+                            }
+                            M = Mn;
+                        }
+                        m_r[rr] = M;
+                        l_r[rr] = tq == 0 ? L : 0.f;
+                    }
+                }
             }
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
@@ -983,7 +1146,9 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
         // ---- scale (log2 domain) and causal / tree / tail mask: positions
         //      before the first maskable one are seen by every row
         const int t0 = h.b * kBlockSize;
-        const int w0 = p.tree_mask ? h.T - h.W : h.T - h.ql + 1;
+        const int w0 = (kPrefixPass && (h.flags & F_PREFIX))
+                           ? INT_MAX
+                           : (p.tree_mask ? h.T - h.W : h.T - h.ql + 1);
 #pragma unroll
         for (int n = 0; n < 2; ++n)
 #pragma unroll
@@ -1227,13 +1392,25 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
                     }
                 }
             } else {
+                // partial (m, l, acc) of this cell for the merge kernel, or of the whole
+                // prefix (cascade prefix pass) for the row's (query row, head)
                 const int64_t cellbase = (int64_t(e_cell) * 2 + e_slot) * p.HG + hl;
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr) {
                     const int row = r0 + g + 8 * rr;
                     if (row >= e_rows)
                         continue;
-                    float *pa = p.part + (cellbase * p.rows + row) * D;
+                    int64_t pidx = cellbase * p.rows + row;
+                    float *pa = p.part;
+                    float *pml = p.ml;
+                    if (kPrefixPass && (h.flags & F_PREFIX)) {
+                        const int j = row / p.G;
+                        pidx = (int64_t(e_cell) * p.total_q + e_q0 + j) * p.Hq +
+                               int64_t(kvh) * p.G + (row - j * p.G);
+                        pa = p.pre_acc;
+                        pml = p.pre_ml;
+                    }
+                    pa += pidx * D;
                     if constexpr (KV8) {
 #pragma unroll
                         for (int ch = 0; ch < D / 16; ++ch) {
@@ -1249,9 +1426,8 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
                                 make_float2(acc[n][2 * rr], acc[n][2 * rr + 1]);
                     }
                     if (tq == 0) {
-                        float *ml = p.ml + (cellbase * p.rows + row) * 2;
-                        ml[0] = m_r[rr];
-                        ml[1] = lf[rr];
+                        pml[pidx * 2] = m_r[rr];
+                        pml[pidx * 2 + 1] = lf[rr];
                     }
                 }
             }
@@ -1493,10 +1669,47 @@ int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int 
     return 0;
 }
 
+// The cascade's prefix pass: one kv head per CTA, 8 consumer warps of 16 score
+// rows (128 rows: 128 / G queries of the group's members per row tile).
+int plan_prefix(int D, int G, int Hkv, int num_groups, int max_group_seqs, int nq,
+                int smem_optin, DecodePlan *pl)
+{
+    if ((D != 64 && D != 128) || G < 1 || G > 128 || Hkv < 1 || num_groups < 1 ||
+        max_group_seqs < 1 || nq < 1)
+        return -1;
+    DecodePlan P{};
+    P.D = D;
+    P.G = G;
+    P.prefix = 1;
+    P.wph = 8;
+    P.ntw = 2;
+    P.rows = (128 / G) * G;  // score rows of a tile
+    P.rows_pad = 128;
+    P.HG = 1;
+    P.n_hg = Hkv;
+    P.threads = 32 * (1 + 8);
+    P.stage_bytes = 2 * (D / 64) * kTileBytes;
+    const int per_stage = P.stage_bytes + int(sizeof(StageHdr)) + 16;
+    const int fixed = 1024 + int(sizeof(Cells)) + 64;
+    P.nst = std::min(8, (smem_optin - fixed) / per_stage);
+    if (P.nst < 2)
+        return -1;
+    P.smem = size_t(fixed) + size_t(P.nst) * per_stage;
+    const int64_t tiles = (int64_t(max_group_seqs) * nq + (128 / G) - 1) / (128 / G);
+    const int64_t grid = int64_t(num_groups) * tiles * Hkv;
+    if (grid > 0x7fffffff)
+        return -1;
+    P.grid = int(grid);
+    P.tickets_max = 0;
+    P.tail_div = 0;
+    *pl = P;
+    return int(tiles);
+}
+
 template <int D, int NTW, int WPH, bool KV8>
 static cudaError_t launch_one(const DecodePlan &pl, const DecodeParams &p, const CUtensorMap &kmap,
                               const CUtensorMap &vmap, cudaStream_t stream, cudaEvent_t ev_before,
-                              cudaEvent_t ev_after)
+                              cudaEvent_t ev_after, bool with_merge = true)
 {
     auto kern = paged_decode_kernel<D, NTW, WPH, KV8>;
     static int configured_smem[64] = {0};  // per device ordinal
@@ -1532,6 +1745,8 @@ static cudaError_t launch_one(const DecodePlan &pl, const DecodeParams &p, const
         return e;
     if (ev_after && (e = cudaEventRecord(ev_after, stream)) != cudaSuccess)
         return e;
+    if (!with_merge)
+        return cudaSuccess;
     // the merge: one CTA per (sequence, head group), a programmatic dependent
     cudaLaunchConfig_t mcfg = {};
     mcfg.gridDim = dim3(unsigned(p.S), unsigned(p.n_hg));
@@ -1550,6 +1765,11 @@ cudaError_t launch_decode(const DecodePlan &pl, const DecodeParams &p, const CUt
                           const CUtensorMap &vmap, cudaStream_t stream, cudaEvent_t eb,
                           cudaEvent_t ea)
 {
+    if (pl.prefix) {  // cascade prefix pass: no merge of its own
+        if (pl.D == 64)
+            return launch_one<64, 2, 8, false>(pl, p, kmap, vmap, stream, eb, ea, false);
+        return launch_one<128, 2, 8, false>(pl, p, kmap, vmap, stream, eb, ea, false);
+    }
     if (pl.kv8) {  // E4M3 pools: D = 128 only
         if (pl.wph == 2)
             return launch_one<128, 2, 2, true>(pl, p, kmap, vmap, stream, eb, ea);

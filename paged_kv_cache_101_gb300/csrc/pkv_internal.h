@@ -19,6 +19,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded waits: 2 s
 // issued, last stage consumed (ns, %globaltimer), units, segments, SM id,
 // 8 spare
 constexpr int kTraceWords = 16;
+constexpr int kMaxPreChunks = 4;  // cascade: prefix partials per row
 
 // device error word codes (workspace offset 0)
 enum : uint32_t {
@@ -26,7 +27,8 @@ enum : uint32_t {
     kErrProducerWait = 2u,  // the producer gave up waiting for a free stage
     kErrDrainWait = 4u,     // a copy did not land while unwinding
     kErrBadBlock = 8u,      // a block-table entry outside [0, num_blocks) (read as zeros)
-    kErrBadQuery = 16u      // variable query counts: a sequence's rows or table row invalid
+    kErrBadQuery = 16u,     // variable query counts: a sequence's rows or table row invalid
+    kErrBadGroup = 32u      // cascade: a prefix group outside the batch or the tables
 };
 
 // Split of the work of one call (computed on the host from the shapes).
@@ -44,6 +46,7 @@ struct DecodePlan {
     int nst;         // pipeline stages
     int whole_box;   // 1: one TMA box per block for K (and V) of all HG heads
     int kv8;         // 1: E4M3 pools (one 128-byte tile per head row), 0: bf16
+    int prefix;      // 1: the cascade's prefix pass (one head per CTA, 8 warps x 16 rows)
     int grid;        // persistent CTAs
     int tickets_max; // cap on dynamically claimed tickets (0: static chunks only)
     int tail_div;    // the last 1/tail_div of the units go out as tickets (0: none)
@@ -82,11 +85,27 @@ struct DecodeParams {
     const int32_t *table_row;   // [S] block-table row of each sequence
     int total_q;                // rows of q and out
     int table_rows;             // rows of block_tables
+    // shared-prefix cascade (null / 0 without): groups [num_groups][3] = (first
+    // sequence, sequences, prefix blocks), members consecutive, groups ascending
+    const int32_t *prefix_groups;
+    int num_groups;
+    int prefix_pass;            // 1: this launch attends the groups' prefixes
+    int pre_tiles;              // prefix pass: row tiles per group
+    int pre_qrows;              // prefix pass: query rows per tile
+    int pre_chunks;             // prefix pass: each group's prefix cut into this many
+                                // block ranges (one partial each, at most kMaxPreChunks)
+    float *pre_ml;              // [chunk][total_q][Hq][2] (m, l) of each row over a prefix chunk
+    float *pre_acc;             // [chunk][total_q][Hq][D] unnormalised acc over the chunk
 };
 
 int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int opt_ctas,
                 int opt_stages, int opt_heads, int opt_tail, int smem_optin, int kv8,
                 DecodePlan *plan);
+
+// The cascade's prefix pass (one head per CTA, 128 score rows per tile); returns
+// the row tiles per group, or -1 if unsupported.
+int plan_prefix(int D, int G, int Hkv, int num_groups, int max_group_seqs, int nq,
+                int smem_optin, DecodePlan *plan);
 
 // ev_before/ev_after (may be null) are recorded around the kernel.
 cudaError_t launch_decode(const DecodePlan &plan, const DecodeParams &p, const CUtensorMap &kmap,

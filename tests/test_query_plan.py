@@ -121,3 +121,21 @@ def test_varlen_host_validation(lib):
     # the geometry check (before any device query): 8 queries x 4 heads = 32 rows
     assert lib.pkv_workspace_size(0, 8, 8, 2, 64) == 256
     assert lib.pkv_workspace_size(0, 9, 8, 2, 64) == 0
+
+
+def cascade(lib, groups=A, ng=2, mg=8, S=4, nq=1, hq=8, hkv=2, d=64, ws=A):
+    return lib.pkv_paged_decode_attention_cascade(A, A, A, 64, A, 8, A, S, nq, hq, hkv, d, 0.125,
+                                                  groups, ng, mg, A, 0, ws, 1 << 30, None)
+
+
+def test_cascade_host_validation(lib):
+    assert cascade(lib, S=0) == 0
+    assert cascade(lib, groups=None) == NULL
+    assert cascade(lib, groups=A + 2) == ALIGN
+    assert cascade(lib, ng=-1) == SHAPE
+    assert cascade(lib, ng=5) == RANGE                   # more groups than sequences
+    assert cascade(lib, mg=9) == RANGE
+    assert cascade(lib, nq=5, mg=4) == 8
+    # the cascade's workspace adds the prefix partials to the plain one
+    assert lib.pkv_workspace_size_cascade(4, 1, 8, 2, 64) == 0 or \
+        lib.pkv_workspace_size_cascade(4, 1, 8, 2, 64) > lib.pkv_workspace_size(4, 1, 8, 2, 64)

@@ -424,3 +424,20 @@ def fp8_pools(w: Workload, seed: Optional[int] = None):
     k_scale = (np.float32(0.25) * (np.float32(1) + h / np.float32(16))).astype(np.float32)
     v_scale = (np.float32(0.3) * (np.float32(1) + h / np.float32(32))).astype(np.float32)
     return k8, v8, k_scale, v_scale
+
+
+def sharers_first(w: Workload) -> Workload:
+    """The same batch with the sequences that share the prefix moved to the front
+    (their order kept), so they form one consecutive group. Rows of q, the new
+    tokens and the slots move with their sequence (any n_query_per_seq)."""
+    order = np.concatenate([np.nonzero(w.shared)[0], np.nonzero(~w.shared)[0]])
+    nq = w.n_query_per_seq
+    rows = (order[:, None] * nq + np.arange(nq)[None, :]).reshape(-1)
+    w.context_lens = w.context_lens[order].copy()
+    w.block_tables = w.block_tables[order].copy()
+    w.shared = w.shared[order].copy()
+    w.q = w.q[rows].copy()
+    w.k_new = w.k_new[rows].copy()
+    w.v_new = w.v_new[rows].copy()
+    w.slot_mapping = w.slot_mapping[rows].copy()
+    return w
