@@ -46,12 +46,16 @@ FALLBACK_HBM_GBS = 6800.0
 # to `source_sha256` (otherwise the bench reports traffic = null).
 NCU_TRAFFIC = {
     "llama3_8b_decode": {
-        "bytes": 582002688 + 3782144,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "acaf26dc30a9fe6106b0f788f2eb288a93b71a51937f73effa1bcf73f1bd3d39",
+        "bytes": 582062848 + 3938816,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "86a53119b0c4574365ee513bc59f10a07299a010129b16cbccf840c00a630e03",
     },
     "spec_verify": {
-        "bytes": 1417726000 + 5026304,
-        "source_sha256": "acaf26dc30a9fe6106b0f788f2eb288a93b71a51937f73effa1bcf73f1bd3d39",
+        "bytes": 1417735000 + 5209344,
+        "source_sha256": "86a53119b0c4574365ee513bc59f10a07299a010129b16cbccf840c00a630e03",
+    },
+    "llama3_8b_decode/fp8": {
+        "bytes": 291328512 + 3662848,
+        "source_sha256": "86a53119b0c4574365ee513bc59f10a07299a010129b16cbccf840c00a630e03",
     },
 }
 
