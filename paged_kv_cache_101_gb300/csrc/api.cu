@@ -535,8 +535,9 @@ pkv_status attention(const void *q, const void *k_cache, const void *v_cache, in
         p.pre_acc = reinterpret_cast<float *>(
             ws + off_pre +
             (size_t(pkv::kMaxPreChunks) * total_q * num_q_heads * 2 * 4 + 255) / 256 * 256);
-        // cut each group's prefix into up to kMaxPreChunks block ranges so the prefix
-        // pass keeps about two CTAs per SM busy
+        // cut each group's prefix into up to kMaxPreChunks block ranges (one
+        // partial each) so the prefix pass keeps about two CTAs per SM busy; more
+        // ranges cost each member's seed more partials to fold (measured slower)
         const int64_t base_ctas = int64_t(ppl.grid);
         int chunks = int((2 * int64_t(d.num_sms) + base_ctas - 1) / base_ctas);
         chunks = chunks < 1 ? 1 : (chunks > pkv::kMaxPreChunks ? pkv::kMaxPreChunks : chunks);

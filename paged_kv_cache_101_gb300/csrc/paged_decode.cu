@@ -604,9 +604,11 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
                             (int64_t(h.q0) + j) * p.Hq + int64_t(kvh) * p.G + (row - j * p.G);
                         const int P = h.b;  // the member's first own block = prefix blocks
                         float M = -INFINITY, L = 0.f;
-                        for (int c = 0; c < p.pre_chunks; ++c) {
-                            if ((c + 1) * P / p.pre_chunks == c * P / p.pre_chunks)
-                                continue;  // an empty block range left no partial
+#pragma unroll
+                        for (int c = 0; c < kMaxPreChunks; ++c) {
+                            if (c >= p.pre_chunks ||
+                                (c + 1) * P / p.pre_chunks == c * P / p.pre_chunks)
+                                continue;  // no range, or an empty one that left no partial
                             const int64_t pi = int64_t(c) * p.total_q * p.Hq + pi0;
                             const float mc = __ldcg(p.pre_ml + pi * 2);
                             const float Mn = fmaxf(M, mc);
@@ -1045,9 +1047,11 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
                             (int64_t(h.q0) + j) * p.Hq + int64_t(kvh) * p.G + (row - j * p.G);
                         const int P = h.b;  // the member's first own block = prefix blocks
                         float M = -INFINITY, L = 0.f;
-                        for (int c = 0; c < p.pre_chunks; ++c) {
-                            if ((c + 1) * P / p.pre_chunks == c * P / p.pre_chunks)
-                                continue;  // an empty block range left no partial
+#pragma unroll
+                        for (int c = 0; c < kMaxPreChunks; ++c) {
+                            if (c >= p.pre_chunks ||
+                                (c + 1) * P / p.pre_chunks == c * P / p.pre_chunks)
+                                continue;  // no range, or an empty one that left no partial
                             const int64_t pi = int64_t(c) * p.total_q * p.Hq + pi0;
                             const float mc = __ldcg(p.pre_ml + pi * 2);
                             const float Mn = fmaxf(M, mc);
