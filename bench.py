@@ -46,16 +46,16 @@ FALLBACK_HBM_GBS = 6800.0
 # to `source_sha256` (otherwise the bench reports traffic = null).
 NCU_TRAFFIC = {
     "llama3_8b_decode": {
-        "bytes": 582062848 + 3938816,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "86a53119b0c4574365ee513bc59f10a07299a010129b16cbccf840c00a630e03",
+        "bytes": 582051584 + 3831552,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "31193e65d38080a22e876b5468f8508545e042553e7364ffe505bb43574fa731",
     },
     "spec_verify": {
-        "bytes": 1417735000 + 5209344,
-        "source_sha256": "86a53119b0c4574365ee513bc59f10a07299a010129b16cbccf840c00a630e03",
+        "bytes": 1417737000 + 5473280,
+        "source_sha256": "31193e65d38080a22e876b5468f8508545e042553e7364ffe505bb43574fa731",
     },
     "llama3_8b_decode/fp8": {
-        "bytes": 291328512 + 3662848,
-        "source_sha256": "86a53119b0c4574365ee513bc59f10a07299a010129b16cbccf840c00a630e03",
+        "bytes": 291324928 + 3497728,
+        "source_sha256": "31193e65d38080a22e876b5468f8508545e042553e7364ffe505bb43574fa731",
     },
 }
 
