@@ -415,11 +415,23 @@ const char *pkv_status_string(int32_t status);
  *                        tickets to the CTAs that finish their static share
  *                        first. Ticket boundaries depend on the sizes only, so
  *                        results stay deterministic.
+ *   PKV_OPT_PACE         pacing of the attention kernel's static chunks: a CTA
+ *                        whose share of its chunk runs ahead of the grid's share
+ *                        of all work (one progress counter in the workspace
+ *                        header) sleeps this many ns before each refill of a
+ *                        stage, so the SMs that stream slower get more of the
+ *                        memory system and the chunks end closer together.
+ *                        0 = auto (default: 300 ns for bf16 pools with at most
+ *                        8 query rows per kv head, off otherwise), 1 = off,
+ *                        2..100000 = that many ns for every shape. Timing only:
+ *                        results are bit-identical with pacing on or off.
+ *   PKV_OPT_PACE_MARGIN  the lead allowed before pacing, in 1/10000 of the
+ *                        work; 0..10000, default 0.
  * All settings give the same result up to fp32 rounding order.
  * Returns the previous value, or -1 for an unknown option or an invalid value.
  */
 enum { PKV_OPT_NUM_CTAS = 1, PKV_OPT_STAGES = 2, PKV_OPT_HEADS_PER_CTA = 3, PKV_OPT_TMA_BOX = 4,
-       PKV_OPT_TAIL = 5 };
+       PKV_OPT_TAIL = 5, PKV_OPT_PACE = 6, PKV_OPT_PACE_MARGIN = 7 };
 int32_t pkv_set_option(int32_t option, int32_t value);
 
 /*

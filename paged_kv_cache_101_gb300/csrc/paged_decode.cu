@@ -227,6 +227,14 @@ __device__ __forceinline__ Smem carve(uint8_t *raw, const DecodeParams &p)
     return s;
 }
 
+// A gpu-scope relaxed load (the L2 copy of a counter other CTAs update).
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *ptr)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
 // ------------------------------------------------------------------ producer
 template <int D, bool KV8>
 __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
@@ -275,7 +283,7 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
     // given header; waits for the stage to be free first. False if that wait
     // gave up.
     auto issue = [&](int phys, int q0, int ql, int W, int b, int T, int hg, int flags, int cellv,
-                     int slot) -> bool {
+                     int slot, int sleep_ns) -> bool {
         if (issued >= uint32_t(p.nst)) {
             int w_ok = 1;
             if (lane == 0)
@@ -284,6 +292,12 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
                 return false;
         }
         if (lane == 0) {
+            if (sleep_ns > 0) {
+                // paced: the refill waits a little (the slot is free already)
+                __nanosleep(uint32_t(sleep_ns));
+                if (p.trace)
+                    p.trace[blockIdx.x * kTraceWords + 8] += 1;
+            }
             StageHdr *h = &sm.hdr[st];
             h->q0 = q0;
             h->b = b;
@@ -372,11 +386,24 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
             const int phys = checked(__shfl_sync(FULLMASK, bt_val, b - bt_base));
             const int flags =
                 F_PREFIX | (b == b_lo ? F_FIRST : 0) | (b == b_hi - 1 ? F_LAST : 0);
-            ok = issue(phys, q0, ql, 0, b, P * kBlockSize, head, flags, c, 0);
+            ok = issue(phys, q0, ql, 0, b, P * kBlockSize, head, flags, c, 0, 0);
         }
     }
+    // Pacing of the static chunks: per-SM streaming rates differ by several
+    // percent, so equal chunks would end at different times. Every 4 units the
+    // producer compares its chunk's progress with the grid's (units issued by
+    // all CTAs, one counter in the workspace, read one round ahead so the load
+    // never stalls the warp) and, while ahead by more than a margin, sleeps
+    // briefly before each refill: the SMs behind get more of the memory system.
+    // Timing only: the partition, and so every result bit, is unchanged.
+    uint32_t g_rd = 0;  // lane 0: the grid's units issued, as last read
+    int64_t k_rd = 0;   // lane 0: this chunk's units issued at that read
+    bool ahead = false;
     for (; !p.prefix_pass;) {
         const int64_t a = C.start(cell), e = C.start(cell + 1);
+        const bool pace = p.pace_ns > 0 && cell < C.G;
+        const float inv_n = a < e ? 1.f / float(e - a) : 0.f, inv_f = 1.f / float(C.F);
+        ahead = false;
         // locate unit f: head group, sequence and block within it
         auto locate = [&](int64_t f, int &hg_o, int &s_o, int &b_o) {
             hg_o = int(f / nb_total);
@@ -435,11 +462,19 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
                 // a whole sequence in one cell is finished in place
                 if (last && seg_b0 == si.b0 && b == b_end - 1)
                     flags |= F_DIRECT;
+                if (pace && lane == 0 && ((u - a) & 3) == 0) {
+                    if (u > a)  // the read issued 4 units ago
+                        ahead = float(k_rd) * inv_n > float(g_rd) * inv_f + p.pace_margin;
+                    g_rd = ld_relaxed_gpu(p.ws + kWsProgress);
+                    k_rd = u - a;
+                }
                 if (!issue(phys, si.q0, si.ql, si.W, b, si.T, hg, flags, int(cell),
-                           cell_first ? 0 : 1)) {
+                           cell_first ? 0 : 1, ahead ? p.pace_ns : 0)) {
                     ok = false;
                     break;
                 }
+                if (pace && lane == 0)
+                    atomicAdd(p.ws + kWsProgress, 1u);  // result unused: a reduction
                 if (last)
                     cell_first = false;
                 // advance to the next unit
@@ -490,9 +525,12 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
         }
     }
     if (lane == 0) {
-        // the last CTA to finish claiming resets the ticket counters for the next call
+        // the last CTA to finish claiming resets the ticket and progress counters
+        // for the next call (the fence orders this CTA's progress updates first)
+        __threadfence();
         if (atomicAdd(p.ws + kWsDone, 1u) == gridDim.x - 1) {
             atomicExch(p.ws + kWsTicket, 0u);
+            atomicExch(p.ws + kWsProgress, 0u);
             atomicExch(p.ws + kWsDone, 0u);
         }
     }

@@ -17,7 +17,7 @@ constexpr int kThreadsMax = 32 * (1 + kMaxConsumerWarps);
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded waits: 2 s
 // per-CTA trace words: entry, first TMA issued, first stage consumed, last TMA
 // issued, last stage consumed (ns, %globaltimer), units, segments, SM id,
-// 8 spare
+// paced stages, 7 spare
 constexpr int kTraceWords = 16;
 constexpr int kMaxPreChunks = 4;  // cascade: prefix partials per row
 
@@ -56,13 +56,13 @@ struct DecodePlan {
 };
 
 // Workspace header words (uint32 at byte offset 4*i).
-enum { kWsErr = 0, kWsTicket = 2, kWsDone = 3, kWsHeaderBytes = 256 };
+enum { kWsErr = 0, kWsTicket = 2, kWsDone = 3, kWsProgress = 4, kWsHeaderBytes = 256 };
 struct DecodeParams {
     const uint16_t *q;
     void *out;
     const int32_t *block_tables;
     const int32_t *context_lens;
-    uint32_t *ws;          // workspace header: error word, ticket and done counters
+    uint32_t *ws;          // workspace header: error word, ticket, done and progress counters
     int32_t *seq_start;    // [S + 1] block prefix sums (written by CTA 0 for the merge)
     float *ml;             // [cells][2][HG][rows] (m, l) partial states
     float *part;           // [cells][2][HG][rows][D] unnormalised partial acc
@@ -76,6 +76,8 @@ struct DecodeParams {
     int ticket_div;        // the last F / ticket_div units go to tickets
     int ticket_units;      // at least this many units per ticket
     float scale_log2;      // scale * log2(e)
+    int pace_ns;           // pacing: sleep per refill while ahead of the grid (0: off)
+    float pace_margin;     // pacing: lead (fraction of the work) allowed before sleeping
     const float *k_scale;  // E4M3 pools: [Hkv] dequantisation scales (null for bf16)
     const float *v_scale;
     // variable query counts (all null for a fixed n_query_per_seq = nq, causal):
