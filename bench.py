@@ -149,6 +149,10 @@ def run_pkv(args, rank, world, dist):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
 
     fp8 = args.kv_dtype == "fp8"
+    fma = args.math == "fma"
+    if fma and (fp8 or cascade):
+        raise SystemExit("--math fma runs the plain bf16 call only")
+    pkv.set_option(pkv.PKV_OPT_MATH, 1 if fma else 0)
     q = up(w.q)
     if fp8:
         k8, v8, ks_h, vs_h = W.fp8_pools(w)
@@ -287,7 +291,8 @@ def run_pkv(args, rank, world, dist):
     peak, peak_kind = measured_peaks()
     achieved = attn_bytes / (kern_mean * 1e-3) / 1e9
     traffic = None
-    nt = NCU_TRAFFIC.get(args.workload + ("/fp8" if fp8 else "") + ("/cascade" if cascade else ""))
+    nt = NCU_TRAFFIC.get(args.workload + ("/fp8" if fp8 else "") + ("/cascade" if cascade else "") +
+                         ("/fma" if fma else ""))
     if nt and nt.get("source_sha256") == kernel_source_sha():
         traffic = nt["bytes"]
     value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
@@ -309,8 +314,9 @@ def run_pkv(args, rank, world, dist):
                 "pools in HBM; inputs > L2 and a 512 MiB L2 flush between timed steps)",
         "config": {
             "workload": args.workload + (" (fp8 KV cache)" if fp8 else "") +
-                        (" (shared-prefix cascade)" if cascade else ""),
-            "kv_dtype": args.kv_dtype,
+                        (" (shared-prefix cascade)" if cascade else "") +
+                        (" (CUDA-core FMA consumers)" if fma else ""),
+            "kv_dtype": args.kv_dtype, "math": args.math,
             "num_seqs": w.num_seqs, "n_query_per_seq": w.n_query_per_seq,
             "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
             "head_dim": w.head_dim, "block_size": 16,
@@ -324,7 +330,8 @@ def run_pkv(args, rank, world, dist):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "paged_decode_kernel" + (" (prefix pass + main pass)" if cascade else ""),
+            "kernel": ("paged_decode_fma_kernel" if fma else "paged_decode_kernel") +
+                      (" (prefix pass + main pass)" if cascade else ""),
             "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs (burst)",
             "traffic": traffic, "kernel_us": round(kern_mean * 1e3, 3),
@@ -817,6 +824,9 @@ def main():
                          "moved to the front of the batch)")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
                     help="KV pool element type (fp8 = E4M3 codes with per-head scales)")
+    ap.add_argument("--math", default="tensor", choices=["tensor", "fma"],
+                    help="attention consumers: tensor cores (default) or the CUDA-core FMA "
+                         "reference path (bf16 pools, plain call)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

@@ -28,6 +28,7 @@ int32_t g_opt_heads = 0;
 int32_t g_opt_box = 0;
 int32_t g_opt_tail = 0;
 int32_t g_opt_pace = 0;
+int32_t g_opt_math = 0;
 int32_t g_opt_pace_margin = 0;
 // Pacing by default: 300 ns per refill while a CTA leads, for the shapes that
 // stream at the memory system's pace (bf16 pools, up to 8 query rows per kv
@@ -236,7 +237,7 @@ size_t workspace_zero_prefix(int32_t num_seqs, int32_t n_query_per_seq, int32_t 
         return 0;
     DecodePlan pl;
     if (plan_decode(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim, 1, d.num_sms,
-                    g_opt_num_ctas, g_opt_stages, g_opt_heads, g_opt_tail, d.smem_optin, 0,
+                    g_opt_num_ctas, g_opt_stages, g_opt_heads, g_opt_tail, d.smem_optin, 0, 0,
                     &pl) != 0)
         return 0;
     return kWsHeaderBytes;
@@ -316,6 +317,12 @@ int32_t pkv_set_option(int32_t option, int32_t value)
         prev = g_opt_pace;
         g_opt_pace = value;
         return prev;
+    case PKV_OPT_MATH:
+        if (value > 1)
+            return -1;
+        prev = g_opt_math;
+        g_opt_math = value;
+        return prev;
     case PKV_OPT_PACE_MARGIN:
         if (value > 10000)
             return -1;
@@ -388,7 +395,7 @@ size_t pkv_workspace_size(int32_t num_seqs, int32_t n_query_per_seq, int32_t num
     pkv::DecodePlan pl;
     if (pkv::plan_decode(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim, 1,
                          d.num_sms, g_opt_num_ctas, g_opt_stages, g_opt_heads, g_opt_tail, d.smem_optin,
-                         0, &pl) != 0)
+                         0, 0, &pl) != 0)
         return 0;
     return pl.ws_bytes;
 }
@@ -462,10 +469,12 @@ pkv_status attention(const void *q, const void *k_cache, const void *v_cache, in
     DeviceInfo d;
     if (device_info(&d) != cudaSuccess)
         return PKV_ERR_CUDA;
+    // the CUDA-core consumers (PKV_OPT_MATH = 1) serve the plain bf16 call only
+    const int fma = (g_opt_math == 1 && !kv8 && !vl.q_start && !cc.groups && head_dim == 128) ? 1 : 0;
     pkv::DecodePlan pl;
     if (pkv::plan_decode(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim,
                          max_blocks_per_seq, d.num_sms, g_opt_num_ctas, g_opt_stages,
-                         g_opt_heads, g_opt_tail, d.smem_optin, kv8, &pl) != 0)
+                         g_opt_heads, g_opt_tail, d.smem_optin, kv8, fma, &pl) != 0)
         return PKV_ERR_UNSUPPORTED;
     // cascade: the prefix pass's plan and the prefix partials after the workspace
     pkv::DecodePlan ppl{};

@@ -1516,6 +1516,330 @@ __global__ void __launch_bounds__(kThreadsMax, 1)
     }
 }
 
+// ------------------------------------------------------------------ CUDA-core consumer
+// The same pipeline with the math on the CUDA cores (fp32 FMA): the reference
+// point against which the tensor-core consumers were chosen. A warp owns RW
+// query rows of one kv head (D = 128, bf16 pools, causal rows).
+//  * Scores: lane (t, h) = (token, 64-dim half) dots its half of K row t with
+//    the same half of every row's query (the queries sit in shared memory as
+//    fp32 and are read as broadcasts); one shuffle joins the two halves.
+//  * Online softmax per row with shuffle reductions over the 16 token lanes
+//    (running max m, per-lane partial sums l, a lazily rescaled accumulator).
+//  * P goes to shared memory token-major; lane i owns dims 4i..4i+3 and adds
+//    P[t][r] * V[t][d] over the block's tokens (P read as broadcasts).
+constexpr int kFmaHalfStride = 68;                // floats: 64 + 4 pad (no bank conflict)
+constexpr int kFmaRowStride = 2 * kFmaHalfStride; // floats per staged query row
+
+__host__ __device__ constexpr int fma_warp_bytes(int rw)
+{
+    return rw * kFmaRowStride * 4 + 16 * rw * 4;  // query rows + P[16][rw]
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+
+template <int RW>
+__device__ void consumer_warp_fma(const DecodeParams &p, const Smem &sm, int cw, int lane,
+                                  float *qs, float *ps)
+{
+    constexpr int D = 128, NH = 2;
+    const unsigned FULL = 0xffffffffu;
+    const int wph = p.ncw / p.HG;
+    const int hl = cw / wph;              // kv head within the group
+    const int r0 = (cw % wph) * RW;       // first row of this warp
+    const int t = lane & 15, h = lane >> 4;  // score lanes: token, 64-dim half
+    // PV lanes: dims 4*lane..+3 = half hv, 16-byte chunk cv, 8-byte sub-offset
+    const int hv = lane >> 4, cv = (lane & 15) >> 1, sub = (lane & 1) * 8;
+
+    float acc[RW][4], m_r[RW], l_r[RW];
+    auto reset_state = [&]() {
+#pragma unroll
+        for (int r = 0; r < RW; ++r) {
+            m_r[r] = -INFINITY;
+            l_r[r] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                acc[r][e] = 0.f;
+        }
+    };
+    auto unpack = [](uint32_t x, float &lo, float &hi) {
+        lo = __uint_as_float(x << 16);
+        hi = __uint_as_float(x & 0xffff0000u);
+    };
+
+    const uint32_t stage_base = smem_u32(sm.stages);
+    uint32_t st = 0, phase = 0;
+    for (;;) {
+        if (!mbar_wait(smem_u32(&sm.full[st]), phase, kWaitLimitNs)) {
+            if (lane == 0)
+                atomicOr(p.ws + kWsErr, kErrConsumerWait);
+            return;
+        }
+        const StageHdr hd = sm.hdr[st];
+        if (p.trace && cw == 0 && lane == 0) {
+            uint64_t *tr = p.trace + blockIdx.x * kTraceWords;
+            if (hd.flags & F_END)
+                tr[4] = global_timer_ns();
+            else if (tr[2] == 0)
+                tr[2] = global_timer_ns();
+            if (hd.flags & F_FIRST)
+                tr[6] += 1;
+        }
+        if (hd.flags & F_END)
+            break;
+        const int kvh = hd.hg * p.HG + hl;
+        const int vrows = p.G * hd.ql;  // valid rows of this kv head
+
+        if (hd.flags & F_FIRST) {
+            // a new segment: fresh state; this warp's query rows into shared memory
+            reset_state();
+            __syncwarp();  // the previous segment's reads of qs are done
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                const int row = r0 + r;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (row < vrows) {
+                    const int j = row / p.G, gq = row - j * p.G;
+                    const uint2 w = __ldg(reinterpret_cast<const uint2 *>(
+                        p.q + ((int64_t(hd.q0) + j) * p.Hq + int64_t(kvh) * p.G + gq) * D +
+                        4 * lane));
+                    unpack(w.x, v.x, v.y);
+                    unpack(w.y, v.z, v.w);
+                }
+                *reinterpret_cast<float4 *>(qs + r * kFmaRowStride + hv * kFmaHalfStride +
+                                            4 * (lane & 15)) = v;
+            }
+            __syncwarp();
+        }
+
+        const uint32_t kb =
+            stage_base + st * uint32_t(p.stage_bytes) + uint32_t(hl * NH * kTileBytes);
+        const uint32_t vb = kb + uint32_t(p.HG * NH * kTileBytes);
+
+        // ---- scores: lane (t, h) over dims 64h .. 64h + 63, 8 at a time
+        float s[RW];
+#pragma unroll
+        for (int r = 0; r < RW; ++r)
+            s[r] = 0.f;
+        const uint32_t krow = kb + uint32_t(h * kTileBytes + t * 128);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint4 kw = lds128(krow + uint32_t((c ^ (t & 7)) << 4));
+            float kf[8];
+            unpack(kw.x, kf[0], kf[1]);
+            unpack(kw.y, kf[2], kf[3]);
+            unpack(kw.z, kf[4], kf[5]);
+            unpack(kw.w, kf[6], kf[7]);
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                const float4 *qv =
+                    reinterpret_cast<const float4 *>(qs + r * kFmaRowStride + h * kFmaHalfStride + 8 * c);
+                const float4 a = qv[0], b = qv[1];
+                float x = s[r];
+                x = fmaf(a.x, kf[0], x);
+                x = fmaf(a.y, kf[1], x);
+                x = fmaf(a.z, kf[2], x);
+                x = fmaf(a.w, kf[3], x);
+                x = fmaf(b.x, kf[4], x);
+                x = fmaf(b.y, kf[5], x);
+                x = fmaf(b.z, kf[6], x);
+                x = fmaf(b.w, kf[7], x);
+                s[r] = x;
+            }
+        }
+        const int t0 = hd.b * kBlockSize;
+#pragma unroll
+        for (int r = 0; r < RW; ++r) {
+            s[r] += __shfl_xor_sync(FULL, s[r], 16);
+            s[r] *= p.scale_log2;
+        }
+        if (__builtin_expect(t0 + kBlockSize - 1 >= hd.T - hd.ql + 1, 0)) {
+            // a sequence's last block(s): causal limit per row (padding rows take
+            // the last query's), which also masks tokens past the context
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                int j = (r0 + r) / p.G;
+                j = j < hd.ql ? j : hd.ql - 1;
+                if (t0 + t > hd.T - hd.ql + j)
+                    s[r] = -INFINITY;
+            }
+        }
+
+        // ---- online softmax: block max over the 16 token lanes of each half
+        //      (both halves hold the same scores), rescale only when it grew
+        bool grew = false;
+        float corr[RW];
+#pragma unroll
+        for (int r = 0; r < RW; ++r) {
+            float bm = s[r];
+            bm = fmaxf(bm, __shfl_xor_sync(FULL, bm, 1));
+            bm = fmaxf(bm, __shfl_xor_sync(FULL, bm, 2));
+            bm = fmaxf(bm, __shfl_xor_sync(FULL, bm, 4));
+            bm = fmaxf(bm, __shfl_xor_sync(FULL, bm, 8));
+            const float mn = fmaxf(m_r[r], bm);
+            grew |= mn > m_r[r];
+            const float mu = mn == -INFINITY ? 0.f : mn;
+            corr[r] = ex2(m_r[r] - mu);  // 1 when the max did not grow, 0 from -inf
+            m_r[r] = mn;
+            const float pr = ex2(s[r] - mu);  // 0 for a masked token
+            l_r[r] = l_r[r] * corr[r] + pr;
+            s[r] = pr;
+        }
+        if (__any_sync(FULL, grew)) {
+#pragma unroll
+            for (int r = 0; r < RW; ++r)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    acc[r][e] *= corr[r];
+        }
+
+        // ---- P to shared memory, token-major
+        __syncwarp();  // the previous block's reads of ps are done
+        if (h == 0) {
+#pragma unroll
+            for (int r4 = 0; r4 < RW / 4; ++r4)
+                *reinterpret_cast<float4 *>(ps + t * RW + 4 * r4) =
+                    make_float4(s[4 * r4], s[4 * r4 + 1], s[4 * r4 + 2], s[4 * r4 + 3]);
+        }
+        __syncwarp();
+
+        // ---- O[r][4 lane .. +3] += P[t][r] * V[t][..]; slots past the context
+        //      (stale or NaN) are zeroed in the last block
+        const int vc = hd.T - t0;
+        const uint32_t vrow = vb + uint32_t(hv * kTileBytes + sub);
+        auto pv = [&](auto masked) {
+            constexpr bool MASKED = decltype(masked)::value;
+#pragma unroll
+            for (int tt = 0; tt < kBlockSize; ++tt) {
+                const uint2 vw = lds64(vrow + uint32_t(tt * 128 + ((cv ^ (tt & 7)) << 4)));
+                float v[4];
+                unpack(vw.x, v[0], v[1]);
+                unpack(vw.y, v[2], v[3]);
+                if constexpr (MASKED) {
+                    if (tt >= vc)
+                        v[0] = v[1] = v[2] = v[3] = 0.f;
+                }
+#pragma unroll
+                for (int r4 = 0; r4 < RW / 4; ++r4) {
+                    const float4 pr = *reinterpret_cast<const float4 *>(ps + tt * RW + 4 * r4);
+                    const float pp[4] = {pr.x, pr.y, pr.z, pr.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            acc[4 * r4 + i][e] = fmaf(pp[i], v[e], acc[4 * r4 + i][e]);
+                }
+            }
+        };
+        if (__builtin_expect(vc < kBlockSize, 0))
+            pv(std::true_type());
+        else
+            pv(std::false_type());
+
+        // epilogue fields, then the stage goes back to the producer
+        int e_q0 = 0, e_cell = 0, e_slot = 0;
+        if (hd.flags & F_LAST) {
+            const StageHdr *hp = &sm.hdr[st];
+            e_q0 = hp->q0;
+            e_cell = hp->cell;
+            e_slot = hp->slot;
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_u32(&sm.empty[st]));
+        if (++st == uint32_t(p.nst)) {
+            st = 0;
+            phase ^= 1u;
+        }
+
+        if (hd.flags & F_LAST) {
+            // full row sums over the 16 token lanes, then output or partial
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                float v = l_r[r];
+                v += __shfl_xor_sync(FULL, v, 1);
+                v += __shfl_xor_sync(FULL, v, 2);
+                v += __shfl_xor_sync(FULL, v, 4);
+                v += __shfl_xor_sync(FULL, v, 8);
+                const int row = r0 + r;
+                if (row >= vrows)
+                    continue;
+                if (hd.flags & F_DIRECT) {
+                    const int j = row / p.G, gq = row - j * p.G;
+                    const int64_t o =
+                        ((int64_t(e_q0) + j) * p.Hq + int64_t(kvh) * p.G + gq) * D + 4 * lane;
+                    const float inv = v > 0.f ? 1.f / v : 0.f;
+                    if (p.out_f32) {
+                        *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + o) = make_float4(
+                            acc[r][0] * inv, acc[r][1] * inv, acc[r][2] * inv, acc[r][3] * inv);
+                    } else {
+                        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[r][0] * inv, acc[r][1] * inv);
+                        const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[r][2] * inv, acc[r][3] * inv);
+                        uint2 w;
+                        w.x = *reinterpret_cast<const uint32_t *>(&lo);
+                        w.y = *reinterpret_cast<const uint32_t *>(&hi);
+                        *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.out) + o) = w;
+                    }
+                } else {
+                    // partial (m, l, acc) of this cell for the merge kernel
+                    const int64_t pidx =
+                        ((int64_t(e_cell) * 2 + e_slot) * p.HG + hl) * p.rows + row;
+                    *reinterpret_cast<float4 *>(p.part + pidx * D + 4 * lane) =
+                        make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+                    if (lane == 0) {
+                        p.ml[pidx * 2] = m_r[r];
+                        p.ml[pidx * 2 + 1] = v;
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <int RW>
+__global__ void __launch_bounds__(kThreadsMax, 1)
+    paged_decode_fma_kernel(const __grid_constant__ CUtensorMap kmap,
+                            const __grid_constant__ CUtensorMap vmap, const DecodeParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const Smem sm = carve(smem_raw, p);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+        for (int i = 0; i < p.nst; ++i) {
+            mbar_init(smem_u32(&sm.full[i]), 1);
+            mbar_init(smem_u32(&sm.empty[i]), uint32_t(p.ncw));
+        }
+        fence_mbar_init();
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    __syncthreads();
+    if (warp == 0) {
+        producer_warp<128, false>(&kmap, &vmap, p, sm, lane);
+    } else {
+        // per-warp query rows and P after the cells record (16-byte aligned)
+        uint8_t *extra = reinterpret_cast<uint8_t *>(
+            (reinterpret_cast<uintptr_t>(sm.cells + 1) + 15) & ~uintptr_t(15));
+        float *qs = reinterpret_cast<float *>(extra + size_t(warp - 1) * fma_warp_bytes(RW));
+        float *ps = qs + RW * kFmaRowStride;
+        consumer_warp_fma<RW>(p, sm, warp - 1, lane, qs, ps);
+    }
+}
+
 // ------------------------------------------------------------------ merge
 // Combine the partials of every sequence that cell boundaries split:
 // M = max m_k, L = sum l_k 2^(m_k - M), out = sum acc_k 2^(m_k - M) / L
@@ -1647,29 +1971,40 @@ __global__ void __launch_bounds__(256)
 static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int opt_ctas,
-                int opt_stages, int opt_heads, int opt_tail, int smem_optin, int kv8,
+                int opt_stages, int opt_heads, int opt_tail, int smem_optin, int kv8, int fma,
                 DecodePlan *pl)
 {
     if (S < 1 || nq < 1 || Hkv < 1 || Hq % Hkv != 0 || (D != 64 && D != 128) || MB < 1)
         return -1;
     if (kv8 && D != 128)
         return -1;  // E4M3 rows are one 128-byte swizzle row
+    if (fma && (kv8 || D != 128))
+        return -1;  // the CUDA-core consumer: bf16 pools, head_dim 128
     DecodePlan P{};
     P.D = D;
     P.kv8 = kv8 ? 1 : 0;
+    P.fma = fma ? 1 : 0;
     P.G = Hq / Hkv;
     P.rows = P.G * nq;
     if (P.rows > kMaxRows)
         return -1;
-    const int nt_total = (P.rows + 7) / 8;
-    if (nt_total <= 2) {
-        P.wph = 1;
-        P.ntw = nt_total;
+    if (P.fma) {
+        // 4 or 8 rows per warp (fp32 registers: RW x 4 accumulators a lane)
+        P.rw = P.rows <= 4 ? 4 : 8;
+        P.wph = (P.rows + P.rw - 1) / P.rw;
+        P.ntw = 0;
+        P.rows_pad = P.wph * P.rw;
     } else {
-        P.wph = 2;
-        P.ntw = 2;
+        const int nt_total = (P.rows + 7) / 8;
+        if (nt_total <= 2) {
+            P.wph = 1;
+            P.ntw = nt_total;
+        } else {
+            P.wph = 2;
+            P.ntw = 2;
+        }
+        P.rows_pad = P.wph * P.ntw * 8;
     }
-    P.rows_pad = P.wph * P.ntw * 8;
     int max_hg = kMaxConsumerWarps / P.wph;
     if (opt_heads > 0 && opt_heads < max_hg)
         max_hg = opt_heads;
@@ -1683,7 +2018,9 @@ int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int 
     P.threads = 32 * (1 + P.HG * P.wph);
     P.stage_bytes = 2 * P.HG * (P.kv8 ? 1 : D / 64) * kTileBytes;
     const int per_stage = P.stage_bytes + int(sizeof(StageHdr)) + 16;
-    const int fixed = 1024 + int(sizeof(Cells)) + 64;
+    int fixed = 1024 + int(sizeof(Cells)) + 64;
+    if (P.fma)  // per consumer warp: its query rows and P in fp32
+        fixed += 16 + P.HG * P.wph * fma_warp_bytes(P.rw);
     int max_st = (smem_optin - fixed) / per_stage;
     if (max_st > 8)
         max_st = 8;
@@ -1748,13 +2085,14 @@ int plan_prefix(int D, int G, int Hkv, int num_groups, int max_group_seqs, int n
     return int(tiles);
 }
 
-template <int D, int NTW, int WPH, bool KV8>
-static cudaError_t launch_one(const DecodePlan &pl, const DecodeParams &p, const CUtensorMap &kmap,
-                              const CUtensorMap &vmap, cudaStream_t stream, cudaEvent_t ev_before,
-                              cudaEvent_t ev_after, bool with_merge = true)
+// Launch one attention kernel (and, unless told not to, its merge) on `stream`;
+// `configured_smem` is the kernel's own record of the shared memory it may use.
+template <typename Kern>
+static cudaError_t launch_kernel(Kern kern, int *configured_smem, const DecodePlan &pl,
+                                 const DecodeParams &p, const CUtensorMap &kmap,
+                                 const CUtensorMap &vmap, cudaStream_t stream,
+                                 cudaEvent_t ev_before, cudaEvent_t ev_after, bool with_merge)
 {
-    auto kern = paged_decode_kernel<D, NTW, WPH, KV8>;
-    static int configured_smem[64] = {0};  // per device ordinal
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
@@ -1797,10 +2135,33 @@ static cudaError_t launch_one(const DecodePlan &pl, const DecodeParams &p, const
     mcfg.stream = stream;
     mcfg.attrs = attr;
     mcfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&mcfg, paged_decode_merge_kernel<D>, p, int(pl.grid));
+    if (pl.D == 64)
+        e = cudaLaunchKernelEx(&mcfg, paged_decode_merge_kernel<64>, p, int(pl.grid));
+    else
+        e = cudaLaunchKernelEx(&mcfg, paged_decode_merge_kernel<128>, p, int(pl.grid));
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
+}
+
+template <int D, int NTW, int WPH, bool KV8>
+static cudaError_t launch_one(const DecodePlan &pl, const DecodeParams &p, const CUtensorMap &kmap,
+                              const CUtensorMap &vmap, cudaStream_t stream, cudaEvent_t ev_before,
+                              cudaEvent_t ev_after, bool with_merge = true)
+{
+    static int configured_smem[64] = {0};  // per device ordinal
+    return launch_kernel(paged_decode_kernel<D, NTW, WPH, KV8>, configured_smem, pl, p, kmap, vmap,
+                         stream, ev_before, ev_after, with_merge);
+}
+
+template <int RW>
+static cudaError_t launch_fma(const DecodePlan &pl, const DecodeParams &p, const CUtensorMap &kmap,
+                              const CUtensorMap &vmap, cudaStream_t stream, cudaEvent_t ev_before,
+                              cudaEvent_t ev_after)
+{
+    static int configured_smem[64] = {0};  // per device ordinal
+    return launch_kernel(paged_decode_fma_kernel<RW>, configured_smem, pl, p, kmap, vmap, stream,
+                         ev_before, ev_after, true);
 }
 
 cudaError_t launch_decode(const DecodePlan &pl, const DecodeParams &p, const CUtensorMap &kmap,
@@ -1811,6 +2172,11 @@ cudaError_t launch_decode(const DecodePlan &pl, const DecodeParams &p, const CUt
         if (pl.D == 64)
             return launch_one<64, 2, 8, false>(pl, p, kmap, vmap, stream, eb, ea, false);
         return launch_one<128, 2, 8, false>(pl, p, kmap, vmap, stream, eb, ea, false);
+    }
+    if (pl.fma) {  // CUDA-core consumers: bf16, D = 128
+        if (pl.rw == 4)
+            return launch_fma<4>(pl, p, kmap, vmap, stream, eb, ea);
+        return launch_fma<8>(pl, p, kmap, vmap, stream, eb, ea);
     }
     if (pl.kv8) {  // E4M3 pools: D = 128 only
         if (pl.wph == 2)

@@ -37,7 +37,7 @@ struct DecodePlan {
     int G;           // query heads per kv head
     int rows;        // G * nq: query rows per kv head
     int wph;         // consumer warps per kv head (1 or 2)
-    int ntw;         // 8-row n-tiles per consumer warp
+    int ntw;         // 8-row n-tiles per consumer warp (0: CUDA-core consumers)
     int rows_pad;    // wph * ntw * 8
     int HG;          // kv heads per head group (one CTA streams one group)
     int n_hg;        // Hkv / HG
@@ -46,6 +46,8 @@ struct DecodePlan {
     int nst;         // pipeline stages
     int whole_box;   // 1: one TMA box per block for K (and V) of all HG heads
     int kv8;         // 1: E4M3 pools (one 128-byte tile per head row), 0: bf16
+    int fma;         // 1: CUDA-core (fp32 FMA) consumers instead of tensor cores
+    int rw;          // CUDA-core consumers: query rows per warp (4 or 8)
     int prefix;      // 1: the cascade's prefix pass (one head per CTA, 8 warps x 16 rows)
     int grid;        // persistent CTAs
     int tickets_max; // cap on dynamically claimed tickets (0: static chunks only)
@@ -101,7 +103,7 @@ struct DecodeParams {
 };
 
 int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int opt_ctas,
-                int opt_stages, int opt_heads, int opt_tail, int smem_optin, int kv8,
+                int opt_stages, int opt_heads, int opt_tail, int smem_optin, int kv8, int fma,
                 DecodePlan *plan);
 
 // The cascade's prefix pass (one head per CTA, 128 score rows per tile); returns

@@ -69,6 +69,10 @@ def test_options(lib):
     assert pkv.set_option(pkv.PKV_OPT_PACE_MARGIN, 50) == 0
     assert pkv.set_option(pkv.PKV_OPT_PACE_MARGIN, 10001) == -1
     assert pkv.set_option(pkv.PKV_OPT_PACE_MARGIN, 0) == 50
+    # consumers: 0 = tensor cores, 1 = CUDA-core FMA
+    assert pkv.set_option(pkv.PKV_OPT_MATH, 1) == 0
+    assert pkv.set_option(pkv.PKV_OPT_MATH, 2) == -1
+    assert pkv.set_option(pkv.PKV_OPT_MATH, 0) == 1
 
 
 A = 0x10000  # a 64 KiB-aligned dummy address: never dereferenced on these paths
