@@ -153,6 +153,7 @@ def run_pkv(args, rank, world, dist):
     if fma and (fp8 or cascade):
         raise SystemExit("--math fma runs the plain bf16 call only")
     pkv.set_option(pkv.PKV_OPT_MATH, 1 if fma else 0)
+    pkv.set_option(pkv.PKV_OPT_PACE, 1 if args.pace else 0)
     q = up(w.q)
     if fp8:
         k8, v8, ks_h, vs_h = W.fp8_pools(w)
@@ -316,7 +317,7 @@ def run_pkv(args, rank, world, dist):
             "workload": args.workload + (" (fp8 KV cache)" if fp8 else "") +
                         (" (shared-prefix cascade)" if cascade else "") +
                         (" (CUDA-core FMA consumers)" if fma else ""),
-            "kv_dtype": args.kv_dtype, "math": args.math,
+            "kv_dtype": args.kv_dtype, "math": args.math, "pace": bool(args.pace),
             "num_seqs": w.num_seqs, "n_query_per_seq": w.n_query_per_seq,
             "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
             "head_dim": w.head_dim, "block_size": 16,
@@ -824,6 +825,8 @@ def main():
                          "moved to the front of the batch)")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
                     help="KV pool element type (fp8 = E4M3 codes with per-head scales)")
+    ap.add_argument("--pace", action="store_true",
+                    help="pace the attention kernel's chunks (PKV_OPT_PACE; off by default)")
     ap.add_argument("--math", default="tensor", choices=["tensor", "fma"],
                     help="attention consumers: tensor cores (default) or the CUDA-core FMA "
                          "reference path (bf16 pools, plain call)")

@@ -415,16 +415,16 @@ const char *pkv_status_string(int32_t status);
  *                        tickets to the CTAs that finish their static share
  *                        first. Ticket boundaries depend on the sizes only, so
  *                        results stay deterministic.
- *   PKV_OPT_PACE         pacing of the attention kernel's static chunks: a CTA
- *                        whose share of its chunk runs ahead of the grid's share
- *                        of all work (one progress counter in the workspace
- *                        header) sleeps this many ns before each refill of a
- *                        stage, so the SMs that stream slower get more of the
- *                        memory system and the chunks end closer together.
- *                        0 = auto (default: 300 ns for bf16 pools with at most
- *                        8 query rows per kv head, off otherwise), 1 = off,
- *                        2..100000 = that many ns for every shape. Timing only:
- *                        results are bit-identical with pacing on or off.
+ *   PKV_OPT_PACE         0 = off (default); 1 = pace the attention kernel's
+ *                        static chunks: a CTA whose share of its chunk runs
+ *                        ahead of the grid's share of all work (one progress
+ *                        counter in the workspace header) keeps one stage fewer
+ *                        in flight, so where HBM is saturated the SMs that
+ *                        stream slower get more of it and the chunks end closer
+ *                        together (1-2 % faster on HBM-bound batches; slower
+ *                        where L2 serves shared blocks or the math bounds the
+ *                        kernel). Timing only: results are bit-identical with
+ *                        pacing on or off.
  *   PKV_OPT_PACE_MARGIN  the lead allowed before pacing, in 1/10000 of the
  *                        work; 0..10000, default 0.
  *   PKV_OPT_MATH         0 = tensor cores (mma.sync, default); 1 = the same

@@ -30,11 +30,6 @@ int32_t g_opt_tail = 0;
 int32_t g_opt_pace = 0;
 int32_t g_opt_math = 0;
 int32_t g_opt_pace_margin = 0;
-// Pacing by default: 300 ns per refill while a CTA leads, for the shapes that
-// stream at the memory system's pace (bf16 pools, up to 8 query rows per kv
-// head). Where the consumers bound the kernel (E4M3 pools, 16-row warps) any
-// refill delay only adds to the time, so it is off there.
-constexpr int kDefaultPaceNs = 300;
 cudaEvent_t g_ev_before = nullptr;
 cudaEvent_t g_ev_after = nullptr;
 void *g_trace = nullptr;
@@ -312,7 +307,7 @@ int32_t pkv_set_option(int32_t option, int32_t value)
         g_opt_box = value;
         return prev;
     case PKV_OPT_PACE:
-        if (value > 100000)
+        if (value > 1)
             return -1;
         prev = g_opt_pace;
         g_opt_pace = value;
@@ -522,7 +517,7 @@ pkv_status attention(const void *q, const void *k_cache, const void *v_cache, in
     p.block_tables = block_tables;
     p.context_lens = context_lens;
     p.ws = reinterpret_cast<uint32_t *>(ws);
-    p.seq_start = reinterpret_cast<int32_t *>(ws + pl.off_seq);
+    p.pieces = reinterpret_cast<int2 *>(ws + pl.off_rec);
     p.ml = reinterpret_cast<float *>(ws + pl.off_ml);
     p.part = reinterpret_cast<float *>(ws + pl.off_part);
     p.trace = trace;
@@ -546,10 +541,7 @@ pkv_status attention(const void *q, const void *k_cache, const void *v_cache, in
     p.ticket_div = pl.tail_div;
     p.ticket_units = 4;
     p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
-    if (g_opt_pace == 0)
-        p.pace_ns = (!kv8 && pl.ntw == 1) ? kDefaultPaceNs : 0;
-    else
-        p.pace_ns = g_opt_pace == 1 ? 0 : g_opt_pace;
+    p.pace = g_opt_pace;
     p.pace_margin = float(g_opt_pace_margin) * 1e-4f;
     p.k_scale = k_scale;
     p.v_scale = v_scale;
@@ -602,7 +594,7 @@ pkv_status attention(const void *q, const void *k_cache, const void *v_cache, in
         pp.ncw = 8;
         pp.tickets_max = 0;
         pp.ticket_div = 0;
-        pp.pace_ns = 0;
+        pp.pace = 0;
         pp.trace = nullptr;
         cudaError_t e = pkv::launch_decode(ppl, pp, pk, pv, static_cast<cudaStream_t>(stream),
                                            ev_b, nullptr);

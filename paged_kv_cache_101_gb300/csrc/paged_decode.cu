@@ -259,20 +259,15 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
     }
     const int base = incl - local;
     const int nb_total = __shfl_sync(FULLMASK, incl, 31);
-    if (blockIdx.x == 0) {
-        // block prefix sums for the merge kernel
-        int run = base;
-        for (int s = s_lo; s < s_hi; ++s) {
-            p.seq_start[s] = run;
-            run += seq_blocks(p, s);
-        }
-        if (lane == 0)
-            p.seq_start[S] = nb_total;
-    }
 
     const Cells C = make_cells(p, nb_total, int(gridDim.x));
     if (lane == 0)
         *sm.cells = C;  // published to the consumers by the first stage's arrive
+    if (blockIdx.x == 0 && lane == 0 && !p.prefix_pass) {
+        // for the merge: the unit count, and whether every cell holds units
+        p.ws[kWsUnits] = uint32_t(nb_total);
+        p.ws[kWsDense] = (C.F1 >= C.G && (C.NT == 0 || C.F2 >= C.NT)) ? 1u : 0u;
+    }
 
     uint32_t st = 0, phase = 0;  // ring position of the next stage to fill
     uint32_t issued = 0;         // stages filled so far
@@ -283,21 +278,25 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
     // given header; waits for the stage to be free first. False if that wait
     // gave up.
     auto issue = [&](int phys, int q0, int ql, int W, int b, int T, int hg, int flags, int cellv,
-                     int slot, int sleep_ns) -> bool {
+                     int slot, bool shallow) -> bool {
         if (issued >= uint32_t(p.nst)) {
+            // the slot's previous fill must have been consumed; a paced CTA
+            // (`shallow`) waits for the fill after it instead, keeping one stage
+            // fewer in flight
+            uint32_t ws = st, wpar = phase ^ 1u;
+            if (shallow && ++ws == uint32_t(p.nst)) {
+                ws = 0;
+                wpar = phase;
+            }
             int w_ok = 1;
             if (lane == 0)
-                w_ok = mbar_wait(smem_u32(&sm.empty[st]), phase ^ 1u, kWaitLimitNs);
+                w_ok = mbar_wait(smem_u32(&sm.empty[ws]), wpar, kWaitLimitNs);
             if (!__shfl_sync(FULLMASK, w_ok, 0))
                 return false;
         }
         if (lane == 0) {
-            if (sleep_ns > 0) {
-                // paced: the refill waits a little (the slot is free already)
-                __nanosleep(uint32_t(sleep_ns));
-                if (p.trace)
-                    p.trace[blockIdx.x * kTraceWords + 8] += 1;
-            }
+            if (shallow && p.trace)
+                p.trace[blockIdx.x * kTraceWords + 8] += 1;
             StageHdr *h = &sm.hdr[st];
             h->q0 = q0;
             h->b = b;
@@ -386,22 +385,22 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
             const int phys = checked(__shfl_sync(FULLMASK, bt_val, b - bt_base));
             const int flags =
                 F_PREFIX | (b == b_lo ? F_FIRST : 0) | (b == b_hi - 1 ? F_LAST : 0);
-            ok = issue(phys, q0, ql, 0, b, P * kBlockSize, head, flags, c, 0, 0);
+            ok = issue(phys, q0, ql, 0, b, P * kBlockSize, head, flags, c, 0, false);
         }
     }
-    // Pacing of the static chunks: per-SM streaming rates differ by several
-    // percent, so equal chunks would end at different times. Every 4 units the
-    // producer compares its chunk's progress with the grid's (units issued by
-    // all CTAs, one counter in the workspace, read one round ahead so the load
-    // never stalls the warp) and, while ahead by more than a margin, sleeps
-    // briefly before each refill: the SMs behind get more of the memory system.
+    // Optional pacing of the static chunks: per-SM streaming rates differ by
+    // several percent, so equal chunks end at different times. Every 4 units the
+    // producer compares its chunk's progress with the grid's (units issued by all
+    // CTAs, one counter in the workspace, read one round ahead so the load never
+    // stalls the warp) and, while ahead by more than a margin, keeps one stage
+    // fewer in flight: where HBM is saturated, the SMs behind get more of it.
     // Timing only: the partition, and so every result bit, is unchanged.
     uint32_t g_rd = 0;  // lane 0: the grid's units issued, as last read
     int64_t k_rd = 0;   // lane 0: this chunk's units issued at that read
     bool ahead = false;
     for (; !p.prefix_pass;) {
         const int64_t a = C.start(cell), e = C.start(cell + 1);
-        const bool pace = p.pace_ns > 0 && cell < C.G;
+        const bool pace = p.pace != 0 && cell < C.G;
         const float inv_n = a < e ? 1.f / float(e - a) : 0.f, inv_f = 1.f / float(C.F);
         ahead = false;
         // locate unit f: head group, sequence and block within it
@@ -455,6 +454,15 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
                 if (first)
                     seg_b0 = b;
                 const bool last = (u == e - 1) || (b == b_end - 1);
+                if (lane == 0) {
+                    // the merge's record: cell (and slot) of the sequence's first
+                    // piece, cell of its last
+                    int2 *rec = p.pieces + int64_t(s) * p.n_hg + hg;
+                    if (b == si.b0)
+                        rec->x = int(cell) * 2 + (cell_first ? 0 : 1);
+                    if (b == b_end - 1)
+                        rec->y = int(cell);
+                }
                 int flags = (first ? F_FIRST : 0) | (last ? F_LAST : 0);
                 // a cascade member's own blocks continue from its prefix partial
                 if (first && si.b0 > 0 && b == si.b0)
@@ -469,7 +477,7 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
                     k_rd = u - a;
                 }
                 if (!issue(phys, si.q0, si.ql, si.W, b, si.T, hg, flags, int(cell),
-                           cell_first ? 0 : 1, ahead ? p.pace_ns : 0)) {
+                           cell_first ? 0 : 1, ahead)) {
                     ok = false;
                     break;
                 }
@@ -1841,33 +1849,35 @@ __global__ void __launch_bounds__(kThreadsMax, 1)
 }
 
 // ------------------------------------------------------------------ merge
-// Combine the partials of every sequence that cell boundaries split:
-// M = max m_k, L = sum l_k 2^(m_k - M), out = sum acc_k 2^(m_k - M) / L
-// over the cells k the sequence spans ("07 -- Inference" section 5.3; m in the
-// log2 domain), folded in groups of CG cells with the same rescaling rule.
-// Sequences with no token get zeros. One CTA per (sequence, head group); a
-// warp takes RPW output rows at a time, lane i dims 4i..4i+3, and issues all
-// loads of a group (m, l, acc of RPW rows x CG cells) before using any, so a
-// group costs one memory round trip. Launched as a programmatic dependent of
-// the main kernel: it waits (griddepcontrol) for it to finish.
+// Combine the partials of every sequence that cell boundaries split. The main
+// pass records, per (sequence, head group), the cell of the first piece (and
+// its slot: 1 if the piece does not open its cell) and the cell of the last;
+// the pieces are the cells between, each in slot 0 of its cell. Per output row:
+//   M = max_k m_k,  f_k = 2^(m_k - M),  L = sum_k l_k f_k,  out = sum_k f_k acc_k / L
+// ("07 -- Inference" section 5.3, m in the log2 domain). With M known first, the
+// acc loads of all pieces are independent and go out together. One CTA per
+// (sequence, head group, 32 rows): a warp takes 4 rows; lane k holds (m, l) of
+// piece k (32 pieces a round, rescaled across rounds), then lane i owns dims
+// 4i..4i+3 of every piece. Sequences with no token get zeros. Launched as a
+// programmatic dependent of the main kernel: it waits (griddepcontrol) for it.
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
     paged_decode_merge_kernel(const DecodeParams p, int grid)
 {
-    constexpr int RPW = 4, CG = 4;
+    constexpr int RPW = 4, PB = 4;  // rows per warp; pieces per batch of acc loads
+    const unsigned FULL = 0xffffffffu;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int s = blockIdx.x, hg = blockIdx.y;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-    const int nb_total = __ldcg(p.seq_start + p.S);
-    const Cells C = make_cells(p, nb_total, grid);
-    const int64_t fs = int64_t(hg) * nb_total + __ldcg(p.seq_start + s);
-    const int64_t fe = int64_t(hg) * nb_total + __ldcg(p.seq_start + s + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nrows = p.HG * p.rows;  // partial rows of this (sequence, head group)
-    const bool has_d = lane * 4 < D;
+    const int r0 = int(blockIdx.z) * (8 * RPW) + warp * RPW;
+    if (r0 >= nrows)
+        return;
     const SeqInfo si = seq_info(p, s);
-    const int vrows = p.G * si.ql;    // rows of each kv head with a query
+    const int vrows = p.G * si.ql;  // rows of each kv head with a query
+    const bool has_d = lane * 4 < D;
 
-    auto valid = [&](int r) { return r - (r / p.rows) * p.rows < vrows; };
+    auto valid = [&](int r) { return r < nrows && r - (r / p.rows) * p.rows < vrows; };
     auto out_offset = [&](int r) -> int64_t {  // r = hl * rows + row
         const int hl = r / p.rows, row = r - hl * p.rows;
         const int j = row / p.G, gq = row - j * p.G;
@@ -1886,84 +1896,111 @@ __global__ void __launch_bounds__(256)
         }
     };
 
-    if (fe == fs) {  // no token (or no query rows): zeros
-        for (int r = warp; r < nrows; r += nwarps)
-            if (has_d && valid(r))
-                store(out_offset(r), make_float4(0.f, 0.f, 0.f, 0.f));
+    if (si.nb == 0) {  // no token (or no query rows): zeros
+#pragma unroll
+        for (int i = 0; i < RPW; ++i)
+            if (has_d && valid(r0 + i))
+                store(out_offset(r0 + i), make_float4(0.f, 0.f, 0.f, 0.f));
         return;
     }
-    const int64_t kb = C.cell_of(fs), ke = C.cell_of(fe - 1);
-    if (kb == ke)
-        return;  // finished in place by the main kernel
+    const int2 rec = __ldcg(p.pieces + int64_t(s) * p.n_hg + hg);
+    const int kb = rec.x >> 1, ke = rec.y;
+    if (ke <= kb)
+        return;  // one piece: finished in place by the main kernel
+    if (kb < 0 || ke >= grid + p.tickets_max)
+        return;  // not a record of this call (a main pass that gave up): nothing to merge
+    const int np = ke - kb + 1;
+    // with fewer units than cells some cells are empty and hold no partial
+    const bool dense = __ldcg(p.ws + kWsDense) != 0u;
+    Cells C{};
+    if (!dense)
+        C = make_cells(p, int(__ldcg(p.ws + kWsUnits)), grid);
+    // (cell, slot) base index of piece k, or -1 for an empty cell
+    auto piece_base = [&](int k) -> int64_t {
+        const int64_t cell = int64_t(kb) + k;
+        if (!dense && C.empty(cell))
+            return -1;
+        return (cell * 2 + (k == 0 ? (rec.x & 1) : 0)) * p.HG;
+    };
 
-    for (int r0 = warp * RPW; r0 < nrows; r0 += nwarps * RPW) {
-        float Mr[RPW], Lr[RPW];
-        float4 ar[RPW];
+    float M[RPW], L[RPW];
+    float4 a[RPW];
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+        M[i] = -INFINITY;
+        L[i] = 0.f;
+        a[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int k0 = 0; k0 < np; k0 += 32) {
+        // ---- (m, l) of pieces k0 + lane: the round's max, weights and sums
+        const int kn = np - k0 < 32 ? np - k0 : 32;
+        const int64_t cb = lane < kn ? piece_base(k0 + lane) : -1;
+        float f[RPW];
 #pragma unroll
         for (int i = 0; i < RPW; ++i) {
-            Mr[i] = -INFINITY;
-            Lr[i] = 0.f;
-            ar[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        for (int64_t k0 = kb; k0 <= ke; k0 += CG) {
-            float mc[CG][RPW], lc[CG][RPW];
-            float4 vc[CG][RPW];
+            const int r = r0 + i;
+            const bool ok = cb >= 0 && r < nrows;
+            const int64_t idx = cb * p.rows + r;
+            const float m = ok ? __ldcg(p.ml + idx * 2) : -INFINITY;
+            const float l = ok ? __ldcg(p.ml + idx * 2 + 1) : 0.f;
+            float mr = m;
 #pragma unroll
-            for (int c = 0; c < CG; ++c) {
-                const int64_t k = k0 + c;
-                int64_t cb = -1;  // (cell, slot) base index
-                if (k <= ke && !C.empty(k))
-                    cb = (k * 2 + (C.start(k) >= fs ? 0 : 1)) * p.HG;
+            for (int o = 16; o >= 1; o >>= 1)
+                mr = fmaxf(mr, __shfl_xor_sync(FULL, mr, o));
+            const float Mn = fmaxf(M[i], mr);
+            const float mu = Mn == -INFINITY ? 0.f : Mn;
+            const float so = ex2(M[i] - mu);  // earlier rounds (0 while M is -inf)
+            f[i] = ex2(m - mu);                // 0 for an absent piece
+            float lr = l * f[i];
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1)
+                lr += __shfl_xor_sync(FULL, lr, o);
+            L[i] = L[i] * so + lr;
+            a[i].x *= so;
+            a[i].y *= so;
+            a[i].z *= so;
+            a[i].w *= so;
+            M[i] = Mn;
+        }
+        // ---- acc of the round's pieces, PB at a time, all rows together
+        for (int kk = 0; kk < kn; kk += PB) {
+            float4 v[PB][RPW];
+            float w[PB][RPW];
+#pragma unroll
+            for (int c = 0; c < PB; ++c) {
+                const int k = kk + c;
+                const int64_t cbk = __shfl_sync(FULL, cb, k & 31);
 #pragma unroll
                 for (int i = 0; i < RPW; ++i) {
                     const int r = r0 + i;
-                    const bool ok = cb >= 0 && r < nrows;
-                    const int64_t idx = cb * p.rows + r;  // (cell, slot, hl, row)
-                    mc[c][i] = ok ? __ldcg(p.ml + idx * 2) : -INFINITY;
-                    lc[c][i] = ok ? __ldcg(p.ml + idx * 2 + 1) : 0.f;
-                    vc[c][i] = (ok && has_d)
-                                   ? __ldcg(reinterpret_cast<const float4 *>(p.part + idx * D) + lane)
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                    w[c][i] = __shfl_sync(FULL, f[i], k & 31);
+                    const bool ok = k < kn && cbk >= 0 && r < nrows && has_d;
+                    v[c][i] = ok ? __ldcg(reinterpret_cast<const float4 *>(
+                                       p.part + (cbk * p.rows + r) * D) + lane)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (!ok)
+                        w[c][i] = 0.f;
                 }
             }
 #pragma unroll
-            for (int i = 0; i < RPW; ++i) {
-                float gm = Mr[i];
+            for (int c = 0; c < PB; ++c)
 #pragma unroll
-                for (int c = 0; c < CG; ++c)
-                    gm = fmaxf(gm, mc[c][i]);
-                if (gm == -INFINITY)
-                    continue;  // nothing seen yet for this row
-                const float so = ex2(Mr[i] - gm);  // 0 while Mr is -inf
-                Lr[i] *= so;
-                ar[i].x *= so;
-                ar[i].y *= so;
-                ar[i].z *= so;
-                ar[i].w *= so;
-#pragma unroll
-                for (int c = 0; c < CG; ++c) {
-                    const float f = ex2(mc[c][i] - gm);  // 0 for an absent cell
-                    Lr[i] += lc[c][i] * f;
-                    ar[i].x += vc[c][i].x * f;
-                    ar[i].y += vc[c][i].y * f;
-                    ar[i].z += vc[c][i].z * f;
-                    ar[i].w += vc[c][i].w * f;
+                for (int i = 0; i < RPW; ++i) {
+                    a[i].x += w[c][i] * v[c][i].x;
+                    a[i].y += w[c][i] * v[c][i].y;
+                    a[i].z += w[c][i] * v[c][i].z;
+                    a[i].w += w[c][i] * v[c][i].w;
                 }
-                Mr[i] = gm;
-            }
         }
-        if (!has_d)
+    }
+    if (!has_d)
+        return;
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+        if (!valid(r0 + i))
             continue;
-#pragma unroll
-        for (int i = 0; i < RPW; ++i) {
-            if (r0 + i >= nrows)
-                break;
-            if (!valid(r0 + i))
-                continue;
-            const float inv = Lr[i] > 0.f ? 1.f / Lr[i] : 0.f;
-            store(out_offset(r0 + i),
-                  make_float4(ar[i].x * inv, ar[i].y * inv, ar[i].z * inv, ar[i].w * inv));
-        }
+        const float inv = L[i] > 0.f ? 1.f / L[i] : 0.f;
+        store(out_offset(r0 + i), make_float4(a[i].x * inv, a[i].y * inv, a[i].z * inv, a[i].w * inv));
     }
 }
 
@@ -2040,8 +2077,8 @@ int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int 
     P.tail_div = opt_tail <= 1 ? 0 : opt_tail;
     P.tickets_max = (P.tail_div > 0 && P.rows <= 16) ? 2 * grid_cap : 0;
     const size_t cells = size_t(grid_cap) + size_t(P.tickets_max);
-    P.off_seq = kWsHeaderBytes;
-    P.off_ml = P.off_seq + round_up(size_t(S + 1) * 4, 256);
+    P.off_rec = kWsHeaderBytes;
+    P.off_ml = P.off_rec + round_up(size_t(S) * P.n_hg * 8, 256);
     P.off_part = P.off_ml + round_up(cells * 2 * P.HG * P.rows * 2 * 4, 256);
     P.ws_bytes = P.off_part + round_up(cells * 2 * P.HG * P.rows * size_t(D) * 4, 256);
     *pl = P;
@@ -2127,9 +2164,9 @@ static cudaError_t launch_kernel(Kern kern, int *configured_smem, const DecodePl
         return e;
     if (!with_merge)
         return cudaSuccess;
-    // the merge: one CTA per (sequence, head group), a programmatic dependent
+    // the merge: one CTA per (sequence, head group, 32 rows), a programmatic dependent
     cudaLaunchConfig_t mcfg = {};
-    mcfg.gridDim = dim3(unsigned(p.S), unsigned(p.n_hg));
+    mcfg.gridDim = dim3(unsigned(p.S), unsigned(p.n_hg), unsigned((p.HG * p.rows + 31) / 32));
     mcfg.blockDim = dim3(256);
     mcfg.dynamicSmemBytes = 0;
     mcfg.stream = stream;

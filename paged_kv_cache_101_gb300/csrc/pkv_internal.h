@@ -54,18 +54,28 @@ struct DecodePlan {
     int tail_div;    // the last 1/tail_div of the units go out as tickets (0: none)
     size_t smem;     // dynamic shared memory bytes
     // workspace layout (byte offsets)
-    size_t off_seq, off_ml, off_part, ws_bytes;
+    size_t off_rec, off_ml, off_part, ws_bytes;
 };
 
 // Workspace header words (uint32 at byte offset 4*i).
-enum { kWsErr = 0, kWsTicket = 2, kWsDone = 3, kWsProgress = 4, kWsHeaderBytes = 256 };
+// kWsUnits: blocks of all sequences (per head group); kWsDense: 1 if no cell is
+// empty (both written by CTA 0 of the main pass for the merge).
+enum {
+    kWsErr = 0,
+    kWsTicket = 2,
+    kWsDone = 3,
+    kWsProgress = 4,
+    kWsUnits = 5,
+    kWsDense = 6,
+    kWsHeaderBytes = 256
+};
 struct DecodeParams {
     const uint16_t *q;
     void *out;
     const int32_t *block_tables;
     const int32_t *context_lens;
     uint32_t *ws;          // workspace header: error word, ticket, done and progress counters
-    int32_t *seq_start;    // [S + 1] block prefix sums (written by CTA 0 for the merge)
+    int2 *pieces;          // [S][n_hg] cells of the first and last piece (for the merge)
     float *ml;             // [cells][2][HG][rows] (m, l) partial states
     float *part;           // [cells][2][HG][rows][D] unnormalised partial acc
     uint64_t *trace;       // optional per-CTA timeline [grid][kTraceWords] (null: off)
@@ -78,8 +88,8 @@ struct DecodeParams {
     int ticket_div;        // the last F / ticket_div units go to tickets
     int ticket_units;      // at least this many units per ticket
     float scale_log2;      // scale * log2(e)
-    int pace_ns;           // pacing: sleep per refill while ahead of the grid (0: off)
-    float pace_margin;     // pacing: lead (fraction of the work) allowed before sleeping
+    int pace;              // pacing: one stage fewer in flight while ahead of the grid (0: off)
+    float pace_margin;     // pacing: lead (fraction of the work) allowed before pacing
     const float *k_scale;  // E4M3 pools: [Hkv] dequantisation scales (null for bf16)
     const float *v_scale;
     // variable query counts (all null for a fixed n_query_per_seq = nq, causal):

@@ -62,9 +62,9 @@ def test_options(lib):
     assert pkv.set_option(pkv.PKV_OPT_STAGES, 0) == 3
     assert pkv.set_option(42, 1) == -1
     assert pkv.set_option(pkv.PKV_OPT_NUM_CTAS, -5) == -1
-    # pacing: 0 = auto, 1 = off, 2..100000 ns; margin 0..10000 (1/10000 of the work)
+    # pacing: 0 = off, 1 = on; margin 0..10000 (1/10000 of the work)
     assert pkv.set_option(pkv.PKV_OPT_PACE, 1) == 0
-    assert pkv.set_option(pkv.PKV_OPT_PACE, 100001) == -1
+    assert pkv.set_option(pkv.PKV_OPT_PACE, 2) == -1
     assert pkv.set_option(pkv.PKV_OPT_PACE, 0) == 1
     assert pkv.set_option(pkv.PKV_OPT_PACE_MARGIN, 50) == 0
     assert pkv.set_option(pkv.PKV_OPT_PACE_MARGIN, 10001) == -1
