@@ -244,28 +244,46 @@ def run_pkv(args, rank, world, dist):
     kern_mean = sum(kern_ms) / len(kern_ms)
     err = pkv.workspace_error(ws)
 
-    # ---- end to end: per-step inputs from pinned host memory, output back to host
-    h_q = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
-    h_q.copy_(q)
-    h_kn = torch.empty(k_new.shape, dtype=torch.bfloat16).pin_memory()
-    h_kn.copy_(k_new)
-    h_vn = torch.empty(v_new.shape, dtype=torch.bfloat16).pin_memory()
-    h_vn.copy_(v_new)
-    h_slots = slots.cpu().pin_memory()
-    h_tables = tables.cpu().pin_memory()
-    h_lens = lens.cpu().pin_memory()
+    # ---- end to end: per-step inputs from pinned host memory, output back to host.
+    # The step's inputs (q, new K/V rows, slots, block tables, lengths) sit in one
+    # pinned host arena and cross in ONE host-to-device copy into a device arena
+    # of the same layout; the library calls then run on views of that arena, and
+    # the output comes back in one device-to-host copy.
+    ins = [("q", q), ("k_new", k_new), ("v_new", v_new), ("slots", slots), ("tables", tables),
+           ("lens", lens)]
+    offs, off = {}, 0
+    for nm, t in ins:
+        offs[nm] = off
+        off = (off + t.numel() * t.element_size() + 255) // 256 * 256
+    arena_bytes = off
+    h_arena = torch.empty(arena_bytes, dtype=torch.uint8).pin_memory()
+    d_arena = torch.empty(arena_bytes, dtype=torch.uint8, device=dev)
+
+    def view(buf, nm, t):
+        n = t.numel() * t.element_size()
+        return buf[offs[nm]:offs[nm] + n].view(t.dtype).view(t.shape)
+
+    for nm, t in ins:
+        view(h_arena, nm, t).copy_(t)
+    e_q, e_kn, e_vn, e_slots, e_tables, e_lens = (view(d_arena, nm, t) for nm, t in ins)
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_slots, h_tables, h_lens))
+    h2d = arena_bytes
     d2h = h_out.numel() * h_out.element_size()
 
     def e2e_step():
-        q.copy_(h_q, non_blocking=True)
-        k_new.copy_(h_kn, non_blocking=True)
-        v_new.copy_(h_vn, non_blocking=True)
-        slots.copy_(h_slots, non_blocking=True)
-        tables.copy_(h_tables, non_blocking=True)
-        lens.copy_(h_lens, non_blocking=True)
-        step()
+        d_arena.copy_(h_arena, non_blocking=True)
+        if fp8:
+            pkv.kv_append_fp8(e_kn, e_vn, e_slots, k_cache, v_cache, k_scale, v_scale)
+            pkv.paged_decode_attention_fp8(e_q, k_cache, v_cache, k_scale, v_scale, e_tables,
+                                           e_lens, w.n_query_per_seq, w.scale, out, ws=ws)
+        elif cascade:
+            pkv.kv_append(e_kn, e_vn, e_slots, k_cache, v_cache)
+            pkv.paged_decode_attention_cascade(e_q, k_cache, v_cache, e_tables, e_lens,
+                                               w.n_query_per_seq, w.scale, out, groups, M, ws=ws)
+        else:
+            pkv.kv_append(e_kn, e_vn, e_slots, k_cache, v_cache)
+            pkv.paged_decode_attention(e_q, k_cache, v_cache, e_tables, e_lens,
+                                       w.n_query_per_seq, w.scale, out, ws=ws)
         h_out.copy_(out, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
@@ -341,7 +359,8 @@ def run_pkv(args, rank, world, dist):
         "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 6), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "path": "pinned host inputs -> H2D -> kv_append + attention -> D2H output"},
+                "path": "one pinned host arena (q, new K/V, slots, tables, lengths) -> one H2D -> "
+                        "kv_append + attention -> one D2H of the output"},
         "gpu_launches": K * (4 if cascade else 3),
         "device_error_word": err,
     }
