@@ -46,16 +46,20 @@ FALLBACK_HBM_GBS = 6800.0
 # to `source_sha256` (otherwise the bench reports traffic = null).
 NCU_TRAFFIC = {
     "llama3_8b_decode": {
-        "bytes": 582051584 + 3831552,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "31193e65d38080a22e876b5468f8508545e042553e7364ffe505bb43574fa731",
+        "bytes": 582060544 + 4124928,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "7193e95592b8bc91194a16add0d66ee3cbb84ac08993630acc18005a37862c04",
+    },
+    "llama3_70b_mix": {
+        "bytes": 1334683000 + 5618688,
+        "source_sha256": "7193e95592b8bc91194a16add0d66ee3cbb84ac08993630acc18005a37862c04",
     },
     "spec_verify": {
-        "bytes": 1417737000 + 5473280,
-        "source_sha256": "31193e65d38080a22e876b5468f8508545e042553e7364ffe505bb43574fa731",
+        "bytes": 1417737000 + 4886272,
+        "source_sha256": "7193e95592b8bc91194a16add0d66ee3cbb84ac08993630acc18005a37862c04",
     },
     "llama3_8b_decode/fp8": {
-        "bytes": 291324928 + 3497728,
-        "source_sha256": "31193e65d38080a22e876b5468f8508545e042553e7364ffe505bb43574fa731",
+        "bytes": 291322368 + 3569664,
+        "source_sha256": "7193e95592b8bc91194a16add0d66ee3cbb84ac08993630acc18005a37862c04",
     },
 }
 
