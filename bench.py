@@ -253,13 +253,14 @@ def run_pkv(args, rank, world, dist):
     # pinned host arena and cross in ONE host-to-device copy into a device arena
     # of the same layout; the library calls then run on views of that arena, and
     # the output comes back in one device-to-host copy.
-    ins = [("q", q), ("k_new", k_new), ("v_new", v_new), ("slots", slots), ("tables", tables),
-           ("lens", lens)]
-    offs, off = {}, 0
-    for nm, t in ins:
-        offs[nm] = off
-        off = (off + t.numel() * t.element_size() + 255) // 256 * 256
-    arena_bytes = off
+    # The plain bf16 step goes through the library's host-buffer entry point
+    # (pkv_decode_step_host: both copies inside the C-ABI call, its arena layout);
+    # the E4M3 and cascade steps use the same layout with the copies made here.
+    ins = [("q", q), ("k_new", k_new), ("v_new", v_new), ("slot_mapping", slots),
+           ("block_tables", tables), ("context_lens", lens)]
+    arena_bytes, offs = pkv.step_arena_layout(w.num_seqs, w.n_query_per_seq, w.num_q_heads,
+                                              w.num_kv_heads, w.head_dim,
+                                              w.block_tables.shape[1])
     h_arena = torch.empty(arena_bytes, dtype=torch.uint8).pin_memory()
     d_arena = torch.empty(arena_bytes, dtype=torch.uint8, device=dev)
 
@@ -275,6 +276,11 @@ def run_pkv(args, rank, world, dist):
     d2h = h_out.numel() * h_out.element_size()
 
     def e2e_step():
+        if not fp8 and not cascade:
+            pkv.decode_step_host(h_arena, d_arena, k_cache, v_cache, w.num_seqs,
+                                 w.n_query_per_seq, w.num_q_heads, w.block_tables.shape[1],
+                                 w.scale, out, h_out, ws=ws)
+            return
         d_arena.copy_(h_arena, non_blocking=True)
         if fp8:
             pkv.kv_append_fp8(e_kn, e_vn, e_slots, k_cache, v_cache, k_scale, v_scale)
@@ -363,7 +369,8 @@ def run_pkv(args, rank, world, dist):
         "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 6), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "path": "one pinned host arena (q, new K/V, slots, tables, lengths) -> one H2D -> "
+                "path": ("pkv_decode_step_host: " if not (fp8 or cascade) else "") +
+                        "one pinned host arena (q, new K/V, slots, tables, lengths) -> one H2D -> "
                         "kv_append + attention -> one D2H of the output"},
         "gpu_launches": K * (4 if cascade else 3),
         "device_error_word": err,

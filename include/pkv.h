@@ -373,7 +373,7 @@ pkv_status pkv_paged_decode_attention_fp8(const void *q, const void *k_cache, co
  * GPU). A geometry whose scratch (pkv_workspace_size) exceeds 32 MiB returns
  * PKV_ERR_WORKSPACE before anything is enqueued; on a 152-SM GB300 every
  * supported geometry (up to 32 query rows per kv head) needs at most ~21 MiB
- * plus 4 bytes per sequence.
+ * plus 8 bytes per (sequence, group of up to 8 kv heads).
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and keeps it; make that
@@ -392,6 +392,57 @@ pkv_status pkv_paged_decode_attention_static(const void *q, const void *k_cache,
                                              int32_t n_query_per_seq, int32_t num_q_heads,
                                              int32_t num_kv_heads, int32_t head_dim, float scale,
                                              void *out, int32_t out_dtype, void *stream);
+
+/*
+ * pkv_step_arena_layout -- byte layout of one decode step's inputs in a single
+ * buffer: q, k_new, v_new, slot_mapping, block_tables, context_lens, in that
+ * order, each at a 256-byte aligned offset, with the shapes and types of
+ * pkv_kv_append (n_new = num_seqs * n_query_per_seq new tokens, one per query
+ * row) and pkv_paged_decode_attention. Writes the six offsets to `offsets`
+ * (may be NULL) and returns the total bytes: 0 for num_seqs == 0, an
+ * unsupported geometry (pkv_paged_decode_attention's rules) or
+ * max_blocks_per_seq < 1.
+ */
+size_t pkv_step_arena_layout(int32_t num_seqs, int32_t n_query_per_seq, int32_t num_q_heads,
+                             int32_t num_kv_heads, int32_t head_dim, int32_t max_blocks_per_seq,
+                             size_t offsets[6]);
+
+/*
+ * pkv_decode_step_host -- one decode step from host memory: the step's inputs
+ * cross to the device, the new tokens are appended, the attention runs, and
+ * its output comes back to the host. Enqueued on `stream` in this order:
+ *   1. one host-to-device copy of `host_arena` (pkv_step_arena_layout's
+ *      layout, arena_bytes long) into `device_arena`;
+ *   2. pkv_kv_append of the arena's k_new / v_new rows at its slot_mapping;
+ *   3. pkv_paged_decode_attention over the arena's q, block_tables and
+ *      context_lens into `out_device`;
+ *   4. one device-to-host copy of `out_device` into `out_host`.
+ * The step is the pair of calls a decode loop makes ("LLM Serving: Continuous
+ * Batching & PagedAttention": each iteration writes the new token's K/V into
+ * its block slot, then attends over the block table); the pages give no host
+ * interface, so this one is the plainest: one copy each way.
+ *
+ *   host_arena     host, arena_bytes >= pkv_step_arena_layout(...) bytes; page-
+ *                  locked (cudaHostAlloc / cudaHostRegister) for the copy to be
+ *                  asynchronous; must stay unchanged until the copy has run.
+ *   device_arena   device, same size, 256-byte aligned; the library reads it
+ *                  only through steps 1-3.
+ *   out_device     device output of step 3 (pkv_paged_decode_attention's `out`).
+ *   out_host       host, num_seqs*n_query_per_seq*num_q_heads*head_dim elements
+ *                  of out_dtype; valid once the stream has reached step 4.
+ *   other arguments as pkv_kv_append and pkv_paged_decode_attention.
+ * Errors: those of the two calls (checked before anything is enqueued where
+ * they do not depend on device data), PKV_ERR_NULL for a missing arena or host
+ * output, PKV_ERR_WORKSPACE if arena_bytes is below the layout's size,
+ * PKV_ERR_CUDA if a copy cannot be enqueued.
+ */
+pkv_status pkv_decode_step_host(const void *host_arena, void *device_arena, size_t arena_bytes,
+                                void *k_cache, void *v_cache, int64_t num_blocks,
+                                int32_t max_blocks_per_seq, int32_t num_seqs,
+                                int32_t n_query_per_seq, int32_t num_q_heads,
+                                int32_t num_kv_heads, int32_t head_dim, float scale,
+                                void *out_device, void *out_host, int32_t out_dtype,
+                                void *workspace, size_t workspace_bytes, void *stream);
 
 /* Text for a status code (static storage; never NULL). */
 const char *pkv_status_string(int32_t status);

@@ -39,6 +39,9 @@ SIGNATURES = {
     "pkv_workspace_size": ([_I32, _I32, _I32, _I32, _I32], _SZ),
     "pkv_paged_decode_attention": ([_P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32,
                                     _F, _P, _I32, _P, _SZ, _P], ctypes.c_int),
+    "pkv_step_arena_layout": ([_I32, _I32, _I32, _I32, _I32, _I32, _P], _SZ),
+    "pkv_decode_step_host": ([_P, _P, _SZ, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _F,
+                              _P, _P, _I32, _P, _SZ, _P], ctypes.c_int),
     "pkv_status_string": ([_I32], ctypes.c_char_p),
     "pkv_set_option": ([_I32, _I32], _I32),
     "pkv_version": ([], _I32),
@@ -572,3 +575,54 @@ def paged_decode_attention_static(q, k_cache, v_cache, block_tables, context_len
     if st != PKV_OK:
         raise PkvError("pkv_paged_decode_attention_static", st)
     return out
+
+
+def step_arena_layout(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim,
+                      max_blocks_per_seq):
+    """(total bytes, {name: byte offset}) of one decode step's inputs packed in one
+    buffer (q, k_new, v_new, slot_mapping, block_tables, context_lens)."""
+    offs = (ctypes.c_size_t * 6)()
+    n = lib().pkv_step_arena_layout(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads,
+                                    head_dim, max_blocks_per_seq, offs)
+    if n == 0:
+        raise PkvError("pkv_step_arena_layout", PKV_ERR_UNSUPPORTED)
+    names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
+    return int(n), dict(zip(names, (int(o) for o in offs)))
+
+
+def decode_step_host(host_arena, device_arena, k_cache, v_cache, num_seqs, n_query_per_seq,
+                     num_q_heads, max_blocks_per_seq, scale, out_device, out_host, ws=None):
+    """One decode step from host memory (``pkv_decode_step_host``): one copy of the
+    packed inputs to ``device_arena``, the KV append, the attention into
+    ``out_device``, one copy of the output to ``out_host``; asynchronous on the
+    current stream. ``host_arena``/``out_host`` are (pinned) CPU tensors."""
+    torch = _torch()
+    _check(k_cache, "k_cache", torch.bfloat16, 4)
+    _check(v_cache, "v_cache", torch.bfloat16, 4)
+    if host_arena.device.type != "cpu" or out_host.device.type != "cpu":
+        raise ValueError("host_arena and out_host must be host tensors")
+    if device_arena.device.type != "cuda" or not device_arena.is_contiguous():
+        raise ValueError("device_arena must be a contiguous CUDA tensor")
+    if not host_arena.is_contiguous() or not out_host.is_contiguous():
+        raise ValueError("host buffers must be contiguous")
+    if out_device.dtype not in (torch.bfloat16, torch.float32) or out_host.dtype != out_device.dtype:
+        raise TypeError("out_device/out_host must both be bfloat16 or both float32")
+    NB, bs, Hkv, D = k_cache.shape
+    if bs != BLOCK_SIZE or v_cache.shape != k_cache.shape:
+        raise ValueError("pools must be [num_blocks, 16, Hkv, D] and equal in shape")
+    nbytes = min(host_arena.numel() * host_arena.element_size(),
+                 device_arena.numel() * device_arena.element_size())
+    if out_host.numel() != out_device.numel():
+        raise ValueError("out_host and out_device differ in size")
+    if ws is None:
+        ws = workspace(k_cache.device, workspace_size(num_seqs, n_query_per_seq, num_q_heads,
+                                                      Hkv, D))
+    st = lib().pkv_decode_step_host(
+        host_arena.data_ptr(), device_arena.data_ptr(), nbytes, k_cache.data_ptr(),
+        v_cache.data_ptr(), NB, max_blocks_per_seq, num_seqs, n_query_per_seq, num_q_heads, Hkv,
+        D, float(scale), out_device.data_ptr(), out_host.data_ptr(),
+        PKV_FP32 if out_device.dtype == torch.float32 else PKV_BF16, ws.data_ptr(), ws.numel(),
+        _stream_handle(k_cache.device))
+    if st != PKV_OK:
+        raise PkvError("pkv_decode_step_host", st)
+    return out_host

@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIBRARY = os.path.join(PKG, "libpkv.so")
 SOURCES = ["api.cu", "kv_append.cu", "copy_blocks.cu", "paged_decode.cu", "static_scratch.cu",
-           "block_manager.cpp", "query_plan.cpp"]
+           "host_step.cu", "block_manager.cpp", "query_plan.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

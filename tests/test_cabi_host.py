@@ -166,6 +166,46 @@ def test_fp8_validation(lib):
     assert ap(A, A, A, -1, A, A, 8, 2, 64, A, A, None) == SHAPE
 
 
+def test_step_arena_layout(lib):
+    n, offs = pkv.step_arena_layout(64, 1, 32, 8, 128, 256)
+    sizes = [64 * 32 * 128 * 2, 64 * 8 * 128 * 2, 64 * 8 * 128 * 2, 64 * 8, 64 * 256 * 4, 64 * 4]
+    names = ["q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens"]
+    prev_end = 0
+    for name, size in zip(names, sizes):
+        o = offs[name]
+        assert o % 256 == 0 and o >= prev_end      # aligned, in order, no overlap
+        prev_end = o + size
+    assert n >= prev_end and n % 256 == 0 and n - prev_end < 256
+    assert lib.pkv_step_arena_layout(4, 5, 8, 2, 64, 8, None) == 0     # nq > 4
+    assert lib.pkv_step_arena_layout(4, 1, 8, 3, 64, 8, None) == 0     # 8 % 3 != 0
+    assert lib.pkv_step_arena_layout(4, 1, 8, 2, 64, 0, None) == 0     # no table columns
+    assert lib.pkv_step_arena_layout(0, 1, 8, 2, 64, 8, None) == 0     # empty step: 0 bytes
+
+
+def step_host(lib, ha=A, da=A, nbytes=1 << 20, k=A, v=A, nb=64, mb=8, S=4, nq=1, hq=8, hkv=2,
+              d=64, od=A, oh=A, dt=0, ws=A, wsb=1 << 30):
+    return lib.pkv_decode_step_host(ha, da, nbytes, k, v, nb, mb, S, nq, hq, hkv, d, 0.125, od,
+                                    oh, dt, ws, wsb, None)
+
+
+def test_decode_step_host_validation(lib):
+    assert step_host(lib, S=0) == OK                    # empty step: nothing enqueued
+    assert step_host(lib, S=-1) == SHAPE
+    assert step_host(lib, mb=0) == SHAPE
+    assert step_host(lib, nq=5) == UNSUP
+    assert step_host(lib, d=96) == UNSUP
+    assert step_host(lib, ha=None) == NULL
+    assert step_host(lib, da=None) == NULL
+    assert step_host(lib, oh=None) == NULL
+    assert step_host(lib, od=None) == NULL
+    assert step_host(lib, k=None) == NULL
+    assert step_host(lib, nbytes=1024) == WORKSPACE     # arena smaller than the layout
+    assert step_host(lib, da=A + 16) == ALIGN
+    assert step_host(lib, dt=2) == DTYPE
+    assert step_host(lib, nb=0) == SHAPE
+    assert step_host(lib, ws=None) == WORKSPACE
+
+
 def test_workspace_size_rejects_bad_geometry(lib):
     assert lib.pkv_workspace_size(4, 5, 8, 2, 64) == 0
     assert lib.pkv_workspace_size(4, 1, 8, 3, 64) == 0
