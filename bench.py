@@ -64,6 +64,23 @@ NCU_TRAFFIC = {
 }
 
 
+def max_over_ranks(values, dist, device):
+    """Each timing's maximum over all ranks (the slowest replica sets the job's
+    time); the values unchanged on one rank."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_gbs(world, bytes_per_replica_step, ms_per_step):
+    """Whole-job throughput: every replica moves its step's bytes in the (max over
+    ranks) step time."""
+    return world * bytes_per_replica_step / (ms_per_step * 1e-3) / 1e9
+
+
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
     for f in ("paged_decode.cu", "pkv_common.cuh", "pkv_internal.h"):
@@ -312,10 +329,7 @@ def run_pkv(args, rank, world, dist):
     e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e_s, e_e)) / Ke
 
     # max over ranks
-    if dist is not None:
-        t = torch.tensor([ms_per_step, kern_mean, e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step, kern_mean, e2e_ms = (float(x) for x in t.tolist())
+    ms_per_step, kern_mean, e2e_ms = max_over_ranks([ms_per_step, kern_mean, e2e_ms], dist, dev)
 
     peak, peak_kind = measured_peaks()
     achieved = attn_bytes / (kern_mean * 1e-3) / 1e9
@@ -324,7 +338,7 @@ def run_pkv(args, rank, world, dist):
                          ("/fma" if fma else ""))
     if nt and nt.get("source_sha256") == kernel_source_sha():
         traffic = nt["bytes"]
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    value = job_gbs(world, step_bytes, ms_per_step)
     res = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -453,10 +467,7 @@ def run_copy(args, rank, world, dist):
         e_e[i].record()
     torch.cuda.synchronize()
     e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e_s, e_e)) / Ke
-    if dist is not None:
-        t = torch.tensor([ms, e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = (float(x) for x in t.tolist())
+    ms, e2e_ms = max_over_ranks([ms, e2e_ms], dist, dev)
 
     peak, peak_kind = measured_peaks()
     achieved = step_bytes / (ms * 1e-3) / 1e9
@@ -603,10 +614,7 @@ def run_tree(args, rank, world, dist):
     ms = sum(a.elapsed_time(b) for a, b in zip(ev_s, ev_e)) / K
     kern = [ev_k0[i].elapsed_time(ev_k1[i]) for i in range(0, K, HOOK)]
     kern_ms = sum(kern) / len(kern)
-    if dist is not None:
-        t = torch.tensor([ms, kern_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, kern_ms = (float(x) for x in t.tolist())
+    ms, kern_ms = max_over_ranks([ms, kern_ms], dist, dev)
     peak, peak_kind = measured_peaks()
     achieved = attn_bytes / (kern_ms * 1e-3) / 1e9
     res = {
@@ -701,10 +709,7 @@ def run_shared_prefix(args, rank, world, dist):
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
-    if dist is not None:
-        t = torch.tensor([ms, ms_plain], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_plain = (float(x) for x in t.tolist())
+    ms, ms_plain = max_over_ranks([ms, ms_plain], dist, dev)
     peak, peak_kind = measured_peaks()
     res = {
         "metric": PREFIX_METRIC, "value": round(world * step_bytes / (ms * 1e-3) / 1e9, 2),
