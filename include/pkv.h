@@ -130,8 +130,9 @@ pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, int64_t num_blocks,
  * SM count). n_query_per_seq may be up to 32 / (num_q_heads / num_kv_heads)
  * (the max_q_len of pkv_paged_decode_attention_varlen). Returns 0 if the geometry is unsupported or no device is usable.
  * The workspace holds the split-K partial states (m, l, acc) that the merge
- * step combines, a per-sequence block prefix sum and a 4-byte device error
- * word at offset 0 (see pkv_paged_decode_attention).
+ * step combines, per (sequence, kv-head group) the cells holding its first and
+ * last partial, and a 4-byte device error word at offset 0 (see
+ * pkv_paged_decode_attention).
  */
 size_t pkv_workspace_size(int32_t num_seqs, int32_t n_query_per_seq, int32_t num_q_heads,
                           int32_t num_kv_heads, int32_t head_dim);
@@ -179,7 +180,7 @@ size_t pkv_workspace_size(int32_t num_seqs, int32_t n_query_per_seq, int32_t num
  *                  ZERO-FILLED before its first use; every call leaves the
  *                  counters it uses at zero again, so one workspace serves any
  *                  sequence of calls (of any shapes that fit it). It holds a
- *                  256-byte header, the block prefix sums and the split-K
+ *                  256-byte header, the merge's piece records and the split-K
  *                  partial states (m, l, acc) per cell (a fixed slice of the
  *                  batch's blocks). Its first 4
  *                  bytes are a sticky device error word: a kernel that gives up

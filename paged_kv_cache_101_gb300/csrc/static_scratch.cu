@@ -1,8 +1,8 @@
 // static_scratch.cu -- pkv_paged_decode_attention_static: decode attention for
 // callers that cannot allocate device memory.
 //
-// The scratch the attention kernels need (split-K partials, block prefix sums,
-// error word) lives in a file-scope device array instead of a caller-provided
+// The scratch the attention kernels need (split-K partials, the merge's piece
+// records, error word) lives in a file-scope device array instead of a caller-provided
 // workspace. Host code cannot use the array's name as a device address (on the
 // host it is only a stand-in symbol), so the first call on each device looks up
 // the real address with cudaGetSymbolAddress, with that device current, and the
