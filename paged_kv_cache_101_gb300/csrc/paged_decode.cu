@@ -712,10 +712,11 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
                 const uint32_t addr = kb + uint32_t(k_tok * 128 + ((chunk ^ sw) << 4));
                 uint32_t r[4];
                 ldsm_x4(addr, r);
-                const uint32_t a0[4] = {e4m3x2_to_f16x2(r[0]), e4m3x2_to_f16x2(r[1]),
-                                        e4m3x2_to_f16x2(r[0] >> 16), e4m3x2_to_f16x2(r[1] >> 16)};
-                const uint32_t a1[4] = {e4m3x2_to_f16x2(r[2]), e4m3x2_to_f16x2(r[3]),
-                                        e4m3x2_to_f16x2(r[2] >> 16), e4m3x2_to_f16x2(r[3] >> 16)};
+                uint32_t a0[4], a1[4];
+                e4m3x4_to_f16x2x2(r[0], a0[0], a0[2]);
+                e4m3x4_to_f16x2x2(r[1], a0[1], a0[3]);
+                e4m3x4_to_f16x2x2(r[2], a1[0], a1[2]);
+                e4m3x4_to_f16x2x2(r[3], a1[1], a1[3]);
                 mma_f16_16816(sc, a0, qf[2 * i][0], qf[2 * i][1]);
                 mma_f16_16816(sc2, a1, qf[2 * i + 1][0], qf[2 * i + 1][1]);
             }
@@ -856,8 +857,8 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
                     uint32_t ae[4], ao[4];
 #pragma unroll
                     for (int m = 0; m < 4; ++m) {
-                        ae[m] = e4m3x2_to_f16x2(__byte_perm(r[m], 0u, 0x0020));
-                        ao[m] = e4m3x2_to_f16x2(__byte_perm(r[m], 0u, 0x0031));
+                        // bytes 0,2 (even dims) then 1,3 (odd dims) in one permute
+                        e4m3x4_to_f16x2x2(__byte_perm(r[m], 0u, 0x3120), ae[m], ao[m]);
                         if constexpr (MASKED) {
                             ae[m] &= m < 2 ? mlo : mhi;
                             ao[m] &= m < 2 ? mlo : mhi;
@@ -1162,12 +1163,14 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
                 const uint32_t addr = kb + uint32_t(k_tok * 128 + ((chunk ^ sw) << 4));
                 uint32_t r[4];
                 ldsm_x4(addr, r);
-                mma_f16_16816(sc[0], qa[2 * i], e4m3x2_to_f16x2(r[0]), e4m3x2_to_f16x2(r[0] >> 16));
-                mma_f16_16816(sc[1], qa[2 * i], e4m3x2_to_f16x2(r[2]), e4m3x2_to_f16x2(r[2] >> 16));
-                mma_f16_16816(sc2[0], qa[2 * i + 1], e4m3x2_to_f16x2(r[1]),
-                              e4m3x2_to_f16x2(r[1] >> 16));
-                mma_f16_16816(sc2[1], qa[2 * i + 1], e4m3x2_to_f16x2(r[3]),
-                              e4m3x2_to_f16x2(r[3] >> 16));
+                uint32_t b[4][2];
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    e4m3x4_to_f16x2x2(r[m], b[m][0], b[m][1]);
+                mma_f16_16816(sc[0], qa[2 * i], b[0][0], b[0][1]);
+                mma_f16_16816(sc[1], qa[2 * i], b[2][0], b[2][1]);
+                mma_f16_16816(sc2[0], qa[2 * i + 1], b[1][0], b[1][1]);
+                mma_f16_16816(sc2[1], qa[2 * i + 1], b[3][0], b[3][1]);
             }
         } else {
 #pragma unroll
@@ -1327,10 +1330,9 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
                         const uint32_t lo_t = r[2 * c], hi_t = r[2 * c + 1];
-                        uint32_t e0 = e4m3x2_to_f16x2(__byte_perm(lo_t, 0u, 0x0020));
-                        uint32_t e1 = e4m3x2_to_f16x2(__byte_perm(hi_t, 0u, 0x0020));
-                        uint32_t o0 = e4m3x2_to_f16x2(__byte_perm(lo_t, 0u, 0x0031));
-                        uint32_t o1 = e4m3x2_to_f16x2(__byte_perm(hi_t, 0u, 0x0031));
+                        uint32_t e0, e1, o0, o1;  // even dims (bytes 0,2), odd (1,3)
+                        e4m3x4_to_f16x2x2(__byte_perm(lo_t, 0u, 0x3120), e0, o0);
+                        e4m3x4_to_f16x2x2(__byte_perm(hi_t, 0u, 0x3120), e1, o1);
                         if constexpr (MASKED) {
                             e0 &= mlo;
                             e1 &= mhi;

@@ -174,6 +174,18 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair)
     return d;
 }
 
+// Four E4M3 codes (bytes 0..3) -> two f16x2: bytes 0,1 -> `p01`, bytes 2,3 -> `p23`
+// (the two code pairs are split as 16-bit halves, no shift). Exact.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t codes, uint32_t &p01, uint32_t &p23)
+{
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+        : "=r"(p01), "=r"(p23)
+        : "r"(codes));
+}
+
 // Two floats -> two E4M3 codes, `lo` in bits 0..7: nearest, ties to even,
 // saturating to +-448 (NaN stays NaN).
 __device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi)
