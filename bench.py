@@ -46,20 +46,20 @@ FALLBACK_HBM_GBS = 6800.0
 # to `source_sha256` (otherwise the bench reports traffic = null).
 NCU_TRAFFIC = {
     "llama3_8b_decode": {
-        "bytes": 582060544 + 4124928,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "7193e95592b8bc91194a16add0d66ee3cbb84ac08993630acc18005a37862c04",
+        "bytes": 582099200 + 4126464,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "6b8deab0846328c0e8919c4af3b864d6966046e3658a4d3cbf8ac7a04b8ab0f4",
     },
     "llama3_70b_mix": {
-        "bytes": 1334683000 + 5618688,
-        "source_sha256": "7193e95592b8bc91194a16add0d66ee3cbb84ac08993630acc18005a37862c04",
+        "bytes": 1334956000 + 5754880,
+        "source_sha256": "6b8deab0846328c0e8919c4af3b864d6966046e3658a4d3cbf8ac7a04b8ab0f4",
     },
     "spec_verify": {
-        "bytes": 1417737000 + 4886272,
-        "source_sha256": "7193e95592b8bc91194a16add0d66ee3cbb84ac08993630acc18005a37862c04",
+        "bytes": 1417773000 + 5332224,
+        "source_sha256": "6b8deab0846328c0e8919c4af3b864d6966046e3658a4d3cbf8ac7a04b8ab0f4",
     },
     "llama3_8b_decode/fp8": {
-        "bytes": 291322368 + 3569664,
-        "source_sha256": "7193e95592b8bc91194a16add0d66ee3cbb84ac08993630acc18005a37862c04",
+        "bytes": 291329536 + 3626496,
+        "source_sha256": "6b8deab0846328c0e8919c4af3b864d6966046e3658a4d3cbf8ac7a04b8ab0f4",
     },
 }
 
