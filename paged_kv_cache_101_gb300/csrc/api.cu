@@ -260,7 +260,7 @@ const char *pkv_status_string(int32_t status)
     }
 }
 
-int32_t pkv_version(void) { return 100; }
+int32_t pkv_version(void) { return 200; }
 
 void pkv_set_trace_buffer(void *device_buffer, size_t bytes)
 {
