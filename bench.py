@@ -5,8 +5,11 @@
 
 Prints ONE JSON line (rank 0). A step is the whole hot path over one batch:
 ``kv_append`` of the step's new tokens, then ``paged_decode_attention`` (main
-kernel + merge kernel). Inputs are seeded synthetic data resident in HBM; an L2
-flush (a 512 MiB memset) separates timed steps and is not timed. ``value`` is
+kernel + merge kernel). Inputs are seeded synthetic data resident in HBM. A step
+that reads at least 4x the L2 capacity evicts its own inputs, so nothing is
+flushed between its timed steps (``--l2 auto``; the line also carries the same
+steps timed after a 512 MiB memset, ``with_write_flush``); smaller steps are
+separated by that memset, untimed. ``value`` is
 the step's algorithmic bytes (Q + K + V + block tables + context lengths read,
 output written, plus the append's rows) per second of step time, in GB/s;
 shared-prefix blocks count once.
@@ -39,6 +42,7 @@ from paged_kv_cache_101_gb300 import roofline as R  # noqa: E402
 METRIC = "paged decode-attention KV-read GB/s vs ~8 TB/s HBM peak; µs per decode step"
 DEFAULT_WORKLOAD = "llama3_8b_decode"
 FLUSH_BYTES = 512 << 20
+L2_BYTES = 129 * 10**6  # GB300 L2 capacity
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM traffic (read + write bytes per launch) of the main attention kernel from
@@ -207,6 +211,15 @@ def run_pkv(args, rank, world, dist):
     app_bytes = R.append_bytes(int(w.slot_mapping.size), w.num_kv_heads, w.head_dim,
                                kv_bytes_per_element=eb)
     step_bytes = attn_bytes + app_bytes
+    # Between timed steps: a step that reads several times the L2 capacity evicts
+    # its own inputs, so nothing is flushed (no dirty flush data is written back
+    # during the timed kernels); smaller steps are separated by the 512 MiB memset.
+    l2_mode = args.l2 if args.l2 != "auto" else (
+        "none" if step_bytes >= 4 * L2_BYTES else "flush")
+
+    def flush_fn():
+        if l2_mode == "flush":
+            flush.zero_()
 
     def step():
         if fp8:
@@ -223,7 +236,7 @@ def run_pkv(args, rank, world, dist):
                                        w.scale, out, ws=ws)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_fn()
         step()
     torch.cuda.synchronize()
 
@@ -246,7 +259,7 @@ def run_pkv(args, rank, world, dist):
     # merge wait for it instead of launching early (programmatic dependent launch).
     HOOK = 4
     for i in range(K):
-        flush.zero_()
+        flush_fn()
         if i % HOOK == 0:
             pkv.set_profiling_events(ev_k0[i], ev_k1[i])
         ev_s[i].record()
@@ -258,6 +271,29 @@ def run_pkv(args, rank, world, dist):
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
+
+    # the same steps again, each after the 512 MiB memset, for comparison
+    write_flush = None
+    if l2_mode == "none":
+        Kf = min(K, 300)
+        wf = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(Kf)]
+        for i in range(Kf):
+            flush.zero_()
+            if i % HOOK == 0:
+                pkv.set_profiling_events(wf[i][2], wf[i][3])
+            wf[i][0].record()
+            step()
+            wf[i][1].record()
+            if i % HOOK == 0:
+                pkv.set_profiling_events(None, None)
+        torch.cuda.synchronize()
+        f_step = sum(e[0].elapsed_time(e[1]) for e in wf) / Kf
+        f_kern = [wf[i][2].elapsed_time(wf[i][3]) for i in range(0, Kf, HOOK)]
+        f_step, f_kern = max_over_ranks([f_step, sum(f_kern) / len(f_kern)], dist, dev)
+        write_flush = {"us_per_step": round(f_step * 1e3, 3), "kernel_us": round(f_kern * 1e3, 3),
+                       "steps": Kf,
+                       "note": "each step after a 512 MiB memset: its dirty lines are written "
+                               "back during the timed kernels"}
 
     step_ms = [a.elapsed_time(b) for a, b in zip(ev_s, ev_e)]
     kern_ms = [ev_k0[i].elapsed_time(ev_k1[i]) for i in range(0, K, HOOK)]
@@ -314,14 +350,14 @@ def run_pkv(args, rank, world, dist):
         h_out.copy_(out, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
-        flush.zero_()
+        flush_fn()
         e2e_step()
     torch.cuda.synchronize()
     Ke = max(1, min(K, 200))
     e_s = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
     e_e = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
     for i in range(Ke):
-        flush.zero_()
+        flush_fn()
         e_s[i].record()
         e2e_step()
         e_e[i].record()
@@ -354,7 +390,8 @@ def run_pkv(args, rank, world, dist):
         "dtype": "bf16 (E4M3 KV cache, f16 products)" if fp8 else "bf16",
         "data": ("synthetic (seeded random E4M3 code pools with per-head scales, N(0,1) bf16 "
                  "Q and new rows; " if fp8 else "synthetic (seeded N(0,1) bf16 K/V/Q; ") +
-                "pools in HBM; inputs > L2 and a 512 MiB L2 flush between timed steps)",
+                "pools in HBM; " + ("inputs several times the L2, no flush)" if l2_mode == "none"
+                                    else "a 512 MiB L2 flush between timed steps)"),
         "config": {
             "workload": args.workload + (" (fp8 KV cache)" if fp8 else "") +
                         (" (shared-prefix cascade)" if cascade else "") +
@@ -365,7 +402,10 @@ def run_pkv(args, rank, world, dist):
             "head_dim": w.head_dim, "block_size": 16,
             "context_tokens": int(w.context_lens.sum()),
             "num_blocks": w.num_blocks, "parallelism": f"replicas x{world}",
-            "l2": "flushed between timed steps (512 MiB memset, untimed)",
+            "l2": ("not flushed: each step reads %.0f MB, %.1fx the %d MB L2, so it evicts "
+                   "its own inputs" % (step_bytes / 1e6, step_bytes / L2_BYTES, L2_BYTES // 10**6)
+                   if l2_mode == "none" else
+                   "flushed between timed steps (512 MiB memset, untimed)"),
             "step": ("kv_append_fp8 + paged_decode_attention_fp8" if fp8 else
                      "kv_append + paged_decode_attention") + " (main + merge kernels)",
             "bytes_per_step": step_bytes, "attention_bytes_unique": attn_bytes,
@@ -389,6 +429,8 @@ def run_pkv(args, rank, world, dist):
         "gpu_launches": K * (4 if cascade else 3),
         "device_error_word": err,
     }
+    if write_flush is not None:
+        res["with_write_flush"] = write_flush
     if clk is not None:
         res["clocks"] = clk
     return res
@@ -860,6 +902,9 @@ def main():
                          "moved to the front of the batch)")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
                     help="KV pool element type (fp8 = E4M3 codes with per-head scales)")
+    ap.add_argument("--l2", default="auto", choices=["auto", "flush", "none"],
+                    help="between timed steps: auto = no flush when a step reads at least 4x "
+                         "the L2 (it evicts its own inputs), else a 512 MiB memset")
     ap.add_argument("--pace", action="store_true",
                     help="pace the attention kernel's chunks (PKV_OPT_PACE; off by default)")
     ap.add_argument("--math", default="tensor", choices=["tensor", "fma"],
