@@ -392,7 +392,16 @@ size_t pkv_workspace_size(int32_t num_seqs, int32_t n_query_per_seq, int32_t num
                          d.num_sms, g_opt_num_ctas, g_opt_stages, g_opt_heads, g_opt_tail, d.smem_optin,
                          0, 0, &pl) != 0)
         return 0;
-    return pl.ws_bytes;
+    size_t bytes = pl.ws_bytes;
+    // the E4M3 call shares this size: its plan may use more cells
+    pkv::DecodePlan pl8;
+    if (head_dim == 128 &&
+        pkv::plan_decode(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim, 1,
+                         d.num_sms, g_opt_num_ctas, g_opt_stages, g_opt_heads, g_opt_tail,
+                         d.smem_optin, 1, 0, &pl8) == 0 &&
+        pl8.ws_bytes > bytes)
+        bytes = pl8.ws_bytes;
+    return bytes;
 }
 
 }  // extern "C"

@@ -1487,8 +1487,10 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
     }
 }
 
-template <int D, int NTW, int WPH, bool KV8>
-__global__ void __launch_bounds__(kThreadsMax, 1)
+// MINB: CTAs per SM the plan runs (2 for the E4M3 5-8-row shape; registers are
+// then capped so that two fit).
+template <int D, int NTW, int WPH, bool KV8, int MINB = 1>
+__global__ void __launch_bounds__(kThreadsMax, MINB)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const DecodeParams p)
 {
@@ -2060,14 +2062,21 @@ int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int 
     int fixed = 1024 + int(sizeof(Cells)) + 64;
     if (P.fma)  // per consumer warp: its query rows and P in fp32
         fixed += 16 + P.HG * P.wph * fma_warp_bytes(P.rw);
-    int max_st = (smem_optin - fixed) / per_stage;
+    // E4M3 with 5 to 8 rows per kv head: two CTAs per SM. These consumers wait on
+    // the latency of the conversions and the doubled math per byte, not on memory,
+    // so twice the warps pay off more than deep rings (measured: 8 rows 130 -> 113
+    // us on the 70B mix; with 4 rows the extra cells and shorter rings cost more).
+    const bool two_per_sm = P.kv8 && P.ntw == 1 && P.wph == 1 && P.rows > 4;
+    const int smem_budget = two_per_sm ? smem_optin / 2 - 1024 : smem_optin;
+    int max_st = (smem_budget - fixed) / per_stage;
     if (max_st > 8)
         max_st = 8;
     if (max_st < 2)
         return -1;
     P.nst = opt_stages > 0 ? std::min(std::max(opt_stages, 2), max_st) : max_st;
     P.smem = size_t(fixed) + size_t(P.nst) * per_stage;
-    const int grid_cap = opt_ctas > 0 ? opt_ctas : num_sms;
+    P.ctas_per_sm = two_per_sm ? 2 : 1;
+    const int grid_cap = opt_ctas > 0 ? opt_ctas : P.ctas_per_sm * num_sms;
     if (grid_cap < 1 || grid_cap > 16384)
         return -1;
     const int64_t f_max = int64_t(P.n_hg) * S * MB;
@@ -2183,14 +2192,14 @@ static cudaError_t launch_kernel(Kern kern, int *configured_smem, const DecodePl
     return cudaGetLastError();
 }
 
-template <int D, int NTW, int WPH, bool KV8>
+template <int D, int NTW, int WPH, bool KV8, int MINB = 1>
 static cudaError_t launch_one(const DecodePlan &pl, const DecodeParams &p, const CUtensorMap &kmap,
                               const CUtensorMap &vmap, cudaStream_t stream, cudaEvent_t ev_before,
                               cudaEvent_t ev_after, bool with_merge = true)
 {
     static int configured_smem[64] = {0};  // per device ordinal
-    return launch_kernel(paged_decode_kernel<D, NTW, WPH, KV8>, configured_smem, pl, p, kmap, vmap,
-                         stream, ev_before, ev_after, with_merge);
+    return launch_kernel(paged_decode_kernel<D, NTW, WPH, KV8, MINB>, configured_smem, pl, p,
+                         kmap, vmap, stream, ev_before, ev_after, with_merge);
 }
 
 template <int RW>
@@ -2218,6 +2227,8 @@ cudaError_t launch_decode(const DecodePlan &pl, const DecodeParams &p, const CUt
         return launch_fma<8>(pl, p, kmap, vmap, stream, eb, ea);
     }
     if (pl.kv8) {  // E4M3 pools: D = 128 only
+        if (pl.ctas_per_sm == 2)
+            return launch_one<128, 1, 1, true, 2>(pl, p, kmap, vmap, stream, eb, ea);
         if (pl.wph == 2)
             return launch_one<128, 2, 2, true>(pl, p, kmap, vmap, stream, eb, ea);
         if (pl.ntw == 2)

@@ -50,6 +50,7 @@ struct DecodePlan {
     int rw;          // CUDA-core consumers: query rows per warp (4 or 8)
     int prefix;      // 1: the cascade's prefix pass (one head per CTA, 8 warps x 16 rows)
     int grid;        // persistent CTAs
+    int ctas_per_sm; // CTAs of the grid resident per SM (1, or 2 for the E4M3 5-8-row shape)
     int tickets_max; // cap on dynamically claimed tickets (0: static chunks only)
     int tail_div;    // the last 1/tail_div of the units go out as tickets (0: none)
     size_t smem;     // dynamic shared memory bytes
