@@ -50,20 +50,24 @@ FALLBACK_HBM_GBS = 6800.0
 # to `source_sha256` (otherwise the bench reports traffic = null).
 NCU_TRAFFIC = {
     "llama3_8b_decode": {
-        "bytes": 582099200 + 4126464,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "6b8deab0846328c0e8919c4af3b864d6966046e3658a4d3cbf8ac7a04b8ab0f4",
+        "bytes": 582041600 + 3893248,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "2bbfe27a24d736bd89dd5c032f59d535a0fb7dfc7dc1b5684ee8b63f1328fc51",
     },
     "llama3_70b_mix": {
-        "bytes": 1334956000 + 5754880,
-        "source_sha256": "6b8deab0846328c0e8919c4af3b864d6966046e3658a4d3cbf8ac7a04b8ab0f4",
+        "bytes": 1335182000 + 5641984,
+        "source_sha256": "2bbfe27a24d736bd89dd5c032f59d535a0fb7dfc7dc1b5684ee8b63f1328fc51",
     },
     "spec_verify": {
-        "bytes": 1417773000 + 5332224,
-        "source_sha256": "6b8deab0846328c0e8919c4af3b864d6966046e3658a4d3cbf8ac7a04b8ab0f4",
+        "bytes": 1417765000 + 5123840,
+        "source_sha256": "2bbfe27a24d736bd89dd5c032f59d535a0fb7dfc7dc1b5684ee8b63f1328fc51",
     },
     "llama3_8b_decode/fp8": {
-        "bytes": 291329536 + 3626496,
-        "source_sha256": "6b8deab0846328c0e8919c4af3b864d6966046e3658a4d3cbf8ac7a04b8ab0f4",
+        "bytes": 291325440 + 3963392,
+        "source_sha256": "2bbfe27a24d736bd89dd5c032f59d535a0fb7dfc7dc1b5684ee8b63f1328fc51",
+    },
+    "llama3_70b_mix/fp8": {
+        "bytes": 666704128 + 5379072,
+        "source_sha256": "2bbfe27a24d736bd89dd5c032f59d535a0fb7dfc7dc1b5684ee8b63f1328fc51",
     },
 }
 
