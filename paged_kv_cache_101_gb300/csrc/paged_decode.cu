@@ -1860,15 +1860,18 @@ __global__ void __launch_bounds__(kThreadsMax, 1)
 //   M = max_k m_k,  f_k = 2^(m_k - M),  L = sum_k l_k f_k,  out = sum_k f_k acc_k / L
 // ("07 -- Inference" section 5.3, m in the log2 domain). With M known first, the
 // acc loads of all pieces are independent and go out together. One CTA per
-// (sequence, head group, 32 rows): a warp takes 4 rows; lane k holds (m, l) of
-// piece k (32 pieces a round, rescaled across rounds), then lane i owns dims
-// 4i..4i+3 of every piece. Sequences with no token get zeros. Launched as a
-// programmatic dependent of the main kernel: it waits (griddepcontrol) for it.
-template <int D>
-__global__ void __launch_bounds__(256, 2)
+// (sequence, head group, 8 * RPW rows): a warp takes RPW rows; lane k holds
+// (m, l) of piece k (32 pieces a round, rescaled across rounds), then lane i owns
+// dims 4i..4i+3 of every piece, PB pieces per batch of acc loads. Sequences with
+// no token get zeros. Launched as a programmatic dependent of the main kernel: it
+// waits (griddepcontrol) for it. Its time after the main kernel is a chain of L2
+// round trips, so the registers are capped for three CTAs per SM (two rows per
+// warp and four pieces per batch for up to 32 rows per head group, more CTAs for
+// few rows; four rows per warp and two pieces per batch above, fewer CTAs).
+template <int D, int RPW, int PB>
+__global__ void __launch_bounds__(256, 3)
     paged_decode_merge_kernel(const DecodeParams p, int grid)
 {
-    constexpr int RPW = 4, PB = 4;  // rows per warp; pieces per batch of acc loads
     const unsigned FULL = 0xffffffffu;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int s = blockIdx.x, hg = blockIdx.y;
@@ -2175,18 +2178,23 @@ static cudaError_t launch_kernel(Kern kern, int *configured_smem, const DecodePl
         return e;
     if (!with_merge)
         return cudaSuccess;
-    // the merge: one CTA per (sequence, head group, 32 rows), a programmatic dependent
+    // the merge: one CTA per (sequence, head group, 8 * RPW rows), a programmatic dependent
+    const bool few_rows = p.HG * p.rows <= 32;
+    const int cta_rows = few_rows ? 16 : 32;
     cudaLaunchConfig_t mcfg = {};
-    mcfg.gridDim = dim3(unsigned(p.S), unsigned(p.n_hg), unsigned((p.HG * p.rows + 31) / 32));
+    mcfg.gridDim = dim3(unsigned(p.S), unsigned(p.n_hg),
+                        unsigned((p.HG * p.rows + cta_rows - 1) / cta_rows));
     mcfg.blockDim = dim3(256);
     mcfg.dynamicSmemBytes = 0;
     mcfg.stream = stream;
     mcfg.attrs = attr;
     mcfg.numAttrs = 1;
     if (pl.D == 64)
-        e = cudaLaunchKernelEx(&mcfg, paged_decode_merge_kernel<64>, p, int(pl.grid));
+        e = few_rows ? cudaLaunchKernelEx(&mcfg, paged_decode_merge_kernel<64, 2, 4>, p, int(pl.grid))
+                     : cudaLaunchKernelEx(&mcfg, paged_decode_merge_kernel<64, 4, 2>, p, int(pl.grid));
     else
-        e = cudaLaunchKernelEx(&mcfg, paged_decode_merge_kernel<128>, p, int(pl.grid));
+        e = few_rows ? cudaLaunchKernelEx(&mcfg, paged_decode_merge_kernel<128, 2, 4>, p, int(pl.grid))
+                     : cudaLaunchKernelEx(&mcfg, paged_decode_merge_kernel<128, 4, 2>, p, int(pl.grid));
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
