@@ -50,24 +50,24 @@ FALLBACK_HBM_GBS = 6800.0
 # to `source_sha256` (otherwise the bench reports traffic = null).
 NCU_TRAFFIC = {
     "llama3_8b_decode": {
-        "bytes": 582041600 + 3893248,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "2bbfe27a24d736bd89dd5c032f59d535a0fb7dfc7dc1b5684ee8b63f1328fc51",
+        "bytes": 582027520 + 3817216,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "f1c2de55ff8fee5ea6e6b73909f29201c570aa0e03794c4faf104daa0dd98ccd",
     },
     "llama3_70b_mix": {
-        "bytes": 1335182000 + 5641984,
-        "source_sha256": "2bbfe27a24d736bd89dd5c032f59d535a0fb7dfc7dc1b5684ee8b63f1328fc51",
+        "bytes": 1334794240 + 5472256,
+        "source_sha256": "f1c2de55ff8fee5ea6e6b73909f29201c570aa0e03794c4faf104daa0dd98ccd",
     },
     "spec_verify": {
-        "bytes": 1417765000 + 5123840,
-        "source_sha256": "2bbfe27a24d736bd89dd5c032f59d535a0fb7dfc7dc1b5684ee8b63f1328fc51",
+        "bytes": 1417699072 + 4819968,
+        "source_sha256": "f1c2de55ff8fee5ea6e6b73909f29201c570aa0e03794c4faf104daa0dd98ccd",
     },
     "llama3_8b_decode/fp8": {
-        "bytes": 291325440 + 3963392,
-        "source_sha256": "2bbfe27a24d736bd89dd5c032f59d535a0fb7dfc7dc1b5684ee8b63f1328fc51",
+        "bytes": 291320576 + 3384576,
+        "source_sha256": "f1c2de55ff8fee5ea6e6b73909f29201c570aa0e03794c4faf104daa0dd98ccd",
     },
     "llama3_70b_mix/fp8": {
-        "bytes": 666704128 + 5379072,
-        "source_sha256": "2bbfe27a24d736bd89dd5c032f59d535a0fb7dfc7dc1b5684ee8b63f1328fc51",
+        "bytes": 666779904 + 5601792,
+        "source_sha256": "f1c2de55ff8fee5ea6e6b73909f29201c570aa0e03794c4faf104daa0dd98ccd",
     },
 }
 
