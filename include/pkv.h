@@ -127,7 +127,7 @@ pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, int64_t num_blocks,
 /*
  * pkv_workspace_size -- bytes of device workspace pkv_paged_decode_attention
  * needs for this geometry on the CURRENT CUDA device (the size depends on its
- * SM count). n_query_per_seq may be up to 32 / (num_q_heads / num_kv_heads)
+ * SM count). n_query_per_seq may be up to 64 / (num_q_heads / num_kv_heads)
  * (the max_q_len of pkv_paged_decode_attention_varlen). Returns 0 if the geometry is unsupported or no device is usable.
  * The workspace holds the split-K partial states (m, l, acc) that the merge
  * step combines, per (sequence, kv-head group) the cells holding its first and
@@ -171,7 +171,7 @@ size_t pkv_workspace_size(int32_t num_seqs, int32_t n_query_per_seq, int32_t num
  *   context_lens   device, int32 [num_seqs]; a value above 16*max_blocks_per_seq
  *                  is clamped to it, a negative value counts as 0.
  *   n_query_per_seq 1..4; num_q_heads % num_kv_heads == 0;
- *                  (num_q_heads/num_kv_heads) * n_query_per_seq <= 32.
+ *                  (num_q_heads/num_kv_heads) * n_query_per_seq <= 64.
  *   head_dim       64 or 128.
  *   scale          usually 1/sqrt(head_dim).
  *   out            device, [num_seqs*n_query_per_seq][num_q_heads][head_dim] of
@@ -269,7 +269,7 @@ pkv_status pkv_paged_decode_attention_cascade(
  *   q_start         device int32 [num_seqs + 1], nondecreasing, q_start[num_seqs] <= total_q.
  *   tree_mask       device uint32 [total_q] or NULL; tree_len device int32
  *                   [num_seqs], given together with tree_mask.
- *   max_q_len       >= 1 with (num_q_heads/num_kv_heads) * max_q_len <= 32 (the
+ *   max_q_len       >= 1 with (num_q_heads/num_kv_heads) * max_q_len <= 64 (the
  *                   kernel's score rows per kv head; unlike the fixed-count call,
  *                   more than 4 is allowed); the workspace is
  *                   pkv_workspace_size(num_seqs, max_q_len, ...).
@@ -372,9 +372,10 @@ pkv_status pkv_paged_decode_attention_fp8(const void *q, const void *k_cache, co
  * the library's module holding it keeps until the process exits (with CUDA's
  * default lazy module loading: from this entry point's first call on that
  * GPU). A geometry whose scratch (pkv_workspace_size) exceeds 32 MiB returns
- * PKV_ERR_WORKSPACE before anything is enqueued; on a 152-SM GB300 every
- * supported geometry (up to 32 query rows per kv head) needs at most ~21 MiB
- * plus 8 bytes per (sequence, group of up to 8 kv heads).
+ * PKV_ERR_WORKSPACE before anything is enqueued; on a 152-SM GB300 a
+ * geometry with up to 32 query rows per kv head needs at most ~21 MiB plus 8
+ * bytes per (sequence, group of up to 8 kv heads), one with 33 to 64 rows up
+ * to ~42 MiB (those above 32 MiB take the workspace call).
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and keeps it; make that

@@ -198,7 +198,7 @@ cudaError_t pool_map(const void *base, int64_t nb, int Hkv, int D, int kind, int
 
 // Host-side checks shared by the workspace query and the attention calls. The
 // fixed-count call takes 1..4 queries per sequence; the variable-count call any
-// count whose score rows (G per query) fit the kernel's 32 rows per kv head.
+// count whose score rows (G per query) fit the kernel's 64 rows per kv head.
 pkv_status check_geometry(int32_t num_seqs, int32_t nq, int32_t Hq, int32_t Hkv, int32_t D,
                           bool varlen = false)
 {
@@ -474,7 +474,10 @@ pkv_status attention(const void *q, const void *k_cache, const void *v_cache, in
     if (device_info(&d) != cudaSuccess)
         return PKV_ERR_CUDA;
     // the CUDA-core consumers (PKV_OPT_MATH = 1) serve the plain bf16 call only
-    const int fma = (g_opt_math == 1 && !kv8 && !vl.q_start && !cc.groups && head_dim == 128) ? 1 : 0;
+    const int fma = (g_opt_math == 1 && !kv8 && !vl.q_start && !cc.groups && head_dim == 128 &&
+                     (num_q_heads / num_kv_heads) * n_query_per_seq <= 32)
+                        ? 1
+                        : 0;
     pkv::DecodePlan pl;
     if (pkv::plan_decode(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim,
                          max_blocks_per_seq, d.num_sms, g_opt_num_ctas, g_opt_stages,

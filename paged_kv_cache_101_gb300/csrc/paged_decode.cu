@@ -25,14 +25,14 @@
 //    tensor loads of K and V for its HG heads into a ring of shared-memory
 //    stages (128-byte swizzle, mbarrier completion with byte counts). Stages are
 //    recycled through "empty" mbarriers the consumers arrive on.
-//  * Math. One or two consumer warps per kv head, bf16 mma.sync m16n8k16 with
+//  * Math. One, two or four consumer warps per kv head, bf16 mma.sync m16n8k16 with
 //    fp32 accumulation, two orientations chosen by the query rows per kv head:
 //    - up to 8 rows (one warp per head): S^T = K.Q^T with M = the block's 16
 //      tokens, N = 8 rows, K = 16 head dims, so no mma work goes to padding
 //      rows. The online softmax runs on the fragments (shuffles across the 8
 //      token lanes); P is transposed in registers with movmatrix and
 //      O^T += V^T.P^T takes V^T fragments from ldmatrix.trans.
-//    - 9 to 32 rows (16 rows per warp): S = Q.K^T with M = 16 rows, N = 8
+//    - 9 to 64 rows (16 rows per warp): S = Q.K^T with M = 16 rows, N = 8
 //      tokens, so the score fragments are the A operand of O += P.V as they
 //      stand (no transposes), row reductions take two shuffles and outputs
 //      leave as pairs.
@@ -2039,12 +2039,13 @@ int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int 
         P.ntw = 0;
         P.rows_pad = P.wph * P.rw;
     } else {
+        // up to 16 rows: one warp per kv head; above, 16-row warps (2 or 4 per head)
         const int nt_total = (P.rows + 7) / 8;
         if (nt_total <= 2) {
             P.wph = 1;
             P.ntw = nt_total;
         } else {
-            P.wph = 2;
+            P.wph = nt_total <= 4 ? 2 : 4;
             P.ntw = 2;
         }
         P.rows_pad = P.wph * P.ntw * 8;
@@ -2237,6 +2238,8 @@ cudaError_t launch_decode(const DecodePlan &pl, const DecodeParams &p, const CUt
     if (pl.kv8) {  // E4M3 pools: D = 128 only
         if (pl.ctas_per_sm == 2)
             return launch_one<128, 1, 1, true, 2>(pl, p, kmap, vmap, stream, eb, ea);
+        if (pl.wph == 4)
+            return launch_one<128, 2, 4, true>(pl, p, kmap, vmap, stream, eb, ea);
         if (pl.wph == 2)
             return launch_one<128, 2, 2, true>(pl, p, kmap, vmap, stream, eb, ea);
         if (pl.ntw == 2)
@@ -2244,12 +2247,16 @@ cudaError_t launch_decode(const DecodePlan &pl, const DecodeParams &p, const CUt
         return launch_one<128, 1, 1, true>(pl, p, kmap, vmap, stream, eb, ea);
     }
     if (pl.D == 64) {
+        if (pl.wph == 4)
+            return launch_one<64, 2, 4, false>(pl, p, kmap, vmap, stream, eb, ea);
         if (pl.wph == 2)
             return launch_one<64, 2, 2, false>(pl, p, kmap, vmap, stream, eb, ea);
         if (pl.ntw == 2)
             return launch_one<64, 2, 1, false>(pl, p, kmap, vmap, stream, eb, ea);
         return launch_one<64, 1, 1, false>(pl, p, kmap, vmap, stream, eb, ea);
     }
+    if (pl.wph == 4)
+        return launch_one<128, 2, 4, false>(pl, p, kmap, vmap, stream, eb, ea);
     if (pl.wph == 2)
         return launch_one<128, 2, 2, false>(pl, p, kmap, vmap, stream, eb, ea);
     if (pl.ntw == 2)

@@ -10,7 +10,7 @@ namespace pkv {
 
 constexpr int kBlockSize = 16;          // tokens per physical block
 constexpr int kTileBytes = 16 * 128;    // one (head, 64-column half) tile: 16 rows x 128 B
-constexpr int kMaxRows = 32;            // query rows per kv head: G * n_query_per_seq
+constexpr int kMaxRows = 64;            // query rows per kv head: G * n_query_per_seq
 constexpr int kMaxConsumerWarps = 8;
 // warp 0 produces, warps 1..ncw consume
 constexpr int kThreadsMax = 32 * (1 + kMaxConsumerWarps);

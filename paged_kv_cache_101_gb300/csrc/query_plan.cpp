@@ -1,7 +1,7 @@
 // query_plan.cpp -- host-side split of long query runs into virtual sequences
 // for pkv_paged_decode_attention_varlen (see include/pkv.h).
 //
-// The attention kernel holds at most 32 score rows per kv head (G * q_len), so a
+// The attention kernel holds at most 64 score rows per kv head (G * q_len), so a
 // prefill chunk or a large candidate tree is cut into runs of at most max_rows
 // query rows. A causal run keeps its rows' causal limits by ending its context
 // where its last row sits ("07 -- Inference" section 2.4: chunked prefill gives

@@ -134,8 +134,9 @@ def test_attention_validation(lib):
     assert attn(lib, nq=5) == UNSUP
     assert attn(lib, d=96) == UNSUP
     assert attn(lib, d=256) == UNSUP
-    assert attn(lib, hq=64, hkv=1, nq=1) == UNSUP       # 64 query rows per kv head
-    assert attn(lib, hq=32, hkv=2, nq=4) == UNSUP       # 16*4 = 64 rows per kv head
+    assert attn(lib, hq=80, hkv=1, nq=1) == UNSUP       # 80 query rows per kv head (max 64)
+    assert attn(lib, hq=32, hkv=1, nq=3) == UNSUP       # 96
+    assert attn(lib, hq=68, hkv=4, nq=4) == UNSUP       # 17*4 = 68 rows per kv head
     assert attn(lib, dt=2) == DTYPE
     assert attn(lib, q=A + 8) == ALIGN
     assert attn(lib, out=A + 4) == ALIGN

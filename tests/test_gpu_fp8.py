@@ -117,7 +117,8 @@ def test_append_fp8_bit_exact(o, hkv, d):
 
 # ------------------------------------------------------------------ attention
 @pytest.mark.parametrize("hq,hkv,nq", [(8, 2, 1), (32, 8, 1), (64, 8, 1), (16, 8, 1),
-                                       (16, 4, 3), (32, 8, 4), (64, 8, 4), (8, 8, 2)])
+                                       (16, 4, 3), (32, 8, 4), (64, 8, 4), (8, 8, 2),
+                                       (64, 4, 4), (48, 4, 3)])
 def test_attention_fp8_geometries(o, hq, hkv, nq):
     lens = [nq + i for i in range(0, 96, 7)] + [16, 17, 31, 32, 33, 200, 513]
     w = W.make_custom(len(lens), nq, hq, hkv, 128, lens, seed=hq * 10 + nq)

@@ -2,7 +2,7 @@
 
 Each case draws a geometry and a set of options that no single targeted test
 combines:
-- head_dim 64 or 128; 1 to 32 query rows per kv head (G x nq); 1 to 12 sequences;
+- head_dim 64 or 128; 1 to 64 query rows per kv head (G x nq); 1 to 12 sequences;
 - lengths from nq to 3,000 tokens, sometimes a shared prefix;
 - persistent grid size, pipeline depth, heads per CTA, TMA box mode, dynamic
   tail, pacing, CUDA-core consumers; bf16 or fp32 output.
@@ -49,7 +49,7 @@ def draw_case(seed):
     while True:
         G = int(rng.choice([1, 2, 3, 4, 5, 8, 16]))
         nq = int(rng.integers(1, 5))
-        if G * nq <= 32:
+        if G * nq <= 64:
             break
     S = int(rng.integers(1, 13))
     T = np.where(rng.random(S) < 0.5, rng.integers(nq, 65, S), rng.integers(nq, 3001, S))

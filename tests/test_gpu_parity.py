@@ -109,7 +109,8 @@ def test_tiny_full(o):
 
 @pytest.mark.parametrize("G,nq,D", [(1, 1, 64), (4, 1, 128), (8, 1, 128), (2, 4, 64),
                                     (4, 4, 128), (8, 4, 128), (8, 2, 64), (3, 3, 128),
-                                    (16, 2, 128), (32, 1, 64), (5, 1, 128)])
+                                    (16, 2, 128), (32, 1, 64), (5, 1, 128),
+                                    (16, 4, 128), (12, 3, 64), (64, 1, 128), (11, 4, 128)])
 def test_gqa_nq_dims(o, G, nq, D):
     Hkv = 2
     T = [nq, nq + 1, 15, 16, 17, 31, 32, 33, 100, 257]

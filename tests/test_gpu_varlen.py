@@ -2,7 +2,8 @@
 pkv_paged_decode_attention_varlen, against the oracle's unsplit definition.
 
 - causal query counts 0..4 per sequence (every length mod 16), for 1, 4 and 8
-  query heads per kv head, bf16 and fp32 outputs;
+  query heads per kv head, and up to 16 (4 heads) or 8 (8 heads) queries: 64 score
+  rows per kv head; bf16 and fp32 outputs;
 - tree masks: the 15-node binary tree of "Chapter 18" section 18.1.2 with 8
   query heads per kv head (120 score rows, split into runs of 4 queries that
   share the sequence's table row), and random trees;
@@ -57,12 +58,13 @@ def run_varlen(w_full_k, w_full_v, tables, cl, qs, q, scale, max_q, tree_mask=No
     return out
 
 
-@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 4), (32, 4)])
+@pytest.mark.parametrize("hq,hkv,mq", [(8, 8, 4), (16, 4, 4), (32, 4, 4), (16, 4, 16),
+                                       (16, 2, 8)])
 @pytest.mark.parametrize("out32", [False, True])
-def test_varlen_causal(o, hq, hkv, out32):
-    rng = np.random.default_rng(hq + out32)
+def test_varlen_causal(o, hq, hkv, mq, out32):
+    rng = np.random.default_rng(hq + out32 + mq)
     G = hq // hkv
-    max_q = min(4, 32 // G)
+    max_q = min(mq, 64 // G)
     S = 48
     qlen = rng.integers(0, max_q + 1, size=S)
     T = np.array([int(n) + i for i, n in enumerate(qlen)], np.int32)    # every length mod 16
@@ -100,10 +102,13 @@ def random_tree(rng, n):
     return masks
 
 
-@pytest.mark.parametrize("kind", ["binary15", "random"])
-def test_tree_masks_split_into_runs(o, kind):
+@pytest.mark.parametrize("kind,hq,run", [("binary15", 64, 4), ("random", 64, 4),
+                                         ("binary15", 32, 16), ("random", 32, 16)])
+def test_tree_masks_split_into_runs(o, kind, hq, run):
+    """8 query heads per kv head in runs of 4 queries (32 rows), and 4 heads in runs
+    of 16 (64 rows: a 15-node tree in one run)."""
     rng = np.random.default_rng(7 if kind == "random" else 8)
-    hq, hkv = 64, 8                                   # 8 query heads per kv head
+    hkv = 8
     if kind == "binary15":
         trees = [binary_tree(4)] * 6
     else:
@@ -118,11 +123,11 @@ def test_tree_masks_split_into_runs(o, kind):
     tl = np.array(nodes, np.int32)
     ref = o.paged_attention_varlen(q, w.k_full, w.v_full, w.block_tables, T, qs, w.scale,
                                    tree_mask=masks, tree_len=tl)
-    r = pkv.split_queries(qs, T, 4, tree_len=tl)       # 4 queries x 8 heads = 32 rows
+    r = pkv.split_queries(qs, T, run, tree_len=tl)
     out = run_varlen(w.k_full, w.v_full, w.block_tables, r["context_lens"], r["q_start"], q,
-                     w.scale, 4, tree_mask=masks, tree_len=r["tree_len"],
+                     w.scale, run, tree_mask=masks, tree_len=r["tree_len"],
                      table_row=r["table_row"])
-    compare(to_f64(out), ref, what=kind)
+    compare(to_f64(out), ref, what=f"{kind}, runs of {run}")
     assert pkv.workspace_error(pkv.workspace(out.device, 0)) == 0
 
 

@@ -116,11 +116,11 @@ def test_varlen_host_validation(lib):
     assert varlen(lib, ntr=2) == SHAPE                   # fewer table rows than sequences
     assert varlen(lib, tq=-1) == SHAPE
     assert varlen(lib, qs=A + 2) == ALIGN
-    assert varlen(lib, mq=9) == 8                        # 4 x 9 = 36 score rows per kv head
-    assert varlen(lib, hq=32, hkv=2, mq=4) == 8          # 64 rows per kv head
-    # the geometry check (before any device query): 8 queries x 4 heads = 32 rows
-    assert lib.pkv_workspace_size(0, 8, 8, 2, 64) == 256
-    assert lib.pkv_workspace_size(0, 9, 8, 2, 64) == 0
+    assert varlen(lib, mq=17) == 8                       # 4 x 17 = 68 score rows per kv head
+    assert varlen(lib, hq=32, hkv=2, mq=5) == 8          # 80 rows per kv head
+    # the geometry check (before any device query): 16 queries x 4 heads = 64 rows
+    assert lib.pkv_workspace_size(0, 16, 8, 2, 64) == 256
+    assert lib.pkv_workspace_size(0, 17, 8, 2, 64) == 0
 
 
 def cascade(lib, groups=A, ng=2, mg=8, S=4, nq=1, hq=8, hkv=2, d=64, ws=A):
