@@ -446,6 +446,40 @@ pkv_status pkv_decode_step_host(const void *host_arena, void *device_arena, size
                                 void *out_device, void *out_host, int32_t out_dtype,
                                 void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * pkv_decode_step_host_pipelined -- pkv_decode_step_host with its phases on
+ * three streams, so that in a loop over steps the copies of a step run while
+ * the kernels of its neighbours stream the pool (the copy engines move host
+ * memory while the SMs read HBM). A buffer slot is (host_arena, device_arena,
+ * out_device, out_host) with three events of its own (cudaEvent_t, e.g. created
+ * with cudaEventDisableTiming; an event never recorded is no wait):
+ *   upload_stream:   waits `computed` (the slot's previous step has read its
+ *                    device arena), copies host_arena -> device_arena, records
+ *                    `uploaded`;
+ *   compute_stream:  waits `uploaded` and `downloaded` (the slot's previous
+ *                    output has left out_device), runs pkv_kv_append and
+ *                    pkv_paged_decode_attention as pkv_decode_step_host does,
+ *                    records `computed`;
+ *   download_stream: waits `computed`, copies out_device -> out_host, records
+ *                    `downloaded`.
+ * With two slots used in turn, step n+1's upload and step n-1's download
+ * overlap step n's kernels, and the kernels of consecutive steps stay in order
+ * on compute_stream (one workspace serves them all). The three streams may be
+ * the same stream (then it is pkv_decode_step_host). out_host is valid once
+ * `downloaded` has completed. With k_scale and v_scale (device float [Hkv]) the
+ * pools are E4M3 and the step calls pkv_kv_append_fp8 and
+ * pkv_paged_decode_attention_fp8 (head_dim 128); both NULL: bf16 pools.
+ * Arguments and errors otherwise as pkv_decode_step_host; PKV_ERR_NULL for a
+ * missing event or only one scale.
+ */
+pkv_status pkv_decode_step_host_pipelined(
+    const void *host_arena, void *device_arena, size_t arena_bytes, void *k_cache, void *v_cache,
+    int64_t num_blocks, int32_t max_blocks_per_seq, int32_t num_seqs, int32_t n_query_per_seq,
+    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, float scale, void *out_device,
+    void *out_host, int32_t out_dtype, void *workspace, size_t workspace_bytes,
+    const float *k_scale, const float *v_scale, void *upload_stream, void *compute_stream,
+    void *download_stream, void *uploaded, void *computed, void *downloaded);
+
 /* Text for a status code (static storage; never NULL). */
 const char *pkv_status_string(int32_t status);
 

@@ -42,6 +42,9 @@ SIGNATURES = {
     "pkv_step_arena_layout": ([_I32, _I32, _I32, _I32, _I32, _I32, _P], _SZ),
     "pkv_decode_step_host": ([_P, _P, _SZ, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _F,
                               _P, _P, _I32, _P, _SZ, _P], ctypes.c_int),
+    "pkv_decode_step_host_pipelined": ([_P, _P, _SZ, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32,
+                                        _I32, _F, _P, _P, _I32, _P, _SZ, _P, _P, _P, _P, _P, _P,
+                                        _P, _P], ctypes.c_int),
     "pkv_status_string": ([_I32], ctypes.c_char_p),
     "pkv_set_option": ([_I32, _I32], _I32),
     "pkv_version": ([], _I32),
@@ -591,14 +594,30 @@ def step_arena_layout(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head
 
 
 def decode_step_host(host_arena, device_arena, k_cache, v_cache, num_seqs, n_query_per_seq,
-                     num_q_heads, max_blocks_per_seq, scale, out_device, out_host, ws=None):
+                     num_q_heads, max_blocks_per_seq, scale, out_device, out_host, ws=None,
+                     streams=None, events=None, k_scale=None, v_scale=None):
     """One decode step from host memory (``pkv_decode_step_host``): one copy of the
     packed inputs to ``device_arena``, the KV append, the attention into
     ``out_device``, one copy of the output to ``out_host``; asynchronous on the
-    current stream. ``host_arena``/``out_host`` are (pinned) CPU tensors."""
+    current stream. ``host_arena``/``out_host`` are (pinned) CPU tensors.
+
+    With ``streams = (upload, compute, download)`` (torch CUDA streams) and
+    ``events = (uploaded, computed, downloaded)`` (torch CUDA events of this
+    buffer slot), it calls ``pkv_decode_step_host_pipelined`` instead: the copies
+    and the kernels go on their own streams, ordered by the slot's events, so a
+    loop that alternates two slots overlaps copies with kernels. Events that were
+    never recorded are recorded once on the compute stream first (torch creates
+    them lazily). ``k_scale``/``v_scale`` (float32 ``[Hkv]``) mark E4M3 (uint8)
+    pools; they need the pipelined form."""
     torch = _torch()
-    _check(k_cache, "k_cache", torch.bfloat16, 4)
-    _check(v_cache, "v_cache", torch.bfloat16, 4)
+    fp8 = k_scale is not None or v_scale is not None
+    if fp8:
+        if streams is None:
+            raise ValueError("E4M3 pools (k_scale/v_scale) take the pipelined form: pass streams")
+        _check_fp8_pools(k_cache, v_cache, k_scale, v_scale)
+    else:
+        _check(k_cache, "k_cache", torch.bfloat16, 4)
+        _check(v_cache, "v_cache", torch.bfloat16, 4)
     if host_arena.device.type != "cpu" or out_host.device.type != "cpu":
         raise ValueError("host_arena and out_host must be host tensors")
     if device_arena.device.type != "cuda" or not device_arena.is_contiguous():
@@ -617,12 +636,27 @@ def decode_step_host(host_arena, device_arena, k_cache, v_cache, num_seqs, n_que
     if ws is None:
         ws = workspace(k_cache.device, workspace_size(num_seqs, n_query_per_seq, num_q_heads,
                                                       Hkv, D))
-    st = lib().pkv_decode_step_host(
+    odt = PKV_FP32 if out_device.dtype == torch.float32 else PKV_BF16
+    if streams is None:
+        st = lib().pkv_decode_step_host(
+            host_arena.data_ptr(), device_arena.data_ptr(), nbytes, k_cache.data_ptr(),
+            v_cache.data_ptr(), NB, max_blocks_per_seq, num_seqs, n_query_per_seq, num_q_heads,
+            Hkv, D, float(scale), out_device.data_ptr(), out_host.data_ptr(), odt, ws.data_ptr(),
+            ws.numel(), _stream_handle(k_cache.device))
+        if st != PKV_OK:
+            raise PkvError("pkv_decode_step_host", st)
+        return out_host
+    if events is None or len(streams) != 3 or len(events) != 3:
+        raise ValueError("streams and events: three of each (upload, compute, download)")
+    for ev in events:
+        if not ev.cuda_event:
+            ev.record(streams[1])
+    st = lib().pkv_decode_step_host_pipelined(
         host_arena.data_ptr(), device_arena.data_ptr(), nbytes, k_cache.data_ptr(),
         v_cache.data_ptr(), NB, max_blocks_per_seq, num_seqs, n_query_per_seq, num_q_heads, Hkv,
-        D, float(scale), out_device.data_ptr(), out_host.data_ptr(),
-        PKV_FP32 if out_device.dtype == torch.float32 else PKV_BF16, ws.data_ptr(), ws.numel(),
-        _stream_handle(k_cache.device))
+        D, float(scale), out_device.data_ptr(), out_host.data_ptr(), odt, ws.data_ptr(),
+        ws.numel(), k_scale.data_ptr() if fp8 else None, v_scale.data_ptr() if fp8 else None,
+        *[s.cuda_stream for s in streams], *[ev.cuda_event for ev in events])
     if st != PKV_OK:
-        raise PkvError("pkv_decode_step_host", st)
+        raise PkvError("pkv_decode_step_host_pipelined", st)
     return out_host

@@ -1,7 +1,9 @@
 // host_step.cu -- one decode step from host memory through the C ABI: one
 // host-to-device copy of the step's inputs (packed in one arena), the KV append
 // and the attention on views of the device arena, one device-to-host copy of
-// the output.
+// the output. The pipelined form puts the two copies and the kernels on three
+// streams, ordered by the caller's events, so that a loop over steps overlaps
+// each step's copies with its neighbours' kernels.
 #include <cuda_runtime.h>
 
 #include <stdint.h>
@@ -17,7 +19,7 @@ bool input_sizes(int32_t S, int32_t nq, int32_t Hq, int32_t Hkv, int32_t D, int3
                  size_t sz[6])
 {
     if (S < 0 || nq < 1 || nq > 4 || Hkv < 1 || Hq < 1 || Hq % Hkv != 0 ||
-        (D != 64 && D != 128) || MB < 1 || (Hq / Hkv) * nq > 32 || S > (1 << 24) ||
+        (D != 64 && D != 128) || MB < 1 || (Hq / Hkv) * nq > 64 || S > (1 << 24) ||
         MB > (1 << 26))
         return false;
     const size_t rows = size_t(S) * size_t(nq);
@@ -51,37 +53,45 @@ size_t pkv_step_arena_layout(int32_t num_seqs, int32_t n_query_per_seq, int32_t 
     return off;
 }
 
-pkv_status pkv_decode_step_host(const void *host_arena, void *device_arena, size_t arena_bytes,
-                                void *k_cache, void *v_cache, int64_t num_blocks,
-                                int32_t max_blocks_per_seq, int32_t num_seqs,
-                                int32_t n_query_per_seq, int32_t num_q_heads,
-                                int32_t num_kv_heads, int32_t head_dim, float scale,
-                                void *out_device, void *out_host, int32_t out_dtype,
-                                void *workspace, size_t workspace_bytes, void *stream)
+}  // extern "C"
+
+namespace {
+
+// A validated step: the arena offsets and the output's bytes.
+struct StepPlan {
+    size_t off[6];
+    size_t need, out_bytes;
+    int64_t n_new;
+};
+
+// The checks of both calls that do not depend on device data, so that a refused
+// step enqueues nothing.
+pkv_status plan_step(const void *host_arena, const void *device_arena, size_t arena_bytes,
+                     const void *k_cache, const void *v_cache, int64_t num_blocks,
+                     int32_t max_blocks_per_seq, int32_t num_seqs, int32_t n_query_per_seq,
+                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                     const void *out_device, const void *out_host, int32_t out_dtype,
+                     const void *workspace, size_t workspace_bytes, StepPlan *sp)
 {
-    size_t sz[6], off[6];
+    size_t sz[6];
     if (!input_sizes(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim,
                      max_blocks_per_seq, sz))
         return num_seqs < 0 || max_blocks_per_seq < 1 ? PKV_ERR_SHAPE : PKV_ERR_UNSUPPORTED;
     if (num_seqs == 0)
         return PKV_OK;
-    const size_t need = pkv_step_arena_layout(num_seqs, n_query_per_seq, num_q_heads,
-                                              num_kv_heads, head_dim, max_blocks_per_seq, off);
+    sp->need = pkv_step_arena_layout(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads,
+                                     head_dim, max_blocks_per_seq, sp->off);
     if (!host_arena || !device_arena || !out_host)
         return PKV_ERR_NULL;
-    if (arena_bytes < need)
+    if (arena_bytes < sp->need)
         return PKV_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(device_arena) % 256 != 0)
         return PKV_ERR_ALIGN;
     if (out_dtype != PKV_BF16 && out_dtype != PKV_FP32)
         return PKV_ERR_DTYPE;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const uint8_t *d = static_cast<const uint8_t *>(device_arena);
-    const int64_t n_new = int64_t(num_seqs) * n_query_per_seq;
-    const size_t out_bytes = size_t(n_new) * size_t(num_q_heads) * size_t(head_dim) *
-                             (out_dtype == PKV_FP32 ? 4 : 2);
-
-    // the device-side checks of both calls first, so a refused step enqueues nothing
+    sp->n_new = int64_t(num_seqs) * n_query_per_seq;
+    sp->out_bytes = size_t(sp->n_new) * size_t(num_q_heads) * size_t(head_dim) *
+                    (out_dtype == PKV_FP32 ? 4 : 2);
     if (!out_device || !k_cache || !v_cache)
         return PKV_ERR_NULL;
     if (num_blocks < 1)
@@ -91,25 +101,128 @@ pkv_status pkv_decode_step_host(const void *host_arena, void *device_arena, size
     if (workspace_bytes < pkv_workspace_size(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads,
                                              head_dim))
         return PKV_ERR_WORKSPACE;
+    return PKV_OK;
+}
 
-    if (cudaMemcpyAsync(device_arena, host_arena, need, cudaMemcpyHostToDevice, st) !=
+// Steps 2 and 3 on `stream`: the append and the attention on the arena's views
+// (E4M3 pools when both scales are given).
+pkv_status compute_step(const StepPlan &sp, const void *device_arena, void *k_cache,
+                        void *v_cache, int64_t num_blocks, int32_t max_blocks_per_seq,
+                        int32_t num_seqs, int32_t n_query_per_seq, int32_t num_q_heads,
+                        int32_t num_kv_heads, int32_t head_dim, float scale, void *out_device,
+                        int32_t out_dtype, void *workspace, size_t workspace_bytes,
+                        const float *k_scale, const float *v_scale, void *stream)
+{
+    const uint8_t *d = static_cast<const uint8_t *>(device_arena);
+    if (k_scale && v_scale) {
+        pkv_status s = pkv_kv_append_fp8(d + sp.off[1], d + sp.off[2],
+                                         reinterpret_cast<const int64_t *>(d + sp.off[3]),
+                                         sp.n_new, k_cache, v_cache, num_blocks, num_kv_heads,
+                                         head_dim, k_scale, v_scale, stream);
+        if (s != PKV_OK)
+            return s;
+        return pkv_paged_decode_attention_fp8(
+            d + sp.off[0], k_cache, v_cache, num_blocks, k_scale, v_scale,
+            reinterpret_cast<const int32_t *>(d + sp.off[4]), max_blocks_per_seq,
+            reinterpret_cast<const int32_t *>(d + sp.off[5]), num_seqs, n_query_per_seq,
+            num_q_heads, num_kv_heads, head_dim, scale, out_device, out_dtype, workspace,
+            workspace_bytes, stream);
+    }
+    pkv_status s = pkv_kv_append(d + sp.off[1], d + sp.off[2],
+                                 reinterpret_cast<const int64_t *>(d + sp.off[3]), sp.n_new,
+                                 k_cache, v_cache, num_blocks, num_kv_heads, head_dim, stream);
+    if (s != PKV_OK)
+        return s;
+    return pkv_paged_decode_attention(d + sp.off[0], k_cache, v_cache, num_blocks,
+                                      reinterpret_cast<const int32_t *>(d + sp.off[4]),
+                                      max_blocks_per_seq,
+                                      reinterpret_cast<const int32_t *>(d + sp.off[5]), num_seqs,
+                                      n_query_per_seq, num_q_heads, num_kv_heads, head_dim, scale,
+                                      out_device, out_dtype, workspace, workspace_bytes, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_decode_step_host(const void *host_arena, void *device_arena, size_t arena_bytes,
+                                void *k_cache, void *v_cache, int64_t num_blocks,
+                                int32_t max_blocks_per_seq, int32_t num_seqs,
+                                int32_t n_query_per_seq, int32_t num_q_heads,
+                                int32_t num_kv_heads, int32_t head_dim, float scale,
+                                void *out_device, void *out_host, int32_t out_dtype,
+                                void *workspace, size_t workspace_bytes, void *stream)
+{
+    StepPlan sp;
+    pkv_status s = plan_step(host_arena, device_arena, arena_bytes, k_cache, v_cache, num_blocks,
+                             max_blocks_per_seq, num_seqs, n_query_per_seq, num_q_heads,
+                             num_kv_heads, head_dim, out_device, out_host, out_dtype, workspace,
+                             workspace_bytes, &sp);
+    if (s != PKV_OK || num_seqs == 0)
+        return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(device_arena, host_arena, sp.need, cudaMemcpyHostToDevice, st) !=
         cudaSuccess)
         return PKV_ERR_CUDA;
-    pkv_status s = pkv_kv_append(d + off[1], d + off[2], reinterpret_cast<const int64_t *>(d + off[3]),
-                                 n_new, k_cache, v_cache, num_blocks, num_kv_heads, head_dim,
-                                 stream);
+    s = compute_step(sp, device_arena, k_cache, v_cache, num_blocks, max_blocks_per_seq, num_seqs,
+                     n_query_per_seq, num_q_heads, num_kv_heads, head_dim, scale, out_device,
+                     out_dtype, workspace, workspace_bytes, nullptr, nullptr, stream);
     if (s != PKV_OK)
         return s;
-    s = pkv_paged_decode_attention(d + off[0], k_cache, v_cache, num_blocks,
-                                   reinterpret_cast<const int32_t *>(d + off[4]),
-                                   max_blocks_per_seq,
-                                   reinterpret_cast<const int32_t *>(d + off[5]), num_seqs,
-                                   n_query_per_seq, num_q_heads, num_kv_heads, head_dim, scale,
-                                   out_device, out_dtype, workspace, workspace_bytes, stream);
-    if (s != PKV_OK)
-        return s;
-    if (cudaMemcpyAsync(out_host, out_device, out_bytes, cudaMemcpyDeviceToHost, st) !=
+    if (cudaMemcpyAsync(out_host, out_device, sp.out_bytes, cudaMemcpyDeviceToHost, st) !=
         cudaSuccess)
+        return PKV_ERR_CUDA;
+    return PKV_OK;
+}
+
+pkv_status pkv_decode_step_host_pipelined(
+    const void *host_arena, void *device_arena, size_t arena_bytes, void *k_cache, void *v_cache,
+    int64_t num_blocks, int32_t max_blocks_per_seq, int32_t num_seqs, int32_t n_query_per_seq,
+    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, float scale, void *out_device,
+    void *out_host, int32_t out_dtype, void *workspace, size_t workspace_bytes,
+    const float *k_scale, const float *v_scale, void *upload_stream, void *compute_stream,
+    void *download_stream, void *uploaded, void *computed, void *downloaded)
+{
+    StepPlan sp;
+    pkv_status s = plan_step(host_arena, device_arena, arena_bytes, k_cache, v_cache, num_blocks,
+                             max_blocks_per_seq, num_seqs, n_query_per_seq, num_q_heads,
+                             num_kv_heads, head_dim, out_device, out_host, out_dtype, workspace,
+                             workspace_bytes, &sp);
+    if (s != PKV_OK || num_seqs == 0)
+        return s;
+    if (!uploaded || !computed || !downloaded || (!k_scale) != (!v_scale))
+        return PKV_ERR_NULL;
+    if (k_scale && head_dim != 128)
+        return PKV_ERR_UNSUPPORTED;  // E4M3 rows are one 128-byte row
+    cudaStream_t up = static_cast<cudaStream_t>(upload_stream);
+    cudaStream_t comp = static_cast<cudaStream_t>(compute_stream);
+    cudaStream_t down = static_cast<cudaStream_t>(download_stream);
+    cudaEvent_t e_up = static_cast<cudaEvent_t>(uploaded);
+    cudaEvent_t e_comp = static_cast<cudaEvent_t>(computed);
+    cudaEvent_t e_down = static_cast<cudaEvent_t>(downloaded);
+    // 1. upload, once this slot's previous step has read its device arena
+    if (cudaStreamWaitEvent(up, e_comp, 0) != cudaSuccess ||
+        cudaMemcpyAsync(device_arena, host_arena, sp.need, cudaMemcpyHostToDevice, up) !=
+            cudaSuccess ||
+        cudaEventRecord(e_up, up) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    // 2-3. append and attention, after the upload and after this slot's previous
+    // output has left out_device
+    if (cudaStreamWaitEvent(comp, e_up, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(comp, e_down, 0) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    s = compute_step(sp, device_arena, k_cache, v_cache, num_blocks, max_blocks_per_seq, num_seqs,
+                     n_query_per_seq, num_q_heads, num_kv_heads, head_dim, scale, out_device,
+                     out_dtype, workspace, workspace_bytes, k_scale, v_scale, compute_stream);
+    if (s != PKV_OK)
+        return s;
+    if (cudaEventRecord(e_comp, comp) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    // 4. download
+    if (cudaStreamWaitEvent(down, e_comp, 0) != cudaSuccess ||
+        cudaMemcpyAsync(out_host, out_device, sp.out_bytes, cudaMemcpyDeviceToHost, down) !=
+            cudaSuccess ||
+        cudaEventRecord(e_down, down) != cudaSuccess)
         return PKV_ERR_CUDA;
     return PKV_OK;
 }

@@ -207,6 +207,33 @@ def test_decode_step_host_validation(lib):
     assert step_host(lib, ws=None) == WORKSPACE
 
 
+def step_piped(lib, ev=A, S=4, ha=A, nq=1, **kw):
+    args = dict(ha=ha, da=A, nbytes=1 << 20, k=A, v=A, nb=64, mb=8, S=S, nq=nq, hq=8, hkv=2, d=64,
+                od=A, oh=A, dt=0, ws=A, wsb=1 << 30)
+    args.update(kw)
+    a = args
+    return lib.pkv_decode_step_host_pipelined(
+        a["ha"], a["da"], a["nbytes"], a["k"], a["v"], a["nb"], a["mb"], a["S"], a["nq"], a["hq"],
+        a["hkv"], a["d"], 0.125, a["od"], a["oh"], a["dt"], a["ws"], a["wsb"], a.get("ks"),
+        a.get("vs"), None, None, None, ev, ev, ev)
+
+
+def test_decode_step_host_pipelined_validation(lib):
+    """The pipelined step makes the same checks before anything is enqueued, and
+    needs its three events."""
+    assert step_piped(lib, S=0) == OK
+    assert step_piped(lib, S=-1) == SHAPE
+    assert step_piped(lib, nq=5) == UNSUP
+    assert step_piped(lib, ha=None) == NULL
+    assert step_piped(lib, ev=None) == NULL
+    assert step_piped(lib, nbytes=1024) == WORKSPACE
+    assert step_piped(lib, da=A + 16) == ALIGN
+    assert step_piped(lib, dt=2) == DTYPE
+    assert step_piped(lib, ws=None) == WORKSPACE
+    assert step_piped(lib, ks=A) == NULL                # one scale without the other
+    assert step_piped(lib, ks=A, vs=A) == UNSUP         # E4M3 pools need head_dim 128
+
+
 def test_workspace_size_rejects_bad_geometry(lib):
     assert lib.pkv_workspace_size(4, 5, 8, 2, 64) == 0
     assert lib.pkv_workspace_size(4, 1, 8, 3, 64) == 0

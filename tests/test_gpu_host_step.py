@@ -1,6 +1,8 @@
 """pkv_decode_step_host: one decode step from a pinned host arena (one copy in,
 append, attention, one copy out) gives bit for bit the pool and the output of
-the device calls it wraps, and the oracle's result within the tolerance."""
+the device calls it wraps, and the oracle's result within the tolerance. Its
+pipelined form (copies and kernels on three streams, two buffer slots in turn)
+gives every step the same bits as the serial one."""
 import numpy as np
 import pytest
 
@@ -63,3 +65,63 @@ def test_host_step_rejects_a_short_arena():
     with pytest.raises(pkv.PkvError):
         pkv.decode_step_host(host, dev_arena, d.k_cache, d.v_cache, w.num_seqs, 1,
                              w.num_q_heads, w.block_tables.shape[1], w.scale, d.out, out_host)
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama3_8b_decode"])
+def test_pipelined_steps_equal_serial_steps(name):
+    """Six steps through pkv_decode_step_host_pipelined, two buffer slots used in
+    turn on three streams, each step with its own queries: every step's host output
+    equals, bit for bit, the same step run alone through pkv_decode_step_host, and
+    the tiny one matches the oracle. Copies of one step overlap the kernels of the
+    next; the slot events keep each arena and output in use until it is free."""
+    w = W.make_workload(name)
+    n_steps = 6
+    rng = np.random.default_rng(31)
+    qs = [W.f32_to_bf16_bits(rng.standard_normal(w.q.shape).astype(np.float32))
+          for _ in range(n_steps)]
+    MB = w.block_tables.shape[1]
+    n, offs = pkv.step_arena_layout(w.num_seqs, w.n_query_per_seq, w.num_q_heads,
+                                    w.num_kv_heads, w.head_dim, MB)
+
+    def host_arena(d, q):
+        d.q.copy_(torch.from_numpy(q.view(np.int16)).cuda().view(torch.bfloat16))
+        return pack(w, d, n, offs, torch)
+
+    # serial reference: each step alone
+    ref_dev = DeviceStep(w, torch)
+    ref_arena = torch.empty(n, dtype=torch.uint8, device="cuda")
+    refs = []
+    for q in qs:
+        h = host_arena(ref_dev, q)
+        oh = torch.empty(ref_dev.out.shape, dtype=torch.bfloat16).pin_memory()
+        pkv.decode_step_host(h, ref_arena, ref_dev.k_cache, ref_dev.v_cache, w.num_seqs,
+                             w.n_query_per_seq, w.num_q_heads, MB, w.scale, ref_dev.out, oh)
+        torch.cuda.synchronize()
+        refs.append(oh.clone())
+
+    # pipelined: two slots, three streams
+    d = DeviceStep(w, torch)
+    hosts = [host_arena(d, q) for q in qs]
+    arenas = [torch.empty(n, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    outs = [torch.empty(d.out.shape, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    outs_h = [torch.full(d.out.shape, float("nan"), dtype=torch.bfloat16).pin_memory()
+              for _ in range(n_steps)]
+    streams = (torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream())
+    events = [tuple(torch.cuda.Event() for _ in range(3)) for _ in range(2)]
+    torch.cuda.synchronize()
+    for i in range(n_steps):
+        b = i % 2
+        pkv.decode_step_host(hosts[i], arenas[b], d.k_cache, d.v_cache, w.num_seqs,
+                             w.n_query_per_seq, w.num_q_heads, MB, w.scale, outs[b], outs_h[i],
+                             streams=streams, events=events[b])
+    torch.cuda.synchronize()
+    for i in range(n_steps):
+        assert torch.equal(outs_h[i].view(torch.int16), refs[i].view(torch.int16)), f"step {i}"
+    assert torch.equal(d.k_cache.view(torch.int16), ref_dev.k_cache.view(torch.int16))
+    if name == "tiny":
+        o = oracle.Oracle()
+        k, v = o.kv_append(w.k_new, w.v_new, w.slot_mapping, w.k_cache, w.v_cache)
+        ref = o.paged_attention(qs[-1], k, v, w.block_tables, w.context_lens, w.n_query_per_seq,
+                                w.scale)
+        compare(to_f64(outs_h[-1]), ref, what="pipelined host step")
+    assert pkv.workspace_error(pkv.workspace(d.q.device, 0)) == 0
