@@ -260,16 +260,24 @@ def run_pkv(args, rank, world, dist):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    # The timed steps run as a user runs them. The main kernel's own time comes
+    # The timed steps run as a user runs them. Unflushed steps are timed as one
+    # block (an event pair around every step would add ~2 us of GPU time to each);
+    # flushed ones one by one, the flush outside. The main kernel's own time comes
     # from a separate pass in which the library records events around it: an event
     # between the append and the main kernel, or between it and the merge, keeps
     # the next kernel from launching early (programmatic dependent launch), so it
     # would stretch the steps it sits in.
-    for i in range(K):
-        flush_fn()
-        ev_s[i].record()
-        step()
-        ev_e[i].record()
+    if l2_mode == "none":
+        ev_s[0].record()
+        for i in range(K):
+            step()
+        ev_e[0].record()
+    else:
+        for i in range(K):
+            flush_fn()
+            ev_s[i].record()
+            step()
+            ev_e[i].record()
     HOOK = 4
     for i in range(0, K, HOOK):
         flush_fn()
@@ -305,9 +313,11 @@ def run_pkv(args, rank, world, dist):
                        "note": "each step after a 512 MiB memset: its dirty lines are written "
                                "back during the timed kernels"}
 
-    step_ms = [a.elapsed_time(b) for a, b in zip(ev_s, ev_e)]
+    if l2_mode == "none":
+        ms_per_step = ev_s[0].elapsed_time(ev_e[0]) / K
+    else:
+        ms_per_step = sum(a.elapsed_time(b) for a, b in zip(ev_s, ev_e)) / K
     kern_ms = [ev_k0[i].elapsed_time(ev_k1[i]) for i in range(0, K, HOOK)]
-    ms_per_step = sum(step_ms) / K
     kern_mean = sum(kern_ms) / len(kern_ms)
     err = pkv.workspace_error(ws)
 
@@ -724,12 +734,19 @@ def run_tree(args, rank, world, dist):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    # timed steps as a user runs them; the main kernel's time from a separate pass
-    for i in range(K):
-        flush_fn()
-        ev_s[i].record()
-        step()
-        ev_e[i].record()
+    # timed steps as a user runs them (unflushed: one block); the main kernel's time
+    # from a separate pass
+    if l2_mode == "none":
+        ev_s[0].record()
+        for i in range(K):
+            step()
+        ev_e[0].record()
+    else:
+        for i in range(K):
+            flush_fn()
+            ev_s[i].record()
+            step()
+            ev_e[i].record()
     HOOK = 4
     for i in range(0, K, HOOK):
         flush_fn()
@@ -740,7 +757,10 @@ def run_tree(args, rank, world, dist):
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
-    ms = sum(a.elapsed_time(b) for a, b in zip(ev_s, ev_e)) / K
+    if l2_mode == "none":
+        ms = ev_s[0].elapsed_time(ev_e[0]) / K
+    else:
+        ms = sum(a.elapsed_time(b) for a, b in zip(ev_s, ev_e)) / K
     kern = [ev_k0[i].elapsed_time(ev_k1[i]) for i in range(0, K, HOOK)]
     kern_ms = sum(kern) / len(kern)
     ms, kern_ms = max_over_ranks([ms, kern_ms], dist, dev)
