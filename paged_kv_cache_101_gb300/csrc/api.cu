@@ -29,6 +29,7 @@ int32_t g_opt_box = 0;
 int32_t g_opt_tail = 0;
 int32_t g_opt_pace = 0;
 int32_t g_opt_math = 0;
+thread_local bool t_meta_ready = false;  // set by a host step around its attention call
 int32_t g_opt_pace_margin = 0;
 cudaEvent_t g_ev_before = nullptr;
 cudaEvent_t g_ev_after = nullptr;
@@ -218,6 +219,8 @@ pkv_status check_geometry(int32_t num_seqs, int32_t nq, int32_t Hq, int32_t Hkv,
 }  // namespace
 
 namespace pkv {
+
+void set_meta_ready(bool ready) { t_meta_ready = ready; }
 
 // Leading workspace bytes that must be zero when a call starts (the header:
 // device error word and work counters); 0 if the geometry is unsupported.
@@ -554,6 +557,7 @@ pkv_status attention(const void *q, const void *k_cache, const void *v_cache, in
     p.ticket_units = 4;
     p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
     p.pace = g_opt_pace;
+    p.meta_ready = (t_meta_ready && !cc.groups) ? 1 : 0;
     p.pace_margin = float(g_opt_pace_margin) * 1e-4f;
     p.k_scale = k_scale;
     p.v_scale = v_scale;

@@ -9,6 +9,7 @@
 #include <stdint.h>
 
 #include "pkv.h"
+#include "pkv_internal.h"
 
 namespace {
 
@@ -121,24 +122,31 @@ pkv_status compute_step(const StepPlan &sp, const void *device_arena, void *k_ca
                                          head_dim, k_scale, v_scale, stream);
         if (s != PKV_OK)
             return s;
-        return pkv_paged_decode_attention_fp8(
+        // the append just enqueued writes only the pool; the arena was in place before it
+        pkv::set_meta_ready(true);
+        s = pkv_paged_decode_attention_fp8(
             d + sp.off[0], k_cache, v_cache, num_blocks, k_scale, v_scale,
             reinterpret_cast<const int32_t *>(d + sp.off[4]), max_blocks_per_seq,
             reinterpret_cast<const int32_t *>(d + sp.off[5]), num_seqs, n_query_per_seq,
             num_q_heads, num_kv_heads, head_dim, scale, out_device, out_dtype, workspace,
             workspace_bytes, stream);
+        pkv::set_meta_ready(false);
+        return s;
     }
     pkv_status s = pkv_kv_append(d + sp.off[1], d + sp.off[2],
                                  reinterpret_cast<const int64_t *>(d + sp.off[3]), sp.n_new,
                                  k_cache, v_cache, num_blocks, num_kv_heads, head_dim, stream);
     if (s != PKV_OK)
         return s;
-    return pkv_paged_decode_attention(d + sp.off[0], k_cache, v_cache, num_blocks,
-                                      reinterpret_cast<const int32_t *>(d + sp.off[4]),
-                                      max_blocks_per_seq,
-                                      reinterpret_cast<const int32_t *>(d + sp.off[5]), num_seqs,
-                                      n_query_per_seq, num_q_heads, num_kv_heads, head_dim, scale,
-                                      out_device, out_dtype, workspace, workspace_bytes, stream);
+    pkv::set_meta_ready(true);
+    s = pkv_paged_decode_attention(d + sp.off[0], k_cache, v_cache, num_blocks,
+                                   reinterpret_cast<const int32_t *>(d + sp.off[4]),
+                                   max_blocks_per_seq,
+                                   reinterpret_cast<const int32_t *>(d + sp.off[5]), num_seqs,
+                                   n_query_per_seq, num_q_heads, num_kv_heads, head_dim, scale,
+                                   out_device, out_dtype, workspace, workspace_bytes, stream);
+    pkv::set_meta_ready(false);
+    return s;
 }
 
 }  // namespace

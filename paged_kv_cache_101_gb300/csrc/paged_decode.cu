@@ -279,6 +279,8 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
     // gave up.
     auto issue = [&](int phys, int q0, int ql, int W, int b, int T, int hg, int flags, int cellv,
                      int slot, bool shallow) -> bool {
+        if (p.meta_ready && issued == 0)
+            asm volatile("griddepcontrol.wait;" ::: "memory");  // the pool is written now
         if (issued >= uint32_t(p.nst)) {
             // the slot's previous fill must have been consumed; a paced CTA
             // (`shallow`) waits for the fill after it instead, keeping one stage
@@ -1509,8 +1511,12 @@ __global__ void __launch_bounds__(kThreadsMax, MINB)
     }
     // This grid may be launched while the previous kernel on the stream (e.g.
     // the KV append writing the pool) still runs: wait for it to complete and
-    // its writes to be visible before reading any global memory.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // its writes to be visible before reading any global memory. When that kernel
+    // is known to write only the pool (meta_ready), the producer plans its cell
+    // first and waits just before its first copy from the pool; the consumers
+    // read nothing before the first stage lands.
+    if (!p.meta_ready)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
     if (p.trace && threadIdx.x == 0) {
         uint32_t smid;
         asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));

@@ -90,6 +90,10 @@ struct DecodeParams {
     int ticket_units;      // at least this many units per ticket
     float scale_log2;      // scale * log2(e)
     int pace;              // pacing: one stage fewer in flight while ahead of the grid (0: off)
+    int meta_ready;        // 1: the kernel before this one on the stream writes none of the
+                           // lengths, tables and queries (the library's own KV append in a
+                           // host step): the producer reads them before the grid dependency
+                           // wait and waits only before its first read of the pool
     float pace_margin;     // pacing: lead (fraction of the work) allowed before pacing
     const float *k_scale;  // E4M3 pools: [Hkv] dequantisation scales (null for bf16)
     const float *v_scale;
@@ -112,6 +116,10 @@ struct DecodeParams {
     float *pre_ml;              // [chunk][total_q][Hq][2] (m, l) of each row over a prefix chunk
     float *pre_acc;             // [chunk][total_q][Hq][D] unnormalised acc over the chunk
 };
+
+// Host steps (host_step.cu) mark the attention call that follows their own KV
+// append on the calling thread: its metadata is in place before that append runs.
+void set_meta_ready(bool ready);
 
 int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int opt_ctas,
                 int opt_stages, int opt_heads, int opt_tail, int smem_optin, int kv8, int fma,

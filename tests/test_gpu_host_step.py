@@ -125,3 +125,42 @@ def test_pipelined_steps_equal_serial_steps(name):
                                 w.scale)
         compare(to_f64(outs_h[-1]), ref, what="pipelined host step")
     assert pkv.workspace_error(pkv.workspace(d.q.device, 0)) == 0
+
+
+def test_pipelined_steps_e4m3_pools():
+    """The pipelined step with per-head scales (E4M3 pools): four steps, two slots,
+    every output bit-identical to kv_append_fp8 + paged_decode_attention_fp8 called
+    directly on the same inputs, and the codes of the pool the same."""
+    w = W.make_workload("llama3_8b_decode")
+    k8, v8, ks, vs = W.fp8_pools(w)
+    MB = w.block_tables.shape[1]
+    n, offs = pkv.step_arena_layout(w.num_seqs, 1, w.num_q_heads, w.num_kv_heads, w.head_dim, MB)
+    ksd, vsd = torch.from_numpy(ks).cuda(), torch.from_numpy(vs).cuda()
+
+    # direct device calls
+    d = DeviceStep(w, torch)
+    kc, vc = torch.from_numpy(k8).cuda(), torch.from_numpy(v8).cuda()
+    pkv.kv_append_fp8(d.k_new, d.v_new, d.slots, kc, vc, ksd, vsd)
+    pkv.paged_decode_attention_fp8(d.q, kc, vc, ksd, vsd, d.tables, d.lens, 1, w.scale, d.out)
+    torch.cuda.synchronize()
+    ref = d.out.cpu()
+
+    host = pack(w, d, n, offs, torch)
+    kp, vp = torch.from_numpy(k8).cuda(), torch.from_numpy(v8).cuda()
+    arenas = [torch.empty(n, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    outs = [torch.empty(d.out.shape, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    outs_h = [torch.full(d.out.shape, float("nan"), dtype=torch.bfloat16).pin_memory()
+              for _ in range(4)]
+    streams = (torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream())
+    events = [tuple(torch.cuda.Event() for _ in range(3)) for _ in range(2)]
+    for i in range(4):
+        pkv.decode_step_host(host, arenas[i % 2], kp, vp, w.num_seqs, 1, w.num_q_heads, MB,
+                             w.scale, outs[i % 2], outs_h[i], streams=streams,
+                             events=events[i % 2], k_scale=ksd, v_scale=vsd)
+    torch.cuda.synchronize()
+    for i in range(4):
+        assert torch.equal(outs_h[i].view(torch.int16), ref.view(torch.int16)), f"step {i}"
+    assert torch.equal(kp, kc) and torch.equal(vp, vc)
+    with pytest.raises(ValueError):  # E4M3 pools take the pipelined form
+        pkv.decode_step_host(host, arenas[0], kp, vp, w.num_seqs, 1, w.num_q_heads, MB, w.scale,
+                             outs[0], outs_h[0], k_scale=ksd, v_scale=vsd)
