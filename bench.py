@@ -52,24 +52,24 @@ FALLBACK_HBM_GBS = 6800.0
 # to `source_sha256` (otherwise the bench reports traffic = null).
 NCU_TRAFFIC = {
     "llama3_8b_decode": {
-        "bytes": 582027520 + 3394816,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "03c6b8f612a4152af4f61d254794f9f5dc36e84cc9cf192788089ef1f8609825",
+        "bytes": 582027520 + 3609856,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "06c2d5a3e63e35719d42fa594c5cae146085a61f094e2c335b73795646279519",
     },
     "llama3_70b_mix": {
-        "bytes": 1334435584 + 5587456,
-        "source_sha256": "03c6b8f612a4152af4f61d254794f9f5dc36e84cc9cf192788089ef1f8609825",
+        "bytes": 1334974208 + 5754624,
+        "source_sha256": "06c2d5a3e63e35719d42fa594c5cae146085a61f094e2c335b73795646279519",
     },
     "spec_verify": {
-        "bytes": 1417696000 + 4996608,
-        "source_sha256": "03c6b8f612a4152af4f61d254794f9f5dc36e84cc9cf192788089ef1f8609825",
+        "bytes": 1417812480 + 4912896,
+        "source_sha256": "06c2d5a3e63e35719d42fa594c5cae146085a61f094e2c335b73795646279519",
     },
     "llama3_8b_decode/fp8": {
-        "bytes": 291321856 + 3453184,
-        "source_sha256": "03c6b8f612a4152af4f61d254794f9f5dc36e84cc9cf192788089ef1f8609825",
+        "bytes": 291322112 + 3507200,
+        "source_sha256": "06c2d5a3e63e35719d42fa594c5cae146085a61f094e2c335b73795646279519",
     },
     "llama3_70b_mix/fp8": {
-        "bytes": 666844928 + 5223168,
-        "source_sha256": "03c6b8f612a4152af4f61d254794f9f5dc36e84cc9cf192788089ef1f8609825",
+        "bytes": 666925568 + 5054976,
+        "source_sha256": "06c2d5a3e63e35719d42fa594c5cae146085a61f094e2c335b73795646279519",
     },
 }
 
