@@ -279,8 +279,6 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
     // gave up.
     auto issue = [&](int phys, int q0, int ql, int W, int b, int T, int hg, int flags, int cellv,
                      int slot, bool shallow) -> bool {
-        if (p.meta_ready && issued == 0)
-            asm volatile("griddepcontrol.wait;" ::: "memory");  // the pool is written now
         if (issued >= uint32_t(p.nst)) {
             // the slot's previous fill must have been consumed; a paced CTA
             // (`shallow`) waits for the fill after it instead, keeping one stage
@@ -438,6 +436,14 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
             bool cell_first = true;
             int bt_base = -(1 << 30);
             int bt_val = 0;
+            if (p.meta_ready && issued == 0) {
+                // the cell's first block-table entries, then the grid dependency wait
+                // before the first copy from the pool
+                bt_base = b;
+                const int idx = b + lane;
+                bt_val = idx < b_end ? __ldg(p.block_tables + int64_t(si.tr) * p.MB + idx) : 0;
+                asm volatile("griddepcontrol.wait;" ::: "memory");
+            }
 
             for (int64_t u = a; u < e; ++u) {
                 if (b < bt_base || b >= bt_base + 32) {
