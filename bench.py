@@ -52,24 +52,24 @@ FALLBACK_HBM_GBS = 6800.0
 # to `source_sha256` (otherwise the bench reports traffic = null).
 NCU_TRAFFIC = {
     "llama3_8b_decode": {
-        "bytes": 582027520 + 3609856,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "06c2d5a3e63e35719d42fa594c5cae146085a61f094e2c335b73795646279519",
+        "bytes": 582041856 + 3558400,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "2a5583ed3ce08b9f5b2631fddc4ccd0dbc46f43aeabfaab2cb778a61c0b04f06",
     },
     "llama3_70b_mix": {
-        "bytes": 1334974208 + 5754624,
-        "source_sha256": "06c2d5a3e63e35719d42fa594c5cae146085a61f094e2c335b73795646279519",
+        "bytes": 1332676864 + 5603584,
+        "source_sha256": "2a5583ed3ce08b9f5b2631fddc4ccd0dbc46f43aeabfaab2cb778a61c0b04f06",
     },
     "spec_verify": {
-        "bytes": 1417812480 + 4912896,
-        "source_sha256": "06c2d5a3e63e35719d42fa594c5cae146085a61f094e2c335b73795646279519",
+        "bytes": 1417695488 + 5033216,
+        "source_sha256": "2a5583ed3ce08b9f5b2631fddc4ccd0dbc46f43aeabfaab2cb778a61c0b04f06",
     },
     "llama3_8b_decode/fp8": {
-        "bytes": 291322112 + 3507200,
-        "source_sha256": "06c2d5a3e63e35719d42fa594c5cae146085a61f094e2c335b73795646279519",
+        "bytes": 291327744 + 3382016,
+        "source_sha256": "2a5583ed3ce08b9f5b2631fddc4ccd0dbc46f43aeabfaab2cb778a61c0b04f06",
     },
     "llama3_70b_mix/fp8": {
-        "bytes": 666925568 + 5054976,
-        "source_sha256": "06c2d5a3e63e35719d42fa594c5cae146085a61f094e2c335b73795646279519",
+        "bytes": 666733312 + 5176576,
+        "source_sha256": "2a5583ed3ce08b9f5b2631fddc4ccd0dbc46f43aeabfaab2cb778a61c0b04f06",
     },
 }
 
