@@ -29,6 +29,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -118,7 +119,9 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        # raw samples (the JSON line carries their summary); PKV_CLOCK_LOG overrides
+        self.path = os.environ.get("PKV_CLOCK_LOG") or os.path.join(
+            tempfile.gettempdir(), f"pkv_clocks_gpu{gpu_index}.csv")
 
     def start(self):
         os.makedirs(os.path.dirname(self.path), exist_ok=True)

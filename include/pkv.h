@@ -54,7 +54,7 @@ typedef enum pkv_status {
     PKV_ERR_RANGE = 5,       /* a size is beyond what the library supports     */
     PKV_ERR_WORKSPACE = 6,   /* workspace missing or smaller than required     */
     PKV_ERR_CUDA = 7,        /* a CUDA runtime/driver call or launch failed    */
-    PKV_ERR_UNSUPPORTED = 8, /* a valid shape this build has no kernel for     */
+    PKV_ERR_UNSUPPORTED = 8, /* a valid shape the library has no kernel for   */
     PKV_ERR_NO_BLOCKS = 9,   /* block manager: not enough free blocks          */
     PKV_ERR_SEQUENCE = 10    /* block manager: unknown or duplicate sequence id */
 } pkv_status;
