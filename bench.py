@@ -5,16 +5,19 @@
 
 Prints ONE JSON line (rank 0). A step is the whole hot path over one batch:
 ``kv_append`` of the step's new tokens, then ``paged_decode_attention`` (main
-kernel + merge kernel). Inputs are seeded synthetic data resident in HBM. A step
-that reads at least 2x the L2 capacity evicts its own inputs (the K/V streams carry
-an evict-first hint; with cache control off, ncu sees the main kernel read 1.00x
-its algorithmic bytes from DRAM between unflushed steps at 2.3x to 23x the L2), so
-nothing is flushed between its timed steps (``--l2 auto``; the line also carries the
-same steps timed after a 512 MiB memset, ``with_write_flush``); smaller steps are
-separated by that memset, untimed. ``value`` is
-the step's algorithmic bytes (Q + K + V + block tables + context lengths read,
-output written, plus the append's rows) per second of step time, in GB/s;
-shared-prefix blocks count once.
+kernel + merge kernel). Inputs are seeded synthetic data resident in HBM. The
+headline is the largest workload, ``long_splitk`` (8 sequences of 32k-131k
+tokens, 2.97 GB a step); the same line carries ``per_config``: every named
+workload's step (us per step, main-kernel us, GB/s, roofline fractions, ncu
+traffic where pinned, the oracle's CPU baseline). A step that reads at least 2x
+the L2 capacity evicts its own inputs (the K/V streams carry an evict-first hint;
+with cache control off, ncu sees the main kernel read 1.00x its algorithmic bytes
+from DRAM between unflushed steps at 2.3x to 23x the L2), so nothing is flushed
+between its timed steps (``--l2 auto``; the headline also carries the same steps
+timed after a 512 MiB memset, ``with_write_flush``); smaller steps are separated
+by that memset, untimed. ``value`` is the step's algorithmic bytes (Q + K + V +
+block tables + context lengths read, output written, plus the append's rows) per
+second of step time, in GB/s; shared-prefix blocks count once.
 
 ``--impl reference`` times the fp64 CPU oracle on the host cores instead (the
 only reference this method has), on a bounded sample of the same workload.
@@ -43,7 +46,7 @@ import workloads as W  # noqa: E402
 from paged_kv_cache_101_gb300 import roofline as R  # noqa: E402
 
 METRIC = "paged decode-attention KV-read GB/s vs ~8 TB/s HBM peak; µs per decode step"
-DEFAULT_WORKLOAD = "llama3_8b_decode"
+DEFAULT_WORKLOAD = "long_splitk"
 FLUSH_BYTES = 512 << 20
 L2_BYTES = 129 * 10**6  # GB300 L2 capacity
 FALLBACK_HBM_GBS = 6800.0
@@ -167,6 +170,192 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ pkv arm
+NOMINAL_HBM_GBS = 8000.0  # the ~8 TB/s the benchmark quotes as the HBM peak
+
+
+class StepRig:
+    """One workload's decode step on the device: pools, inputs, workspace and the
+    step (append + attention) as a user calls it, with the L2 rule between steps."""
+
+    def __init__(self, w, args, dev, fp8=False, cascade=False):
+        import torch
+
+        import paged_kv_cache_101_gb300 as pkv
+        self.torch, self.pkv, self.dev, self.args = torch, pkv, dev, args
+        self.fp8, self.cascade = fp8, cascade
+        if cascade:
+            w = W.sharers_first(w)  # the sharing sequences form one consecutive group
+        self.w = w
+
+        def up(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(
+                torch.bfloat16)
+
+        self.q = up(w.q)
+        self.k_scale = self.v_scale = None
+        if fp8:
+            k8, v8, ks_h, vs_h = W.fp8_pools(w)
+            self.k_cache = torch.from_numpy(k8).to(dev)
+            self.v_cache = torch.from_numpy(v8).to(dev)
+            self.k_scale = torch.from_numpy(ks_h).to(dev)
+            self.v_scale = torch.from_numpy(vs_h).to(dev)
+            del k8, v8
+        else:
+            self.k_cache, self.v_cache = up(w.k_cache), up(w.v_cache)
+        self.k_new, self.v_new = up(w.k_new), up(w.v_new)
+        self.slots = torch.from_numpy(w.slot_mapping).to(dev)
+        self.tables = torch.from_numpy(w.block_tables).to(dev)
+        self.lens = torch.from_numpy(w.context_lens).to(dev)
+        self.out = torch.empty(self.q.shape, dtype=torch.bfloat16, device=dev)
+        self.M = int(w.shared.sum()) if cascade else 0
+        if cascade:
+            self.groups = torch.tensor([[0, self.M, w.meta["prefix_tokens"] // 16]],
+                                       dtype=torch.int32, device=dev)
+            self.ws = pkv.workspace(dev, int(pkv.lib().pkv_workspace_size_cascade(
+                w.num_seqs, w.n_query_per_seq, w.num_q_heads, w.num_kv_heads, w.head_dim)))
+        else:
+            self.ws = pkv.workspace(dev, pkv.workspace_size(
+                w.num_seqs, w.n_query_per_seq, w.num_q_heads, w.num_kv_heads, w.head_dim))
+        self.flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        eb = 1 if fp8 else 2
+        self.attn_bytes = R.workload_bytes(w, unique=True, kv_bytes_per_element=eb)
+        self.attn_bytes_logical = R.workload_bytes(w, unique=False, kv_bytes_per_element=eb)
+        self.app_bytes = R.append_bytes(int(w.slot_mapping.size), w.num_kv_heads, w.head_dim,
+                                        kv_bytes_per_element=eb)
+        self.step_bytes = self.attn_bytes + self.app_bytes
+        # Between timed steps: a step that reads at least twice the L2 capacity evicts
+        # its own inputs, so nothing is flushed (no dirty flush data is written back
+        # during the timed kernels); smaller steps are separated by the 512 MiB memset.
+        self.l2_mode = args.l2 if args.l2 != "auto" else (
+            "none" if self.step_bytes >= 2 * L2_BYTES else "flush")
+
+    def flush(self):
+        if self.l2_mode == "flush":
+            self.flush_buf.zero_()
+
+    def attend(self, q, tables, lens, out):
+        pkv, w = self.pkv, self.w
+        if self.fp8:
+            pkv.paged_decode_attention_fp8(q, self.k_cache, self.v_cache, self.k_scale,
+                                           self.v_scale, tables, lens, w.n_query_per_seq,
+                                           w.scale, out, ws=self.ws)
+        elif self.cascade:
+            pkv.paged_decode_attention_cascade(q, self.k_cache, self.v_cache, tables, lens,
+                                               w.n_query_per_seq, w.scale, out, self.groups,
+                                               self.M, ws=self.ws)
+        else:
+            pkv.paged_decode_attention(q, self.k_cache, self.v_cache, tables, lens,
+                                       w.n_query_per_seq, w.scale, out, ws=self.ws)
+
+    def append(self, k_new, v_new, slots):
+        if self.fp8:
+            self.pkv.kv_append_fp8(k_new, v_new, slots, self.k_cache, self.v_cache,
+                                   self.k_scale, self.v_scale)
+        else:
+            self.pkv.kv_append(k_new, v_new, slots, self.k_cache, self.v_cache)
+
+    def step(self):
+        self.append(self.k_new, self.v_new, self.slots)
+        self.attend(self.q, self.tables, self.lens, self.out)
+
+    def time_steps(self, K, warmup):
+        """(ms per step, main-kernel ms) over K steps after `warmup` untimed ones.
+
+        The timed steps run as a user runs them. Unflushed steps are timed as one
+        block (an event pair around every step would add ~2 us of GPU time to each);
+        flushed ones one by one, the flush outside. The main kernel's own time comes
+        from a separate pass in which the library records events around it: an event
+        between the append and the main kernel, or between it and the merge, keeps
+        the next kernel from launching early (programmatic dependent launch), so it
+        would stretch the steps it sits in."""
+        torch, pkv = self.torch, self.pkv
+        for _ in range(warmup):
+            self.flush()
+            self.step()
+        torch.cuda.synchronize()
+        ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        hook = 4
+        ev_k = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(0, K, hook)]
+        for a, b in ev_k:
+            a.record()  # create the underlying events before the timed region
+            b.record()
+        torch.cuda.synchronize()
+        if self.l2_mode == "none":
+            ev_s[0].record()
+            for _ in range(K):
+                self.step()
+            ev_e[0].record()
+        else:
+            for i in range(K):
+                self.flush()
+                ev_s[i].record()
+                self.step()
+                ev_e[i].record()
+        for a, b in ev_k:
+            self.flush()
+            pkv.set_profiling_events(a, b)
+            self.step()
+            pkv.set_profiling_events(None, None)
+        torch.cuda.synchronize()
+        if self.l2_mode == "none":
+            ms = ev_s[0].elapsed_time(ev_e[0]) / K
+        else:
+            ms = sum(a.elapsed_time(b) for a, b in zip(ev_s, ev_e)) / K
+        kern = [a.elapsed_time(b) for a, b in ev_k]
+        return ms, sum(kern) / len(kern)
+
+    def write_flush(self, K):
+        """The same steps, each after the 512 MiB memset: (ms per step, kernel ms)."""
+        torch, pkv = self.torch, self.pkv
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+        for i in range(K):
+            self.flush_buf.zero_()
+            ev[i][0].record()
+            self.step()
+            ev[i][1].record()
+        for i in range(0, K, 4):
+            self.flush_buf.zero_()
+            pkv.set_profiling_events(ev[i][2], ev[i][3])
+            self.step()
+            pkv.set_profiling_events(None, None)
+        torch.cuda.synchronize()
+        f_step = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+        f_kern = [ev[i][2].elapsed_time(ev[i][3]) for i in range(0, K, 4)]
+        return f_step, sum(f_kern) / len(f_kern)
+
+
+def traffic_pin(key):
+    nt = NCU_TRAFFIC.get(key)
+    if nt and nt.get("source_sha256") == kernel_source_sha():
+        return nt["bytes"]
+    return None
+
+
+def roofline_entry(rig, kern_ms, traffic, kernel_name):
+    peak, peak_kind = measured_peaks()
+    achieved = rig.attn_bytes / (kern_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
+            "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "peak_source": f"{peak_kind} hbm_gbs (burst)",
+            "frac_of_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+            "traffic": traffic, "kernel_us": round(kern_ms * 1e3, 3),
+            "algorithmic_bytes_per_launch": rig.attn_bytes}
+
+
+def use_cascade(w, mode):
+    """The cascade for a workload with prefix sharers: forced on or off, or as the
+    library's rule decides for its batch (sharers first, one group)."""
+    import paged_kv_cache_101_gb300 as pkv
+    if not w.shared.any() or mode == "off":
+        return False
+    if mode == "on":
+        return True
+    lens = np.concatenate([w.context_lens[w.shared], w.context_lens[~w.shared]])
+    return pkv.cascade_pays(lens, [[0, int(w.shared.sum()), w.meta["prefix_tokens"] // 16]])
+
+
 def run_pkv(args, rank, world, dist):
     import torch
 
@@ -174,166 +363,132 @@ def run_pkv(args, rank, world, dist):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    w = W.make_workload(args.workload)
-    cascade = bool(args.cascade) and bool(w.shared.any())
-    if cascade:
-        w = W.sharers_first(w)  # the sharing sequences form one consecutive group
-
-    def up(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
-
     fp8 = args.kv_dtype == "fp8"
     fma = args.math == "fma"
+    w0 = W.make_workload(args.workload)
+    cascade = use_cascade(w0, args.cascade)
     if fma and (fp8 or cascade):
         raise SystemExit("--math fma runs the plain bf16 call only")
     pkv.set_option(pkv.PKV_OPT_MATH, 1 if fma else 0)
     pkv.set_option(pkv.PKV_OPT_PACE, 1 if args.pace else 0)
-    q = up(w.q)
-    if fp8:
-        k8, v8, ks_h, vs_h = W.fp8_pools(w)
-        k_cache = torch.from_numpy(k8).to(dev)
-        v_cache = torch.from_numpy(v8).to(dev)
-        k_scale = torch.from_numpy(ks_h).to(dev)
-        v_scale = torch.from_numpy(vs_h).to(dev)
-        del k8, v8
-    else:
-        k_cache, v_cache = up(w.k_cache), up(w.v_cache)
-    k_new, v_new = up(w.k_new), up(w.v_new)
-    slots = torch.from_numpy(w.slot_mapping).to(dev)
-    tables = torch.from_numpy(w.block_tables).to(dev)
-    lens = torch.from_numpy(w.context_lens).to(dev)
-    out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
-    if cascade:
-        M = int(w.shared.sum())
-        groups = torch.tensor([[0, M, w.meta["prefix_tokens"] // 16]], dtype=torch.int32,
-                              device=dev)
-        ws = pkv.workspace(dev, int(pkv.lib().pkv_workspace_size_cascade(
-            w.num_seqs, w.n_query_per_seq, w.num_q_heads, w.num_kv_heads, w.head_dim)))
-    else:
-        ws = pkv.workspace(dev, pkv.workspace_size(w.num_seqs, w.n_query_per_seq, w.num_q_heads,
-                                                    w.num_kv_heads, w.head_dim))
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-
-    eb = 1 if fp8 else 2
-    attn_bytes = R.workload_bytes(w, unique=True, kv_bytes_per_element=eb)
-    attn_bytes_logical = R.workload_bytes(w, unique=False, kv_bytes_per_element=eb)
-    app_bytes = R.append_bytes(int(w.slot_mapping.size), w.num_kv_heads, w.head_dim,
-                               kv_bytes_per_element=eb)
-    step_bytes = attn_bytes + app_bytes
-    # Between timed steps: a step that reads at least twice the L2 capacity evicts
-    # its own inputs, so nothing is flushed (no dirty flush data is written back
-    # during the timed kernels); smaller steps are separated by the 512 MiB memset.
-    l2_mode = args.l2 if args.l2 != "auto" else (
-        "none" if step_bytes >= 2 * L2_BYTES else "flush")
-
-    def flush_fn():
-        if l2_mode == "flush":
-            flush.zero_()
-
-    def step():
-        if fp8:
-            pkv.kv_append_fp8(k_new, v_new, slots, k_cache, v_cache, k_scale, v_scale)
-            pkv.paged_decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, tables, lens,
-                                           w.n_query_per_seq, w.scale, out, ws=ws)
-        elif cascade:
-            pkv.kv_append(k_new, v_new, slots, k_cache, v_cache)
-            pkv.paged_decode_attention_cascade(q, k_cache, v_cache, tables, lens,
-                                               w.n_query_per_seq, w.scale, out, groups, M, ws=ws)
-        else:
-            pkv.kv_append(k_new, v_new, slots, k_cache, v_cache)
-            pkv.paged_decode_attention(q, k_cache, v_cache, tables, lens, w.n_query_per_seq,
-                                       w.scale, out, ws=ws)
-
-    for _ in range(args.warmup):
-        flush_fn()
-        step()
-    torch.cuda.synchronize()
-
+    pkv.set_option(pkv.PKV_OPT_HEADS_PER_CTA, args.heads)
+    pkv.set_option(pkv.PKV_OPT_TMA_BOX, args.box)
+    rig = StepRig(w0, args, dev, fp8=fp8, cascade=cascade)
+    del w0
+    w = rig.w
     K = args.steps
-    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev_k0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev_k1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    for ev in ev_k0 + ev_k1:
-        ev.record()  # create the underlying events before the timed region
-    torch.cuda.synchronize()
 
     clocks = ClockSampler(dev.index)
     clocks.start()
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    # The timed steps run as a user runs them. Unflushed steps are timed as one
-    # block (an event pair around every step would add ~2 us of GPU time to each);
-    # flushed ones one by one, the flush outside. The main kernel's own time comes
-    # from a separate pass in which the library records events around it: an event
-    # between the append and the main kernel, or between it and the merge, keeps
-    # the next kernel from launching early (programmatic dependent launch), so it
-    # would stretch the steps it sits in.
-    if l2_mode == "none":
-        ev_s[0].record()
-        for i in range(K):
-            step()
-        ev_e[0].record()
-    else:
-        for i in range(K):
-            flush_fn()
-            ev_s[i].record()
-            step()
-            ev_e[i].record()
-    HOOK = 4
-    for i in range(0, K, HOOK):
-        flush_fn()
-        pkv.set_profiling_events(ev_k0[i], ev_k1[i])
-        step()
-        pkv.set_profiling_events(None, None)
-    torch.cuda.synchronize()
+    ms_per_step, kern_mean = rig.time_steps(K, args.warmup)
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
 
     # the same steps again, each after the 512 MiB memset, for comparison
     write_flush = None
-    if l2_mode == "none":
+    if rig.l2_mode == "none":
         Kf = min(K, 300)
-        wf = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(Kf)]
-        for i in range(Kf):
-            flush.zero_()
-            wf[i][0].record()
-            step()
-            wf[i][1].record()
-        for i in range(0, Kf, HOOK):
-            flush.zero_()
-            pkv.set_profiling_events(wf[i][2], wf[i][3])
-            step()
-            pkv.set_profiling_events(None, None)
-        torch.cuda.synchronize()
-        f_step = sum(e[0].elapsed_time(e[1]) for e in wf) / Kf
-        f_kern = [wf[i][2].elapsed_time(wf[i][3]) for i in range(0, Kf, HOOK)]
-        f_step, f_kern = max_over_ranks([f_step, sum(f_kern) / len(f_kern)], dist, dev)
+        f_step, f_kern = max_over_ranks(list(rig.write_flush(Kf)), dist, dev)
         write_flush = {"us_per_step": round(f_step * 1e3, 3), "kernel_us": round(f_kern * 1e3, 3),
                        "steps": Kf,
                        "note": "each step after a 512 MiB memset: its dirty lines are written "
                                "back during the timed kernels"}
+    err = pkv.workspace_error(rig.ws)
+    e2e_ms, e2e_mode, h2d, d2h = run_e2e(rig, args, dev)
 
-    if l2_mode == "none":
-        ms_per_step = ev_s[0].elapsed_time(ev_e[0]) / K
-    else:
-        ms_per_step = sum(a.elapsed_time(b) for a, b in zip(ev_s, ev_e)) / K
-    kern_ms = [ev_k0[i].elapsed_time(ev_k1[i]) for i in range(0, K, HOOK)]
-    kern_mean = sum(kern_ms) / len(kern_ms)
-    err = pkv.workspace_error(ws)
+    # max over ranks
+    ms_per_step, kern_mean, e2e_ms = max_over_ranks([ms_per_step, kern_mean, e2e_ms], dist, dev)
+    traffic = traffic_pin(args.workload + ("/fp8" if fp8 else "") +
+                          ("/cascade" if cascade else "") + ("/fma" if fma else ""))
+    step_bytes = rig.step_bytes
+    value = job_gbs(world, step_bytes, ms_per_step)
+    res = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 6),
+        "us_per_step": round(ms_per_step * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 (E4M3 KV cache, f16 products)" if fp8 else "bf16",
+        "data": ("synthetic (seeded random E4M3 code pools with per-head scales, N(0,1) bf16 "
+                 "Q and new rows; " if fp8 else "synthetic (seeded N(0,1) bf16 K/V/Q; ") +
+                "pools in HBM; " + ("inputs several times the L2, no flush)"
+                                    if rig.l2_mode == "none"
+                                    else "a 512 MiB L2 flush between timed steps)"),
+        "config": {
+            "workload": args.workload + (" (fp8 KV cache)" if fp8 else "") +
+                        (" (shared-prefix cascade)" if cascade else "") +
+                        (" (CUDA-core FMA consumers)" if fma else ""),
+            "kv_dtype": args.kv_dtype, "math": args.math, "pace": bool(args.pace),
+            "num_seqs": w.num_seqs, "n_query_per_seq": w.n_query_per_seq,
+            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "block_size": 16,
+            "context_tokens": int(w.context_lens.sum()),
+            "num_blocks": w.num_blocks, "parallelism": f"replicas x{world}",
+            "l2": l2_note(rig),
+            "step": ("kv_append_fp8 + paged_decode_attention_fp8" if fp8 else
+                     "kv_append + paged_decode_attention") + " (main + merge kernels)",
+            "bytes_per_step": step_bytes, "attention_bytes_unique": rig.attn_bytes,
+            "attention_bytes_logical": rig.attn_bytes_logical,
+        },
+        "roofline": roofline_entry(
+            rig, kern_mean, traffic,
+            ("paged_decode_fma_kernel" if fma else "paged_decode_kernel") +
+            (" (prefix pass + main pass)" if cascade else "")),
+        "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 6), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "path": ("pkv_decode_step_host_pipelined: " if rig.l2_mode == "none" and
+                         not cascade else "pkv_decode_step_host: " if not (fp8 or cascade)
+                         else "") +
+                        "one pinned host arena (q, new K/V, slots, tables, lengths) -> one H2D -> "
+                        "kv_append + attention -> one D2H of the output",
+                "mode": e2e_mode},
+        "gpu_launches": K * (4 if cascade else 3),
+        "device_error_word": err,
+    }
+    if write_flush is not None:
+        res["with_write_flush"] = write_flush
+    if clk is not None:
+        res["clocks"] = clk
+    del rig
+    torch.cuda.empty_cache()
+    return res
 
-    # ---- end to end: per-step inputs from pinned host memory, output back to host.
-    # The step's inputs (q, new K/V rows, slots, block tables, lengths) sit in one
-    # pinned host arena and cross in ONE host-to-device copy into a device arena
-    # of the same layout; the library calls then run on views of that arena, and
-    # the output comes back in one device-to-host copy.
-    # The plain bf16 step goes through the library's host-buffer entry point
-    # (pkv_decode_step_host: both copies inside the C-ABI call, its arena layout);
-    # the E4M3 and cascade steps use the same layout with the copies made here.
-    ins = [("q", q), ("k_new", k_new), ("v_new", v_new), ("slot_mapping", slots),
-           ("block_tables", tables), ("context_lens", lens)]
+
+def l2_note(rig):
+    if rig.l2_mode == "none":
+        return ("not flushed: each step reads %.0f MB, %.1fx the %d MB L2, so it evicts its own "
+                "inputs" % (rig.step_bytes / 1e6, rig.step_bytes / L2_BYTES, L2_BYTES // 10**6))
+    return "flushed between timed steps (512 MiB memset, untimed)"
+
+
+def run_e2e(rig, args, dev):
+    """End to end: per-step inputs from pinned host memory, output back to host.
+
+    The step's inputs (q, new K/V rows, slots, block tables, lengths) sit in one
+    pinned host arena and cross in ONE host-to-device copy into a device arena of
+    the same layout; the library calls then run on views of that arena, and the
+    output comes back in one device-to-host copy. The plain bf16 step goes through
+    the library's host-buffer entry point (pkv_decode_step_host: both copies inside
+    the C-ABI call, its arena layout); the E4M3 and cascade steps use the same
+    layout with the copies made here. Returns (ms per step, mode, H2D, D2H bytes)."""
+    import torch
+    pkv, w = rig.pkv, rig.w
+    fp8, cascade = rig.fp8, rig.cascade
+    K = args.steps
+    ins = [("q", rig.q), ("k_new", rig.k_new), ("v_new", rig.v_new),
+           ("slot_mapping", rig.slots), ("block_tables", rig.tables),
+           ("context_lens", rig.lens)]
     arena_bytes, offs = pkv.step_arena_layout(w.num_seqs, w.n_query_per_seq, w.num_q_heads,
                                               w.num_kv_heads, w.head_dim,
                                               w.block_tables.shape[1])
@@ -346,34 +501,25 @@ def run_pkv(args, rank, world, dist):
 
     for nm, t in ins:
         view(h_arena, nm, t).copy_(t)
-    e_q, e_kn, e_vn, e_slots, e_tables, e_lens = (view(d_arena, nm, t) for nm, t in ins)
+    out = rig.out
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = arena_bytes
     d2h = h_out.numel() * h_out.element_size()
+    e_q, e_kn, e_vn, e_slots, e_tables, e_lens = (view(d_arena, nm, t) for nm, t in ins)
 
     def e2e_step():
         if not fp8 and not cascade:
-            pkv.decode_step_host(h_arena, d_arena, k_cache, v_cache, w.num_seqs,
+            pkv.decode_step_host(h_arena, d_arena, rig.k_cache, rig.v_cache, w.num_seqs,
                                  w.n_query_per_seq, w.num_q_heads, w.block_tables.shape[1],
-                                 w.scale, out, h_out, ws=ws)
+                                 w.scale, out, h_out, ws=rig.ws)
             return
         d_arena.copy_(h_arena, non_blocking=True)
-        if fp8:
-            pkv.kv_append_fp8(e_kn, e_vn, e_slots, k_cache, v_cache, k_scale, v_scale)
-            pkv.paged_decode_attention_fp8(e_q, k_cache, v_cache, k_scale, v_scale, e_tables,
-                                           e_lens, w.n_query_per_seq, w.scale, out, ws=ws)
-        elif cascade:
-            pkv.kv_append(e_kn, e_vn, e_slots, k_cache, v_cache)
-            pkv.paged_decode_attention_cascade(e_q, k_cache, v_cache, e_tables, e_lens,
-                                               w.n_query_per_seq, w.scale, out, groups, M, ws=ws)
-        else:
-            pkv.kv_append(e_kn, e_vn, e_slots, k_cache, v_cache)
-            pkv.paged_decode_attention(e_q, k_cache, v_cache, e_tables, e_lens,
-                                       w.n_query_per_seq, w.scale, out, ws=ws)
+        rig.append(e_kn, e_vn, e_slots)
+        rig.attend(e_q, e_tables, e_lens, out)
         h_out.copy_(out, non_blocking=True)
 
     Ke = max(1, min(K, 200))
-    if l2_mode == "none":
+    if rig.l2_mode == "none":
         # Steps in flight two at a time: the upload, compute and download phases on
         # their own streams, two buffer slots (device arena, device output) used in
         # turn, ordered by each slot's events: a step's copies overlap its
@@ -392,11 +538,11 @@ def run_pkv(args, rank, world, dist):
             up, comp, down = streams
             ev_up, ev_comp, ev_down = slots_ev[b]
             if not cascade:
-                pkv.decode_step_host(h_arena, d_arenas[b], k_cache, v_cache, w.num_seqs,
+                pkv.decode_step_host(h_arena, d_arenas[b], rig.k_cache, rig.v_cache, w.num_seqs,
                                      w.n_query_per_seq, w.num_q_heads, w.block_tables.shape[1],
-                                     w.scale, outs[b], h_outs[b], ws=ws, streams=streams,
-                                     events=slots_ev[b], k_scale=k_scale if fp8 else None,
-                                     v_scale=v_scale if fp8 else None)
+                                     w.scale, outs[b], h_outs[b], ws=rig.ws, streams=streams,
+                                     events=slots_ev[b], k_scale=rig.k_scale,
+                                     v_scale=rig.v_scale)
                 return
             p_q, p_kn, p_vn, p_slots, p_tables, p_lens = views[b]
             up.wait_event(ev_comp)
@@ -406,16 +552,8 @@ def run_pkv(args, rank, world, dist):
             comp.wait_event(ev_up)
             comp.wait_event(ev_down)
             with torch.cuda.stream(comp):
-                if fp8:
-                    pkv.kv_append_fp8(p_kn, p_vn, p_slots, k_cache, v_cache, k_scale, v_scale)
-                    pkv.paged_decode_attention_fp8(p_q, k_cache, v_cache, k_scale, v_scale,
-                                                   p_tables, p_lens, w.n_query_per_seq, w.scale,
-                                                   outs[b], ws=ws)
-                else:
-                    pkv.kv_append(p_kn, p_vn, p_slots, k_cache, v_cache)
-                    pkv.paged_decode_attention_cascade(p_q, k_cache, v_cache, p_tables, p_lens,
-                                                       w.n_query_per_seq, w.scale, outs[b],
-                                                       groups, M, ws=ws)
+                rig.append(p_kn, p_vn, p_slots)
+                rig.attend(p_q, p_tables, p_lens, outs[b])
                 ev_comp.record(comp)
             down.wait_event(ev_comp)
             with torch.cuda.stream(down):
@@ -436,96 +574,68 @@ def run_pkv(args, rank, world, dist):
             main.wait_stream(st_)
         t1.record(main)
         torch.cuda.synchronize()
-        e2e_ms = t0.elapsed_time(t1) / Ke
-        e2e_mode = "pipelined: two steps in flight, copies overlapping kernels"
-    else:
-        for _ in range(max(1, args.warmup)):
-            flush_fn()
-            e2e_step()
-        torch.cuda.synchronize()
-        e_s = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
-        e_e = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
-        for i in range(Ke):
-            flush_fn()
-            e_s[i].record()
-            e2e_step()
-            e_e[i].record()
-        torch.cuda.synchronize()
-        e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e_s, e_e)) / Ke
-        e2e_mode = "serial: one step at a time (L2 flushed between steps)"
+        return (t0.elapsed_time(t1) / Ke,
+                "pipelined: two steps in flight, copies overlapping kernels", h2d, d2h)
+    for _ in range(max(1, args.warmup)):
+        rig.flush()
+        e2e_step()
+    torch.cuda.synchronize()
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    for i in range(Ke):
+        rig.flush()
+        e_s[i].record()
+        e2e_step()
+        e_e[i].record()
+    torch.cuda.synchronize()
+    return (sum(a.elapsed_time(b) for a, b in zip(e_s, e_e)) / Ke,
+            "serial: one step at a time (L2 flushed between steps)", h2d, d2h)
 
-    # max over ranks
-    ms_per_step, kern_mean, e2e_ms = max_over_ranks([ms_per_step, kern_mean, e2e_ms], dist, dev)
 
-    peak, peak_kind = measured_peaks()
-    achieved = attn_bytes / (kern_mean * 1e-3) / 1e9
-    traffic = None
-    nt = NCU_TRAFFIC.get(args.workload + ("/fp8" if fp8 else "") + ("/cascade" if cascade else "") +
-                         ("/fma" if fma else ""))
-    if nt and nt.get("source_sha256") == kernel_source_sha():
-        traffic = nt["bytes"]
-    value = job_gbs(world, step_bytes, ms_per_step)
-    res = {
-        "metric": METRIC,
-        "value": round(value, 2),
-        "unit": "GB/s",
-        "n_gpus": world,
-        "steps": K,
-        "warmup": args.warmup,
-        "ms_per_step": round(ms_per_step, 6),
-        "us_per_step": round(ms_per_step * 1e3, 3),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "bf16 (E4M3 KV cache, f16 products)" if fp8 else "bf16",
-        "data": ("synthetic (seeded random E4M3 code pools with per-head scales, N(0,1) bf16 "
-                 "Q and new rows; " if fp8 else "synthetic (seeded N(0,1) bf16 K/V/Q; ") +
-                "pools in HBM; " + ("inputs several times the L2, no flush)" if l2_mode == "none"
-                                    else "a 512 MiB L2 flush between timed steps)"),
-        "config": {
-            "workload": args.workload + (" (fp8 KV cache)" if fp8 else "") +
-                        (" (shared-prefix cascade)" if cascade else "") +
-                        (" (CUDA-core FMA consumers)" if fma else ""),
-            "kv_dtype": args.kv_dtype, "math": args.math, "pace": bool(args.pace),
-            "num_seqs": w.num_seqs, "n_query_per_seq": w.n_query_per_seq,
-            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
-            "head_dim": w.head_dim, "block_size": 16,
-            "context_tokens": int(w.context_lens.sum()),
-            "num_blocks": w.num_blocks, "parallelism": f"replicas x{world}",
-            "l2": ("not flushed: each step reads %.0f MB, %.1fx the %d MB L2, so it evicts "
-                   "its own inputs" % (step_bytes / 1e6, step_bytes / L2_BYTES, L2_BYTES // 10**6)
-                   if l2_mode == "none" else
-                   "flushed between timed steps (512 MiB memset, untimed)"),
-            "step": ("kv_append_fp8 + paged_decode_attention_fp8" if fp8 else
-                     "kv_append + paged_decode_attention") + " (main + merge kernels)",
-            "bytes_per_step": step_bytes, "attention_bytes_unique": attn_bytes,
-            "attention_bytes_logical": attn_bytes_logical,
-        },
-        "roofline": {
-            "bound": "hbm",
-            "kernel": ("paged_decode_fma_kernel" if fma else "paged_decode_kernel") +
-                      (" (prefix pass + main pass)" if cascade else ""),
-            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs (burst)",
-            "traffic": traffic, "kernel_us": round(kern_mean * 1e3, 3),
-            "algorithmic_bytes_per_launch": attn_bytes,
-        },
-        "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms, 6), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h,
-                "path": ("pkv_decode_step_host_pipelined: " if l2_mode == "none" and not cascade
-                         else "pkv_decode_step_host: " if not (fp8 or cascade) else "") +
-                        "one pinned host arena (q, new K/V, slots, tables, lengths) -> one H2D -> "
-                        "kv_append + attention -> one D2H of the output",
-                "mode": e2e_mode},
-        "gpu_launches": K * (4 if cascade else 3),
-        "device_error_word": err,
-    }
-    if write_flush is not None:
-        res["with_write_flush"] = write_flush
-    if clk is not None:
-        res["clocks"] = clk
-    return res
+def run_per_config(args, rank, world, dist, headline):
+    """Every named workload's decode step (bf16 pools, plain call): us per step,
+    main-kernel us, step and kernel GB/s, roofline fractions, ncu traffic where
+    pinned, and the oracle timed on a bounded sample on the host cores."""
+    import torch
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    entries = {}
+    for name in W.WORKLOAD_ORDER:
+        if name == args.workload and headline is not None:
+            res = headline
+            e = {"us_per_step": res["us_per_step"], "kernel_us": res["roofline"]["kernel_us"],
+                 "step_gbs": res["value"], "kernel_gbs": res["roofline"]["achieved"],
+                 "frac": res["roofline"]["frac"],
+                 "frac_of_8tbs": res["roofline"]["frac_of_8tbs"],
+                 "traffic": res["roofline"]["traffic"],
+                 "bytes_per_step": res["config"]["bytes_per_step"],
+                 "attention_bytes_unique": res["config"]["attention_bytes_unique"],
+                 "attention_bytes_logical": res["config"]["attention_bytes_logical"],
+                 "l2": res["config"]["l2"], "steps": res["steps"]}
+            if "cpu_baseline" in res:
+                e["cpu_baseline"] = res["cpu_baseline"]
+            entries[name] = e
+            continue
+        rig = StepRig(W.make_workload(name), args, dev)
+        ms, kern = rig.time_steps(args.steps, args.warmup)
+        ms, kern = max_over_ranks([ms, kern], dist, dev)
+        rf = roofline_entry(rig, kern, traffic_pin(name), "paged_decode_kernel")
+        e = {"us_per_step": round(ms * 1e3, 3), "kernel_us": rf["kernel_us"],
+             "step_gbs": round(job_gbs(world, rig.step_bytes, ms), 2),
+             "kernel_gbs": rf["achieved"], "frac": rf["frac"],
+             "frac_of_8tbs": rf["frac_of_8tbs"], "traffic": rf["traffic"],
+             "bytes_per_step": rig.step_bytes, "attention_bytes_unique": rig.attn_bytes,
+             "attention_bytes_logical": rig.attn_bytes_logical, "l2": l2_note(rig),
+             "steps": args.steps, "device_error_word": rig.pkv.workspace_error(rig.ws)}
+        del rig
+        torch.cuda.empty_cache()
+        if rank == 0 and not args.no_cpu_baseline:
+            a = argparse.Namespace(**vars(args))
+            a.workload = name
+            a.cpu_seconds = args.cpu_seconds / 2
+            e["cpu_baseline"] = cpu_baseline(a)
+        entries[name] = e
+    return entries
 
 
 # ------------------------------------------------------------------ copy-on-write copy
@@ -799,18 +909,22 @@ PREFIX_METRIC = "shared-prompt decode attention GB/s (unique KV bytes); µs per 
 
 
 def run_shared_prefix(args, rank, world, dist):
-    """Decode step of 256 sequences (8B-layer heads) that share a 4,096-token system
-    prompt, each with a private suffix of 16..511 tokens: the cascade (prompt
-    attended once per group row tile) against the plain call on the same inputs."""
+    """Decode step of 256 sequences (8B-layer heads) that share a system prompt
+    (--prefix-tokens, 4,096 by default), each with a private suffix of 16 ..
+    --suffix-max - 1 tokens: the cascade (prompt attended once per group row tile)
+    and the plain call on the same inputs; the line's value is the path the
+    library's rule (pkv_cascade_pays) picks."""
     import torch
 
     import paged_kv_cache_101_gb300 as pkv
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    S, P_TOK = 256, 4096
+    S, P_TOK = 256, int(args.prefix_tokens)
+    if P_TOK < 16 or P_TOK % 16 or args.suffix_max <= 16:
+        raise SystemExit("--prefix-tokens must be a positive multiple of 16, --suffix-max > 16")
     rng = np.random.default_rng(1234 + 23)
-    lens = P_TOK + rng.integers(16, 512, size=S)
+    lens = P_TOK + rng.integers(16, int(args.suffix_max), size=S)
     w = W.make_custom(S, 1, 32, 8, 128, lens, seed=1234 + 23, shared=np.ones(S, bool),
                       prefix_tokens=P_TOK)
 
@@ -863,7 +977,10 @@ def run_shared_prefix(args, rank, world, dist):
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
-    ms, ms_plain = max_over_ranks([ms, ms_plain], dist, dev)
+    ms_casc, ms_plain = max_over_ranks([ms, ms_plain], dist, dev)
+    # the step as the library's rule runs it by default; both paths are reported
+    chosen = "cascade" if pkv.cascade_pays(w.context_lens, [[0, S, P_TOK // 16]]) else "plain"
+    ms = ms_casc if chosen == "cascade" else ms_plain
     peak, peak_kind = measured_peaks()
     res = {
         "metric": PREFIX_METRIC, "value": round(world * step_bytes / (ms * 1e-3) / 1e9, 2),
@@ -871,16 +988,19 @@ def run_shared_prefix(args, rank, world, dist):
         "ms_per_step": round(ms, 6), "us_per_step": round(ms * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16; 512 MiB L2 flush between steps)",
-        "config": {"workload": "256 sequences sharing a 4096-token system prompt, private "
-                               "suffixes U[16, 512), 8B-layer heads (32/8, d 128)",
+        "config": {"workload": f"256 sequences sharing a {P_TOK}-token system prompt, private "
+                               f"suffixes U[16, {args.suffix_max}), 8B-layer heads (32/8, d 128)",
                    "context_tokens": int(w.context_lens.sum()), "bytes_per_step": step_bytes,
                    "attention_bytes_unique": attn_bytes,
                    "attention_bytes_logical": R.workload_bytes(w, unique=False),
                    "parallelism": f"replicas x{world}"},
+        "chosen_by_rule": chosen,
+        "cascade": {"us_per_step": round(ms_casc * 1e3, 3),
+                    "value": round(world * step_bytes / (ms_casc * 1e-3) / 1e9, 2)},
         "plain_call": {"us_per_step": round(ms_plain * 1e3, 3),
                        "value": round(world * step_bytes / (ms_plain * 1e-3) / 1e9, 2)},
-        "speedup_vs_plain": round(ms_plain / ms, 3),
-        "roofline": {"bound": "hbm", "kernel": "step (append + prefix pass + main + merge)",
+        "speedup_vs_plain": round(ms_plain / ms_casc, 3),
+        "roofline": {"bound": "hbm", "kernel": f"step ({chosen} path)",
                      "achieved": round(step_bytes / (ms * 1e-3) / 1e9, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(step_bytes / (ms * 1e-3) / 1e9 / peak, 4),
                      "peak_source": f"{peak_kind} hbm_gbs (burst)", "traffic": None},
@@ -1009,9 +1129,14 @@ def main():
                          "copy-on-write block copy alone; tree_verify: a 15-node candidate "
                          "tree per sequence scored with tree masks")
     ap.add_argument("--pairs", type=int, default=4096, help="block pairs per copy_blocks step")
-    ap.add_argument("--cascade", action="store_true",
-                    help="attend the workload's shared prefix once per group (its sharers "
-                         "moved to the front of the batch)")
+    ap.add_argument("--cascade", default="auto", choices=["auto", "on", "off"],
+                    help="shared-prefix cascade for a workload with sharers (moved to the "
+                         "front of the batch): auto = the library's rule "
+                         "(pkv_cascade_pays), on, off")
+    ap.add_argument("--prefix-tokens", type=int, default=4096,
+                    help="shared_prefix op: tokens of the shared system prompt")
+    ap.add_argument("--suffix-max", type=int, default=512,
+                    help="shared_prefix op: private suffixes of 16 .. suffix-max - 1 tokens")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
                     help="KV pool element type (fp8 = E4M3 codes with per-head scales)")
     ap.add_argument("--l2", default="auto", choices=["auto", "flush", "none"],
@@ -1020,6 +1145,12 @@ def main():
                          "else a 512 MiB memset")
     ap.add_argument("--pace", action="store_true",
                     help="pace the attention kernel's chunks (PKV_OPT_PACE; off by default)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per_config entries (every named workload's step)")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="PKV_OPT_HEADS_PER_CTA: cap on kv heads per CTA (0 = the planner's)")
+    ap.add_argument("--box", type=int, default=0, choices=[0, 1, 2],
+                    help="PKV_OPT_TMA_BOX: 0 = whole-block boxes when accepted, 1 = per tile")
     ap.add_argument("--math", default="tensor", choices=["tensor", "fma"],
                     help="attention consumers: tensor cores (default) or the CUDA-core FMA "
                          "reference path (bf16 pools, plain call)")
@@ -1051,9 +1182,12 @@ def main():
             dist.destroy_process_group()
         return
     res = run_pkv(args, rank, world, dist)
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(args)
+    if not args.no_per_config and args.kv_dtype == "bf16" and args.cascade == "auto" and \
+            args.math == "tensor" and args.heads == 0 and args.box == 0 and not args.pace:
+        res["per_config"] = run_per_config(args, rank, world, dist, res)
     if rank == 0:
-        if not args.no_cpu_baseline:
-            res["cpu_baseline"] = cpu_baseline(args)
         print(json.dumps(res), flush=True)
     if dist is not None:
         dist.destroy_process_group()

@@ -235,6 +235,26 @@ pkv_status pkv_paged_decode_attention(const void *q, const void *k_cache, const 
 size_t pkv_workspace_size_cascade(int32_t num_seqs, int32_t n_query_per_seq, int32_t num_q_heads,
                                   int32_t num_kv_heads, int32_t head_dim);
 
+/*
+ * pkv_cascade_pays -- host planner: 1 if pkv_paged_decode_attention_cascade is
+ * expected to beat pkv_paged_decode_attention for this batch, 0 if not, -1 for
+ * invalid input (a negative count, a NULL array with a nonzero count, a group
+ * outside the batch).
+ *
+ * Passage: "ML Interview Prep, Lesson 13" section 3.5 "Sharing" (shared blocks
+ * are read by every sharer). The plain call reads every member's copy of the
+ * shared prefix; after the first, those reads mostly hit L2, so they cost
+ * little while they are few next to the step's unique bytes and bound the
+ * kernel once they are not. The rule: repeated prefix tokens, sum over groups of
+ * (members whose context extends past the prefix - 1) * 16 * P, at least the
+ * unique tokens (all context tokens minus the repeated ones).
+ *
+ *   context_lens   host int32 [num_seqs], as the attention call's
+ *   prefix_groups  host int32 [num_groups][3], as the cascade call's
+ */
+int32_t pkv_cascade_pays(const int32_t *context_lens, int32_t num_seqs,
+                         const int32_t *prefix_groups, int32_t num_groups);
+
 pkv_status pkv_paged_decode_attention_cascade(
     const void *q, const void *k_cache, const void *v_cache, int64_t num_blocks,
     const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
@@ -367,11 +387,13 @@ pkv_status pkv_paged_decode_attention_fp8(const void *q, const void *k_cache, co
  * and the caller still passes every input and output buffer.
  *
  * Arguments, results and errors are those of pkv_paged_decode_attention
- * without `workspace`/`workspace_bytes`. The scratch instead lives in one
+ * without `workspace`/`workspace_bytes`: the same host checks run in the same
+ * order and return the same status. The scratch instead lives in one
  * static device array of 32 MiB (32 * 2^20 bytes), which every GPU that loads
  * the library's module holding it keeps until the process exits (with CUDA's
  * default lazy module loading: from this entry point's first call on that
- * GPU). A geometry whose scratch (pkv_workspace_size) exceeds 32 MiB returns
+ * GPU). A call whose plan (sized as the workspace call would size it, tuning
+ * options included) needs more than 32 MiB of scratch returns
  * PKV_ERR_WORKSPACE before anything is enqueued; on a 152-SM GB300 a
  * geometry with up to 32 query rows per kv head needs at most ~21 MiB plus 8
  * bytes per (sequence, group of up to 8 kv heads), one with 33 to 64 rows up
@@ -385,6 +407,11 @@ pkv_status pkv_paged_decode_attention_fp8(const void *q, const void *k_cache, co
  * it keeps the last call's contents: calls that overlap on the GPU (on
  * different streams, or from several threads) race on it and give
  * unspecified results. Serialise them, e.g. on one stream.
+ *
+ * Device-side problems (a block-table entry outside [0, num_blocks), a bounded
+ * wait that gave up) are recorded in the array's error word, as in a caller's
+ * workspace: read it with pkv_static_error_word after the call and before the
+ * next static call, which clears it.
  */
 pkv_status pkv_paged_decode_attention_static(const void *q, const void *k_cache,
                                              const void *v_cache, int64_t num_blocks,
@@ -394,6 +421,22 @@ pkv_status pkv_paged_decode_attention_static(const void *q, const void *k_cache,
                                              int32_t n_query_per_seq, int32_t num_q_heads,
                                              int32_t num_kv_heads, int32_t head_dim, float scale,
                                              void *out, int32_t out_dtype, void *stream);
+
+/*
+ * pkv_static_error_word -- the device error word of the static scratch that
+ * pkv_paged_decode_attention_static uses on the current device: the bits a
+ * workspace's first 4 bytes hold after pkv_paged_decode_attention (8 = a
+ * block-table entry outside [0, num_blocks), read as zeros; 1, 2, 4 = a
+ * bounded wait gave up).
+ *
+ * No counterpart on the pages either: it lets a caller that cannot allocate
+ * see device-side errors of its static calls. Enqueues one 4-byte
+ * device-to-host copy on `stream` (after the stream's earlier work) into
+ * `host_word` and waits for the stream; allocates nothing. PKV_ERR_NULL for a
+ * NULL `host_word`, PKV_ERR_CUDA if the copy fails. The word is cleared by
+ * the next static call.
+ */
+pkv_status pkv_static_error_word(uint32_t *host_word, void *stream);
 
 /*
  * pkv_step_arena_layout -- byte layout of one decode step's inputs in a single

@@ -52,6 +52,7 @@ SIGNATURES = {
     "pkv_set_trace_buffer": ([_P, _SZ], None),
     "pkv_paged_decode_attention_static": ([_P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _I32,
                                            _I32, _F, _P, _I32, _P], ctypes.c_int),
+    "pkv_static_error_word": ([_P, _P], ctypes.c_int),
     "pkv_copy_blocks": ([_P, _P, _I64, _I32, _I32, _P, _P, _I32, _P], ctypes.c_int),
     "pkv_paged_decode_attention_varlen": ([_P, _P, _P, _I64, _P, _I32, _I32, _P, _P, _P, _P, _P,
                                            _I32, _I32, _I32, _I32, _I32, _I32, _F, _P, _I32, _P,
@@ -60,6 +61,7 @@ SIGNATURES = {
     "pkv_paged_decode_attention_cascade": ([_P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _I32,
                                             _I32, _F, _P, _I32, _I32, _P, _I32, _P, _SZ, _P],
                                            ctypes.c_int),
+    "pkv_cascade_pays": ([_P, _I32, _P, _I32], _I32),
     "pkv_split_queries": ([_P, _P, _P, _I32, _I32, _P, _P, _P, _P, _I32, _P], ctypes.c_int),
     "pkv_kv_append_fp8": ([_P, _P, _P, _I64, _P, _P, _I64, _I32, _I32, _P, _P, _P], ctypes.c_int),
     "pkv_paged_decode_attention_fp8": ([_P, _P, _P, _I64, _P, _P, _P, _I32, _P, _I32, _I32, _I32,
@@ -578,6 +580,33 @@ def paged_decode_attention_static(q, k_cache, v_cache, block_tables, context_len
     if st != PKV_OK:
         raise PkvError("pkv_paged_decode_attention_static", st)
     return out
+
+
+def cascade_pays(context_lens, prefix_groups) -> bool:
+    """The library's rule for choosing the shared-prefix cascade over the plain call
+    (host arrays: context lengths [S], groups [num_groups][3])."""
+    import numpy as np
+    lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    groups = np.ascontiguousarray(prefix_groups, dtype=np.int32).reshape(-1, 3)
+    r = lib().pkv_cascade_pays(lens.ctypes.data, lens.size, groups.ctypes.data,
+                               groups.shape[0])
+    if r < 0:
+        raise ValueError("pkv_cascade_pays: invalid input")
+    return bool(r)
+
+
+def static_error_word(device=None) -> int:
+    """The device error word of the static scratch (``paged_decode_attention_static``)
+    on ``device``, read after the current stream's work."""
+    torch = _torch()
+    dev = torch.device(device) if device is not None else torch.device(
+        "cuda", torch.cuda.current_device())
+    word = ctypes.c_uint32(0)
+    with torch.cuda.device(dev):
+        st = lib().pkv_static_error_word(ctypes.addressof(word), _stream_handle(dev))
+    if st != PKV_OK:
+        raise PkvError("pkv_static_error_word", st)
+    return int(word.value)
 
 
 def step_arena_layout(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim,

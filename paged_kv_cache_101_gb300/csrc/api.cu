@@ -222,25 +222,6 @@ namespace pkv {
 
 void set_meta_ready(bool ready) { t_meta_ready = ready; }
 
-// Leading workspace bytes that must be zero when a call starts (the header:
-// device error word and work counters); 0 if the geometry is unsupported.
-size_t workspace_zero_prefix(int32_t num_seqs, int32_t n_query_per_seq, int32_t num_q_heads,
-                             int32_t num_kv_heads, int32_t head_dim)
-{
-    if (check_geometry(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim) != PKV_OK ||
-        num_seqs < 1)
-        return 0;
-    DeviceInfo d;
-    if (device_info(&d) != cudaSuccess)
-        return 0;
-    DecodePlan pl;
-    if (plan_decode(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim, 1, d.num_sms,
-                    g_opt_num_ctas, g_opt_stages, g_opt_heads, g_opt_tail, d.smem_optin, 0, 0,
-                    &pl) != 0)
-        return 0;
-    return kWsHeaderBytes;
-}
-
 }  // namespace pkv
 
 extern "C" {
@@ -444,8 +425,14 @@ pkv_status attention(const void *q, const void *k_cache, const void *v_cache, in
                      const int32_t *context_lens, int32_t num_seqs, int32_t n_query_per_seq,
                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, float scale,
                      void *out, int32_t out_dtype, void *workspace, size_t workspace_bytes,
-                     void *stream, const Varlen &vl = Varlen(), const Cascade &cc = Cascade())
+                     void *stream, const Varlen &vl = Varlen(), const Cascade &cc = Cascade(),
+                     size_t *need_only = nullptr)
 {
+    // need_only != null: run every host check (a workspace taken as given and
+    // aligned), store the workspace bytes the call's plan needs (0: nothing to
+    // do) and return before any CUDA work is enqueued
+    if (need_only)
+        *need_only = 0;
     pkv_status st = check_geometry(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim,
                                    vl.q_start != nullptr);
     if (st != PKV_OK)
@@ -462,10 +449,11 @@ pkv_status attention(const void *q, const void *k_cache, const void *v_cache, in
         return PKV_ERR_NULL;
     if (kv8 && (!k_scale || !v_scale))
         return PKV_ERR_NULL;
-    if (!workspace)
+    if (!workspace && !need_only)
         return PKV_ERR_WORKSPACE;
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
-        !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(workspace, 256))
+        !aligned(block_tables, 4) || !aligned(context_lens, 4) ||
+        (!need_only && !aligned(workspace, 256)))
         return PKV_ERR_ALIGN;
     if (kv8 && (!aligned(k_scale, 4) || !aligned(v_scale, 4)))
         return PKV_ERR_ALIGN;
@@ -499,11 +487,16 @@ pkv_status attention(const void *q, const void *k_cache, const void *v_cache, in
         if (pre_tiles < 1)
             return PKV_ERR_UNSUPPORTED;
         off_pre = (pl.ws_bytes + 255) / 256 * 256;
-        const int64_t total_q = int64_t(num_seqs) * n_query_per_seq;
-        if (workspace_bytes < off_pre + prefix_region_bytes(total_q, num_q_heads, head_dim))
-            return PKV_ERR_WORKSPACE;
     }
-    if (workspace_bytes < pl.ws_bytes)
+    const size_t need =
+        cc.groups ? off_pre + prefix_region_bytes(int64_t(num_seqs) * n_query_per_seq,
+                                                  num_q_heads, head_dim)
+                  : pl.ws_bytes;
+    if (need_only) {
+        *need_only = need;
+        return PKV_OK;
+    }
+    if (workspace_bytes < need)
         return PKV_ERR_WORKSPACE;
     uint64_t *trace = nullptr;
     if (g_trace && g_trace_bytes >= size_t(pl.grid) * pkv::kTraceWords * 8 &&
@@ -753,3 +746,20 @@ pkv_status pkv_kv_append_fp8(const void *k_new, const void *v_new, const int64_t
 }
 
 }  // extern "C"
+
+namespace pkv {
+
+pkv_status attention_need(const void *q, const void *k_cache, const void *v_cache,
+                          int64_t num_blocks, const int32_t *block_tables,
+                          int32_t max_blocks_per_seq, const int32_t *context_lens,
+                          int32_t num_seqs, int32_t n_query_per_seq, int32_t num_q_heads,
+                          int32_t num_kv_heads, int32_t head_dim, void *out, int32_t out_dtype,
+                          size_t *need)
+{
+    return attention(q, k_cache, v_cache, num_blocks, 0, nullptr, nullptr, block_tables,
+                     max_blocks_per_seq, context_lens, num_seqs, n_query_per_seq, num_q_heads,
+                     num_kv_heads, head_dim, 1.f, out, out_dtype, nullptr, 0, nullptr, Varlen(),
+                     Cascade(), need);
+}
+
+}  // namespace pkv

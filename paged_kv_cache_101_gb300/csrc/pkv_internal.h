@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "pkv.h"
+
 namespace pkv {
 
 constexpr int kBlockSize = 16;          // tokens per physical block
@@ -135,8 +137,15 @@ cudaError_t launch_decode(const DecodePlan &plan, const DecodeParams &p, const C
                           const CUtensorMap &vmap, cudaStream_t stream, cudaEvent_t ev_before,
                           cudaEvent_t ev_after);
 
-size_t workspace_zero_prefix(int32_t num_seqs, int32_t n_query_per_seq, int32_t num_q_heads,
-                             int32_t num_kv_heads, int32_t head_dim);
+// The host-side checks of pkv_paged_decode_attention, in its order, with the
+// workspace taken as given; on PKV_OK *need holds the workspace bytes the call's
+// plan needs (0 when there is nothing to do). Enqueues nothing.
+pkv_status attention_need(const void *q, const void *k_cache, const void *v_cache,
+                          int64_t num_blocks,
+                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                          const int32_t *context_lens, int32_t num_seqs, int32_t n_query_per_seq,
+                          int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, void *out,
+                          int32_t out_dtype, size_t *need);
 
 cudaError_t launch_kv_append(const void *k_new, const void *v_new, const int64_t *slot_mapping,
                              int64_t n_new, void *k_cache, void *v_cache, int64_t num_blocks,

@@ -1,5 +1,6 @@
-// query_plan.cpp -- host-side split of long query runs into virtual sequences
-// for pkv_paged_decode_attention_varlen (see include/pkv.h).
+// query_plan.cpp -- host-side planners (see include/pkv.h): the split of long
+// query runs into virtual sequences for pkv_paged_decode_attention_varlen, and the
+// rule that picks the shared-prefix cascade or the plain call.
 //
 // The attention kernel holds at most 64 score rows per kv head (G * q_len), so a
 // prefill chunk or a large candidate tree is cut into runs of at most max_rows
@@ -11,6 +12,12 @@
 #include <stdint.h>
 
 #include "pkv.h"
+
+namespace {
+// the cascade pays once the repeated prefix tokens reach kCascadeNum / kCascadeDen
+// of the step's unique tokens
+constexpr int64_t kCascadeNum = 1, kCascadeDen = 1;
+}  // namespace
 
 extern "C" pkv_status pkv_split_queries(const int32_t *q_start, const int32_t *context_lens,
                                         const int32_t *tree_len, int32_t num_seqs,
@@ -62,4 +69,41 @@ extern "C" pkv_status pkv_split_queries(const int32_t *q_start, const int32_t *c
     }
     *num_virtual = v;
     return PKV_OK;
+}
+
+// Whether the shared-prefix cascade is expected to beat the plain call. The
+// plain call streams every member's copy of its group's prefix: the first copy
+// from HBM, the others mostly from L2 while the prefix stays resident. Those
+// repeated prefix reads cost L2 bandwidth and, once they rival the step's unique
+// bytes, they bound the plain kernel; the cascade reads each prefix once per row
+// tile instead, for the price of a second launch and one partial fold per member
+// row. So the rule compares the repeated prefix tokens with the unique tokens.
+extern "C" int32_t pkv_cascade_pays(const int32_t *context_lens, int32_t num_seqs,
+                                    const int32_t *prefix_groups, int32_t num_groups)
+{
+    if (num_seqs < 0 || num_groups < 0)
+        return -1;
+    if (num_seqs == 0 || num_groups == 0)
+        return 0;
+    if (!context_lens || !prefix_groups)
+        return -1;
+    int64_t total = 0;
+    for (int32_t s = 0; s < num_seqs; ++s)
+        total += context_lens[s] > 0 ? context_lens[s] : 0;
+    int64_t repeated = 0;
+    for (int32_t g = 0; g < num_groups; ++g) {
+        const int32_t f = prefix_groups[3 * g], cnt = prefix_groups[3 * g + 1];
+        const int32_t P = prefix_groups[3 * g + 2];
+        if (f < 0 || cnt < 0 || P < 0 || int64_t(f) + cnt > num_seqs)
+            return -1;
+        // members that attend the prefix through the cascade: those whose context
+        // holds more than the prefix (the others fall back to the plain path)
+        int64_t members = 0;
+        for (int32_t s = f; s < f + cnt; ++s)
+            members += int64_t(context_lens[s]) > int64_t(16) * P ? 1 : 0;
+        if (members > 1)
+            repeated += (members - 1) * int64_t(16) * P;
+    }
+    const int64_t unique = total - repeated;
+    return repeated * kCascadeDen >= kCascadeNum * unique ? 1 : 0;
 }

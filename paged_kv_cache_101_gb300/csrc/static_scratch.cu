@@ -41,8 +41,6 @@ void *static_scratch_address()
     return g_static_ptr[dev];
 }
 
-bool aligned_to(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
 }  // namespace
 
 extern "C" pkv_status pkv_paged_decode_attention_static(
@@ -51,28 +49,15 @@ extern "C" pkv_status pkv_paged_decode_attention_static(
     int32_t num_seqs, int32_t n_query_per_seq, int32_t num_q_heads, int32_t num_kv_heads,
     int32_t head_dim, float scale, void *out, int32_t out_dtype, void *stream)
 {
-    // Let the regular entry point report invalid arguments (it checks them all
-    // before touching the device); only then set up and clear the scratch.
-    const bool plausible = num_seqs > 0 && q && k_cache && v_cache && block_tables &&
-                           context_lens && out && num_blocks >= 1 && max_blocks_per_seq >= 1 &&
-                           (out_dtype == PKV_BF16 || out_dtype == PKV_FP32) &&
-                           aligned_to(q, 16) && aligned_to(k_cache, 16) && aligned_to(v_cache, 16) &&
-                           aligned_to(out, 16) && aligned_to(block_tables, 4) &&
-                           aligned_to(context_lens, 4) && max_blocks_per_seq <= (1 << 26) &&
-                           num_blocks <= 0x7fffffffLL && num_seqs <= (1 << 24) &&
-                           num_kv_heads <= 65535;
-    if (!plausible)
-        return pkv_paged_decode_attention(q, k_cache, v_cache, num_blocks, block_tables,
-                                          max_blocks_per_seq, context_lens, num_seqs,
-                                          n_query_per_seq, num_q_heads, num_kv_heads, head_dim,
-                                          scale, out, out_dtype, nullptr, 0, stream);
-    const size_t need = pkv_workspace_size(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads,
-                                           head_dim);
-    if (need == 0)  // unsupported geometry or no usable device: full validation says which
-        return pkv_paged_decode_attention(q, k_cache, v_cache, num_blocks, block_tables,
-                                          max_blocks_per_seq, context_lens, num_seqs,
-                                          n_query_per_seq, num_q_heads, num_kv_heads, head_dim,
-                                          scale, out, out_dtype, nullptr, 0, stream);
+    // Every host check of the workspace entry point, in its order, and the
+    // scratch bytes of the very plan the call below will run (grid, options).
+    size_t need = 0;
+    const pkv_status st = pkv::attention_need(q, k_cache, v_cache, num_blocks, block_tables,
+                                              max_blocks_per_seq, context_lens, num_seqs,
+                                              n_query_per_seq, num_q_heads, num_kv_heads,
+                                              head_dim, out, out_dtype, &need);
+    if (st != PKV_OK || need == 0)
+        return st;  // an invalid argument, or nothing to do (num_seqs == 0)
     if (need > kStaticScratchBytes)
         return PKV_ERR_WORKSPACE;  // this geometry needs more than the static maximum
     void *scratch = static_scratch_address();
@@ -80,14 +65,27 @@ extern "C" pkv_status pkv_paged_decode_attention_static(
         return PKV_ERR_CUDA;
     // The header (device error word, work counters) must start at zero; every
     // other byte of the scratch is written by the kernels before it is read.
-    const size_t zero = pkv::workspace_zero_prefix(num_seqs, n_query_per_seq, num_q_heads,
-                                                   num_kv_heads, head_dim);
-    if (zero == 0 || zero > kStaticScratchBytes)
-        return PKV_ERR_CUDA;
-    if (cudaMemsetAsync(scratch, 0, zero, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    if (cudaMemsetAsync(scratch, 0, pkv::kWsHeaderBytes, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
         return PKV_ERR_CUDA;
     return pkv_paged_decode_attention(q, k_cache, v_cache, num_blocks, block_tables,
                                       max_blocks_per_seq, context_lens, num_seqs, n_query_per_seq,
                                       num_q_heads, num_kv_heads, head_dim, scale, out, out_dtype,
                                       scratch, kStaticScratchBytes, stream);
+}
+
+extern "C" pkv_status pkv_static_error_word(uint32_t *host_word, void *stream)
+{
+    if (host_word == nullptr)
+        return PKV_ERR_NULL;
+    void *scratch = static_scratch_address();
+    if (scratch == nullptr)
+        return PKV_ERR_CUDA;
+    // A plain 4-byte read of the header's first word after the stream's work.
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(host_word, scratch, sizeof(uint32_t), cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    return PKV_OK;
 }

@@ -80,31 +80,18 @@ def compare(got: np.ndarray, ref: np.ndarray, atol=ATOL, rtol=RTOL, what=""):
     return float(err.max()), max_rel
 
 
-def sample_pairs(w: W.Workload, n_random: int = 8, seed: int = 0) -> np.ndarray:
-    """A [S, Hkv] mask of (sequence, kv head) pairs the oracle checks at full size:
-    every kv head of the longest, shortest and first sequences, of two prefix
-    sharers, plus random pairs."""
-    S, H = w.num_seqs, w.num_kv_heads
-    mask = np.zeros((S, H), dtype=bool)
-    T = w.context_lens
-    for s in {int(np.argmax(T)), int(np.argmin(T)), 0, S - 1}:
-        mask[s, :] = True
-    sharers = np.nonzero(w.shared)[0]
-    for s in sharers[:2]:
-        mask[s, :] = True
-    rng = np.random.default_rng(seed)
-    for _ in range(n_random):
-        mask[rng.integers(S), rng.integers(H)] = True
-    return mask
+_REFERENCES = {}
 
 
-def rows_of(mask: np.ndarray, w: W.Workload):
-    """Index arrays (row, q-head) of the output selected by a pair mask."""
-    G = w.num_q_heads // w.num_kv_heads
-    rows, heads = [], []
-    for s, h in np.argwhere(mask):
-        for j in range(w.n_query_per_seq):
-            for g in range(G):
-                rows.append(s * w.n_query_per_seq + j)
-                heads.append(h * G + g)
-    return np.array(rows), np.array(heads)
+def full_reference(o, w: W.Workload, key: str) -> np.ndarray:
+    """The oracle's whole attention output ``[S*nq, Hq, D]`` (fp64) for one decode
+    step of ``w`` (append, then attend), computed once per ``key`` in a test run."""
+    ref = _REFERENCES.get(key)
+    if ref is None:
+        ref, _, _ = o.step(w)
+        _REFERENCES[key] = ref
+    return ref
+
+
+def report(what: str, max_abs: float, max_rel: float, n: int):
+    print(f"{what}: all {n} outputs compared, max_abs={max_abs:.3e} max_rel={max_rel:.3e}")

@@ -18,7 +18,7 @@ import pytest
 import oracle
 import paged_kv_cache_101_gb300 as pkv
 import workloads as W
-from gpu_helpers import DeviceStep, compare, rows_of, sample_pairs, to_f64
+from gpu_helpers import DeviceStep, compare, full_reference, report, to_f64
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -112,11 +112,10 @@ def test_70b_mix_sharers_first(o, ctas):
     ws = cascade_ws(w)
     cascade(d, [[0, M, w.meta["prefix_tokens"] // 16]], M, ws=ws)
     torch.cuda.synchronize()
-    mask = sample_pairs(w, n_random=12)
-    mask[:3, :] = True                     # members
-    ref, _, _ = o.step(w, pair_mask=mask)
-    rows, heads = rows_of(mask, w)
-    compare(to_f64(d.out)[rows, heads], ref[rows, heads], what="70b mix cascade")
+    ref = full_reference(o, w, "llama3_70b_mix/sharers_first")
+    got = to_f64(d.out)
+    max_abs, max_rel = compare(got, ref, what=f"70b mix cascade, {ctas} CTAs")
+    report(f"70b mix cascade, {ctas} CTAs", max_abs, max_rel, got.size)
     assert pkv.workspace_error(ws) == 0
 
 

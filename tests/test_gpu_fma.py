@@ -16,7 +16,7 @@ import pytest
 import oracle
 import paged_kv_cache_101_gb300 as pkv
 import workloads as W
-from gpu_helpers import ATOL, DeviceStep, bf16_dev, compare, rows_of, sample_pairs, to_f64
+from gpu_helpers import ATOL, DeviceStep, bf16_dev, compare, full_reference, report, to_f64
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -98,10 +98,10 @@ def test_full_size(o, name):
     d = DeviceStep(w, torch)
     d.step()
     torch.cuda.synchronize()
-    mask = sample_pairs(w, n_random=6)
-    ref, _, _ = o.step(w, pair_mask=mask)
-    rows, heads = rows_of(mask, w)
-    compare(to_f64(d.out)[rows, heads], ref[rows, heads], what=name)
+    ref = full_reference(o, w, name)
+    got = to_f64(d.out)
+    max_abs, max_rel = compare(got, ref, what=f"{name}, CUDA-core consumers")
+    report(f"{name}, CUDA-core consumers", max_abs, max_rel, got.size)
     assert pkv.workspace_error(pkv.workspace(d.q.device, 0)) == 0
 
 

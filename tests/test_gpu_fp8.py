@@ -15,7 +15,7 @@ import pytest
 import oracle
 import paged_kv_cache_101_gb300 as pkv
 import workloads as W
-from gpu_helpers import bf16_dev, compare, rows_of, sample_pairs, to_f64
+from gpu_helpers import bf16_dev, compare, report, to_f64
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -165,17 +165,16 @@ def test_attention_fp8_shared_prefix(o):
     run(o, w)
 
 
-@pytest.mark.parametrize("name", ["llama3_8b_decode", "spec_verify"])
+@pytest.mark.parametrize("name", [n for n in W.WORKLOAD_ORDER if W.WORKLOADS[n]["D"] == 128])
 def test_attention_fp8_full_size(o, name):
     w = W.make_workload(name)
     d = Fp8Step(w)
     d.step()
     torch.cuda.synchronize()
-    mask = sample_pairs(w, n_random=6)
-    ref, k, v = d.reference(o, pair_mask=mask)
-    rows, heads = rows_of(mask, w)
+    ref, k, v = d.reference(o)
     got = to_f64(d.out)
-    compare(got[rows, heads], ref[rows, heads], what=name)
+    max_abs, max_rel = compare(got, ref, what=f"{name}, E4M3 pools")
+    report(f"{name}, E4M3 pools", max_abs, max_rel, got.size)
     # the append touched only its slots
     kc = d.kc.cpu().numpy().reshape(-1, w.num_kv_heads, w.head_dim)
     assert np.array_equal(kc[w.slot_mapping], k.reshape(-1, w.num_kv_heads, w.head_dim)[w.slot_mapping])

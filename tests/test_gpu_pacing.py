@@ -13,7 +13,7 @@ import pytest
 import oracle
 import paged_kv_cache_101_gb300 as pkv
 import workloads as W
-from gpu_helpers import DeviceStep, bf16_dev, compare, rows_of, sample_pairs, to_f64
+from gpu_helpers import DeviceStep, bf16_dev, compare, full_reference, to_f64
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -56,12 +56,8 @@ def test_pacing_is_bit_identical(name):
                                                    w.num_kv_heads, w.head_dim))
     ws.zero_()
     run_settings(lambda: d.attend(ws=ws), d.out, ws)
-    # and the output is the oracle's on sampled (sequence, kv head) pairs
-    o = oracle.Oracle()
-    mask = sample_pairs(w, n_random=4)
-    ref, _, _ = o.step(w, pair_mask=mask)
-    rows, heads = rows_of(mask, w)
-    compare(to_f64(d.out)[rows, heads], ref[rows, heads], what=name)
+    # and the whole output is the oracle's
+    compare(to_f64(d.out), full_reference(oracle.Oracle(), w, name), what=name)
 
 
 def test_pacing_is_bit_identical_fp8():

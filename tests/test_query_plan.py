@@ -1,5 +1,5 @@
-"""pkv_split_queries (host) and the host checks of the variable-query-count
-attention call.
+"""The host planners: pkv_split_queries and the host checks of the
+variable-query-count attention call, and pkv_cascade_pays (cascade or plain call).
 
 The split must keep every query row's visibility: attention over the virtual
 sequences, computed by the oracle, equals attention over the original ones bit
@@ -139,3 +139,34 @@ def test_cascade_host_validation(lib):
     # the cascade's workspace adds the prefix partials to the plain one
     assert lib.pkv_workspace_size_cascade(4, 1, 8, 2, 64) == 0 or \
         lib.pkv_workspace_size_cascade(4, 1, 8, 2, 64) > lib.pkv_workspace_size(4, 1, 8, 2, 64)
+
+
+# ------------------------------------------------------------------ cascade rule
+def shared_prompt_lengths(S=256, prefix=4096, suffix_max=512, seed=1234 + 23):
+    """The shared-prompt batch the benchmark times: a 4,096-token system prompt and
+    private suffixes of 16 .. suffix_max - 1 tokens."""
+    rng = np.random.default_rng(seed)
+    return (prefix + rng.integers(16, suffix_max, size=S)).astype(np.int32)
+
+
+def test_cascade_rule_picks_the_cascade_for_a_long_shared_prompt(lib):
+    lens = shared_prompt_lengths()
+    assert pkv.cascade_pays(lens, [[0, lens.size, 4096 // 16]])
+
+
+def test_cascade_rule_picks_the_plain_call_for_the_70b_mix(lib):
+    T, shared, prefix = W.workload_lengths("llama3_70b_mix")
+    lens = np.concatenate([T[shared], T[~shared]]).astype(np.int32)   # sharers first
+    assert not pkv.cascade_pays(lens, [[0, int(shared.sum()), prefix // 16]])
+
+
+def test_cascade_rule_edges(lib):
+    lens = np.full(8, 600, np.int32)
+    assert not pkv.cascade_pays(lens, np.zeros((0, 3), np.int32))       # no group
+    assert not pkv.cascade_pays(lens, [[0, 1, 32]])                     # a lone member
+    # members whose context is the prefix alone fall back, so they repeat nothing
+    assert not pkv.cascade_pays(np.full(8, 512, np.int32), [[0, 8, 32]])
+    # 7 repeated copies of 512 tokens against 8 * 88 + 512 unique tokens
+    assert pkv.cascade_pays(lens, [[0, 8, 32]])
+    with pytest.raises(ValueError):
+        pkv.cascade_pays(lens, [[4, 8, 32]])                            # past the batch
