@@ -97,7 +97,8 @@ def job_gbs(world, bytes_per_replica_step, ms_per_step):
 
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
-    for f in ("paged_decode.cu", "pkv_common.cuh", "pkv_internal.h"):
+    for f in ("paged_decode.cu", "paged_decode_umma.cu", "pkv_cells.cuh", "pkv_common.cuh",
+              "pkv_internal.h", "pkv_umma.cuh"):
         with open(os.path.join(ROOT, "paged_kv_cache_101_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
@@ -373,6 +374,8 @@ def run_pkv(args, rank, world, dist):
     pkv.set_option(pkv.PKV_OPT_PACE, 1 if args.pace else 0)
     pkv.set_option(pkv.PKV_OPT_HEADS_PER_CTA, args.heads)
     pkv.set_option(pkv.PKV_OPT_TMA_BOX, args.box)
+    pkv.set_option(pkv.PKV_OPT_UMMA, 1 if args.umma_off else 0)
+    pkv.set_option(pkv.PKV_OPT_PREFETCH, args.prefetch)
     rig = StepRig(w0, args, dev, fp8=fp8, cascade=cascade)
     del w0
     w = rig.w
@@ -785,8 +788,12 @@ def run_tree(args, rank, world, dist):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    base_lens = W.workload_lengths(args.workload)[0]
-    geo = W.WORKLOADS[args.workload]
+    pkv.set_option(pkv.PKV_OPT_UMMA, 1 if args.umma_off else 0)
+    pkv.set_option(pkv.PKV_OPT_PREFETCH, args.prefetch)
+    # the 8B layer's lengths and heads unless a workload is named
+    name = args.workload if args.workload_given else "llama3_8b_decode"
+    base_lens = W.workload_lengths(name)[0]
+    geo = W.WORKLOADS[name]
     Hq, Hkv, D = geo["Hq"], geo["Hkv"], geo["D"]
     masks = binary_tree_masks(4)
     n = masks.size
@@ -887,7 +894,7 @@ def run_tree(args, rank, world, dist):
         "data": "synthetic (seeded N(0,1) bf16; " + (
             "each step reads %.1fx the L2: no flush between steps)" % (step_bytes / L2_BYTES)
             if l2_mode == "none" else "512 MiB L2 flush between steps)"),
-        "config": {"workload": f"tree verify: {args.workload} lengths + 15-node binary tree",
+        "config": {"workload": f"tree verify: {name} lengths + 15-node binary tree",
                    "num_seqs": S, "tree_nodes": n, "runs": V, "max_queries_per_run": max_q,
                    "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": D,
                    "context_tokens": int(T.sum()), "bytes_per_step": step_bytes,
@@ -1151,11 +1158,16 @@ def main():
                     help="PKV_OPT_HEADS_PER_CTA: cap on kv heads per CTA (0 = the planner's)")
     ap.add_argument("--box", type=int, default=0, choices=[0, 1, 2],
                     help="PKV_OPT_TMA_BOX: 0 = whole-block boxes when accepted, 1 = per tile")
+    ap.add_argument("--prefetch", type=int, default=0,
+                    help="PKV_OPT_PREFETCH: 0 = default L2 prefetch distance, n = n - 1 blocks")
+    ap.add_argument("--umma-off", action="store_true",
+                    help="PKV_OPT_UMMA = 1: the mma.sync kernels for every shape (A/B)")
     ap.add_argument("--math", default="tensor", choices=["tensor", "fma"],
                     help="attention consumers: tensor cores (default) or the CUDA-core FMA "
                          "reference path (bf16 pools, plain call)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    args.workload_given = any(a == "--workload" or a.startswith("--workload=") for a in sys.argv)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -1185,7 +1197,8 @@ def main():
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args)
     if not args.no_per_config and args.kv_dtype == "bf16" and args.cascade == "auto" and \
-            args.math == "tensor" and args.heads == 0 and args.box == 0 and not args.pace:
+            args.math == "tensor" and args.heads == 0 and args.box == 0 and not args.pace and \
+            not args.umma_off and args.prefetch == 0:
         res["per_config"] = run_per_config(args, rank, world, dist, res)
     if rank == 0:
         print(json.dumps(res), flush=True)

@@ -16,7 +16,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIBRARY = os.path.join(PKG, "libpkv.so")
-SOURCES = ["api.cu", "kv_append.cu", "copy_blocks.cu", "paged_decode.cu", "static_scratch.cu",
+SOURCES = ["api.cu", "kv_append.cu", "copy_blocks.cu", "paged_decode.cu", "paged_decode_umma.cu",
+           "static_scratch.cu",
            "host_step.cu", "block_manager.cpp", "query_plan.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

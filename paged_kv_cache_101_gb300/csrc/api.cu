@@ -29,6 +29,8 @@ int32_t g_opt_box = 0;
 int32_t g_opt_tail = 0;
 int32_t g_opt_pace = 0;
 int32_t g_opt_math = 0;
+int32_t g_opt_umma = 0;
+int32_t g_opt_prefetch = 0;
 thread_local bool t_meta_ready = false;  // set by a host step around its attention call
 int32_t g_opt_pace_margin = 0;
 cudaEvent_t g_ev_before = nullptr;
@@ -197,6 +199,62 @@ cudaError_t pool_map(const void *base, int64_t nb, int Hkv, int D, int kind, int
     return cudaSuccess;
 }
 
+// q [rows][Hq][D] bf16 (D = 128) seen as (64, 2, Hq, rows, 1): one box (64, 1, G,
+// box_rows, 1) brings one 64-dim half of box_rows queries x G heads as [row][g][64],
+// stored with the 128-byte swizzle; rows past the end read as zeros.
+CUresult encode_q(CUtensorMap *map, const void *q, int64_t rows, int Hq, int G, int box_rows)
+{
+    const cuuint64_t row = cuuint64_t(Hq) * 256;
+    const cuuint64_t dims[5] = {64, 2, cuuint64_t(Hq), cuuint64_t(rows), 1};
+    const cuuint64_t strides[4] = {128, 256, row, row * cuuint64_t(rows)};
+    const cuuint32_t box[5] = {64, 1, cuuint32_t(G), cuuint32_t(box_rows), 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(q), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+struct QMapEntry {
+    const void *q = nullptr;
+    int64_t rows = 0;
+    int hq = 0, g = 0, box_rows = 0, dev = -1;
+    CUtensorMap map;
+};
+QMapEntry g_qmaps[8];
+int g_qmap_next = 0;
+
+cudaError_t q_map(const void *q, int64_t rows, int Hq, int G, int box_rows, CUtensorMap *out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    e = get_encoder();
+    if (e != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (auto &m : g_qmaps)
+        if (m.q == q && m.rows == rows && m.hq == Hq && m.g == G && m.box_rows == box_rows &&
+            m.dev == dev) {
+            *out = m.map;
+            return cudaSuccess;
+        }
+    QMapEntry &m = g_qmaps[g_qmap_next];
+    g_qmap_next = (g_qmap_next + 1) % 8;
+    if (encode_q(&m.map, q, rows, Hq, G, box_rows) != CUDA_SUCCESS) {
+        m.q = nullptr;
+        return cudaErrorInvalidValue;
+    }
+    m.q = q;
+    m.rows = rows;
+    m.hq = Hq;
+    m.g = G;
+    m.box_rows = box_rows;
+    m.dev = dev;
+    *out = m.map;
+    return cudaSuccess;
+}
+
 // Host-side checks shared by the workspace query and the attention calls. The
 // fixed-count call takes 1..4 queries per sequence; the variable-count call any
 // count whose score rows (G per query) fit the kernel's 64 rows per kv head.
@@ -302,6 +360,18 @@ int32_t pkv_set_option(int32_t option, int32_t value)
         prev = g_opt_math;
         g_opt_math = value;
         return prev;
+    case PKV_OPT_UMMA:
+        if (value > 1)
+            return -1;
+        prev = g_opt_umma;
+        g_opt_umma = value;
+        return prev;
+    case PKV_OPT_PREFETCH:
+        if (value > 4097)
+            return -1;
+        prev = g_opt_prefetch;
+        g_opt_prefetch = value;
+        return prev;
     case PKV_OPT_PACE_MARGIN:
         if (value > 10000)
             return -1;
@@ -374,17 +444,19 @@ size_t pkv_workspace_size(int32_t num_seqs, int32_t n_query_per_seq, int32_t num
     pkv::DecodePlan pl;
     if (pkv::plan_decode(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim, 1,
                          d.num_sms, g_opt_num_ctas, g_opt_stages, g_opt_heads, g_opt_tail, d.smem_optin,
-                         0, 0, &pl) != 0)
+                         0, 0, 0, &pl) != 0)
         return 0;
     size_t bytes = pl.ws_bytes;
-    // the E4M3 call shares this size: its plan may use more cells
-    pkv::DecodePlan pl8;
-    if (head_dim == 128 &&
-        pkv::plan_decode(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim, 1,
-                         d.num_sms, g_opt_num_ctas, g_opt_stages, g_opt_heads, g_opt_tail,
-                         d.smem_optin, 1, 0, &pl8) == 0 &&
-        pl8.ws_bytes > bytes)
-        bytes = pl8.ws_bytes;
+    // the tcgen05 kernel (one kv head per CTA) and the E4M3 call share this size:
+    // their plans may need more records or cells
+    pkv::DecodePlan alt;
+    for (int kind = 0; kind < 2; ++kind)
+        if (head_dim == 128 &&
+            pkv::plan_decode(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim, 1,
+                             d.num_sms, g_opt_num_ctas, g_opt_stages, g_opt_heads, g_opt_tail,
+                             d.smem_optin, kind, 0, 1 - kind, &alt) == 0 &&
+            alt.ws_bytes > bytes)
+            bytes = alt.ws_bytes;
     return bytes;
 }
 
@@ -469,10 +541,13 @@ pkv_status attention(const void *q, const void *k_cache, const void *v_cache, in
                      (num_q_heads / num_kv_heads) * n_query_per_seq <= 32)
                         ? 1
                         : 0;
+    // the tcgen05 kernel serves 17..64 query rows per kv head, except for a cascade
+    // (its members' running states start from prefix partials)
+    const int umma = (g_opt_umma == 0 && !cc.groups) ? 1 : 0;
     pkv::DecodePlan pl;
     if (pkv::plan_decode(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim,
                          max_blocks_per_seq, d.num_sms, g_opt_num_ctas, g_opt_stages,
-                         g_opt_heads, g_opt_tail, d.smem_optin, kv8, fma, &pl) != 0)
+                         g_opt_heads, g_opt_tail, d.smem_optin, kv8, fma, umma, &pl) != 0)
         return PKV_ERR_UNSUPPORTED;
     // cascade: the prefix pass's plan and the prefix partials after the workspace
     pkv::DecodePlan ppl{};
@@ -503,13 +578,20 @@ pkv_status attention(const void *q, const void *k_cache, const void *v_cache, in
         aligned(g_trace, 8))
         trace = static_cast<uint64_t *>(g_trace);
 
-    CUtensorMap kmap, vmap;
+    CUtensorMap kmap, vmap, qmap;
     int whole_box = 0;
-    if (g_opt_box != 1 &&
+    if (pl.umma) {
+        // one (head, half) box per block: the tiles land in the super-stage's rows
+        if (pool_map(k_cache, num_blocks, num_kv_heads, head_dim, 0, 0, &kmap) != cudaSuccess ||
+            pool_map(v_cache, num_blocks, num_kv_heads, head_dim, 0, 0, &vmap) != cudaSuccess ||
+            q_map(q, vl.q_start ? vl.total_q : int64_t(num_seqs) * n_query_per_seq, num_q_heads,
+                  pl.G, n_query_per_seq, &qmap) != cudaSuccess)
+            return PKV_ERR_CUDA;
+    } else if (g_opt_box != 1 &&
         pool_map(k_cache, num_blocks, num_kv_heads, head_dim, pl.HG, kv8, &kmap) == cudaSuccess &&
         pool_map(v_cache, num_blocks, num_kv_heads, head_dim, pl.HG, kv8, &vmap) == cudaSuccess)
         whole_box = 1;
-    if (!whole_box) {
+    if (!whole_box && !pl.umma) {
         if (g_opt_box == 2)
             return PKV_ERR_UNSUPPORTED;  // whole-block boxes requested but refused
         if (pool_map(k_cache, num_blocks, num_kv_heads, head_dim, 0, kv8, &kmap) != cudaSuccess ||
@@ -552,6 +634,7 @@ pkv_status attention(const void *q, const void *k_cache, const void *v_cache, in
     p.pace = g_opt_pace;
     p.meta_ready = (t_meta_ready && !cc.groups) ? 1 : 0;
     p.pace_margin = float(g_opt_pace_margin) * 1e-4f;
+    p.pf_units = g_opt_prefetch == 0 ? 24 : g_opt_prefetch - 1;
     p.k_scale = k_scale;
     p.v_scale = v_scale;
     p.q_start = vl.q_start;
@@ -611,8 +694,11 @@ pkv_status attention(const void *q, const void *k_cache, const void *v_cache, in
             return PKV_ERR_CUDA;
         ev_b = nullptr;  // the timing hook spans the prefix pass and the main kernel
     }
-    cudaError_t e = pkv::launch_decode(pl, p, kmap, vmap, static_cast<cudaStream_t>(stream),
-                                       ev_b, g_ev_after);
+    cudaError_t e =
+        pl.umma ? pkv::launch_decode_umma(pl, p, kmap, vmap, qmap, static_cast<cudaStream_t>(stream),
+                                          ev_b, g_ev_after)
+                : pkv::launch_decode(pl, p, kmap, vmap, static_cast<cudaStream_t>(stream), ev_b,
+                                     g_ev_after);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

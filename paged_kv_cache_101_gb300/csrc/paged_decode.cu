@@ -49,6 +49,7 @@
 #include <climits>
 #include <type_traits>
 
+#include "pkv_cells.cuh"
 #include "pkv_common.cuh"
 #include "pkv_internal.h"
 
@@ -66,145 +67,6 @@ struct StageHdr {
     int16_t W;      // mask window: per-row masks rule the last W positions
 };
 static_assert(sizeof(StageHdr) == 32, "stage header: two 16-byte words");
-// F_PREFIX: a stage of the cascade's prefix pass; F_PRE: the first stage of a
-// cascade member's own blocks, whose running state starts from its prefix partial
-enum : int32_t { F_FIRST = 1, F_LAST = 2, F_DIRECT = 4, F_END = 8, F_PREFIX = 16, F_PRE = 32 };
-
-// The fixed partition of the flat unit space [0, F): cells 0..G-1 split
-// [0, F1) evenly (cell c is CTA c's chunk); cells G..G+NT-1 split [F1, F) evenly
-// (tickets, claimed dynamically).
-struct Cells {
-    int64_t F, F1, F2;
-    int32_t G, NT;
-
-    __device__ __forceinline__ int64_t start(int64_t k) const
-    {
-        return k <= G ? k * F1 / G : F1 + (k - G) * F2 / NT;
-    }
-    __device__ __forceinline__ bool empty(int64_t k) const { return start(k) == start(k + 1); }
-    // the cell holding unit f (0 <= f < F)
-    __device__ __forceinline__ int64_t cell_of(int64_t f) const
-    {
-        if (f < F1)
-            return ((f + 1) * G + F1 - 1) / F1 - 1;
-        return G + ((f - F1 + 1) * NT + F2 - 1) / F2 - 1;
-    }
-};
-
-// The cells of a call: G static chunks, then up to tickets_max tickets over the
-// last F / ticket_div units. A function of the sizes only (the merge kernel
-// rebuilds the same cells).
-__device__ __forceinline__ Cells make_cells(const DecodeParams &p, int nb_total, int grid)
-{
-    Cells C;
-    C.F = int64_t(p.n_hg) * nb_total;
-    C.G = grid;
-    C.NT = 0;
-    C.F2 = 0;
-    if (p.tickets_max > 0 && p.ticket_div > 0) {
-        const int64_t f2 = C.F / p.ticket_div;
-        const int64_t nt = f2 / (p.ticket_units > 0 ? p.ticket_units : 1);
-        if (nt > 0) {
-            C.NT = int(nt < p.tickets_max ? nt : p.tickets_max);
-            C.F2 = f2;
-        }
-    }
-    C.F1 = C.F - C.F2;
-    return C;
-}
-
-__device__ __forceinline__ int seq_tokens(const DecodeParams &p, int s)
-{
-    int T = __ldg(p.context_lens + s);
-    T = T < 0 ? 0 : T;
-    const int cap = p.MB * kBlockSize;
-    return T > cap ? cap : T;
-}
-
-// Per-sequence view of the inputs. Fixed query count: rows s*nq .. +nq, block
-// table row s, causal. Variable counts (q_start): rows q_start[s] ..
-// q_start[s+1]-1 (at most nq), table row table_row[s] (or s), and with tree
-// masks a window of tree_len[s] positions. Inconsistent device values (rows
-// outside [0, total_q), more rows than nq, a table row outside the tables)
-// leave the sequence without queries and set kErrBadQuery.
-struct SeqInfo {
-    int T;   // tokens (clamped to the table)
-    int nb;  // blocks to stream (0 if the sequence has no query rows)
-    int q0;  // first query row
-    int ql;  // query rows
-    int W;   // mask window (causal: ql)
-    int tr;  // block-table row
-    int b0;  // first block streamed: a cascade member's prefix is attended apart
-};
-
-// Cascade: the group holding sequence s (groups ascending by first sequence),
-// or -1. Each row of pre-computed groups is (first sequence, sequences, blocks).
-__device__ __forceinline__ int group_of(const DecodeParams &p, int s)
-{
-    int lo = 0, hi = p.num_groups - 1;
-    while (lo <= hi) {
-        const int mid = (lo + hi) >> 1;
-        const int f = __ldg(p.prefix_groups + 3 * mid);
-        if (s < f) {
-            hi = mid - 1;
-        } else if (s >= f + __ldg(p.prefix_groups + 3 * mid + 1)) {
-            lo = mid + 1;
-        } else {
-            return mid;
-        }
-    }
-    return -1;
-}
-
-__device__ __forceinline__ SeqInfo seq_info(const DecodeParams &p, int s)
-{
-    SeqInfo i;
-    i.T = seq_tokens(p, s);
-    i.q0 = s * p.nq;
-    i.ql = p.nq;
-    i.tr = s;
-    bool bad = false;
-    if (p.q_start) {
-        const int a = __ldg(p.q_start + s), e = __ldg(p.q_start + s + 1);
-        bad = a < 0 || e < a || e > p.total_q || e - a > p.nq;
-        i.q0 = a;
-        i.ql = bad ? 0 : e - a;
-    }
-    if (p.table_row) {
-        i.tr = __ldg(p.table_row + s);
-        if (i.tr < 0 || i.tr >= p.table_rows) {
-            bad = true;
-            i.ql = 0;
-        }
-    }
-    i.W = i.ql;
-    if (p.tree_mask) {
-        const int w = __ldg(p.tree_len + s);
-        i.W = w < 0 ? 0 : (w > 32 ? 32 : w);
-    }
-    if (bad)
-        atomicOr(p.ws + kWsErr, kErrBadQuery);
-    const int nb = i.ql > 0 ? (i.T + kBlockSize - 1) / kBlockSize : 0;
-    i.b0 = 0;
-    if (p.prefix_groups && nb > 0) {
-        // a member skips its group's prefix when every query row sees all of it
-        const int gi = group_of(p, s);
-        if (gi >= 0) {
-            // the same validity rule as the prefix pass: a group it skips is not
-            // skipped here either
-            const int f = __ldg(p.prefix_groups + 3 * gi);
-            const int cnt = __ldg(p.prefix_groups + 3 * gi + 1);
-            const int P = __ldg(p.prefix_groups + 3 * gi + 2);
-            const bool group_ok = f >= 0 && cnt >= 0 && f + cnt <= p.S && P >= 0 && P <= p.MB;
-            if (group_ok && P > 0 && P < nb && kBlockSize * P <= i.T - i.ql)
-                i.b0 = P;
-        }
-    }
-    i.nb = nb - i.b0;  // blocks streamed by the main pass
-    return i;
-}
-
-__device__ __forceinline__ int seq_blocks(const DecodeParams &p, int s) { return seq_info(p, s).nb; }
 
 struct Smem {
     uint8_t *stages;
@@ -225,14 +87,6 @@ __device__ __forceinline__ Smem carve(uint8_t *raw, const DecodeParams &p)
     s.empty = s.full + p.nst;
     s.cells = reinterpret_cast<Cells *>(s.empty + p.nst);
     return s;
-}
-
-// A gpu-scope relaxed load (the L2 copy of a counter other CTAs update).
-__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *ptr)
-{
-    uint32_t v;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
-    return v;
 }
 
 // ------------------------------------------------------------------ producer
@@ -2028,7 +1882,7 @@ static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int opt_ctas,
                 int opt_stages, int opt_heads, int opt_tail, int smem_optin, int kv8, int fma,
-                DecodePlan *pl)
+                int umma, DecodePlan *pl)
 {
     if (S < 1 || nq < 1 || Hkv < 1 || Hq % Hkv != 0 || (D != 64 && D != 128) || MB < 1)
         return -1;
@@ -2044,6 +1898,36 @@ int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int 
     P.rows = P.G * nq;
     if (P.rows > kMaxRows)
         return -1;
+    if (umma && !P.kv8 && !P.fma && D == 128 && P.rows > 16) {
+        // tcgen05 consumers: one kv head per CTA, super-stages of 8 blocks, the
+        // query rows padded to the MMA's N (32 or 64)
+        P.umma = 1;
+        P.rows_pad = P.rows <= 32 ? 32 : 64;
+        P.wph = 1;
+        P.ntw = 0;
+        P.HG = 1;
+        P.n_hg = Hkv;
+        P.threads = 320;
+        P.stage_bytes = 65536;
+        P.nst = umma_stages(P.rows_pad);
+        P.smem = umma_smem_bytes(P.rows_pad);
+        if (int(P.smem) > smem_optin)
+            return -1;
+        P.ctas_per_sm = 1;
+        const int grid_cap = opt_ctas > 0 ? opt_ctas : num_sms;
+        if (grid_cap < 1 || grid_cap > 16384)
+            return -1;
+        P.grid = int(std::min<int64_t>(grid_cap, int64_t(P.n_hg) * S * MB));
+        P.tail_div = 0;
+        P.tickets_max = 0;
+        const size_t cells = size_t(grid_cap);
+        P.off_rec = kWsHeaderBytes;
+        P.off_ml = P.off_rec + round_up(size_t(S) * P.n_hg * 8, 256);
+        P.off_part = P.off_ml + round_up(cells * 2 * P.rows * 2 * 4, 256);
+        P.ws_bytes = P.off_part + round_up(cells * 2 * P.rows * size_t(D) * 4, 256);
+        *pl = P;
+        return 0;
+    }
     if (P.fma) {
         // 4 or 8 rows per warp (fp32 registers: RW x 4 accumulators a lane)
         P.rw = P.rows <= 4 ? 4 : 8;
@@ -2191,7 +2075,16 @@ static cudaError_t launch_kernel(Kern kern, int *configured_smem, const DecodePl
         return e;
     if (!with_merge)
         return cudaSuccess;
+    return launch_merge(pl, p, stream);
+}
+
+cudaError_t launch_merge(const DecodePlan &pl, const DecodeParams &p, cudaStream_t stream)
+{
     // the merge: one CTA per (sequence, head group, 8 * RPW rows), a programmatic dependent
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaError_t e;
     const bool few_rows = p.HG * p.rows <= 32;
     const int cta_rows = few_rows ? 16 : 32;
     cudaLaunchConfig_t mcfg = {};

@@ -33,7 +33,8 @@ pytestmark = pytest.mark.gpu
 
 OK, NULL, SHAPE, DTYPE, ALIGN, RANGE, WORKSPACE, CUDA, UNSUP = range(9)
 OPTIONS = (pkv.PKV_OPT_NUM_CTAS, pkv.PKV_OPT_STAGES, pkv.PKV_OPT_HEADS_PER_CTA,
-           pkv.PKV_OPT_TMA_BOX, pkv.PKV_OPT_TAIL, pkv.PKV_OPT_PACE, pkv.PKV_OPT_MATH)
+           pkv.PKV_OPT_TMA_BOX, pkv.PKV_OPT_TAIL, pkv.PKV_OPT_PACE, pkv.PKV_OPT_MATH,
+           pkv.PKV_OPT_UMMA, pkv.PKV_OPT_PREFETCH)
 
 
 @pytest.fixture(scope="module")
@@ -62,11 +63,11 @@ def call_args(d, out, **over):
     a = dict(q=d.q.data_ptr(), k=d.k_cache.data_ptr(), v=d.v_cache.data_ptr(), nb=w.num_blocks,
              tables=d.tables.data_ptr(), mb=w.max_blocks_per_seq, lens=d.lens.data_ptr(),
              S=w.num_seqs, nq=w.n_query_per_seq, Hq=w.num_q_heads, Hkv=w.num_kv_heads,
-             D=w.head_dim, scale=float(w.scale), out=out.data_ptr(),
+             D=w.head_dim, scale=float(w.scale), out_ptr=out.data_ptr(),
              dtype=pkv.PKV_FP32 if out.dtype == torch.float32 else pkv.PKV_BF16)
     a.update(over)
     return [a[k] for k in ("q", "k", "v", "nb", "tables", "mb", "lens", "S", "nq", "Hq", "Hkv",
-                           "D", "scale", "out", "dtype")]
+                           "D", "scale", "out_ptr", "dtype")]
 
 
 def static_call(lib, d, out, stream=None, **over):
@@ -119,8 +120,8 @@ def test_static_scratch_fp32_output_on_a_second_stream(lib):
 
 
 def test_static_scratch_refuses_oversized_geometry(lib):
-    # 32 query rows per kv head and 1000 CTAs: ~130 MiB of split-K scratch
-    w = W.make_custom(4, 4, 64, 8, 128, [40, 50, 60, 70], seed=7)
+    # 64 query rows per kv head and 1000 CTAs: over 60 MiB of split-K scratch
+    w = W.make_custom(4, 4, 128, 8, 128, [40, 50, 60, 70], seed=7)
     d = DeviceStep(w, torch)
     pkv.set_option(pkv.PKV_OPT_NUM_CTAS, 1000)    # scratch grows with the grid
     out = torch.zeros_like(d.out)
@@ -137,7 +138,7 @@ INVALID = [
     ("no pool blocks", dict(nb=0)),
     ("no table columns", dict(mb=0)),
     ("q not 16-byte aligned", "q+2"),
-    ("null output", dict(out=0)),
+    ("null output", dict(out_ptr=0)),
     ("null tables", dict(tables=0)),
     ("negative sequence count", dict(S=-1)),
 ]
