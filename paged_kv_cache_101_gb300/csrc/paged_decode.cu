@@ -1907,7 +1907,7 @@ int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int 
         P.ntw = 0;
         P.HG = 1;
         P.n_hg = Hkv;
-        P.threads = 320;
+        P.threads = 352;
         P.stage_bytes = 65536;
         P.nst = umma_stages(P.rows_pad);
         P.smem = umma_smem_bytes(P.rows_pad);

@@ -30,15 +30,17 @@
 //    more than 2^8 (exact: the output is normalised by a sum taken with the same
 //    max), and writes its part of the P^T row as a bf16 hi + lo pair (P = hi + lo
 //    to 2^-16) to shared memory.
-//  * Values, d on M: O^T[128 dims][N rows] += V^T . P^T (M = 128, N, K = 16 tokens
-//    per MMA, twice: hi and lo), and the row sums L[.][N rows] += 1 . P^T with an
-//    all-ones A operand held in TMEM, both accumulated in TMEM across the segment.
-//  * A segment's end: thread d of a team reads its TMEM rows of O^T and L, divides
-//    and writes the output (whole sequence in the cell), or writes the partial
-//    (m, l, acc) the merge kernel folds.
+//    Row sums are reduced over each warp's 32 tokens by a butterfly and kept per
+//    lane.
+//  * Values, d on M: O^T[128 dims][hi | lo] += V^T . [P_hi | P_lo]^T (M = 128,
+//    N = 2 x rows, K = 16 tokens per MMA), accumulated in TMEM across the segment.
+//  * A segment's end: thread d of a team reads its TMEM rows of O^T (hi + lo),
+//    divides by the row sums and writes the output (whole sequence in the cell),
+//    or writes the partial (m, l, acc) the merge kernel folds.
 //
 // Warps: 0 produces (TMA), 1 issues the MMAs (one elected lane) and owns the TMEM
-// allocation, 2-9 run the softmax and the epilogue. Every mbarrier wait is bounded
+// allocation, 2-9 run the softmax and the epilogue, 10 prefetches the tiles into L2
+// ahead of their loads. Every mbarrier wait is bounded
 // (2 s); the softmax warps decide to leave their loop only at their per-stage
 // named-barrier reduction, so no warp is left waiting on a named barrier.
 #include <cuda_bf16.h>
@@ -84,14 +86,14 @@ struct UCfg {
     // in MN-major 128-byte-swizzle atoms of 64 elements ([atom][128 tokens][128 B])
     static constexpr uint32_t PBUF = N * 512;
     static constexpr uint32_t P_ATOM = 16384;        // one 64-element atom of 128 token rows
-    // TMEM columns: S^T x 2 [0, 2N); O^T hi | lo [2N, 4N); row sums L hi | lo
-    // [4N, 6N); the all-ones A operand of the row sums (8 columns)
-    static constexpr uint32_t O_COL = 2 * N, L_COL = 4 * N, ONES_COL = 6 * N;
-    static constexpr uint32_t NCOLS = 6 * N + 8 <= 256 ? 256 : 512;
+    // TMEM columns: S^T x 2 [0, 2N); O^T hi | lo [2N, 4N)
+    static constexpr uint32_t O_COL = 2 * N;
+    static constexpr uint32_t NCOLS = 4 * N <= 128 ? 128 : 256;
     static constexpr uint32_t OFF_Q = NS * kSsBytes;
     static constexpr uint32_t OFF_P = OFF_Q + 2 * QBUF;
-    static constexpr uint32_t OFF_RED = OFF_P + PBUF;  // red_m [N][4], mrow [N], frow [N]
-    static constexpr uint32_t OFF_HDR = OFF_RED + 6 * N * 4;
+    // red_m [N][4], red_l [N][4], mrow [N], frow [N]
+    static constexpr uint32_t OFF_RED = OFF_P + PBUF;
+    static constexpr uint32_t OFF_HDR = OFF_RED + 10 * N * 4;
     // barriers: full[NS], empty[NS], q_full[2], q_free[2], s_full[2], s_free[2],
     // p_full, p_free, o_free, done
     static constexpr int NBAR = 2 * NS + 12;
@@ -106,7 +108,8 @@ struct USmem {
     UHdr *hdr;
     uint64_t *bar;
     uint32_t *tslot;
-    float *red_m, *mrow, *frow;
+    float *red_m, *red_l, *mrow, *frow;
+    volatile int *progress;  // blocks of the cell handed to shared memory (producer -> prefetch)
     __device__ uint8_t *stage(int i) const { return base + uint32_t(i) * kSsBytes; }
     __device__ uint8_t *qbuf(int b) const { return base + UCfg<N>::OFF_Q + uint32_t(b) * UCfg<N>::QBUF; }
     __device__ uint32_t full(int i) const { return smem_u32(bar + i); }
@@ -130,10 +133,12 @@ __device__ __forceinline__ USmem<N> ucarve(uint8_t *raw)
     s.hdr = reinterpret_cast<UHdr *>(s.base + C::OFF_HDR);
     s.bar = reinterpret_cast<uint64_t *>(s.base + C::OFF_BAR);
     s.tslot = reinterpret_cast<uint32_t *>(s.base + C::OFF_TSLOT);
+    s.progress = reinterpret_cast<volatile int *>(s.tslot + 2);
     float *red = reinterpret_cast<float *>(s.base + C::OFF_RED);
     s.red_m = red;
-    s.mrow = red + 4 * N;
-    s.frow = red + 5 * N;
+    s.red_l = red + 4 * N;
+    s.mrow = red + 8 * N;
+    s.frow = red + 9 * N;
     return s;
 }
 
@@ -170,7 +175,8 @@ __device__ void producer_umma(const CUtensorMap *kmap, const CUtensorMap *vmap,
     }
 
     uint32_t st = 0, phase = 0, issued = 0;
-    int qseg = 0;  // segments started: Q buffer qseg & 1
+    int handed = 0;  // blocks of the cell handed to shared memory so far
+    int qseg = 0;    // segments started: Q buffer qseg & 1
     bool ok = true;
     const uint64_t pol = policy_evict_first();
     const uint32_t qbytes = uint32_t(2 * 128 * p.G * p.nq);
@@ -202,39 +208,6 @@ __device__ void producer_umma(const CUtensorMap *kmap, const CUtensorMap *vmap,
         SeqInfo si = seq_info(p, s);
         b += si.b0;
         bool cell_first = true;
-        // L2 prefetch: a second cursor walks the same units up to p.pf_units blocks
-        // ahead of those handed to shared memory and prefetches their tiles, so the
-        // super-stages' loads meet L2 latency, not DRAM latency
-        int pf_hg = hg, pf_s = s, pf_b = b;
-        SeqInfo pf_si = si;
-        int64_t pf_u = a, main_u = a;
-        auto prefetch_ahead = [&]() {
-            while (pf_u < e && pf_u < main_u + p.pf_units) {
-                const int pf_end = pf_si.b0 + pf_si.nb;
-                const int64_t left = e - pf_u;
-                const int n0 = min(kSsBlocks, pf_end - pf_b);
-                const int n = int64_t(n0) < left ? n0 : int(left);
-                if (lane < 4 * n) {
-                    const int phys =
-                        __ldg(p.block_tables + int64_t(pf_si.tr) * p.MB + pf_b + (lane >> 2));
-                    if (phys >= 0 && int64_t(phys) < p.num_blocks)
-                        tma_prefetch_l2_5d((lane >> 1) & 1 ? vmap : kmap, 0, lane & 1, pf_hg, 0,
-                                           phys);
-                }
-                pf_u += n;
-                pf_b += n;
-                if (pf_b == pf_end && pf_u < e) {
-                    do {
-                        if (++pf_s == S) {
-                            pf_s = 0;
-                            ++pf_hg;
-                        }
-                        pf_si = seq_info(p, pf_s);
-                    } while (pf_si.nb == 0);
-                    pf_b = pf_si.b0;
-                }
-            }
-        };
         for (int64_t u = a; u < e && ok;) {
             const int b_end = si.b0 + si.nb;
             const int64_t left = e - u;
@@ -264,8 +237,6 @@ __device__ void producer_umma(const CUtensorMap *kmap, const CUtensorMap *vmap,
                     }
                 }
                 const bool first = c0 == 0, last = c0 + nbv == seg_len;
-                prefetch_ahead();
-                main_u += nbv;
                 int w_ok = 1;
                 if (lane == 0) {
                     if (issued >= uint32_t(C::NS))
@@ -312,6 +283,9 @@ __device__ void producer_umma(const CUtensorMap *kmap, const CUtensorMap *vmap,
                                      pol);
                 }
                 __syncwarp();
+                handed += nbv;
+                if (lane == 0)
+                    *sm.progress = handed;  // for the L2 prefetch warp
                 ++issued;
                 if (++st == uint32_t(C::NS)) {
                     st = 0;
@@ -338,6 +312,8 @@ __device__ void producer_umma(const CUtensorMap *kmap, const CUtensorMap *vmap,
         }
     }
 
+    if (lane == 0)
+        *sm.progress = INT_MAX;  // the prefetch warp may finish its walk
     if (ok) {
         // end-of-work marker (no bytes: a plain arrival)
         int w_ok = 1;
@@ -375,6 +351,96 @@ __device__ void producer_umma(const CUtensorMap *kmap, const CUtensorMap *vmap,
     }
 }
 
+// ------------------------------------------------------------------ L2 prefetch
+// Walks the same units as the producer, in the same order, and prefetches each
+// block's K and V tiles into L2 (no shared memory, no completion) while keeping
+// at most p.pf_units blocks ahead of the blocks the producer has handed to shared
+// memory: the super-stages' loads then meet L2 latency rather than DRAM latency,
+// so the few 64 KiB super-stages shared memory holds suffice. A hint only: a
+// prefetch that is late, early or skipped changes no result.
+template <int N>
+__device__ void prefetch_umma(const CUtensorMap *kmap, const CUtensorMap *vmap,
+                              const DecodeParams &p, const USmem<N> &sm, int lane)
+{
+    const unsigned FULLMASK = 0xffffffffu;
+    const int S = p.S;
+    const int per = (S + 31) / 32;
+    const int s_lo = min(S, lane * per), s_hi = min(S, s_lo + per);
+    int local = 0;
+    for (int s = s_lo; s < s_hi; ++s)
+        local += seq_blocks(p, s);
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(FULLMASK, incl, o);
+        if (lane >= o)
+            incl += v;
+    }
+    const int base = incl - local;
+    const int nb_total = __shfl_sync(FULLMASK, incl, 31);
+    const Cells Cc = make_cells(p, nb_total, int(gridDim.x));
+    const int64_t a = Cc.start(blockIdx.x), e = Cc.start(blockIdx.x + 1);
+    if (a >= e || p.pf_units <= 0)
+        return;
+    const int hg0 = int(a / nb_total);
+    const int r0 = int(a - int64_t(hg0) * nb_total);
+    const unsigned own = __ballot_sync(FULLMASK, local > 0 && r0 >= base && r0 < base + local);
+    const int src = __ffs(own) - 1;
+    int s_f = 0, b_f = 0;
+    if (lane == src) {
+        int run = base;
+        for (int s = s_lo; s < s_hi; ++s) {
+            const int nb = seq_blocks(p, s);
+            if (r0 < run + nb) {
+                s_f = s;
+                b_f = r0 - run;
+                break;
+            }
+            run += nb;
+        }
+    }
+    int hg = hg0;
+    int s = __shfl_sync(FULLMASK, s_f, src);
+    SeqInfo si = seq_info(p, s);
+    int b = __shfl_sync(FULLMASK, b_f, src) + si.b0;
+    int64_t u = a;
+    uint64_t t0 = 0;
+    while (u < e) {
+        // stay within p.pf_units blocks of what the producer has handed over
+        const int done = *sm.progress;
+        if (int64_t(done) + p.pf_units <= u - a) {
+            if (t0 == 0)
+                t0 = global_timer_ns();
+            else if (global_timer_ns() - t0 > kWaitLimitNs)
+                return;  // the producer stopped: nothing left worth prefetching
+            __nanosleep(256);
+            continue;
+        }
+        t0 = 0;
+        const int b_end = si.b0 + si.nb;
+        const int64_t left = e - u;
+        const int n0 = min(kSsBlocks, b_end - b);
+        const int n = int64_t(n0) < left ? n0 : int(left);
+        if (lane < 4 * n) {  // lane 4j + 2t + h: block j, tensor t, half h
+            const int phys = __ldg(p.block_tables + int64_t(si.tr) * p.MB + b + (lane >> 2));
+            if (phys >= 0 && int64_t(phys) < p.num_blocks)
+                tma_prefetch_l2_5d((lane >> 1) & 1 ? vmap : kmap, 0, lane & 1, hg, 0, phys);
+        }
+        u += n;
+        b += n;
+        if (b == b_end && u < e) {
+            do {
+                if (++s == S) {
+                    s = 0;
+                    ++hg;
+                }
+                si = seq_info(p, s);
+            } while (si.nb == 0);
+            b = si.b0;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ MMA issue
 // One thread issues, in order of readiness, the scores of the next super-stage
 // (once its tiles and, for a segment's first, its queries have landed and the S^T
@@ -386,8 +452,7 @@ __device__ void mma_umma(const DecodeParams &p, const USmem<N> &sm, uint32_t tme
     using C = UCfg<N>;
     constexpr uint32_t kIdS = umma_idesc_bf16(128, N, false, false);       // K, Q: K-major
     constexpr uint32_t kIdO = umma_idesc_bf16(128, 2 * N, true, true);     // V^T, P^T: MN-major
-    constexpr uint32_t kIdL = umma_idesc_bf16(128, 2 * N, false, true);    // ones (TMEM), P^T
-    const uint32_t o_col = tmem + C::O_COL, l_col = tmem + C::L_COL, ones = tmem + C::ONES_COL;
+    const uint32_t o_col = tmem + C::O_COL;
     // descriptors at the tiles' starts; a step adds its byte offset >> 4 (no field
     // carries: every tile lies below 256 KiB)
     const uint64_t d_p = umma_sdesc(smem_u32(sm.base + C::OFF_P), N == 32 ? 1024 : C::P_ATOM,
@@ -410,7 +475,7 @@ __device__ void mma_umma(const DecodeParams &p, const USmem<N> &sm, uint32_t tme
         // ---- scores of super-stage ns
         if (!end_seen && ns - npv < 2) {
             const int st = int(ns % uint32_t(C::NS));
-            if (mbar_try_wait(sm.full(st), (ns / uint32_t(C::NS)) & 1u)) {
+            if (mbar_test_wait(sm.full(st), (ns / uint32_t(C::NS)) & 1u)) {
                 const UHdr h = sm.hdr[st];
                 if (h.flags & F_END) {
                     end_seen = true;
@@ -419,8 +484,8 @@ __device__ void mma_umma(const DecodeParams &p, const USmem<N> &sm, uint32_t tme
                     const bool first = (h.flags & F_FIRST) != 0;
                     const int g = first ? g_s + 1 : g_s;
                     const uint32_t bsel = ns & 1u;
-                    if ((!first || mbar_try_wait(sm.q_full(g & 1), uint32_t((g >> 1) & 1))) &&
-                        mbar_try_wait(sm.s_free(int(bsel)), ((ns >> 1) & 1u) ^ 1u)) {
+                    if ((!first || mbar_test_wait(sm.q_full(g & 1), uint32_t((g >> 1) & 1))) &&
+                        mbar_test_wait(sm.s_free(int(bsel)), ((ns >> 1) & 1u) ^ 1u)) {
                         tc_fence_after();
                         g_s = g;
                         const uint64_t dk = d_k0 + uint64_t(st) * kStageStep;
@@ -446,10 +511,10 @@ __device__ void mma_umma(const DecodeParams &p, const USmem<N> &sm, uint32_t tme
             }
         }
         // ---- values and row sums of super-stage npv
-        if (npv < ns && mbar_try_wait(sm.p_full(), npv & 1u)) {
+        if (npv < ns && mbar_test_wait(sm.p_full(), npv & 1u)) {
             const bool seg_first = (first_of >> (npv & 1u)) & 1u;
             const int g = (npv & 1u) ? seg_odd : seg_even;
-            if (!seg_first || mbar_try_wait(sm.o_free(), uint32_t(g & 1) ^ 1u)) {
+            if (!seg_first || mbar_test_wait(sm.o_free(), uint32_t(g & 1) ^ 1u)) {
                 tc_fence_after();
                 const int st = int(npv % uint32_t(C::NS));
                 const uint64_t dv = d_v0 + uint64_t(st) * kStageStep;
@@ -458,10 +523,6 @@ __device__ void mma_umma(const DecodeParams &p, const USmem<N> &sm, uint32_t tme
                     umma_bf16(o_col, dv + uint64_t(kk * 2048 >> 4), d_p + uint64_t(kk * 2048 >> 4),
                               kIdO, !(seg_first && kk == 0));
                 umma_commit(sm.empty(st));
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    umma_bf16_tmem_a(l_col, ones, d_p + uint64_t(kk * 2048 >> 4), kIdL,
-                                     !(seg_first && kk == 0));
                 umma_commit(sm.p_free());
                 ++npv;
                 progressed = true;
@@ -483,11 +544,11 @@ __device__ void mma_umma(const DecodeParams &p, const USmem<N> &sm, uint32_t tme
 }
 
 // ------------------------------------------------------------------ softmax + epilogue
-// Row maxima of R values per lane over the warp's 32 lanes (a butterfly that halves
-// the values each step): on return v[0] holds the maximum of row
+// Row maxima (or sums) of R values per lane over the warp's 32 lanes (a butterfly
+// that halves the values each step): on return v[0] holds the result of row
 // (lane >> (5 - log2 R)), the same in the 32 / R lanes that share that row.
-template <int R>
-__device__ __forceinline__ void warp_row_max(float (&v)[R], int lane)
+template <int R, bool SUM = false>
+__device__ __forceinline__ void warp_row_reduce(float (&v)[R], int lane)
 {
 #pragma unroll
     for (int step = 0; step < 5; ++step) {
@@ -500,11 +561,13 @@ __device__ __forceinline__ void warp_row_max(float (&v)[R], int lane)
                 if (k < len) {
                     const float send = upper ? v[k] : v[k + len];
                     const float keep = upper ? v[k + len] : v[k];
-                    v[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, off));
+                    const float got = __shfl_xor_sync(0xffffffffu, send, off);
+                    v[k] = SUM ? keep + got : fmaxf(keep, got);
                 }
             }
         } else {
-            v[0] = fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], off));
+            const float got = __shfl_xor_sync(0xffffffffu, v[0], off);
+            v[0] = SUM ? v[0] + got : fmaxf(v[0], got);
         }
     }
 }
@@ -524,23 +587,14 @@ __device__ void softmax_umma(const DecodeParams &p, const USmem<N> &sm, uint32_t
     const int tt = team * 128 + t;             // index among the 256 softmax threads
     const int row0 = team * R2;
     const uint32_t lane_base = tmem + (uint32_t(q4 * 32) << 16);
-    // this team's rows in the hi and lo column halves of O^T and of the row sums
+    // this team's rows in the hi and lo column halves of O^T
     const uint32_t o_col = lane_base + C::O_COL + uint32_t(row0);
-    const uint32_t l_col = lane_base + C::L_COL + uint32_t(row0);
+    const int own = lane >> (5 - LOG_R2);  // the row (of the team's) whose sum this lane keeps
+    float lsum = 0.f;                      // that row's sum over this warp's tokens
     uint8_t *pbuf = sm.base + C::OFF_P;
     volatile int *exit_flag = reinterpret_cast<volatile int *>(sm.tslot + 1);
     if (tt == 0)
         *exit_flag = 0;
-    if (team == 0) {
-        // the all-ones A operand of the row sums: 16 bf16 ones per lane (8 columns)
-        const float one2 = __uint_as_float(0x3F803F80u);
-        const float ones[32] = {one2, one2, one2, one2, one2, one2, one2, one2,
-                                one2, one2, one2, one2, one2, one2, one2, one2,
-                                one2, one2, one2, one2, one2, one2, one2, one2,
-                                one2, one2, one2, one2, one2, one2, one2, one2};
-        tmem_st32<0>(lane_base + C::ONES_COL, ones);
-        tmem_wait_st();
-    }
     tc_fence_before();
     bar_sync_named(1, 256);
 
@@ -591,6 +645,8 @@ __device__ void softmax_umma(const DecodeParams &p, const USmem<N> &sm, uint32_t
             tc_fence_before();
             mbar_arrive(sm.s_free(int(bsel)));
             first = (h.flags & F_FIRST) != 0;
+            if (first)
+                lsum = 0.f;
             // scale (log2 domain); tokens outside the stage's blocks or past the
             // context, and positions a row does not see, are masked
             const int tok = h.b0 * kBlockSize + t;
@@ -629,8 +685,7 @@ __device__ void softmax_umma(const DecodeParams &p, const USmem<N> &sm, uint32_t
 #pragma unroll
             for (int r = 0; r < R2; ++r)
                 bm[r] = x[r];
-            warp_row_max<R2>(bm, lane);
-            const int own = lane >> (5 - LOG_R2);  // the row this lane's result belongs to
+            warp_row_reduce<R2>(bm, lane);
             if ((lane & ((1 << (5 - LOG_R2)) - 1)) == 0)
                 sm.red_m[(row0 + own) * 4 + q4] = bm[0];
             bar_sync_named(1, 256);
@@ -654,9 +709,10 @@ __device__ void softmax_umma(const DecodeParams &p, const USmem<N> &sm, uint32_t
                 // (O^T, then the row sums) once the previous stage's MMAs have landed
                 wait(sm.p_free(), (i - 1) & 1u);
                 tc_fence_after();
+                lsum *= sm.frow[row0 + own];
 #pragma unroll 1
-                for (int acc = 0; acc < 4; ++acc) {  // O^T hi, lo; row sums hi, lo
-                    const uint32_t col = (acc < 2 ? o_col : l_col) + uint32_t((acc & 1) * N);
+                for (int acc = 0; acc < 2; ++acc) {  // O^T hi, lo
+                    const uint32_t col = o_col + uint32_t(acc * N);
                     float a[32];
                     if constexpr (R2 == 16)
                         tmem_ld16(col, a);
@@ -682,6 +738,14 @@ __device__ void softmax_umma(const DecodeParams &p, const USmem<N> &sm, uint32_t
             const float mr = mrow(r);
             const float mu = mr == -INFINITY ? 0.f : mr;
             x[r] = ex2(x[r] - mu);  // 0 for a masked token
+        }
+        {
+            float rs[R2];
+#pragma unroll
+            for (int r = 0; r < R2; ++r)
+                rs[r] = x[r];
+            warp_row_reduce<R2, true>(rs, lane);
+            lsum += rs[0];
         }
         if (i > 0)
             wait(sm.p_free(), (i - 1) & 1u);  // the previous stage's MMAs have read P^T
@@ -723,6 +787,9 @@ __device__ void softmax_umma(const DecodeParams &p, const USmem<N> &sm, uint32_t
             // the hi and lo halves of O^T and of the row sums, added, 16 rows at a time;
             // the output (the whole sequence in this cell) or the partial (m, l, acc)
             // for the merge kernel leaves as each chunk is read
+            if ((lane & ((1 << (5 - LOG_R2)) - 1)) == 0)
+                sm.red_l[(row0 + own) * 4 + q4] = lsum;
+            bar_sync_named(1, 256);
             const int rows_v = p.G * h.ql;
             const int d = t;
             const int64_t cb = int64_t(h.cell) * 2 + h.slot;
@@ -737,12 +804,12 @@ __device__ void softmax_umma(const DecodeParams &p, const USmem<N> &sm, uint32_t
 #pragma unroll
                     for (int r = 0; r < 16; ++r)
                         o[r] = a[r] + b[r];
-                    tmem_ld16(l_col + 16 * c16, a);
-                    tmem_ld16(l_col + N + 16 * c16, b);
-                    tmem_wait_ld();
 #pragma unroll
-                    for (int r = 0; r < 16; ++r)
-                        l[r] = a[r] + b[r];
+                    for (int r = 0; r < 16; ++r) {
+                        const float4 w =
+                            *reinterpret_cast<const float4 *>(sm.red_l + 4 * (row0 + 16 * c16 + r));
+                        l[r] = (w.x + w.y) + (w.z + w.w);
+                    }
                 }
 #pragma unroll
                 for (int r = 0; r < 16; ++r) {
@@ -777,7 +844,7 @@ __device__ void softmax_umma(const DecodeParams &p, const USmem<N> &sm, uint32_t
 }  // namespace
 
 template <int N>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     paged_decode_umma_kernel(const __grid_constant__ CUtensorMap kmap,
                              const __grid_constant__ CUtensorMap vmap,
                              const __grid_constant__ CUtensorMap qmap, const DecodeParams p)
@@ -805,6 +872,7 @@ __global__ void __launch_bounds__(320, 1)
         mbar_init(sm.o_free(), 256);
         mbar_init(sm.done(), 1);
         fence_mbar_init();
+        *sm.progress = 0;
     }
     // Q rows past a segment's G * nq (padding up to N) are never written by the
     // copies: they hold zeros so the padding scores stay finite
@@ -825,8 +893,10 @@ __global__ void __launch_bounds__(320, 1)
         if (lane == 0)
             mma_umma<N>(p, sm, tmem);
         __syncwarp();
-    } else {
+    } else if (warp < 10) {
         softmax_umma<N>(p, sm, tmem, warp, lane);
+    } else {
+        prefetch_umma<N>(&kmap, &vmap, p, sm, lane);
     }
     tc_fence_before();
     __syncthreads();
@@ -861,7 +931,7 @@ static cudaError_t launch_umma_n(const DecodePlan &pl, const DecodeParams &p,
         return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(pl.grid));
-    cfg.blockDim = dim3(320);
+    cfg.blockDim = dim3(352);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
