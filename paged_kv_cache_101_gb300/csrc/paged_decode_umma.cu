@@ -21,9 +21,12 @@
 //    grid streams one contiguous cell, and a stage is one block of the group's K
 //    and V ([head][64-dim half][16 tokens][64] bf16, the 128-byte swizzle TMA
 //    writes) in a ring of shared-memory stages released block by block.
-//  * Scores, rows on M: S_h[64 rows][16 tokens] = Q_h . K_h^T per head (M = 64,
-//    N = 16, K = 128 dims) into TMEM. Q_h holds the sequence's G * nq query rows
-//    (zero rows up to 64) and is staged by TMA at every segment's start.
+//  * Scores, rows on M: S_h[64 rows][16 tokens] = Q_h . K_h^T per head and block
+//    (M = 64, N = 16, K = 128 dims) into TMEM. Q_h holds the sequence's G * nq
+//    query rows (zero rows up to 64) and is staged by TMA at every segment's start.
+//    Blocks go through scores, softmax and values in groups of two consecutive
+//    blocks of a segment, and two groups are in flight (S and P double-buffered in
+//    TMEM), so the MMA-softmax-MMA round trip is paid once per 32 KiB.
 //  * Softmax: the thread of row r (lane r % 16 of the warp in TMEM lane quarter
 //    r / 16, the M = 64 data-path layout) reads its 16 scores, masks, keeps the
 //    row's running max m and sum l in registers, raises m only when a score exceeds
@@ -74,12 +77,17 @@ constexpr int kM = 64;                      // MMA rows: up to 64 query rows per
 constexpr uint32_t kQHead = kM * 256;       // Q of one head: [2 halves][64 rows][128 B]
 constexpr uint32_t kStageBytes = kHG * 8192;
 constexpr float kLazyLog2 = 8.f;            // raise the running max past a 2^8 lead
-// TMEM columns of head h: S [2 x 16], P [2 buffers x (hi 8 | lo 8)], O [128]
-constexpr uint32_t kColsHead = 192;
+// Blocks are scored, exponentiated and multiplied in groups of up to two
+// consecutive blocks of a segment; a group's last block carries kGroupEnd.
+constexpr int kNBG = 2;
+constexpr int32_t kGroupEnd = 64;
+// TMEM columns of head h: S [2 groups][2 blocks][16], P [2 groups][2 blocks]
+// [hi 8 | lo 8], O [128]
+constexpr uint32_t kColsHead = 256;
 constexpr uint32_t kNCols = 512;
-__host__ __device__ constexpr uint32_t col_s(int h, int b) { return uint32_t(h) * kColsHead + uint32_t(b) * 16; }
-__host__ __device__ constexpr uint32_t col_p(int h, int b) { return uint32_t(h) * kColsHead + 32 + uint32_t(b) * 16; }
-__host__ __device__ constexpr uint32_t col_o(int h) { return uint32_t(h) * kColsHead + 64; }
+__host__ __device__ constexpr uint32_t col_s(int h, int g, int k) { return uint32_t(h) * kColsHead + uint32_t(g * kNBG + k) * 16; }
+__host__ __device__ constexpr uint32_t col_p(int h, int g, int k) { return uint32_t(h) * kColsHead + 64 + uint32_t(g * kNBG + k) * 16; }
+__host__ __device__ constexpr uint32_t col_o(int h) { return uint32_t(h) * kColsHead + 128; }
 
 // Shared memory: NS stages, the group's Q, the stage headers and the barriers.
 struct USmem {
@@ -231,7 +239,8 @@ __device__ void producer_umma(const CUtensorMap *kmap, const CUtensorMap *vmap,
                 h->T = si.T;
                 h->hg = hg;
                 h->flags = (first ? F_FIRST : 0) | (last ? F_LAST : 0) |
-                           (last && seg_b0 == si.b0 && b == b_end - 1 ? F_DIRECT : 0);
+                           (last && seg_b0 == si.b0 && b == b_end - 1 ? F_DIRECT : 0) |
+                           (last || ((b - seg_b0) % kNBG) == kNBG - 1 ? kGroupEnd : 0);
                 h->slot = cell_first ? 0 : 1;
                 h->cell = int(cell);
                 h->ql = int16_t(si.ql);
@@ -327,9 +336,10 @@ __device__ void producer_umma(const CUtensorMap *kmap, const CUtensorMap *vmap,
 
 // ------------------------------------------------------------------ MMA issue
 // One thread issues, in order of readiness, the scores of the next block (once its
-// tiles and, for a segment's first, the queries have landed and the S buffer is
-// free) and the values of the oldest scored block (once both heads' P is in TMEM):
-// neither waits for the other's inputs. Polls never suspend the thread.
+// tiles and, for a segment's first, the queries have landed and, for a group's
+// first, the group's S buffer is free) and the values of the oldest scored group
+// (once both heads' P of it is in TMEM): neither waits for the other's inputs.
+// Polls never suspend the thread.
 __device__ void mma_umma(const DecodeParams &p, const USmem &sm, uint32_t tmem)
 {
     const int NS = sm.ns;
@@ -342,20 +352,22 @@ __device__ void mma_umma(const DecodeParams &p, const USmem &sm, uint32_t tmem)
     const uint64_t d_q0 = umma_sdesc(smem_u32(sm.q(0)), 16, 1024, kSw128);
     constexpr uint64_t kStageStep = kStageBytes >> 4;
 
-    uint32_t ns = 0, npv = 0;  // blocks scored, and whose values are issued
-    int segs = -1;             // segments scored
-    // whether each of the (at most two) scored, value-pending blocks opens its
-    // segment, and that segment's index, by parity
-    uint32_t first_of = 0;
-    int seg_even = 0, seg_odd = 0;
+    uint32_t nb = 0;            // blocks scored
+    uint32_t gs = 0, kk_s = 0;  // groups whose scoring started; blocks of the open one
+    uint32_t gpv = 0;           // groups whose values are issued
+    int segs = -1;              // segments scored
+    // per group buffer (parity): its stages, block count, segment, and whether it
+    // opens its segment
+    int g_st[2][kNBG] = {}, g_n[2] = {}, g_seg[2] = {};
+    bool g_first[2] = {};
     bool end_seen = false, ok = true;
     uint64_t t_idle = 0;
-    while (ok && !(end_seen && npv == ns)) {
+    while (ok && !(end_seen && gpv == gs && kk_s == 0)) {
         bool progressed = false;
-        // ---- scores of block ns: S_h = Q_h . K_h^T over the 8 16-dim steps
-        if (!end_seen && ns - npv < 2) {
-            const int st = int(ns % uint32_t(NS));
-            if (mbar_test_wait(sm.full(st), (ns / uint32_t(NS)) & 1u)) {
+        // ---- scores of block nb: S_h = Q_h . K_h^T over the 8 16-dim steps
+        if (!end_seen && (kk_s > 0 || gs - gpv < 2)) {
+            const int st = int(nb % uint32_t(NS));
+            if (mbar_test_wait(sm.full(st), (nb / uint32_t(NS)) & 1u)) {
                 const UHdr h = sm.hdr[st];
                 if (h.flags & F_END) {
                     end_seen = true;
@@ -363,9 +375,9 @@ __device__ void mma_umma(const DecodeParams &p, const USmem &sm, uint32_t tmem)
                 } else {
                     const bool first = (h.flags & F_FIRST) != 0;
                     const int g = first ? segs + 1 : segs;
-                    const uint32_t bsel = ns & 1u;
-                    if ((!first || mbar_test_wait(sm.q_full(), uint32_t(g & 1))) &&
-                        mbar_test_wait(sm.s_free(int(bsel)), ((ns >> 1) & 1u) ^ 1u)) {
+                    const uint32_t gb = gs & 1u;
+                    if ((kk_s > 0 || mbar_test_wait(sm.s_free(int(gb)), ((gs >> 1) & 1u) ^ 1u)) &&
+                        (!first || mbar_test_wait(sm.q_full(), uint32_t(g & 1)))) {
                         tc_fence_after();
                         segs = g;
                         const uint64_t dk = d_k0 + uint64_t(st) * kStageStep;
@@ -378,46 +390,50 @@ __device__ void mma_umma(const DecodeParams &p, const USmem &sm, uint32_t tmem)
                                                              (kk & 3) * 32) >> 4;
                                 const uint64_t qo = uint64_t(hl * kQHead + (kk >> 2) * (kM * 128) +
                                                              (kk & 3) * 32) >> 4;
-                                umma_bf16(tmem + col_s(hl, int(bsel)), d_q0 + qo, dk + ko, kIdS,
-                                          kk > 0);
+                                umma_bf16(tmem + col_s(hl, int(gb), int(kk_s)), d_q0 + qo, dk + ko,
+                                          kIdS, kk > 0);
                             }
                         }
-                        umma_commit(sm.s_full(int(bsel)));
                         if (h.flags & F_LAST)
                             umma_commit(sm.q_free());  // the segment's Q is read
-                        if (bsel)
-                            seg_odd = g;
-                        else
-                            seg_even = g;
-                        first_of = (first_of & ~(1u << bsel)) | (uint32_t(first) << bsel);
-                        ++ns;
+                        if (kk_s == 0) {
+                            g_first[gb] = first;
+                            g_seg[gb] = g;
+                        }
+                        g_st[gb][kk_s] = st;
+                        ++kk_s;
+                        ++nb;
+                        if (h.flags & kGroupEnd) {
+                            umma_commit(sm.s_full(int(gb)));
+                            g_n[gb] = int(kk_s);
+                            kk_s = 0;
+                            ++gs;
+                        }
                         progressed = true;
                     }
                 }
             }
         }
-        // ---- values of block npv: O_h += P_hi . V_h + P_lo . V_h
-        const uint32_t pb = npv & 1u;
-        if (npv < ns && mbar_test_wait(sm.p_full(int(pb)), (npv >> 1) & 1u)) {
-            const bool seg_first = (first_of >> pb) & 1u;
-            const int g = pb ? seg_odd : seg_even;
-            if (!seg_first || mbar_test_wait(sm.o_free(), uint32_t(g & 1) ^ 1u)) {
-                tc_fence_after();
-                const int st = int(npv % uint32_t(NS));
+        // ---- values of group gpv: O_h += P_hi . V_h + P_lo . V_h, block by block
+        const uint32_t pb = gpv & 1u;
+        if (gpv < gs && mbar_test_wait(sm.p_full(int(pb)), (gpv >> 1) & 1u) &&
+            (!g_first[pb] || mbar_test_wait(sm.o_free(), uint32_t(g_seg[pb] & 1) ^ 1u))) {
+            tc_fence_after();
+            for (int k = 0; k < g_n[pb]; ++k) {
+                const int st = g_st[pb][k];
                 const uint64_t dv = d_v0 + uint64_t(st) * kStageStep;
 #pragma unroll
                 for (int hl = 0; hl < kHG; ++hl) {
                     const uint64_t dvh = dv + uint64_t(hl * 4096 >> 4);
-                    umma_bf16_tmem_a(tmem + col_o(hl), tmem + col_p(hl, int(pb)), dvh, kIdO,
-                                     !seg_first);
-                    umma_bf16_tmem_a(tmem + col_o(hl), tmem + col_p(hl, int(pb)) + 8, dvh, kIdO,
-                                     true);
+                    const uint32_t pc = tmem + col_p(hl, int(pb), k);
+                    umma_bf16_tmem_a(tmem + col_o(hl), pc, dvh, kIdO, !(g_first[pb] && k == 0));
+                    umma_bf16_tmem_a(tmem + col_o(hl), pc + 8, dvh, kIdO, true);
                 }
                 umma_commit(sm.empty(st));
-                umma_commit(sm.p_free(int(pb)));
-                ++npv;
-                progressed = true;
             }
+            umma_commit(sm.p_free(int(pb)));
+            ++gpv;
+            progressed = true;
         }
         if (progressed) {
             t_idle = 0;
@@ -458,25 +474,46 @@ __device__ void softmax_umma(const DecodeParams &p, const USmem &sm, uint32_t tm
         return wait_ok;
     };
 
-    for (uint32_t i = 0;; ++i) {
-        const int st = int(i % uint32_t(NS));
-        const uint32_t bsel = i & 1u;
-        if (!wait(sm.full(st), (i / uint32_t(NS)) & 1u))
+    uint32_t i = 0;  // blocks consumed
+    for (uint32_t g = 0;; ++g) {
+        const uint32_t gb = g & 1u;
+        // the group's blocks (one or two) and their headers
+        int stk[kNBG];
+        UHdr hk[kNBG];
+        int n = 0;
+        bool end = false;
+        for (; n < kNBG; ++n) {
+            const uint32_t bi = i + uint32_t(n);
+            stk[n] = int(bi % uint32_t(NS));
+            if (!wait(sm.full(stk[n]), (bi / uint32_t(NS)) & 1u)) {
+                end = true;
+                break;
+            }
+            hk[n] = sm.hdr[stk[n]];
+            if (hk[n].flags & F_END) {
+                end = true;
+                break;
+            }
+            if (hk[n].flags & kGroupEnd) {
+                ++n;
+                break;
+            }
+        }
+        if (end)
             break;
-        const UHdr h = sm.hdr[st];
-        if (h.flags & F_END)
-            break;
+        const UHdr &h = hk[0];
+        const UHdr &hl_last = hk[n - 1];
         const int kvh = h.hg * kHG + hl;
-        if (!wait(sm.s_full(int(bsel)), (i >> 1) & 1u))
+        if (!wait(sm.s_full(int(gb)), (g >> 1) & 1u))
             break;
         tc_fence_after();
         float x[32];
-        tmem_ld16(lane_base + col_s(hl, int(bsel)), x);
+        tmem_ld32<0>(lane_base + col_s(hl, int(gb), 0), x);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0)
-            mbar_arrive(sm.s_free(int(bsel)));
+            mbar_arrive(sm.s_free(int(gb)));
         const bool first = (h.flags & F_FIRST) != 0;
         if (first) {
             m = -INFINITY;
@@ -484,28 +521,33 @@ __device__ void softmax_umma(const DecodeParams &p, const USmem &sm, uint32_t tm
         }
         // scale (log2 domain); tokens past the context, and positions the row does
         // not see, are masked
-        const int t0 = h.b * kBlockSize;
         int j = r / p.G;
         j = j < h.ql ? j : h.ql - 1;  // padding rows: the last query's rule
         const int w0 = p.tree_mask ? h.T - h.W : h.T - h.ql + 1;
-        const bool masked_block = t0 + kBlockSize - 1 >= w0;
+        const int t_end = hk[n - 1].b * kBlockSize + kBlockSize;  // one past the group's tokens
+        const bool masked_group = t_end - 1 >= w0;
         uint32_t bits = 0u;
-        if (masked_block && p.tree_mask)
+        if (masked_group && p.tree_mask)
             bits = __ldg(p.tree_mask + h.q0 + j);
         float bm = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            const int tok = t0 + c;
-            bool vis = tok < h.T;
-            if (masked_block && tok >= w0)
-                vis = vis && (p.tree_mask ? ((bits >> (tok - w0)) & 1u) != 0u
-                                          : tok <= h.T - h.ql + j);
-            x[c] = vis ? x[c] * p.scale_log2 : -INFINITY;
-            bm = fmaxf(bm, x[c]);
+        for (int k = 0; k < kNBG; ++k) {
+            const int t0 = (k < n ? hk[k].b : 0) * kBlockSize;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const int tok = t0 + c;
+                bool vis = k < n && tok < h.T;
+                if (masked_group && tok >= w0)
+                    vis = vis && (p.tree_mask ? ((bits >> (tok - w0)) & 1u) != 0u
+                                              : tok <= h.T - h.ql + j);
+                float &v = x[16 * k + c];
+                v = vis ? v * p.scale_log2 : -INFINITY;
+                bm = fmaxf(bm, v);
+            }
         }
-        // raise the running max (the first block always sets it); an accumulator
-        // holding earlier blocks of the segment is rescaled by the same factor, once
-        // the previous block's P.V has landed
+        // raise the running max (the first group always sets it); an accumulator
+        // holding earlier groups of the segment is rescaled by the same factor, once
+        // the previous group's P.V has landed
         const bool need = bm > m + kLazyLog2 || (first && bm > m);
         float f = 1.f;
         if (need) {
@@ -514,8 +556,8 @@ __device__ void softmax_umma(const DecodeParams &p, const USmem &sm, uint32_t tm
             l *= f;
         }
         if (__any_sync(0xffffffffu, need && row_lane && !first)) {
-            if (i > 0)
-                wait(sm.p_free(int((i - 1) & 1u)), ((i - 1) >> 1) & 1u);
+            if (g > 0)
+                wait(sm.p_free(int((g - 1) & 1u)), ((g - 1) >> 1) & 1u);
             tc_fence_after();
             const uint32_t oc = lane_base + col_o(hl);
 #pragma unroll 1
@@ -530,27 +572,34 @@ __device__ void softmax_umma(const DecodeParams &p, const USmem &sm, uint32_t tm
                 tmem_wait_st();
             }
         }
-        // P = 2^(x - m) as bf16 hi + lo
+        // P = 2^(x - m) as bf16 hi + lo, block by block
         const float mu = m == -INFINITY ? 0.f : m;
-        uint32_t phi[8], plo[8];
+        uint32_t phi[kNBG][8], plo[kNBG][8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const float a0 = ex2(x[2 * c] - mu), a1 = ex2(x[2 * c + 1] - mu);
-            l += a0 + a1;
-            phi[c] = pack_bf16x2(a0, a1);
-            plo[c] = pack_bf16x2(a0 - bf16lo_f32(phi[c]), a1 - bf16hi_f32(phi[c]));
+        for (int k = 0; k < kNBG; ++k)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float a0 = ex2(x[16 * k + 2 * c] - mu), a1 = ex2(x[16 * k + 2 * c + 1] - mu);
+                l += a0 + a1;
+                phi[k][c] = pack_bf16x2(a0, a1);
+                plo[k][c] = pack_bf16x2(a0 - bf16lo_f32(phi[k][c]), a1 - bf16hi_f32(phi[k][c]));
+            }
+        if (g >= 2)  // the group two back has read this P buffer
+            wait(sm.p_free(int(gb)), ((g - 2) >> 1) & 1u);
+#pragma unroll
+        for (int k = 0; k < kNBG; ++k) {
+            if (k < n) {
+                tmem_st8(lane_base + col_p(hl, int(gb), k), phi[k]);
+                tmem_st8(lane_base + col_p(hl, int(gb), k) + 8, plo[k]);
+            }
         }
-        if (i >= 2)  // the block two back has read this P buffer
-            wait(sm.p_free(int(bsel)), ((i - 2) >> 1) & 1u);
-        tmem_st8(lane_base + col_p(hl, int(bsel)), phi);
-        tmem_st8(lane_base + col_p(hl, int(bsel)) + 8, plo);
-        const int vc = h.T - t0;  // tokens of this block in the context
+        const int vc = h.T - hk[n - 1].b * kBlockSize;  // tokens of the last block in context
         if (__builtin_expect(vc < kBlockSize, 0)) {
             // the sequence's last block: its slots past the context (stale, or NaN)
             // must not reach P.V even times a zero weight. The head's 4 warps clear
-            // those rows of its V tile (both halves; whole rows, so the swizzle
-            // does not matter) and fence the writes for the tensor cores.
-            uint8_t *vt = sm.stage(st) + kStageBytes / 2 + uint32_t(hl) * 4096u;
+            // those rows of its V tile (both halves; whole rows, so the swizzle does
+            // not matter) and fence the writes for the tensor cores.
+            uint8_t *vt = sm.stage(stk[n - 1]) + kStageBytes / 2 + uint32_t(hl) * 4096u;
             for (int k = q4 * 32 + lane; k < (kBlockSize - vc) * 16; k += 128) {
                 const int row = vc + (k >> 4), c = k & 15;
                 *reinterpret_cast<uint4 *>(vt + (c >> 3) * 2048 + row * 128 + (c & 7) * 16) =
@@ -562,18 +611,20 @@ __device__ void softmax_umma(const DecodeParams &p, const USmem &sm, uint32_t tm
         tc_fence_before();
         __syncwarp();
         if (lane == 0)
-            mbar_arrive(sm.p_full(int(bsel)));
+            mbar_arrive(sm.p_full(int(gb)));
+        i += uint32_t(n);
 
-        if (h.flags & F_LAST) {
+        if (hl_last.flags & F_LAST) {
             // ---- the segment's end: this row of O_h, over the row sum
-            wait(sm.p_free(int(bsel)), (i >> 1) & 1u);
+            wait(sm.p_free(int(gb)), (g >> 1) & 1u);
             tc_fence_after();
-            const int rows_v = p.G * h.ql;
+            const UHdr &he = hl_last;
+            const int rows_v = p.G * he.ql;
             const bool live = row_lane && r < rows_v;
             const int jr = r / p.G;
-            const int64_t cb = int64_t(h.cell) * 2 + h.slot;
+            const int64_t cb = int64_t(he.cell) * 2 + he.slot;
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            const int64_t orow = (int64_t(h.q0) + jr) * p.Hq + int64_t(kvh) * p.G + (r - jr * p.G);
+            const int64_t orow = (int64_t(he.q0) + jr) * p.Hq + int64_t(kvh) * p.G + (r - jr * p.G);
             const int64_t prow = (cb * p.HG + hl) * p.rows + r;
             const uint32_t oc = lane_base + col_o(hl);
 #pragma unroll 1
@@ -583,7 +634,7 @@ __device__ void softmax_umma(const DecodeParams &p, const USmem &sm, uint32_t tm
                 tmem_wait_ld();
                 if (!live)
                     continue;
-                if (h.flags & F_DIRECT) {
+                if (he.flags & F_DIRECT) {
                     if (p.out_f32) {
                         float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) +
                                                                  orow * 128 + 32 * c32);
@@ -609,7 +660,7 @@ __device__ void softmax_umma(const DecodeParams &p, const USmem &sm, uint32_t tm
                         dst[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
                 }
             }
-            if (live && !(h.flags & F_DIRECT)) {
+            if (live && !(he.flags & F_DIRECT)) {
                 p.ml[prow * 2] = m;
                 p.ml[prow * 2 + 1] = l;
             }
