@@ -374,7 +374,8 @@ def run_pkv(args, rank, world, dist):
     pkv.set_option(pkv.PKV_OPT_PACE, 1 if args.pace else 0)
     pkv.set_option(pkv.PKV_OPT_HEADS_PER_CTA, args.heads)
     pkv.set_option(pkv.PKV_OPT_TMA_BOX, args.box)
-    pkv.set_option(pkv.PKV_OPT_UMMA, 1 if args.umma_off else 0)
+    pkv.set_option(pkv.PKV_OPT_UMMA, 1 if args.umma else 0)
+    pkv.set_option(pkv.PKV_OPT_PREFETCH, args.prefetch)
     rig = StepRig(w0, args, dev, fp8=fp8, cascade=cascade)
     del w0
     w = rig.w
@@ -787,7 +788,8 @@ def run_tree(args, rank, world, dist):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    pkv.set_option(pkv.PKV_OPT_UMMA, 1 if args.umma_off else 0)
+    pkv.set_option(pkv.PKV_OPT_UMMA, 1 if args.umma else 0)
+    pkv.set_option(pkv.PKV_OPT_PREFETCH, args.prefetch)
     # the 8B layer's lengths and heads unless a workload is named
     name = args.workload if args.workload_given else "llama3_8b_decode"
     base_lens = W.workload_lengths(name)[0]
@@ -1156,8 +1158,10 @@ def main():
                     help="PKV_OPT_HEADS_PER_CTA: cap on kv heads per CTA (0 = the planner's)")
     ap.add_argument("--box", type=int, default=0, choices=[0, 1, 2],
                     help="PKV_OPT_TMA_BOX: 0 = whole-block boxes when accepted, 1 = per tile")
-    ap.add_argument("--umma-off", action="store_true",
-                    help="PKV_OPT_UMMA = 1: the mma.sync kernels for every shape (A/B)")
+    ap.add_argument("--prefetch", type=int, default=0,
+                    help="PKV_OPT_PREFETCH: 0 = default L2 prefetch distance, n = n - 1 blocks")
+    ap.add_argument("--umma", action="store_true",
+                    help="PKV_OPT_UMMA = 1: the tcgen05 kernel for 17-64 query rows per kv head")
     ap.add_argument("--math", default="tensor", choices=["tensor", "fma"],
                     help="attention consumers: tensor cores (default) or the CUDA-core FMA "
                          "reference path (bf16 pools, plain call)")
@@ -1194,7 +1198,7 @@ def main():
         res["cpu_baseline"] = cpu_baseline(args)
     if not args.no_per_config and args.kv_dtype == "bf16" and args.cascade == "auto" and \
             args.math == "tensor" and args.heads == 0 and args.box == 0 and not args.pace and \
-            not args.umma_off:
+            not args.umma and args.prefetch == 0:
         res["per_config"] = run_per_config(args, rank, world, dist, res)
     if rank == 0:
         print(json.dumps(res), flush=True)

@@ -563,19 +563,21 @@ const char *pkv_status_string(int32_t status);
  *                        point for that choice. It applies to
  *                        pkv_paged_decode_attention with head_dim 128 only
  *                        (the other entry points always use tensor cores).
- *   PKV_OPT_UMMA         0 = kv heads with 17 to 64 query rows on bf16 pools with
- *                        head_dim 128 and an even number of kv heads use the
- *                        fifth-generation tensor cores
- *                        (tcgen05: MMAs from shared memory into tensor memory,
- *                        default), the other shapes the warp-level mma.sync
- *                        kernels; 1 = the mma.sync kernels for every shape (kept
+ *   PKV_OPT_UMMA         0 = the warp-level mma.sync kernels for every shape
+ *                        (default); 1 = kv heads with 17 to 64 query rows on bf16
+ *                        pools with head_dim 128 use the fifth-generation tensor
+ *                        cores instead (tcgen05: MMAs from shared memory into
+ *                        tensor memory; measured slower on this KV layout, kept
  *                        for comparison). The cascade always runs on mma.sync.
+ *   PKV_OPT_PREFETCH     tcgen05 kernel: 0 = prefetch the K/V tiles into L2 64
+ *                        blocks ahead of their loads into shared memory
+ *                        (default); n >= 1 = n - 1 blocks ahead (1 = none).
  * All settings give the same result up to fp32 rounding order.
  * Returns the previous value, or -1 for an unknown option or an invalid value.
  */
 enum { PKV_OPT_NUM_CTAS = 1, PKV_OPT_STAGES = 2, PKV_OPT_HEADS_PER_CTA = 3, PKV_OPT_TMA_BOX = 4,
        PKV_OPT_TAIL = 5, PKV_OPT_PACE = 6, PKV_OPT_PACE_MARGIN = 7, PKV_OPT_MATH = 8,
-       PKV_OPT_UMMA = 9 };
+       PKV_OPT_UMMA = 9, PKV_OPT_PREFETCH = 10 };
 int32_t pkv_set_option(int32_t option, int32_t value);
 
 /*

@@ -28,7 +28,8 @@ PKV_OK = 0
 PKV_ERR_NO_BLOCKS, PKV_ERR_SEQUENCE = 9, 10
 PKV_BF16, PKV_FP32 = 0, 1
 (PKV_OPT_NUM_CTAS, PKV_OPT_STAGES, PKV_OPT_HEADS_PER_CTA, PKV_OPT_TMA_BOX, PKV_OPT_TAIL,
- PKV_OPT_PACE, PKV_OPT_PACE_MARGIN, PKV_OPT_MATH, PKV_OPT_UMMA) = 1, 2, 3, 4, 5, 6, 7, 8, 9
+ PKV_OPT_PACE, PKV_OPT_PACE_MARGIN, PKV_OPT_MATH, PKV_OPT_UMMA,
+ PKV_OPT_PREFETCH) = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10
 BLOCK_SIZE = 16
 
 # function name -> (argtypes, restype); mirrors include/pkv.h

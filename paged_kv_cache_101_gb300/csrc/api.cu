@@ -30,6 +30,7 @@ int32_t g_opt_tail = 0;
 int32_t g_opt_pace = 0;
 int32_t g_opt_math = 0;
 int32_t g_opt_umma = 0;
+int32_t g_opt_prefetch = 0;
 thread_local bool t_meta_ready = false;  // set by a host step around its attention call
 int32_t g_opt_pace_margin = 0;
 cudaEvent_t g_ev_before = nullptr;
@@ -365,6 +366,12 @@ int32_t pkv_set_option(int32_t option, int32_t value)
         prev = g_opt_umma;
         g_opt_umma = value;
         return prev;
+    case PKV_OPT_PREFETCH:
+        if (value > 4097)
+            return -1;
+        prev = g_opt_prefetch;
+        g_opt_prefetch = value;
+        return prev;
     case PKV_OPT_PACE_MARGIN:
         if (value > 10000)
             return -1;
@@ -534,9 +541,10 @@ pkv_status attention(const void *q, const void *k_cache, const void *v_cache, in
                      (num_q_heads / num_kv_heads) * n_query_per_seq <= 32)
                         ? 1
                         : 0;
-    // the tcgen05 kernel serves 17..64 query rows per kv head, except for a cascade
-    // (its members' running states start from prefix partials)
-    const int umma = (g_opt_umma == 0 && !cc.groups) ? 1 : 0;
+    // the tcgen05 kernel (opt-in: measured slower than the mma.sync kernel on the
+    // paged layout) serves 17..64 query rows per kv head, except for a cascade (its
+    // members' running states start from prefix partials)
+    const int umma = (g_opt_umma == 1 && !cc.groups) ? 1 : 0;
     pkv::DecodePlan pl;
     if (pkv::plan_decode(num_seqs, n_query_per_seq, num_q_heads, num_kv_heads, head_dim,
                          max_blocks_per_seq, d.num_sms, g_opt_num_ctas, g_opt_stages,
@@ -573,14 +581,18 @@ pkv_status attention(const void *q, const void *k_cache, const void *v_cache, in
 
     CUtensorMap kmap, vmap, qmap;
     int whole_box = 0;
-    if (pl.umma && q_map(q, vl.q_start ? vl.total_q : int64_t(num_seqs) * n_query_per_seq,
-                         num_q_heads, pl.G, n_query_per_seq, &qmap) != cudaSuccess)
-        return PKV_ERR_CUDA;
-    if (g_opt_box != 1 &&
+    if (pl.umma) {
+        // one (head, half) box per block: the tiles land in the super-stage's rows
+        if (pool_map(k_cache, num_blocks, num_kv_heads, head_dim, 0, 0, &kmap) != cudaSuccess ||
+            pool_map(v_cache, num_blocks, num_kv_heads, head_dim, 0, 0, &vmap) != cudaSuccess ||
+            q_map(q, vl.q_start ? vl.total_q : int64_t(num_seqs) * n_query_per_seq, num_q_heads,
+                  pl.G, n_query_per_seq, &qmap) != cudaSuccess)
+            return PKV_ERR_CUDA;
+    } else if (g_opt_box != 1 &&
         pool_map(k_cache, num_blocks, num_kv_heads, head_dim, pl.HG, kv8, &kmap) == cudaSuccess &&
         pool_map(v_cache, num_blocks, num_kv_heads, head_dim, pl.HG, kv8, &vmap) == cudaSuccess)
         whole_box = 1;
-    if (!whole_box) {
+    if (!whole_box && !pl.umma) {
         if (g_opt_box == 2)
             return PKV_ERR_UNSUPPORTED;  // whole-block boxes requested but refused
         if (pool_map(k_cache, num_blocks, num_kv_heads, head_dim, 0, kv8, &kmap) != cudaSuccess ||
@@ -623,6 +635,7 @@ pkv_status attention(const void *q, const void *k_cache, const void *v_cache, in
     p.pace = g_opt_pace;
     p.meta_ready = (t_meta_ready && !cc.groups) ? 1 : 0;
     p.pace_margin = float(g_opt_pace_margin) * 1e-4f;
+    p.pf_units = g_opt_prefetch == 0 ? 64 : g_opt_prefetch - 1;
     p.k_scale = k_scale;
     p.v_scale = v_scale;
     p.q_start = vl.q_start;

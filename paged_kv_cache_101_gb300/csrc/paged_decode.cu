@@ -1898,21 +1898,21 @@ int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int 
     P.rows = P.G * nq;
     if (P.rows > kMaxRows)
         return -1;
-    if (umma && !P.kv8 && !P.fma && D == 128 && P.rows > 16 && Hkv % 2 == 0 &&
-        umma_max_stages(smem_optin) >= 2) {
-        // the tcgen05 kernel: two kv heads per CTA, per-block stages, the query rows
-        // padded to the MMA's M = 64
+    if (umma && !P.kv8 && !P.fma && D == 128 && P.rows > 16) {
+        // tcgen05 consumers: one kv head per CTA, super-stages of 8 blocks, the
+        // query rows padded to the MMA's N (32 or 64)
         P.umma = 1;
-        P.rows_pad = 64;
+        P.rows_pad = P.rows <= 32 ? 32 : 64;
         P.wph = 1;
         P.ntw = 0;
-        P.HG = 2;
-        P.n_hg = Hkv / 2;
-        P.threads = 320;
-        P.stage_bytes = 2 * 2 * (D / 64) * kTileBytes;
-        const int max_st = umma_max_stages(smem_optin);
-        P.nst = opt_stages > 0 ? std::min(std::max(opt_stages, 2), max_st) : max_st;
-        P.smem = umma_smem_bytes(P.nst);
+        P.HG = 1;
+        P.n_hg = Hkv;
+        P.threads = 352;
+        P.stage_bytes = 65536;
+        P.nst = umma_stages(P.rows_pad);
+        P.smem = umma_smem_bytes(P.rows_pad);
+        if (int(P.smem) > smem_optin)
+            return -1;
         P.ctas_per_sm = 1;
         const int grid_cap = opt_ctas > 0 ? opt_ctas : num_sms;
         if (grid_cap < 1 || grid_cap > 16384)
@@ -1923,8 +1923,8 @@ int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int 
         const size_t cells = size_t(grid_cap);
         P.off_rec = kWsHeaderBytes;
         P.off_ml = P.off_rec + round_up(size_t(S) * P.n_hg * 8, 256);
-        P.off_part = P.off_ml + round_up(cells * 2 * P.HG * P.rows * 2 * 4, 256);
-        P.ws_bytes = P.off_part + round_up(cells * 2 * P.HG * P.rows * size_t(D) * 4, 256);
+        P.off_part = P.off_ml + round_up(cells * 2 * P.rows * 2 * 4, 256);
+        P.ws_bytes = P.off_part + round_up(cells * 2 * P.rows * size_t(D) * 4, 256);
         *pl = P;
         return 0;
     }

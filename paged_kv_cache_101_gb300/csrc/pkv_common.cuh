@@ -111,6 +111,16 @@ __device__ __forceinline__ void tma_load_5d_hint(uint32_t dst, const void *desc,
         : "memory");
 }
 
+// Prefetch one box of a 5-D tiled tensor into L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_5d(const void *desc, int c0, int c1, int c2,
+                                                   int c3, int c4)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(
+                     desc),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first()
 {
     uint64_t p;

@@ -51,7 +51,7 @@ struct DecodePlan {
     int fma;         // 1: CUDA-core (fp32 FMA) consumers instead of tensor cores
     int rw;          // CUDA-core consumers: query rows per warp (4 or 8)
     int prefix;      // 1: the cascade's prefix pass (one head per CTA, 8 warps x 16 rows)
-    int umma;        // 1: the tcgen05 kernel (two kv heads per CTA, rows padded to 64)
+    int umma;        // 1: tcgen05 consumers (one head per CTA, rows padded to rows_pad = N)
     int grid;        // persistent CTAs
     int ctas_per_sm; // CTAs of the grid resident per SM (1, or 2 for the E4M3 5-8-row shape)
     int tickets_max; // cap on dynamically claimed tickets (0: static chunks only)
@@ -98,6 +98,7 @@ struct DecodeParams {
                            // host step): the producer reads them before the grid dependency
                            // wait and waits only before its first read of the pool
     float pace_margin;     // pacing: lead (fraction of the work) allowed before pacing
+    int pf_units;          // tcgen05 kernel: blocks prefetched into L2 ahead of the loads
     const float *k_scale;  // E4M3 pools: [Hkv] dequantisation scales (null for bf16)
     const float *v_scale;
     // variable query counts (all null for a fixed n_query_per_seq = nq, causal):
@@ -130,11 +131,11 @@ int plan_decode(int S, int nq, int Hq, int Hkv, int D, int MB, int num_sms, int 
                 int opt_stages, int opt_heads, int opt_tail, int smem_optin, int kv8, int fma,
                 int umma, DecodePlan *plan);
 
-// The tcgen05 kernel (paged_decode_umma.cu): shared memory for `ns` stages, the
-// most stages `smem_optin` bytes hold (0: none); the launch of it and its merge.
-// qmap views q as (64, 2, Hq, rows, 1) with a box of (64, 1, G, n_query_per_seq, 1).
-size_t umma_smem_bytes(int ns);
-int umma_max_stages(int smem_optin);
+// The tcgen05 kernel (paged_decode_umma.cu): shared memory and super-stages for
+// N = 32 or 64 padded rows; the launch of it and its merge. qmap views q as
+// (64, 2, Hq, rows, 1) with a box of (64, 1, G, n_query_per_seq, 1).
+size_t umma_smem_bytes(int n);
+int umma_stages(int n);
 cudaError_t launch_decode_umma(const DecodePlan &plan, const DecodeParams &p,
                                const CUtensorMap &kmap, const CUtensorMap &vmap,
                                const CUtensorMap &qmap, cudaStream_t stream, cudaEvent_t ev_before,

@@ -184,15 +184,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[32])
         : "memory");
 }
 
-// Warp-wide TMEM store of 8 columns of 32-bit words (32 lanes x 32 bits each).
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8])
-{
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
-                     taddr),
-                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-                 : "memory");
-}
-
 // Named barrier `id` over `n` threads (a multiple of 32); the _or form returns
 // whether any participating thread passed true.
 __device__ __forceinline__ void bar_sync_named(int id, int n)

@@ -23,7 +23,7 @@ def o():
 
 
 OPTIONS = (pkv.PKV_OPT_NUM_CTAS, pkv.PKV_OPT_STAGES, pkv.PKV_OPT_HEADS_PER_CTA,
-           pkv.PKV_OPT_TMA_BOX, pkv.PKV_OPT_TAIL, pkv.PKV_OPT_UMMA)
+           pkv.PKV_OPT_TMA_BOX, pkv.PKV_OPT_TAIL, pkv.PKV_OPT_UMMA, pkv.PKV_OPT_PREFETCH)
 
 
 @pytest.fixture(autouse=True)

@@ -1,13 +1,14 @@
 """GPU parity of the fifth-generation tensor-core (tcgen05) kernel against the oracle.
 
-Kv heads with 17 to 64 query rows (bf16 pools, head_dim 128, an even number of kv
-heads) run on the tcgen05 kernel: per-block stages of two kv heads, scores with
-the query rows on the MMA's M (64), the softmax one thread per row, P in tensor
-memory as the A operand of P.V. Every case is compared element by element with
-the fp64 oracle (|err| <= 2e-3 + 1e-2 |ref|): row counts from 17 to 64, every
-context length mod 16, grids that cut segments at any block, causal draft queries
-and tree masks, strict fp32 output, a large running-max jump, and the same calls
-on the mma.sync kernels (PKV_OPT_UMMA = 1) for the A/B.
+With PKV_OPT_UMMA = 1, kv heads with 17 to 64 query rows (bf16 pools, head_dim
+128) run on the tcgen05 kernel: super-stages of up to 8 blocks of one (sequence, kv head), scores with the
+tokens on the MMA's M, the softmax one thread per token, P.V into tensor memory.
+Every case is compared element by element with the fp64 oracle
+(|err| <= 2e-3 + 1e-2 |ref|): row counts across both tile widths (N = 32, 64),
+every context length mod 16 and around the 128-token super-stage, grids that cut
+segments mid-super-stage, causal draft queries and tree masks, strict fp32 output,
+a large running-max jump, and the same calls on the mma.sync kernels (the default,
+PKV_OPT_UMMA = 0) for the A/B.
 """
 import numpy as np
 import pytest
@@ -21,7 +22,7 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 OPTIONS = (pkv.PKV_OPT_NUM_CTAS, pkv.PKV_OPT_STAGES, pkv.PKV_OPT_HEADS_PER_CTA,
-           pkv.PKV_OPT_TMA_BOX, pkv.PKV_OPT_TAIL, pkv.PKV_OPT_UMMA)
+           pkv.PKV_OPT_TMA_BOX, pkv.PKV_OPT_TAIL, pkv.PKV_OPT_UMMA, pkv.PKV_OPT_PREFETCH)
 
 
 @pytest.fixture(scope="module")
@@ -33,6 +34,7 @@ def o():
 def _defaults():
     for opt in OPTIONS:
         pkv.set_option(opt, 0)
+    pkv.set_option(pkv.PKV_OPT_UMMA, 1)   # the tcgen05 kernel (opt-in)
     yield
     for opt in OPTIONS:
         pkv.set_option(opt, 0)
@@ -65,7 +67,7 @@ def test_rows_and_lengths(o, G, nq):
     run(o, w)
 
 
-def test_every_length_mod_16(o):
+def test_every_length_mod_16_around_a_super_stage(o):
     T = list(range(4, 70)) + list(range(120, 140)) + [255, 256, 257, 383, 384, 385]
     w = W.make_custom(len(T), 4, 64, 8, 128, T, seed=510)
     run(o, w)
@@ -77,6 +79,15 @@ def test_grid_sizes(o, ctas):
     pkv.set_option(pkv.PKV_OPT_NUM_CTAS, ctas)
     T = [3000, 20, 5, 777, 4096, 129, 4, 16, 17, 2500, 130, 1023]
     w = W.make_custom(len(T), 4, 64, 8, 128, T, seed=511)
+    run(o, w)
+
+
+@pytest.mark.parametrize("pf", [1, 2, 9, 100])
+def test_prefetch_distances(o, pf):
+    """The L2 prefetch cursor (none, 1 block, 8, 99 blocks ahead) changes no result."""
+    pkv.set_option(pkv.PKV_OPT_PREFETCH, pf)
+    T = [3000, 20, 5, 777, 129, 4, 17, 1023]
+    w = W.make_custom(len(T), 4, 64, 8, 128, T, seed=517)
     run(o, w)
 
 
@@ -114,13 +125,14 @@ def test_matches_mma_sync_kernel(o):
     """The same call on both kernels: each within tolerance of the oracle."""
     T = [900, 33, 4000, 6, 260, 1300, 77]
     w = W.make_custom(len(T), 4, 64, 8, 128, T, seed=515)
-    for umma_off in (0, 1):
-        pkv.set_option(pkv.PKV_OPT_UMMA, umma_off)
+    for umma in (1, 0):
+        pkv.set_option(pkv.PKV_OPT_UMMA, umma)
         run(o, w)
 
 
 def test_spec_verify_full_size(o):
     w = W.make_workload("spec_verify")
+    assert pkv.set_option(pkv.PKV_OPT_UMMA, 1) == 1
     d = DeviceStep(w, torch)
     d.step()
     torch.cuda.synchronize()

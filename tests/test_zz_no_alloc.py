@@ -34,7 +34,7 @@ pytestmark = pytest.mark.gpu
 OK, NULL, SHAPE, DTYPE, ALIGN, RANGE, WORKSPACE, CUDA, UNSUP = range(9)
 OPTIONS = (pkv.PKV_OPT_NUM_CTAS, pkv.PKV_OPT_STAGES, pkv.PKV_OPT_HEADS_PER_CTA,
            pkv.PKV_OPT_TMA_BOX, pkv.PKV_OPT_TAIL, pkv.PKV_OPT_PACE, pkv.PKV_OPT_MATH,
-           pkv.PKV_OPT_UMMA)
+           pkv.PKV_OPT_UMMA, pkv.PKV_OPT_PREFETCH)
 
 
 @pytest.fixture(scope="module")
