@@ -354,7 +354,8 @@ def use_cascade(w, mode):
     if mode == "on":
         return True
     lens = np.concatenate([w.context_lens[w.shared], w.context_lens[~w.shared]])
-    return pkv.cascade_pays(lens, [[0, int(w.shared.sum()), w.meta["prefix_tokens"] // 16]])
+    return pkv.cascade_pays(lens, [[0, int(w.shared.sum()), w.meta["prefix_tokens"] // 16]],
+                            w.num_kv_heads, w.head_dim)
 
 
 def run_pkv(args, rank, world, dist):
@@ -986,7 +987,8 @@ def run_shared_prefix(args, rank, world, dist):
     clk = clocks.stop()
     ms_casc, ms_plain = max_over_ranks([ms, ms_plain], dist, dev)
     # the step as the library's rule runs it by default; both paths are reported
-    chosen = "cascade" if pkv.cascade_pays(w.context_lens, [[0, S, P_TOK // 16]]) else "plain"
+    chosen = "cascade" if pkv.cascade_pays(w.context_lens, [[0, S, P_TOK // 16]], 8,
+                                           128) else "plain"
     ms = ms_casc if chosen == "cascade" else ms_plain
     peak, peak_kind = measured_peaks()
     res = {

@@ -239,21 +239,28 @@ size_t pkv_workspace_size_cascade(int32_t num_seqs, int32_t n_query_per_seq, int
  * pkv_cascade_pays -- host planner: 1 if pkv_paged_decode_attention_cascade is
  * expected to beat pkv_paged_decode_attention for this batch, 0 if not, -1 for
  * invalid input (a negative count, a NULL array with a nonzero count, a group
- * outside the batch).
+ * outside the batch, non-positive head sizes).
  *
  * Passage: "ML Interview Prep, Lesson 13" section 3.5 "Sharing" (shared blocks
  * are read by every sharer). The plain call reads every member's copy of the
  * shared prefix; after the first, those reads mostly hit L2, so they cost
- * little while they are few next to the step's unique bytes and bound the
- * kernel once they are not. The rule: repeated prefix tokens, sum over groups of
- * (members whose context extends past the prefix - 1) * 16 * P, at least the
- * unique tokens (all context tokens minus the repeated ones).
+ * little while they are few, and bound the kernel once they are not. The
+ * cascade avoids them for a roughly fixed price (a second launch, its prefix
+ * pass, one partial fold per member row). The rule, with repeated prefix tokens
+ * = the sum over groups of (members whose context extends past the prefix - 1)
+ * * 16 * P and unique tokens = all context tokens minus the repeated ones:
+ * repeated >= unique, and the repeated tokens' K and V (num_kv_heads * head_dim
+ * bf16 each) weigh at least 1.5 GB. Measured on GB300 (256 sequences, 8 kv
+ * heads of 128 dims): a 4,096-token prompt with suffixes under 512 tokens runs
+ * 1.7x faster with the cascade; 512-token prompts and the 70B-shaped mix run
+ * faster without.
  *
  *   context_lens   host int32 [num_seqs], as the attention call's
  *   prefix_groups  host int32 [num_groups][3], as the cascade call's
  */
 int32_t pkv_cascade_pays(const int32_t *context_lens, int32_t num_seqs,
-                         const int32_t *prefix_groups, int32_t num_groups);
+                         const int32_t *prefix_groups, int32_t num_groups,
+                         int32_t num_kv_heads, int32_t head_dim);
 
 pkv_status pkv_paged_decode_attention_cascade(
     const void *q, const void *k_cache, const void *v_cache, int64_t num_blocks,

@@ -62,7 +62,7 @@ SIGNATURES = {
     "pkv_paged_decode_attention_cascade": ([_P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _I32,
                                             _I32, _F, _P, _I32, _I32, _P, _I32, _P, _SZ, _P],
                                            ctypes.c_int),
-    "pkv_cascade_pays": ([_P, _I32, _P, _I32], _I32),
+    "pkv_cascade_pays": ([_P, _I32, _P, _I32, _I32, _I32], _I32),
     "pkv_split_queries": ([_P, _P, _P, _I32, _I32, _P, _P, _P, _P, _I32, _P], ctypes.c_int),
     "pkv_kv_append_fp8": ([_P, _P, _P, _I64, _P, _P, _I64, _I32, _I32, _P, _P, _P], ctypes.c_int),
     "pkv_paged_decode_attention_fp8": ([_P, _P, _P, _I64, _P, _P, _P, _I32, _P, _I32, _I32, _I32,
@@ -583,14 +583,15 @@ def paged_decode_attention_static(q, k_cache, v_cache, block_tables, context_len
     return out
 
 
-def cascade_pays(context_lens, prefix_groups) -> bool:
+def cascade_pays(context_lens, prefix_groups, num_kv_heads, head_dim) -> bool:
     """The library's rule for choosing the shared-prefix cascade over the plain call
-    (host arrays: context lengths [S], groups [num_groups][3])."""
+    (host arrays: context lengths [S], groups [num_groups][3]; the pools' kv heads
+    and head dim)."""
     import numpy as np
     lens = np.ascontiguousarray(context_lens, dtype=np.int32)
     groups = np.ascontiguousarray(prefix_groups, dtype=np.int32).reshape(-1, 3)
     r = lib().pkv_cascade_pays(lens.ctypes.data, lens.size, groups.ctypes.data,
-                               groups.shape[0])
+                               groups.shape[0], int(num_kv_heads), int(head_dim))
     if r < 0:
         raise ValueError("pkv_cascade_pays: invalid input")
     return bool(r)

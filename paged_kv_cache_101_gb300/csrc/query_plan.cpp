@@ -14,9 +14,12 @@
 #include "pkv.h"
 
 namespace {
-// the cascade pays once the repeated prefix tokens reach kCascadeNum / kCascadeDen
-// of the step's unique tokens
-constexpr int64_t kCascadeNum = 1, kCascadeDen = 1;
+// The cascade pays once the repeated prefix bytes reach the step's unique bytes and
+// 1.5 GB: below that the plain call re-reads the prefix from L2 faster than the
+// cascade's prefix pass and member seeding cost (measured on GB300, 256 sequences
+// with 8 kv heads of 128 dims: prefixes of 512 to 4,096 tokens, suffixes up to
+// 4,096 tokens).
+constexpr double kCascadeMinRepeatedBytes = 1.5e9;
 }  // namespace
 
 extern "C" pkv_status pkv_split_queries(const int32_t *q_start, const int32_t *context_lens,
@@ -76,12 +79,14 @@ extern "C" pkv_status pkv_split_queries(const int32_t *q_start, const int32_t *c
 // from HBM, the others mostly from L2 while the prefix stays resident. Those
 // repeated prefix reads cost L2 bandwidth and, once they rival the step's unique
 // bytes, they bound the plain kernel; the cascade reads each prefix once per row
-// tile instead, for the price of a second launch and one partial fold per member
-// row. So the rule compares the repeated prefix tokens with the unique tokens.
+// tile instead, for the price of a second launch, its prefix pass and one
+// partial fold per member row. So the rule compares the repeated prefix bytes
+// with the unique bytes and with that fixed price.
 extern "C" int32_t pkv_cascade_pays(const int32_t *context_lens, int32_t num_seqs,
-                                    const int32_t *prefix_groups, int32_t num_groups)
+                                    const int32_t *prefix_groups, int32_t num_groups,
+                                    int32_t num_kv_heads, int32_t head_dim)
 {
-    if (num_seqs < 0 || num_groups < 0)
+    if (num_seqs < 0 || num_groups < 0 || num_kv_heads < 1 || head_dim < 1)
         return -1;
     if (num_seqs == 0 || num_groups == 0)
         return 0;
@@ -105,5 +110,7 @@ extern "C" int32_t pkv_cascade_pays(const int32_t *context_lens, int32_t num_seq
             repeated += (members - 1) * int64_t(16) * P;
     }
     const int64_t unique = total - repeated;
-    return repeated * kCascadeDen >= kCascadeNum * unique ? 1 : 0;
+    const double token_bytes = 2.0 * 2.0 * double(num_kv_heads) * double(head_dim);  // K + V, bf16
+    const double rep_bytes = double(repeated) * token_bytes;
+    return repeated >= unique && rep_bytes >= kCascadeMinRepeatedBytes ? 1 : 0;
 }

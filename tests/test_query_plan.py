@@ -143,30 +143,40 @@ def test_cascade_host_validation(lib):
 
 # ------------------------------------------------------------------ cascade rule
 def shared_prompt_lengths(S=256, prefix=4096, suffix_max=512, seed=1234 + 23):
-    """The shared-prompt batch the benchmark times: a 4,096-token system prompt and
-    private suffixes of 16 .. suffix_max - 1 tokens."""
+    """A shared-prompt batch like the benchmark's: a system prompt of `prefix`
+    tokens and private suffixes of 16 .. suffix_max - 1 tokens."""
     rng = np.random.default_rng(seed)
     return (prefix + rng.integers(16, suffix_max, size=S)).astype(np.int32)
 
 
-def test_cascade_rule_picks_the_cascade_for_a_long_shared_prompt(lib):
-    lens = shared_prompt_lengths()
-    assert pkv.cascade_pays(lens, [[0, lens.size, 4096 // 16]])
+# (prompt tokens, largest suffix, faster path measured on GB300 at 8 kv heads x 128
+# dims); a tie (under 1 %) is listed under the rule's answer
+MEASURED = [(4096, 512, True), (2048, 512, True), (4096, 4096, True), (1024, 512, False),
+            (512, 512, False), (512, 4096, False), (1024, 2048, False), (2048, 4096, True)]
+
+
+@pytest.mark.parametrize("prefix,suffix,cascade", MEASURED)
+def test_cascade_rule_matches_the_measured_faster_path(lib, prefix, suffix, cascade):
+    lens = shared_prompt_lengths(prefix=prefix, suffix_max=suffix)
+    assert pkv.cascade_pays(lens, [[0, lens.size, prefix // 16]], 8, 128) == cascade
 
 
 def test_cascade_rule_picks_the_plain_call_for_the_70b_mix(lib):
     T, shared, prefix = W.workload_lengths("llama3_70b_mix")
     lens = np.concatenate([T[shared], T[~shared]]).astype(np.int32)   # sharers first
-    assert not pkv.cascade_pays(lens, [[0, int(shared.sum()), prefix // 16]])
+    assert not pkv.cascade_pays(lens, [[0, int(shared.sum()), prefix // 16]], 8, 128)
 
 
 def test_cascade_rule_edges(lib):
     lens = np.full(8, 600, np.int32)
-    assert not pkv.cascade_pays(lens, np.zeros((0, 3), np.int32))       # no group
-    assert not pkv.cascade_pays(lens, [[0, 1, 32]])                     # a lone member
+    assert not pkv.cascade_pays(lens, np.zeros((0, 3), np.int32), 8, 128)    # no group
+    assert not pkv.cascade_pays(lens, [[0, 1, 32]], 8, 128)                 # a lone member
     # members whose context is the prefix alone fall back, so they repeat nothing
-    assert not pkv.cascade_pays(np.full(8, 512, np.int32), [[0, 8, 32]])
-    # 7 repeated copies of 512 tokens against 8 * 88 + 512 unique tokens
-    assert pkv.cascade_pays(lens, [[0, 8, 32]])
+    assert not pkv.cascade_pays(np.full(8, 512, np.int32), [[0, 8, 32]], 8, 128)
+    # repeated >= unique, but 7 copies of 512 tokens are far below the fixed price
+    assert not pkv.cascade_pays(lens, [[0, 8, 32]], 8, 128)
+    # 4,000 sequences of a 4,096-token prompt: far above it
+    big = np.full(4000, 4096 + 8, np.int32)
+    assert pkv.cascade_pays(big, [[0, 4000, 256]], 8, 128)
     with pytest.raises(ValueError):
-        pkv.cascade_pays(lens, [[4, 8, 32]])                            # past the batch
+        pkv.cascade_pays(lens, [[4, 8, 32]], 8, 128)                        # past the batch
