@@ -406,8 +406,13 @@ def run_pkv(args, rank, world, dist):
 
     # max over ranks
     ms_per_step, kern_mean, e2e_ms = max_over_ranks([ms_per_step, kern_mean, e2e_ms], dist, dev)
+    # the tcgen05 kernel runs when it is opted in and the batch has 17-64 score rows per
+    # kv head on bf16 pools of head_dim 128 (the library's own rule)
+    umma = bool(args.umma) and not (fp8 or fma or cascade) and w.head_dim == 128 and \
+        16 < w.n_query_per_seq * (w.num_q_heads // w.num_kv_heads) <= 64
     traffic = traffic_pin(args.workload + ("/fp8" if fp8 else "") +
-                          ("/cascade" if cascade else "") + ("/fma" if fma else ""))
+                          ("/cascade" if cascade else "") + ("/fma" if fma else "") +
+                          ("/umma" if umma else ""))
     step_bytes = rig.step_bytes
     value = job_gbs(world, step_bytes, ms_per_step)
     res = {
@@ -446,7 +451,8 @@ def run_pkv(args, rank, world, dist):
         },
         "roofline": roofline_entry(
             rig, kern_mean, traffic,
-            ("paged_decode_fma_kernel" if fma else "paged_decode_kernel") +
+            ("paged_decode_fma_kernel" if fma else "paged_decode_umma_kernel" if umma
+             else "paged_decode_kernel") +
             (" (prefix pass + main pass)" if cascade else "")),
         "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 6), "h2d_bytes_per_step": h2d,
@@ -900,7 +906,9 @@ def run_tree(args, rank, world, dist):
                    "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": D,
                    "context_tokens": int(T.sum()), "bytes_per_step": step_bytes,
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm",
+                     "kernel": "paged_decode_umma_kernel" if args.umma else "paged_decode_kernel",
+                     "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_kind} hbm_gbs (burst)", "traffic": None,
                      "kernel_us": round(kern_ms * 1e3, 3), "algorithmic_bytes_per_launch": attn_bytes},
