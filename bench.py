@@ -56,24 +56,28 @@ FALLBACK_HBM_GBS = 6800.0
 # to `source_sha256` (otherwise the bench reports traffic = null).
 NCU_TRAFFIC = {
     "llama3_8b_decode": {
-        "bytes": 582041856 + 3558400,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "2a5583ed3ce08b9f5b2631fddc4ccd0dbc46f43aeabfaab2cb778a61c0b04f06",
+        "bytes": 580933632 + 2392320,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "41715bbbe1fb19a8f77c0fc8357bf63b59523dcd3aba934538e07a2d746b4fef",
     },
     "llama3_70b_mix": {
-        "bytes": 1332676864 + 5603584,
-        "source_sha256": "2a5583ed3ce08b9f5b2631fddc4ccd0dbc46f43aeabfaab2cb778a61c0b04f06",
+        "bytes": 1344529408 + 476928,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "41715bbbe1fb19a8f77c0fc8357bf63b59523dcd3aba934538e07a2d746b4fef",
+    },
+    "long_splitk": {
+        "bytes": 2968239104 + 4545280,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "41715bbbe1fb19a8f77c0fc8357bf63b59523dcd3aba934538e07a2d746b4fef",
     },
     "spec_verify": {
-        "bytes": 1417695488 + 5033216,
-        "source_sha256": "2a5583ed3ce08b9f5b2631fddc4ccd0dbc46f43aeabfaab2cb778a61c0b04f06",
+        "bytes": 1406888960 + 6053376,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "41715bbbe1fb19a8f77c0fc8357bf63b59523dcd3aba934538e07a2d746b4fef",
     },
     "llama3_8b_decode/fp8": {
-        "bytes": 291327744 + 3382016,
-        "source_sha256": "2a5583ed3ce08b9f5b2631fddc4ccd0dbc46f43aeabfaab2cb778a61c0b04f06",
+        "bytes": 290379264 + 815360,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "41715bbbe1fb19a8f77c0fc8357bf63b59523dcd3aba934538e07a2d746b4fef",
     },
     "llama3_70b_mix/fp8": {
-        "bytes": 666733312 + 5176576,
-        "source_sha256": "2a5583ed3ce08b9f5b2631fddc4ccd0dbc46f43aeabfaab2cb778a61c0b04f06",
+        "bytes": 663066624 + 1613824,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "41715bbbe1fb19a8f77c0fc8357bf63b59523dcd3aba934538e07a2d746b4fef",
     },
 }
 
