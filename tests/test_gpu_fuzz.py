@@ -5,7 +5,10 @@ combines:
 - head_dim 64 or 128; 1 to 64 query rows per kv head (G x nq); 1 to 12 sequences;
 - lengths from nq to 3,000 tokens, sometimes a shared prefix;
 - persistent grid size, pipeline depth, heads per CTA, TMA box mode, dynamic
-  tail, pacing, CUDA-core consumers; bf16 or fp32 output.
+  tail, pacing, CUDA-core consumers; bf16 or fp32 output;
+- a second set with the tcgen05 kernel opted in: mostly 17 to 64 rows per kv head
+  at head_dim 128 (the rows it takes), with random L2 prefetch distances and grid
+  sizes, and some geometries it leaves to the mma.sync kernels.
 
 Then it checks append + attention against the fp64 oracle (the pool bit for bit,
 the output within 2e-3 + 1e-2*|ref|), and that the device error word stays 0. Every
@@ -25,7 +28,7 @@ pytestmark = pytest.mark.gpu
 
 OPTIONS = (pkv.PKV_OPT_NUM_CTAS, pkv.PKV_OPT_STAGES, pkv.PKV_OPT_HEADS_PER_CTA,
            pkv.PKV_OPT_TMA_BOX, pkv.PKV_OPT_TAIL, pkv.PKV_OPT_PACE, pkv.PKV_OPT_PACE_MARGIN,
-           pkv.PKV_OPT_MATH)
+           pkv.PKV_OPT_MATH, pkv.PKV_OPT_UMMA, pkv.PKV_OPT_PREFETCH)
 
 
 @pytest.fixture(scope="module")
@@ -86,4 +89,48 @@ def test_random_geometry_and_options(o, seed):
     assert np.array_equal(bf16_host(d.k_cache), k_ref)
     assert np.array_equal(bf16_host(d.v_cache), v_ref)
     compare(to_f64(d.out), ref, what=f"case {seed}: {c['opts']}")
+    assert pkv.workspace_error(pkv.workspace(d.q.device, 0)) == 0
+
+
+def draw_tcgen05_case(seed):
+    rng = np.random.default_rng(7000 + seed)
+    D = 128 if rng.random() < 0.85 else 64
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    while True:
+        G = int(rng.choice([2, 4, 6, 8, 12, 16, 32]))
+        nq = int(rng.integers(1, 5))
+        if G * nq <= 64 and (G * nq > 16 or rng.random() < 0.15):
+            break
+    S = int(rng.integers(1, 10))
+    T = np.where(rng.random(S) < 0.4, rng.integers(nq, 140, S), rng.integers(nq, 4001, S))
+    shared, prefix = None, 0
+    if rng.random() < 0.25 and S >= 2:
+        prefix = int(rng.choice([16, 128, 256]))
+        shared = rng.random(S) < 0.6
+        T = np.where(shared, np.maximum(T, prefix + nq), T)
+    opts = {
+        pkv.PKV_OPT_UMMA: 1,
+        pkv.PKV_OPT_NUM_CTAS: int(rng.choice([0, 1, 3, 37, 152, 400])),
+        pkv.PKV_OPT_PREFETCH: int(rng.choice([0, 1, 2, 9, 65, 200])),
+    }
+    out32 = bool(rng.random() < 0.3)
+    return dict(D=D, Hkv=Hkv, G=G, nq=nq, S=S, T=T.astype(np.int64), shared=shared,
+                prefix=prefix, opts=opts, out32=out32)
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_geometry_tcgen05(o, seed):
+    c = draw_tcgen05_case(seed)
+    for opt, v in c["opts"].items():
+        assert pkv.set_option(opt, v) >= 0
+    w = W.make_custom(c["S"], c["nq"], c["G"] * c["Hkv"], c["Hkv"], c["D"], c["T"],
+                      seed=8000 + seed, shared=c["shared"], prefix_tokens=c["prefix"])
+    d = DeviceStep(w, torch, out_dtype=torch.float32 if c["out32"] else None)
+    ref, k_ref, v_ref = o.step(w)
+    d.step()
+    torch.cuda.synchronize()
+    assert np.array_equal(bf16_host(d.k_cache), k_ref)
+    assert np.array_equal(bf16_host(d.v_cache), v_ref)
+    compare(to_f64(d.out), ref, what=f"tcgen05 case {seed}: G={c['G']} nq={c['nq']} D={c['D']} "
+                                     f"{c['opts']}")
     assert pkv.workspace_error(pkv.workspace(d.q.device, 0)) == 0
