@@ -1099,23 +1099,27 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
             }
         }
 
-        // ---- online softmax over the lane's two rows (g: e = 0,1; g+8: e = 2,3)
-        float bmax[2];
-        bool grew = false;
+        // ---- online softmax over the lane's two rows (g: e = 0,1; g+8: e = 2,3).
+        //      The running max is raised only once a score passes it by more than
+        //      2^8 (log2 units): most blocks then skip the row reductions. P can
+        //      reach 2^8 in between, and the result stays exact because the sum is
+        //      taken against the same max.
+        constexpr float kLazyLog2 = 8.f;
+        bool lead = false;
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-            float bm = fmaxf(fmaxf(sc[0][2 * rr], sc[0][2 * rr + 1]),
-                             fmaxf(sc[1][2 * rr], sc[1][2 * rr + 1]));
-            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
-            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
-            bmax[rr] = bm;
-            grew |= bm > m_r[rr];
-        }
-        if (__any_sync(0xffffffffu, grew)) {
+        for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+                lead |= fmaxf(sc[n][2 * rr], sc[n][2 * rr + 1]) > m_r[rr] + kLazyLog2;
+        if (__any_sync(0xffffffffu, lead)) {
             float corr[2];
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
-                const float mn = fmaxf(m_r[rr], bmax[rr]);
+                float bm = fmaxf(fmaxf(sc[0][2 * rr], sc[0][2 * rr + 1]),
+                                 fmaxf(sc[1][2 * rr], sc[1][2 * rr + 1]));
+                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+                const float mn = fmaxf(m_r[rr], bm);
                 const float mu = (mn == -INFINITY) ? 0.f : mn;
                 corr[rr] = ex2(m_r[rr] - mu);
                 m_r[rr] = mn;

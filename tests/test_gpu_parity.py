@@ -144,6 +144,41 @@ def test_shared_prefix_small(o):
     run_small(o, w)
 
 
+def aligned_queries(w, T, nq, G, Hkv, D, gain, rng, ramp=False):
+    """Queries pushed toward keys of the sequence's second half, so the running max of
+    a row rises in the middle of its segment: by `gain` at once, or (ramp) by a series
+    of steps just under 2^8 in log2 units, one every few blocks."""
+    q = W.bf16_bits_to_f32(w.q).reshape(len(T), nq, G * Hkv, D)
+    for s, Ts in enumerate(T):
+        k = W.bf16_bits_to_f32(w.dense_k[s])              # [Ts, Hkv, D] after the append
+        for h in range(Hkv):
+            if ramp:
+                picks = np.linspace(Ts // 4, Ts - nq - 1, 6).astype(int)
+                for i, t in enumerate(picks):
+                    kk = k[t, h] / max(np.linalg.norm(k[t, h]), 1e-3)
+                    q[s, :, G * h:G * h + G, :] += (2.0 + 1.2 * i) * kk[None, None, :]
+            else:
+                t = int(rng.integers(Ts // 2, Ts - nq))
+                q[s, :, G * h:G * h + G, :] += gain * k[t, h][None, None, :]
+    w.q = W.f32_to_bf16_bits(q.reshape(w.q.shape).astype(np.float32))
+
+
+@pytest.mark.parametrize("G,nq", [(4, 1), (8, 1), (4, 4), (16, 2), (16, 4)])
+@pytest.mark.parametrize("ramp", [False, True])
+def test_running_max_rises_mid_segment(o, G, nq, ramp):
+    """The 16-row consumers raise their running max only past a 2^8 lead: a jump far
+    past it, and a ramp of rises that each stay under it (P then reaches up to 2^8
+    before the max moves), both give the definition; so do the 8-row consumers."""
+    Hkv = 2
+    T = [700, 1500, 260, 3000]
+    w = W.make_custom(len(T), nq, G * Hkv, Hkv, 128, T, seed=87 + G + 3 * nq,
+                      keep_dense=True)
+    aligned_queries(w, T, nq, G, Hkv, 128, 6.0, np.random.default_rng(G * 10 + nq), ramp=ramp)
+    run_small(o, w, check_pool=False)
+    pkv.set_option(pkv.PKV_OPT_NUM_CTAS, 37)               # segments cut mid-sequence
+    run_small(o, w, check_pool=False)
+
+
 @pytest.mark.parametrize("ctas", [1, 2, 7, 64, 300, 1000])
 def test_split_grid_invariance(o, ctas):
     """Any persistent-grid size gives the definition (within rounding)."""
