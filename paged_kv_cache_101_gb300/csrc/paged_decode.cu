@@ -632,25 +632,26 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
             }
         }
 
-        // ---- online softmax (rows 2tq, 2tq+1 live in this lane). The
-        //      accumulator is rescaled only when some row's running max grew
-        //      (otherwise every factor would be exactly 1).
-        float bmax[2];
-        bool grew = false;
+        // ---- online softmax (rows 2tq, 2tq+1 live in this lane). The running
+        //      max is raised only once a score passes it by more than 2^8 (log2
+        //      units), so most blocks skip the row reductions; P can reach 2^8 in
+        //      between, and the result stays exact because the sum is taken
+        //      against the same max. The accumulator is rescaled only when a row's
+        //      max moves (otherwise every factor would be exactly 1).
+        constexpr float kLazyLog2 = 8.f;
+        bool lead = false;
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            float bm = fmaxf(sc[r], sc[r + 2]);
-            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
-            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
-            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
-            bmax[r] = bm;
-            grew |= bm > m_r[r];
-        }
-        if (__any_sync(0xffffffffu, grew)) {
+        for (int r = 0; r < 2; ++r)
+            lead |= fmaxf(sc[r], sc[r + 2]) > m_r[r] + kLazyLog2;
+        if (__any_sync(0xffffffffu, lead)) {
             float corr[2];
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                const float mn = fmaxf(m_r[r], bmax[r]);
+                float bm = fmaxf(sc[r], sc[r + 2]);
+                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+                const float mn = fmaxf(m_r[r], bm);
                 const float mu = (mn == -INFINITY) ? 0.f : mn;
                 corr[r] = ex2(m_r[r] - mu);
                 m_r[r] = mn;
@@ -675,7 +676,7 @@ __device__ void consumer_warp_m8(const DecodeParams &p, const Smem &sm, int cw, 
         }
 
         // ---- P = hi + lo (bf16 each), transposed into mma B fragments
-        //      (E4M3: P in f16, a single part: relative error <= 2^-12)
+        //      (E4M3: P in f16, a single part: relative error <= 2^-11)
         uint32_t bh[2], bl[2];
         if constexpr (KV8) {
             bh[0] = movmatrix_trans(pack_f16x2(sc[0], sc[1]));
@@ -1149,7 +1150,7 @@ __device__ void consumer_warp_m16(const DecodeParams &p, const Smem &sm, int cw,
         }
 
         // ---- P (16 rows x 16 tokens) as the A operand, split into bf16 hi + lo
-        //      (E4M3: P in f16, a single part: relative error <= 2^-12)
+        //      (E4M3: P in f16, a single part: relative error <= 2^-11)
         uint32_t ph[4], plo[4];
         if constexpr (KV8) {
 #pragma unroll
