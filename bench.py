@@ -56,28 +56,32 @@ FALLBACK_HBM_GBS = 6800.0
 # to `source_sha256` (otherwise the bench reports traffic = null).
 NCU_TRAFFIC = {
     "llama3_8b_decode": {
-        "bytes": 580933632 + 2392320,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "41715bbbe1fb19a8f77c0fc8357bf63b59523dcd3aba934538e07a2d746b4fef",
+        "bytes": 580940544 + 2474496,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "9c527484b7c966c8a447799bc34008e2be6fcc111f730075f9e0f29473c7c8b0",
     },
     "llama3_70b_mix": {
-        "bytes": 1344529408 + 476928,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "41715bbbe1fb19a8f77c0fc8357bf63b59523dcd3aba934538e07a2d746b4fef",
+        "bytes": 1344300288 + 436224,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "9c527484b7c966c8a447799bc34008e2be6fcc111f730075f9e0f29473c7c8b0",
     },
     "long_splitk": {
-        "bytes": 2968239104 + 4545280,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "41715bbbe1fb19a8f77c0fc8357bf63b59523dcd3aba934538e07a2d746b4fef",
+        "bytes": 2968420352 + 4402944,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "9c527484b7c966c8a447799bc34008e2be6fcc111f730075f9e0f29473c7c8b0",
     },
     "spec_verify": {
-        "bytes": 1406888960 + 6053376,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "41715bbbe1fb19a8f77c0fc8357bf63b59523dcd3aba934538e07a2d746b4fef",
+        "bytes": 1406902528 + 5829632,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "9c527484b7c966c8a447799bc34008e2be6fcc111f730075f9e0f29473c7c8b0",
     },
     "llama3_8b_decode/fp8": {
-        "bytes": 290379264 + 815360,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "41715bbbe1fb19a8f77c0fc8357bf63b59523dcd3aba934538e07a2d746b4fef",
+        "bytes": 290386944 + 819200,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "9c527484b7c966c8a447799bc34008e2be6fcc111f730075f9e0f29473c7c8b0",
     },
     "llama3_70b_mix/fp8": {
-        "bytes": 663066624 + 1613824,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "41715bbbe1fb19a8f77c0fc8357bf63b59523dcd3aba934538e07a2d746b4fef",
+        "bytes": 663244544 + 2080000,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "9c527484b7c966c8a447799bc34008e2be6fcc111f730075f9e0f29473c7c8b0",
+    },
+    "spec_verify/umma": {
+        "bytes": 1441864192 + 20644864,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "9c527484b7c966c8a447799bc34008e2be6fcc111f730075f9e0f29473c7c8b0",
     },
 }
 

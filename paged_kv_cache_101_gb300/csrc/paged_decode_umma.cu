@@ -44,13 +44,11 @@
 // (2 s); the softmax warps decide to leave their loop only at their per-stage
 // named-barrier reduction, so no warp is left waiting on a named barrier.
 //
-// The kernel is opt-in (PKV_OPT_UMMA = 1). On GB300 it runs the 32-row
-// speculative-verify batch in about 279 us against 265 us for the mma.sync kernel,
-// and ties it on 60-row tree verification. The tokens-on-M tile needs a uniform
-// row stride across scattered blocks, so the TMA moves one 2 KiB box per (block,
-// half, tensor): 32 boxes per super-stage against 2 for the mma.sync kernel's
-// whole-block boxes. Issuing them takes about 1.3 us of the 1.8 us super-stage
-// cycle.
+// The kernel is opt-in (PKV_OPT_UMMA = 1): on GB300 the mma.sync kernels run the
+// same 32- and 60-row batches faster. The tokens-on-M tile needs a uniform row
+// stride across scattered blocks, so the TMA moves one 2 KiB box per (block, half,
+// tensor): 32 boxes per super-stage against 2 for the mma.sync kernel's whole-block
+// boxes, and each super-stage's softmax and values MMAs form one serial chain.
 #include <cuda_bf16.h>
 
 #include <climits>
