@@ -268,7 +268,8 @@ class StepRig:
         self.attend(self.q, self.tables, self.lens, self.out)
 
     def time_steps(self, K, warmup):
-        """(ms per step, main-kernel ms) over K steps after `warmup` untimed ones.
+        """(ms per step, main-kernel ms, append ms, attention-call ms) over K steps
+        after `warmup` untimed ones.
 
         The timed steps run as a user runs them. Unflushed steps are timed as one
         block (an event pair around every step would add ~2 us of GPU time to each);
@@ -276,7 +277,10 @@ class StepRig:
         from a separate pass in which the library records events around it: an event
         between the append and the main kernel, or between it and the merge, keeps
         the next kernel from launching early (programmatic dependent launch), so it
-        would stretch the steps it sits in."""
+        would stretch the steps it sits in. The append and the attention call
+        (main kernel + merge) are timed per call in a third pass, with events
+        around each; the event between them keeps the attention call from
+        overlapping the append, so the two add up to a little more than a step."""
         torch, pkv = self.torch, self.pkv
         for _ in range(warmup):
             self.flush()
@@ -307,13 +311,24 @@ class StepRig:
             pkv.set_profiling_events(a, b)
             self.step()
             pkv.set_profiling_events(None, None)
+        ev_c = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                for _ in range(0, K, hook)]
+        for e0, e1, e2 in ev_c:
+            self.flush()
+            e0.record()
+            self.append(self.k_new, self.v_new, self.slots)
+            e1.record()
+            self.attend(self.q, self.tables, self.lens, self.out)
+            e2.record()
         torch.cuda.synchronize()
         if self.l2_mode == "none":
             ms = ev_s[0].elapsed_time(ev_e[0]) / K
         else:
             ms = sum(a.elapsed_time(b) for a, b in zip(ev_s, ev_e)) / K
         kern = [a.elapsed_time(b) for a, b in ev_k]
-        return ms, sum(kern) / len(kern)
+        app = [e0.elapsed_time(e1) for e0, e1, _ in ev_c]
+        att = [e1.elapsed_time(e2) for _, e1, e2 in ev_c]
+        return ms, sum(kern) / len(kern), sum(app) / len(app), sum(att) / len(att)
 
     def write_flush(self, K):
         """The same steps, each after the 512 MiB memset: (ms per step, kernel ms)."""
@@ -395,7 +410,7 @@ def run_pkv(args, rank, world, dist):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    ms_per_step, kern_mean = rig.time_steps(K, args.warmup)
+    ms_per_step, kern_mean, append_ms, attn_ms = rig.time_steps(K, args.warmup)
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
@@ -413,7 +428,8 @@ def run_pkv(args, rank, world, dist):
     e2e_ms, e2e_mode, h2d, d2h = run_e2e(rig, args, dev)
 
     # max over ranks
-    ms_per_step, kern_mean, e2e_ms = max_over_ranks([ms_per_step, kern_mean, e2e_ms], dist, dev)
+    ms_per_step, kern_mean, e2e_ms, append_ms, attn_ms = max_over_ranks(
+        [ms_per_step, kern_mean, e2e_ms, append_ms, attn_ms], dist, dev)
     # the tcgen05 kernel runs when it is opted in and the batch has 17-64 score rows per
     # kv head on bf16 pools of head_dim 128 (the library's own rule)
     umma = bool(args.umma) and not (fp8 or fma or cascade) and w.head_dim == 128 and \
@@ -432,6 +448,8 @@ def run_pkv(args, rank, world, dist):
         "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 6),
         "us_per_step": round(ms_per_step * 1e3, 3),
+        "append_us": round(append_ms * 1e3, 3),
+        "attention_us": round(attn_ms * 1e3, 3),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -622,6 +640,7 @@ def run_per_config(args, rank, world, dist, headline):
         if name == args.workload and headline is not None:
             res = headline
             e = {"us_per_step": res["us_per_step"], "kernel_us": res["roofline"]["kernel_us"],
+                 "append_us": res["append_us"], "attention_us": res["attention_us"],
                  "step_gbs": res["value"], "kernel_gbs": res["roofline"]["achieved"],
                  "frac": res["roofline"]["frac"],
                  "frac_of_8tbs": res["roofline"]["frac_of_8tbs"],
@@ -635,10 +654,11 @@ def run_per_config(args, rank, world, dist, headline):
             entries[name] = e
             continue
         rig = StepRig(W.make_workload(name), args, dev)
-        ms, kern = rig.time_steps(args.steps, args.warmup)
-        ms, kern = max_over_ranks([ms, kern], dist, dev)
+        ms, kern, app, att = rig.time_steps(args.steps, args.warmup)
+        ms, kern, app, att = max_over_ranks([ms, kern, app, att], dist, dev)
         rf = roofline_entry(rig, kern, traffic_pin(name), "paged_decode_kernel")
         e = {"us_per_step": round(ms * 1e3, 3), "kernel_us": rf["kernel_us"],
+             "append_us": round(app * 1e3, 3), "attention_us": round(att * 1e3, 3),
              "step_gbs": round(job_gbs(world, rig.step_bytes, ms), 2),
              "kernel_gbs": rf["achieved"], "frac": rf["frac"],
              "frac_of_8tbs": rf["frac_of_8tbs"], "traffic": rf["traffic"],
