@@ -47,6 +47,7 @@
 
 #include <algorithm>
 #include <climits>
+#include <cstddef>
 #include <type_traits>
 
 #include "pkv_cells.cuh"
@@ -67,6 +68,10 @@ struct StageHdr {
     int16_t W;      // mask window: per-row masks rule the last W positions
 };
 static_assert(sizeof(StageHdr) == 32, "stage header: two 16-byte words");
+static_assert(offsetof(StageHdr, hg) == 12 && offsetof(StageHdr, flags) == 16 &&
+                  offsetof(StageHdr, cell) == 24 && offsetof(StageHdr, ql) == 28 &&
+                  offsetof(StageHdr, W) == 30,
+              "the producer writes the header as two int4 in field order");
 
 struct Smem {
     uint8_t *stages;
@@ -151,16 +156,11 @@ __device__ void producer_warp(const CUtensorMap *kmap, const CUtensorMap *vmap,
         if (lane == 0) {
             if (shallow && p.trace)
                 p.trace[blockIdx.x * kTraceWords + 8] += 1;
-            StageHdr *h = &sm.hdr[st];
-            h->q0 = q0;
-            h->b = b;
-            h->T = T;
-            h->hg = hg;
-            h->flags = flags;
-            h->slot = slot;
-            h->cell = cellv;
-            h->ql = int16_t(ql);
-            h->W = int16_t(W);
+            // the header in two 16-byte stores (field order of StageHdr)
+            int4 *h = reinterpret_cast<int4 *>(&sm.hdr[st]);
+            h[0] = make_int4(q0, b, T, hg);
+            h[1] = make_int4(flags, slot, cellv,
+                             int((uint32_t(uint16_t(ql))) | (uint32_t(uint16_t(W)) << 16)));
             const uint32_t bar = smem_u32(&sm.full[st]);
             mbar_arrive_expect_tx(bar, uint32_t(p.stage_bytes));
             const uint32_t kdst = smem_u32(sm.stages + size_t(st) * p.stage_bytes);
