@@ -20,7 +20,7 @@
 //    output). A sequence cut by cell boundaries leaves one partial (m, l, acc)
 //    per cell in the workspace; a small merge kernel, launched as a
 //    programmatic dependent, combines them (same rescaling rule).
-//  * Staging. Warp 0 is the producer: it walks its cells, reads block-table
+//  * Staging. The last warp is the producer: it walks its cells, reads block-table
 //    entries 32 at a time (one coalesced load), and for each block issues TMA
 //    tensor loads of K and V for its HG heads into a ring of shared-memory
 //    stages (128-byte swizzle, mbarrier completion with byte counts). Stages are
@@ -1389,13 +1389,18 @@ __global__ void __launch_bounds__(kThreadsMax, MINB)
         p.trace[blockIdx.x * kTraceWords + 7] = smid;
     }
     __syncthreads();
-    if (warp == 0) {
+    // The producer is the last warp: it shares an SM sub-partition with two consumer
+    // warps, and in the last slot the warp schedulers favour those consumers over it
+    // (it has stages of slack); in warp 0 it slowed them (measured: speculative verify
+    // 248.2 -> 243.6 us with the producer last).
+    const int producer = int(blockDim.x >> 5) - 1;
+    if (warp == producer) {
         producer_warp<D, KV8>(&kmap, &vmap, p, sm, lane);
     } else {
         if constexpr (NTW == 2)
-            consumer_warp_m16<D, WPH, KV8>(p, sm, warp - 1, lane);
+            consumer_warp_m16<D, WPH, KV8>(p, sm, warp, lane);
         else
-            consumer_warp_m8<D, KV8>(p, sm, warp - 1, lane);
+            consumer_warp_m8<D, KV8>(p, sm, warp, lane);
     }
 }
 
