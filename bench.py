@@ -56,32 +56,32 @@ FALLBACK_HBM_GBS = 6800.0
 # to `source_sha256` (otherwise the bench reports traffic = null).
 NCU_TRAFFIC = {
     "llama3_8b_decode": {
-        "bytes": 580940544 + 2474496,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "9c527484b7c966c8a447799bc34008e2be6fcc111f730075f9e0f29473c7c8b0",
+        "bytes": 580904448 + 2450688,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "3e1efdda2bc58e7d4b1c139b79b3acb5b35fc136b982d3da667b3f12517aa816",
     },
     "llama3_70b_mix": {
-        "bytes": 1344300288 + 436224,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "9c527484b7c966c8a447799bc34008e2be6fcc111f730075f9e0f29473c7c8b0",
+        "bytes": 1344164864 + 531712,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "3e1efdda2bc58e7d4b1c139b79b3acb5b35fc136b982d3da667b3f12517aa816",
     },
     "long_splitk": {
-        "bytes": 2968420352 + 4402944,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "9c527484b7c966c8a447799bc34008e2be6fcc111f730075f9e0f29473c7c8b0",
+        "bytes": 2968278784 + 4226048,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "3e1efdda2bc58e7d4b1c139b79b3acb5b35fc136b982d3da667b3f12517aa816",
     },
     "spec_verify": {
-        "bytes": 1406902528 + 5829632,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "9c527484b7c966c8a447799bc34008e2be6fcc111f730075f9e0f29473c7c8b0",
+        "bytes": 1406898688 + 6107648,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "3e1efdda2bc58e7d4b1c139b79b3acb5b35fc136b982d3da667b3f12517aa816",
     },
     "llama3_8b_decode/fp8": {
-        "bytes": 290386944 + 819200,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "9c527484b7c966c8a447799bc34008e2be6fcc111f730075f9e0f29473c7c8b0",
+        "bytes": 290381824 + 1053952,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "3e1efdda2bc58e7d4b1c139b79b3acb5b35fc136b982d3da667b3f12517aa816",
     },
     "llama3_70b_mix/fp8": {
-        "bytes": 663244544 + 2080000,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "9c527484b7c966c8a447799bc34008e2be6fcc111f730075f9e0f29473c7c8b0",
+        "bytes": 663726080 + 2384640,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "3e1efdda2bc58e7d4b1c139b79b3acb5b35fc136b982d3da667b3f12517aa816",
     },
     "spec_verify/umma": {
-        "bytes": 1441864192 + 20644864,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "9c527484b7c966c8a447799bc34008e2be6fcc111f730075f9e0f29473c7c8b0",
+        "bytes": 1450832128 + 20602368,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "3e1efdda2bc58e7d4b1c139b79b3acb5b35fc136b982d3da667b3f12517aa816",
     },
 }
 
