@@ -630,8 +630,9 @@ def run_e2e(rig, args, dev):
 
 def run_per_config(args, rank, world, dist, headline):
     """Every named workload's decode step (bf16 pools, plain call): us per step,
-    main-kernel us, step and kernel GB/s, roofline fractions, ncu traffic where
-    pinned, and the oracle timed on a bounded sample on the host cores."""
+    main-kernel us, append and attention-call us, step and kernel GB/s, its
+    `roofline` object (fractions, ncu traffic where pinned), and the oracle timed on
+    a bounded sample on the host cores."""
     import torch
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
@@ -648,7 +649,8 @@ def run_per_config(args, rank, world, dist, headline):
                  "bytes_per_step": res["config"]["bytes_per_step"],
                  "attention_bytes_unique": res["config"]["attention_bytes_unique"],
                  "attention_bytes_logical": res["config"]["attention_bytes_logical"],
-                 "l2": res["config"]["l2"], "steps": res["steps"]}
+                 "l2": res["config"]["l2"], "steps": res["steps"],
+                 "roofline": res["roofline"]}
             if "cpu_baseline" in res:
                 e["cpu_baseline"] = res["cpu_baseline"]
             entries[name] = e
@@ -664,7 +666,8 @@ def run_per_config(args, rank, world, dist, headline):
              "frac_of_8tbs": rf["frac_of_8tbs"], "traffic": rf["traffic"],
              "bytes_per_step": rig.step_bytes, "attention_bytes_unique": rig.attn_bytes,
              "attention_bytes_logical": rig.attn_bytes_logical, "l2": l2_note(rig),
-             "steps": args.steps, "device_error_word": rig.pkv.workspace_error(rig.ws)}
+             "steps": args.steps, "device_error_word": rig.pkv.workspace_error(rig.ws),
+             "roofline": rf}
         del rig
         torch.cuda.empty_cache()
         if rank == 0 and not args.no_cpu_baseline:
