@@ -558,10 +558,10 @@ const char *pkv_status_string(int32_t status);
  *                        counter in the workspace header) keeps one stage fewer
  *                        in flight, so where HBM is saturated the SMs that
  *                        stream slower get more of it and the chunks end closer
- *                        together (1-2 % faster on HBM-bound batches; slower
- *                        where L2 serves shared blocks or the math bounds the
- *                        kernel). Timing only: results are bit-identical with
- *                        pacing on or off.
+ *                        together (measured on GB300: within 1 % on HBM-bound
+ *                        batches, slower where L2 serves shared blocks or the
+ *                        math bounds the kernel). Timing only: results are
+ *                        bit-identical with pacing on or off.
  *   PKV_OPT_PACE_MARGIN  the lead allowed before pacing, in 1/10000 of the
  *                        work; 0..10000, default 0.
  *   PKV_OPT_MATH         0 = tensor cores (default); 1 = the same
