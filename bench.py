@@ -192,6 +192,7 @@ class StepRig:
         import paged_kv_cache_101_gb300 as pkv
         self.torch, self.pkv, self.dev, self.args = torch, pkv, dev, args
         self.fp8, self.cascade = fp8, cascade
+        self.two_calls = bool(getattr(args, "two_calls", False))
         if cascade:
             w = W.sharers_first(w)  # the sharing sequences form one consecutive group
         self.w = w
@@ -264,8 +265,17 @@ class StepRig:
             self.pkv.kv_append(k_new, v_new, slots, self.k_cache, self.v_cache)
 
     def step(self):
-        self.append(self.k_new, self.v_new, self.slots)
-        self.attend(self.q, self.tables, self.lens, self.out)
+        if self.cascade or self.two_calls:
+            self.append(self.k_new, self.v_new, self.slots)
+            self.attend(self.q, self.tables, self.lens, self.out)
+            return
+        # one call: append, then attention (its prologue overlaps the append)
+        w = self.w
+        self.pkv.decode_step(self.q, self.k_new, self.v_new, self.slots, self.k_cache,
+                             self.v_cache, self.tables, self.lens, w.n_query_per_seq, w.scale,
+                             self.out, ws=self.ws,
+                             k_scale=self.k_scale if self.fp8 else None,
+                             v_scale=self.v_scale if self.fp8 else None)
 
     def time_steps(self, K, warmup):
         """(ms per step, main-kernel ms, append ms, attention-call ms) over K steps
@@ -470,8 +480,10 @@ def run_pkv(args, rank, world, dist):
             "context_tokens": int(w.context_lens.sum()),
             "num_blocks": w.num_blocks, "parallelism": f"replicas x{world}",
             "l2": l2_note(rig),
-            "step": ("kv_append_fp8 + paged_decode_attention_fp8" if fp8 else
-                     "kv_append + paged_decode_attention") + " (main + merge kernels)",
+            "step": ("kv_append + paged_decode_attention_cascade" if cascade else
+                     "pkv_decode_step: kv_append" + ("_fp8" if fp8 else "") +
+                     " + paged_decode_attention" + ("_fp8" if fp8 else "")) +
+                    " (append, main + merge kernels)",
             "bytes_per_step": step_bytes, "attention_bytes_unique": rig.attn_bytes,
             "attention_bytes_logical": rig.attn_bytes_logical,
         },
@@ -1201,6 +1213,9 @@ def main():
                     help="PKV_OPT_TMA_BOX: 0 = whole-block boxes when accepted, 1 = per tile")
     ap.add_argument("--prefetch", type=int, default=0,
                     help="PKV_OPT_PREFETCH: 0 = default L2 prefetch distance, n = n - 1 blocks")
+    ap.add_argument("--two-calls", action="store_true",
+                    help="time each step as pkv_kv_append + the attention call instead of "
+                         "one pkv_decode_step (whose attention prologue overlaps the append)")
     ap.add_argument("--umma", action="store_true",
                     help="PKV_OPT_UMMA = 1: the tcgen05 kernel for 17-64 query rows per kv head")
     ap.add_argument("--math", default="tensor", choices=["tensor", "fma"],

@@ -460,6 +460,44 @@ size_t pkv_step_arena_layout(int32_t num_seqs, int32_t n_query_per_seq, int32_t 
                              size_t offsets[6]);
 
 /*
+ * pkv_decode_step -- one decode step on device buffers: the step's new K/V rows
+ * are appended (pkv_kv_append, or pkv_kv_append_fp8 with scales), then the
+ * attention runs over the updated pool (pkv_paged_decode_attention, or
+ * pkv_paged_decode_attention_fp8), both on `stream`.
+ *
+ * Passage: "ML Interview Prep, Lesson 13" section 3.5 and "LLM Inference Serving"
+ * (block-table pseudo-code): each decode step writes the new token's K/V into
+ * its slot, then attends over the sequence's blocks.
+ *
+ *   q, block_tables, context_lens, out, workspace: as pkv_paged_decode_attention
+ *   k_new, v_new   device [num_seqs * n_query_per_seq, num_kv_heads, head_dim]
+ *                  bf16 (one new row per query row, in row order)
+ *   slot_mapping   device int64 [num_seqs * n_query_per_seq], as pkv_kv_append
+ *   k_scale, v_scale  device float [num_kv_heads]: E4M3 pools (head_dim 128);
+ *                  both NULL: bf16 pools; one alone: PKV_ERR_NULL
+ *
+ * Same results, bit for bit, as the two calls in turn. The difference is
+ * timing: the append writes only the pools, and q, the tables and the lengths
+ * must be complete when the call's work starts on `stream`, so the attention
+ * kernel reads the lengths and tables and plans its work while the append
+ * still runs, and waits for the append only before its first read of the pool.
+ * q, the tables, the lengths and out must not overlap the pools.
+ *
+ * Errors: every argument check of both calls (and the workspace size and
+ * alignment the attention's plan needs) runs before anything is enqueued; on an
+ * error nothing is enqueued and the pools are unchanged. PKV_ERR_CUDA if a
+ * launch fails (the append may then have run).
+ */
+pkv_status pkv_decode_step(const void *q, const void *k_new, const void *v_new,
+                           const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                           int64_t num_blocks, const int32_t *block_tables,
+                           int32_t max_blocks_per_seq, const int32_t *context_lens,
+                           int32_t num_seqs, int32_t n_query_per_seq, int32_t num_q_heads,
+                           int32_t num_kv_heads, int32_t head_dim, float scale, void *out,
+                           int32_t out_dtype, void *workspace, size_t workspace_bytes,
+                           const float *k_scale, const float *v_scale, void *stream);
+
+/*
  * pkv_decode_step_host -- one decode step from host memory: the step's inputs
  * cross to the device, the new tokens are appended, the attention runs, and
  * its output comes back to the host. Enqueued on `stream` in this order:

@@ -25,6 +25,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIBRARY_PATH = os.path.join(_HERE, "libpkv.so")
 
 PKV_OK = 0
+(PKV_ERR_NULL, PKV_ERR_SHAPE, PKV_ERR_DTYPE, PKV_ERR_ALIGN, PKV_ERR_RANGE, PKV_ERR_WORKSPACE,
+ PKV_ERR_CUDA, PKV_ERR_UNSUPPORTED) = range(1, 9)   # pkv_status, include/pkv.h
 PKV_ERR_NO_BLOCKS, PKV_ERR_SEQUENCE = 9, 10
 PKV_BF16, PKV_FP32 = 0, 1
 (PKV_OPT_NUM_CTAS, PKV_OPT_STAGES, PKV_OPT_HEADS_PER_CTA, PKV_OPT_TMA_BOX, PKV_OPT_TAIL,
@@ -41,6 +43,8 @@ SIGNATURES = {
     "pkv_paged_decode_attention": ([_P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32,
                                     _F, _P, _I32, _P, _SZ, _P], ctypes.c_int),
     "pkv_step_arena_layout": ([_I32, _I32, _I32, _I32, _I32, _I32, _P], _SZ),
+    "pkv_decode_step": ([_P, _P, _P, _P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _I32,
+                         _I32, _F, _P, _I32, _P, _SZ, _P, _P, _P], _I32),
     "pkv_decode_step_host": ([_P, _P, _SZ, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _F,
                               _P, _P, _I32, _P, _SZ, _P], ctypes.c_int),
     "pkv_decode_step_host_pipelined": ([_P, _P, _SZ, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32,
@@ -548,6 +552,56 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, n_qu
         ws.numel(), _stream_handle(q.device))
     if st != PKV_OK:
         raise PkvError("pkv_paged_decode_attention", st)
+    return out
+
+
+def decode_step(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables, context_lens,
+                n_query_per_seq, scale, out, ws=None, k_scale=None, v_scale=None):
+    """One decode step in one call: append the new rows ``[S * nq, Hkv, D]`` at
+    ``slot_mapping``, then attend (bf16 pools; E4M3 uint8 pools with ``k_scale`` and
+    ``v_scale``). Same results as ``kv_append`` then ``paged_decode_attention``; the
+    attention kernel plans its work while the append runs."""
+    torch = _torch()
+    _check(q, "q", torch.bfloat16, 3)
+    _check(k_new, "k_new", torch.bfloat16, 3)
+    _check(v_new, "v_new", torch.bfloat16, 3)
+    _check(slot_mapping, "slot_mapping", torch.int64, 1)
+    _check(block_tables, "block_tables", torch.int32, 2)
+    _check(context_lens, "context_lens", torch.int32, 1)
+    if (k_scale is None) != (v_scale is None):
+        raise ValueError("give both scales (E4M3 pools) or neither (bf16 pools)")
+    if k_scale is not None:
+        NB, Hkv, D = _check_fp8_pools(k_cache, v_cache, k_scale, v_scale)
+    else:
+        _check(k_cache, "k_cache", torch.bfloat16, 4)
+        _check(v_cache, "v_cache", torch.bfloat16, 4)
+        NB, bs, Hkv, D = k_cache.shape
+        if bs != BLOCK_SIZE or v_cache.shape != k_cache.shape:
+            raise ValueError("pools must be [num_blocks, 16, Hkv, D] and equal in shape")
+    if out.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("out must be bfloat16 or float32")
+    _check(out, "out", out.dtype, 3)
+    S = context_lens.shape[0]
+    nq = int(n_query_per_seq)
+    Hq = q.shape[1]
+    if q.shape != (S * nq, Hq, D) or out.shape != q.shape or block_tables.shape[0] != S:
+        raise ValueError("q/out must be [num_seqs * n_query_per_seq, Hq, D], tables [num_seqs, MB]")
+    if (k_new.shape != (S * nq, Hkv, D) or v_new.shape != k_new.shape
+            or slot_mapping.shape[0] != S * nq):
+        raise ValueError("k_new/v_new must be [num_seqs * n_query_per_seq, Hkv, D] with one slot "
+                         "per row")
+    need = workspace_size(S, nq, Hq, Hkv, D)
+    if ws is None:
+        ws = workspace(q.device, need)
+    st = lib().pkv_decode_step(
+        q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(),
+        k_cache.data_ptr(), v_cache.data_ptr(), NB, block_tables.data_ptr(),
+        block_tables.shape[1], context_lens.data_ptr(), S, nq, Hq, Hkv, D, float(scale),
+        out.data_ptr(), PKV_FP32 if out.dtype == torch.float32 else PKV_BF16, ws.data_ptr(),
+        ws.numel(), None if k_scale is None else k_scale.data_ptr(),
+        None if v_scale is None else v_scale.data_ptr(), _stream_handle(q.device))
+    if st != PKV_OK:
+        raise PkvError("pkv_decode_step", st)
     return out
 
 

@@ -849,4 +849,18 @@ pkv_status attention_need(const void *q, const void *k_cache, const void *v_cach
                      Cascade(), need);
 }
 
+pkv_status attention_check(const void *q, const void *k_cache, const void *v_cache,
+                           int64_t num_blocks, int kv8, const float *k_scale,
+                           const float *v_scale, const int32_t *block_tables,
+                           int32_t max_blocks_per_seq, const int32_t *context_lens,
+                           int32_t num_seqs, int32_t n_query_per_seq, int32_t num_q_heads,
+                           int32_t num_kv_heads, int32_t head_dim, void *out, int32_t out_dtype,
+                           size_t *need)
+{
+    return attention(q, k_cache, v_cache, num_blocks, kv8, k_scale, v_scale, block_tables,
+                     max_blocks_per_seq, context_lens, num_seqs, n_query_per_seq, num_q_heads,
+                     num_kv_heads, head_dim, 1.f, out, out_dtype, nullptr, 0, nullptr, Varlen(),
+                     Cascade(), need);
+}
+
 }  // namespace pkv

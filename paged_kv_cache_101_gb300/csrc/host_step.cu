@@ -153,6 +153,58 @@ pkv_status compute_step(const StepPlan &sp, const void *device_arena, void *k_ca
 
 extern "C" {
 
+pkv_status pkv_decode_step(const void *q, const void *k_new, const void *v_new,
+                           const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                           int64_t num_blocks, const int32_t *block_tables,
+                           int32_t max_blocks_per_seq, const int32_t *context_lens,
+                           int32_t num_seqs, int32_t n_query_per_seq, int32_t num_q_heads,
+                           int32_t num_kv_heads, int32_t head_dim, float scale, void *out,
+                           int32_t out_dtype, void *workspace, size_t workspace_bytes,
+                           const float *k_scale, const float *v_scale, void *stream)
+{
+    if ((k_scale == nullptr) != (v_scale == nullptr))
+        return PKV_ERR_NULL;
+    const int kv8 = k_scale ? 1 : 0;
+    // every check of both calls before anything is enqueued: the attention's (with
+    // the workspace its plan needs), then the append's own (it checks before it
+    // enqueues)
+    size_t need = 0;
+    pkv_status s = pkv::attention_check(q, k_cache, v_cache, num_blocks, kv8, k_scale, v_scale,
+                                        block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                                        n_query_per_seq, num_q_heads, num_kv_heads, head_dim, out,
+                                        out_dtype, &need);
+    if (s != PKV_OK)
+        return s;
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need)
+            return PKV_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+            return PKV_ERR_ALIGN;
+    }
+    const int64_t n_new = int64_t(num_seqs) * n_query_per_seq;
+    s = kv8 ? pkv_kv_append_fp8(k_new, v_new, slot_mapping, n_new, k_cache, v_cache, num_blocks,
+                                num_kv_heads, head_dim, k_scale, v_scale, stream)
+            : pkv_kv_append(k_new, v_new, slot_mapping, n_new, k_cache, v_cache, num_blocks,
+                            num_kv_heads, head_dim, stream);
+    if (s != PKV_OK)
+        return s;
+    // the append just enqueued writes only the pools, and the caller's q, tables and
+    // lengths were complete before it ran: the attention plans its cells while the
+    // append runs and waits for it only before its first read of the pool
+    pkv::set_meta_ready(true);
+    s = kv8 ? pkv_paged_decode_attention_fp8(q, k_cache, v_cache, num_blocks, k_scale, v_scale,
+                                             block_tables, max_blocks_per_seq, context_lens,
+                                             num_seqs, n_query_per_seq, num_q_heads, num_kv_heads,
+                                             head_dim, scale, out, out_dtype, workspace,
+                                             workspace_bytes, stream)
+            : pkv_paged_decode_attention(q, k_cache, v_cache, num_blocks, block_tables,
+                                         max_blocks_per_seq, context_lens, num_seqs,
+                                         n_query_per_seq, num_q_heads, num_kv_heads, head_dim,
+                                         scale, out, out_dtype, workspace, workspace_bytes, stream);
+    pkv::set_meta_ready(false);
+    return s;
+}
+
 pkv_status pkv_decode_step_host(const void *host_arena, void *device_arena, size_t arena_bytes,
                                 void *k_cache, void *v_cache, int64_t num_blocks,
                                 int32_t max_blocks_per_seq, int32_t num_seqs,

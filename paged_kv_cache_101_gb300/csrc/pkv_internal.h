@@ -163,6 +163,15 @@ pkv_status attention_need(const void *q, const void *k_cache, const void *v_cach
                           const int32_t *context_lens, int32_t num_seqs, int32_t n_query_per_seq,
                           int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, void *out,
                           int32_t out_dtype, size_t *need);
+// The same checks for either pool type (kv8: E4M3 pools with per-head scales), with
+// the workspace taken as given: the bytes the call's plan needs go to *need.
+pkv_status attention_check(const void *q, const void *k_cache, const void *v_cache,
+                           int64_t num_blocks, int kv8, const float *k_scale,
+                           const float *v_scale, const int32_t *block_tables,
+                           int32_t max_blocks_per_seq, const int32_t *context_lens,
+                           int32_t num_seqs, int32_t n_query_per_seq, int32_t num_q_heads,
+                           int32_t num_kv_heads, int32_t head_dim, void *out, int32_t out_dtype,
+                           size_t *need);
 
 cudaError_t launch_kv_append(const void *k_new, const void *v_new, const int64_t *slot_mapping,
                              int64_t n_new, void *k_cache, void *v_cache, int64_t num_blocks,
