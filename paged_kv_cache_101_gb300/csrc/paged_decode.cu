@@ -2096,7 +2096,11 @@ cudaError_t launch_merge(const DecodePlan &pl, const DecodeParams &p, cudaStream
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaError_t e;
     const bool few_rows = p.HG * p.rows <= 32;
-    const int cta_rows = few_rows ? 16 : 32;
+    // fewer (sequence, head group) pairs than cells: sequences span many cells, so a
+    // merge folds many pieces; one row per warp and 8 pieces per batch of loads
+    // halve its chain of L2 round trips
+    const bool many_pieces = few_rows && int64_t(p.S) * p.n_hg < int64_t(pl.grid);
+    const int cta_rows = many_pieces ? 8 : few_rows ? 16 : 32;
     cudaLaunchConfig_t mcfg = {};
     mcfg.gridDim = dim3(unsigned(p.S), unsigned(p.n_hg),
                         unsigned((p.HG * p.rows + cta_rows - 1) / cta_rows));
@@ -2108,6 +2112,8 @@ cudaError_t launch_merge(const DecodePlan &pl, const DecodeParams &p, cudaStream
     if (pl.D == 64)
         e = few_rows ? cudaLaunchKernelEx(&mcfg, paged_decode_merge_kernel<64, 2, 4>, p, int(pl.grid))
                      : cudaLaunchKernelEx(&mcfg, paged_decode_merge_kernel<64, 4, 2>, p, int(pl.grid));
+    else if (many_pieces)
+        e = cudaLaunchKernelEx(&mcfg, paged_decode_merge_kernel<128, 1, 8>, p, int(pl.grid));
     else
         e = few_rows ? cudaLaunchKernelEx(&mcfg, paged_decode_merge_kernel<128, 2, 4>, p, int(pl.grid))
                      : cudaLaunchKernelEx(&mcfg, paged_decode_merge_kernel<128, 4, 2>, p, int(pl.grid));
