@@ -56,32 +56,32 @@ FALLBACK_HBM_GBS = 6800.0
 # to `source_sha256` (otherwise the bench reports traffic = null).
 NCU_TRAFFIC = {
     "llama3_8b_decode": {
-        "bytes": 580904448 + 2450688,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "3e1efdda2bc58e7d4b1c139b79b3acb5b35fc136b982d3da667b3f12517aa816",
+        "bytes": 580901376 + 2423808,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "2c0af3dfec4a02dd989b85e9dd044094e427b12c3ed490098a75434865f23896",
     },
     "llama3_70b_mix": {
-        "bytes": 1344164864 + 531712,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "3e1efdda2bc58e7d4b1c139b79b3acb5b35fc136b982d3da667b3f12517aa816",
+        "bytes": 1344542976 + 442624,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "2c0af3dfec4a02dd989b85e9dd044094e427b12c3ed490098a75434865f23896",
     },
     "long_splitk": {
-        "bytes": 2968278784 + 4226048,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "3e1efdda2bc58e7d4b1c139b79b3acb5b35fc136b982d3da667b3f12517aa816",
+        "bytes": 2968272896 + 4363776,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "2c0af3dfec4a02dd989b85e9dd044094e427b12c3ed490098a75434865f23896",
     },
     "spec_verify": {
-        "bytes": 1406898688 + 6107648,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "3e1efdda2bc58e7d4b1c139b79b3acb5b35fc136b982d3da667b3f12517aa816",
+        "bytes": 1406908928 + 6244352,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "2c0af3dfec4a02dd989b85e9dd044094e427b12c3ed490098a75434865f23896",
     },
     "llama3_8b_decode/fp8": {
-        "bytes": 290381824 + 1053952,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "3e1efdda2bc58e7d4b1c139b79b3acb5b35fc136b982d3da667b3f12517aa816",
+        "bytes": 290347008 + 989696,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "2c0af3dfec4a02dd989b85e9dd044094e427b12c3ed490098a75434865f23896",
     },
     "llama3_70b_mix/fp8": {
-        "bytes": 663726080 + 2384640,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "3e1efdda2bc58e7d4b1c139b79b3acb5b35fc136b982d3da667b3f12517aa816",
+        "bytes": 663453440 + 2262528,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "2c0af3dfec4a02dd989b85e9dd044094e427b12c3ed490098a75434865f23896",
     },
     "spec_verify/umma": {
-        "bytes": 1450832128 + 20602368,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "3e1efdda2bc58e7d4b1c139b79b3acb5b35fc136b982d3da667b3f12517aa816",
+        "bytes": 1442352896 + 20516864,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "source_sha256": "2c0af3dfec4a02dd989b85e9dd044094e427b12c3ed490098a75434865f23896",
     },
 }
 
