@@ -27,6 +27,7 @@ sequences: weak scaling, no data-path collective).
 from __future__ import annotations
 
 import argparse
+import copy
 import hashlib
 import json
 import os
@@ -1115,21 +1116,73 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
-def sample_workload(name: str, max_seqs: int):
-    """The first ``max_seqs`` sequences of a workload (same lengths, pool and values)."""
-    w = W.make_workload(name)
-    if w.num_seqs <= max_seqs:
-        return w, f"all {w.num_seqs} sequences"
-    keep = max_seqs
+def sample_workload(name: str, max_seqs: int, max_tokens: int = 0, w=None):
+    """The first ``max_seqs`` sequences of a workload (same lengths, pool and values).
+    With ``max_tokens`` the sample also stops at that many context tokens: the last
+    sequence kept is cut to a shorter context, its new tokens moved to that context's
+    last positions, so a step over the sample is still an append + attention."""
+    w = W.make_workload(name) if w is None else w
+    total = len(W.workload_lengths(name)[0])
+    nq = w.n_query_per_seq
+    keep = min(max_seqs, w.num_seqs)
+    cut = None
+    if max_tokens > 0:
+        run, k = 0, 0
+        while k < keep:
+            T = int(w.context_lens[k])
+            if run + T > max_tokens:
+                L = max(max_tokens - run, nq + 15)
+                if k == 0 or L > nq + 15:
+                    cut = (k, min(L, T))
+                    k += 1
+                break
+            run += T
+            k += 1
+        keep = max(k, 1)
+    nrow = keep * nq
     w.context_lens = w.context_lens[:keep].copy()
     w.block_tables = w.block_tables[:keep].copy()
-    w.q = w.q[: keep * w.n_query_per_seq].copy()
-    w.k_new = w.k_new[: keep * w.n_query_per_seq].copy()
-    w.v_new = w.v_new[: keep * w.n_query_per_seq].copy()
-    w.slot_mapping = w.slot_mapping[: keep * w.n_query_per_seq].copy()
+    w.q = w.q[:nrow].copy()
+    w.k_new = w.k_new[:nrow].copy()
+    w.v_new = w.v_new[:nrow].copy()
+    w.slot_mapping = w.slot_mapping[:nrow].copy()
     w.shared = w.shared[:keep].copy()
     w.num_seqs = keep
-    return w, f"first {keep} of {len(W.workload_lengths(name)[0])} sequences"
+    desc = f"all {total} sequences" if keep == total else f"first {keep} of {total} sequences"
+    if cut is not None and cut[1] < int(w.context_lens[cut[0]]):
+        k, L = cut
+        w.context_lens[k] = L
+        for j in range(nq):
+            pos = L - nq + j
+            w.slot_mapping[k * nq + j] = int(w.block_tables[k, pos // 16]) * 16 + pos % 16
+        desc += f", the last cut to its first {L} tokens"
+    if keep < total or cut is not None:
+        compact_pool(w)
+    return w, desc
+
+
+def compact_pool(w):
+    """Keep only the pool blocks the sample's sequences use (same values, ids renumbered
+    in order): an oracle step copies the pool for its append, so a small sample of a
+    large workload must not carry the whole pool."""
+    nb = (np.maximum(w.context_lens.astype(np.int64), 0) + 15) // 16
+    used = set()
+    for s in range(w.num_seqs):
+        used.update(int(b) for b in w.block_tables[s, :nb[s]])
+    used.update(int(x) // 16 for x in w.slot_mapping if x >= 0)
+    ids = np.array(sorted(used), dtype=np.int64)
+    remap = np.zeros(w.num_blocks, dtype=np.int64)
+    remap[ids] = np.arange(ids.size)
+    tables = np.zeros_like(w.block_tables)
+    for s in range(w.num_seqs):
+        tables[s, :nb[s]] = remap[w.block_tables[s, :nb[s]]]
+    w.block_tables = tables
+    w.slot_mapping = np.where(w.slot_mapping >= 0,
+                              remap[np.maximum(w.slot_mapping, 0) // 16] * 16 + w.slot_mapping % 16,
+                              w.slot_mapping).astype(w.slot_mapping.dtype)
+    w.k_cache = np.ascontiguousarray(w.k_cache[ids])
+    w.v_cache = np.ascontiguousarray(w.v_cache[ids])
+    w.num_blocks = int(ids.size)
 
 
 CPU_SAMPLE_SEQS = {"tiny": 4, "llama3_8b_decode": 64, "llama3_70b_mix": 64, "long_splitk": 2,
@@ -1145,11 +1198,29 @@ def cpu_baseline(args):
                       f"step(s) (append + fp64 attention), {el:.1f} s on {threads} threads"}
 
 
+REF_BUDGET_S = 120.0  # the reference arm's warm-up + timed steps, about
+
+
 def run_reference(args):
+    """The fp64 oracle on the host cores, --warmup + --steps steps of a sample of the
+    workload sized so that the whole run takes about REF_BUDGET_S: one timed probe step
+    on the usual sample, then, if (steps + warmup) of those would take longer, a
+    sample of proportionally fewer context tokens."""
     threads = host_cores()
-    w, desc = sample_workload(args.workload, CPU_SAMPLE_SEQS.get(args.workload, 8))
+    nseq = CPU_SAMPLE_SEQS.get(args.workload, 8)
+    w_full = W.make_workload(args.workload)
+    w, desc = sample_workload(args.workload, nseq, w=copy.deepcopy(w_full))
     step_fn, step_bytes = oracle_step_fn(w, args.kv_dtype, threads)
-    for _ in range(args.warmup):
+    t0 = time.perf_counter()
+    step_fn()  # the probe, counted as a warm-up step
+    t_probe = time.perf_counter() - t0
+    per_step = REF_BUDGET_S / max(1, args.steps + args.warmup)
+    if t_probe > per_step:
+        tokens = int(np.sum(w.context_lens))
+        budget = max(int(tokens * per_step / t_probe), 1)
+        w, desc = sample_workload(args.workload, nseq, max_tokens=budget, w=w_full)
+        step_fn, step_bytes = oracle_step_fn(w, args.kv_dtype, threads)
+    for _ in range(max(args.warmup - 1, 0)):
         step_fn()
     times = []
     for _ in range(args.steps):
