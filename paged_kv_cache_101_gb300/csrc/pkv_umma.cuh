@@ -54,19 +54,6 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
         : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]: A (M x 16, bf16 pairs packed in 8 columns, row i
-// in lane i for M = 128) is read from tensor memory.
-__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                 uint32_t idesc, bool accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred acc;\n\t"
-        "setp.ne.b32 acc, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, acc;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(uint32_t(accumulate))
-        : "memory");
-}
-
 // One arrival on `bar` once every tcgen05.mma this thread issued before has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar)
 {
