@@ -58,31 +58,31 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     "llama3_8b_decode": {
         "bytes": 580901376 + 2423808,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "af8f4775c40c071cf1947bbc6d8281084cb87bdff5aa0dd5a4cdb042cdedaa9a",
+        "source_sha256": "4efd1c10e0e0af91e272fe6ce26ab7f2b292e5c09dab6cebe31b3c12d97ebbca",
     },
     "llama3_70b_mix": {
         "bytes": 1344542976 + 442624,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "af8f4775c40c071cf1947bbc6d8281084cb87bdff5aa0dd5a4cdb042cdedaa9a",
+        "source_sha256": "4efd1c10e0e0af91e272fe6ce26ab7f2b292e5c09dab6cebe31b3c12d97ebbca",
     },
     "long_splitk": {
         "bytes": 2968272896 + 4363776,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "af8f4775c40c071cf1947bbc6d8281084cb87bdff5aa0dd5a4cdb042cdedaa9a",
+        "source_sha256": "4efd1c10e0e0af91e272fe6ce26ab7f2b292e5c09dab6cebe31b3c12d97ebbca",
     },
     "spec_verify": {
         "bytes": 1406908928 + 6244352,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "af8f4775c40c071cf1947bbc6d8281084cb87bdff5aa0dd5a4cdb042cdedaa9a",
+        "source_sha256": "4efd1c10e0e0af91e272fe6ce26ab7f2b292e5c09dab6cebe31b3c12d97ebbca",
     },
     "llama3_8b_decode/fp8": {
         "bytes": 290347008 + 989696,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "af8f4775c40c071cf1947bbc6d8281084cb87bdff5aa0dd5a4cdb042cdedaa9a",
+        "source_sha256": "4efd1c10e0e0af91e272fe6ce26ab7f2b292e5c09dab6cebe31b3c12d97ebbca",
     },
     "llama3_70b_mix/fp8": {
         "bytes": 663453440 + 2262528,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "af8f4775c40c071cf1947bbc6d8281084cb87bdff5aa0dd5a4cdb042cdedaa9a",
+        "source_sha256": "4efd1c10e0e0af91e272fe6ce26ab7f2b292e5c09dab6cebe31b3c12d97ebbca",
     },
     "spec_verify/umma": {
         "bytes": 1442352896 + 20516864,  # dram__bytes_read.sum + dram__bytes_write.sum
-        "source_sha256": "af8f4775c40c071cf1947bbc6d8281084cb87bdff5aa0dd5a4cdb042cdedaa9a",
+        "source_sha256": "4efd1c10e0e0af91e272fe6ce26ab7f2b292e5c09dab6cebe31b3c12d97ebbca",
     },
 }
 

@@ -128,13 +128,6 @@ __device__ __forceinline__ uint64_t policy_evict_first()
     return p;
 }
 
-__device__ __forceinline__ uint64_t policy_evict_last()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
 // ---------------------------------------------------------------- warp MMA
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4])
 {
@@ -188,18 +181,9 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
     return d;
 }
 
-// Two E4M3 codes (bits 0..7 and 8..15) -> f16x2 with the first in bits 0..15.
-// Exact: every E4M3 value (NaN included) is an f16 value.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair)
-{
-    uint32_t d;
-    const uint16_t x = uint16_t(pair);
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(x));
-    return d;
-}
-
 // Four E4M3 codes (bytes 0..3) -> two f16x2: bytes 0,1 -> `p01`, bytes 2,3 -> `p23`
-// (the two code pairs are split as 16-bit halves, no shift). Exact.
+// (the two code pairs are split as 16-bit halves, no shift). Exact: every E4M3 value
+// (NaN included) is an f16 value.
 __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t codes, uint32_t &p01, uint32_t &p23)
 {
     asm("{\n\t.reg .b16 lo, hi;\n\t"
